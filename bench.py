@@ -1,0 +1,426 @@
+"""Benchmark of the routed MoE layer forward pass on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step is one pass of the whole layer (router + top-k, residency bind with
+its fill copies, dispatch, expert FFN, combine) over one batch of the
+workload: one decode token for the default 'decode' workload (hidden 4096,
+256 experts, top-6, intermediate 2048, 37% of experts resident, LRU, Zipf(1.1)
+routing), the whole 8192-token block for 'prefill', four stacked layers for
+'long_prefill'.  Inputs are synthetic (seeded; see moe_inputs) and resident
+in HBM before the timed region; each step is a CUDA-graph replay of one
+moe_layer_forward call, timed with CUDA events on its stream, and L2 is
+flushed (256 MB write) between steps outside the events.  Prints one JSON
+line on rank 0.  --impl reference times the CPU fp64 oracle instead.
+"""
+import argparse
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from moe_inputs import CONFIGS, gen  # noqa: E402
+
+METRIC = "MoE-layer tokens/s (decode, prefill) and % of GB300 HBM / bf16 tensor peak"
+UNIT = "tokens/s"
+CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.path = None
+        self.gpu_index = gpu_index
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={CLOCK_QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ algorithmic work
+def expert_ffn_flops(cfg):
+    return 2.0 * cfg.T * cfg.k * 3 * cfg.H * cfg.I
+
+
+def router_flops(cfg):
+    return 2.0 * cfg.T * cfg.H * cfg.E
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, rank, world):
+    import torch
+    import edge_moe_serving_gb300 as moe
+    from moe_inputs.device import DeviceCache, DeviceLayer, to_dev_bf16
+
+    cfg = CONFIGS[args.workload]
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    decode_like = cfg.steps > 1
+    n_steps = args.warmup + args.steps
+    stream = torch.cuda.Stream(device=dev)
+
+    dc = DeviceCache(cfg, dev)
+    layers = [DeviceLayer(cfg, l, dev) for l in range(cfg.n_layers)]
+    # per-step inputs (decode: a stream of tokens; prefill: one block per layer, reused every step)
+    if decode_like:
+        xs = [to_dev_bf16(gen.x_bits(cfg, 0, s), dev) for s in range(n_steps)]
+    else:
+        xs = [to_dev_bf16(gen.x_bits(cfg, l, 0), dev) for l in range(cfg.n_layers)]
+    T, H = cfg.T, cfg.H
+    mode = moe.MOE_FFN_AUTO
+    ws_bytes = moe.moe_layer_workspace_size(layers[0].struct, dc.struct, T, mode)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stats = torch.zeros(8, dtype=torch.int32, device=dev)
+    x_in = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def layer_call(l, x, s):
+        moe.moe_layer_forward(layers[l].struct, dc.struct, x, T, out, cfg.phi_q16, cfg.min_fill, cfg.fill_policy,
+                              1000 + l, mode, None, ws, ws_bytes, status, stats, s)
+
+    def step_body(s):
+        # decode: the step's token was staged into x_in; prefill: every layer's block is resident
+        if decode_like:
+            layer_call(0, x_in, s)
+        else:
+            for l in range(cfg.n_layers):
+                layer_call(l, xs[l], s)
+
+    # one eager call sets kernel attributes and occupancy caches before capture
+    with torch.cuda.stream(stream):
+        x_in.copy_(xs[0])
+        step_body(stream)
+    torch.cuda.synchronize()
+    dc.reset()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step_body(stream)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # warm-up steps (untimed), then K timed steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for s in range(args.warmup):
+            if decode_like:
+                x_in.copy_(xs[s])
+            graph.replay()
+            flush.zero_()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            s = args.warmup + i
+            if decode_like:
+                x_in.copy_(xs[s])
+            ev[i][0].record(stream)
+            graph.replay()
+            ev[i][1].record(stream)
+            flush.zero_()
+    torch.cuda.synchronize()
+    barrier()
+    bracket_s = time.perf_counter() - t0
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_s = sum(step_ms) / 1e3
+    dev_status = int(status.cpu().numpy().view(np.uint32)[0])
+
+    # max over ranks
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_s], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_s = float(t.item())
+    tokens_per_step = T * (1 if decode_like else 1)
+    value = world * args.steps * tokens_per_step / total_s
+
+    # ---- dominant kernel: the expert FFN call, events on its stream (eager pass)
+    roof = measure_ffn_roofline(cfg, dc, layers, xs, decode_like, stream, peaks, args, moe, torch)
+
+    # ---- end to end through the public call with host buffers
+    e2e = measure_e2e(cfg, dc, layers, decode_like, stream, args, moe, torch, ws, ws_bytes, status, stats)
+
+    launches_per_call = kernels_per_call(cfg)
+    result = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_s * 1e3 / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(cfg, world),
+        "impl": "ours",
+        "step_ms_p10_p50_p90": [round(float(np.percentile(step_ms, q)), 5) for q in (10, 50, 90)],
+        "bracket_ms_per_step": round(bracket_s * 1e3 / args.steps, 5),
+        "device_status": dev_status,
+        "roofline": roof,
+        "clocks": clk,
+        "e2e": e2e,
+        "gpu_launches": launches_per_call * cfg.n_layers * args.steps,
+    }
+    return result
+
+
+def kernels_per_call(cfg):
+    """Kernels one moe_layer_forward call launches for this workload."""
+    R = cfg.T * cfg.k
+    route = 1
+    bind = 2                      # bind + fill copy
+    dispatch = 1 if R <= 4096 else 3
+    gather = 1 if cfg.T > 8 else 0
+    ffn = 2
+    combine = 1
+    return route + bind + dispatch + gather + ffn + combine
+
+
+def workload_config(cfg, world):
+    return {"workload": cfg.name, "tokens_per_layer_call": cfg.T, "hidden": cfg.H, "experts": cfg.E,
+            "top_k": cfg.k, "intermediate": cfg.I, "layers_per_step": cfg.n_layers,
+            "cache_slots": cfg.cache_slots if cfg.cache_slots is not None else cfg.n_layers * cfg.E,
+            "phi_q16": cfg.phi_q16, "fill_policy": "random" if cfg.fill_policy else "lowest_id",
+            "routing_bias": cfg.bias, "l2": "flushed between steps (256 MB write)",
+            "parallelism": f"replicas x{world}", "graph": "one CUDA graph replay per step"}
+
+
+def measure_ffn_roofline(cfg, dc, layers, xs, decode_like, stream, peaks, args, moe, torch):
+    """Time moe_expert_ffn_grouped alone (CUDA events on its stream) for the
+    step inputs of the timed run; algorithmic work per call: the weights of
+    the active experts (HBM-bound decode) or the FFN FLOPs (prefill)."""
+    dev = xs[0].device
+    T, k, E = cfg.T, cfg.k, cfg.E
+    R = T * k
+    n = min(args.steps, 16)
+    ids = torch.empty(R, dtype=torch.int32, device=dev)
+    w = torch.empty(R, dtype=torch.float32, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    perm = torch.empty(R, dtype=torch.int32, device=dev)
+    inv = torch.empty(R, dtype=torch.int32, device=dev)
+    y = torch.empty((R, cfg.H), dtype=torch.float32, device=dev)
+    xp = torch.empty((R, cfg.H), dtype=torch.bfloat16, device=dev) if T > 8 else None
+    mode = moe.MOE_FFN_AUTO
+    wsb = max(moe.moe_route_topk_workspace_size(T, E), moe.moe_dispatch_workspace_size(T, k, E),
+              moe.moe_expert_ffn_workspace_size(T, k, E, cfg.H, cfg.I, mode))
+    wsx = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    times, byts, flops = [], [], []
+    with torch.cuda.stream(stream):
+        for i in range(n):
+            l = 0 if decode_like else i % cfg.n_layers
+            x = xs[args.warmup + i] if decode_like else xs[l]
+            moe.moe_route_topk(x, T, cfg.H, layers[l].w_router, layers[l].bias, E, k, ids, w, None, wsx, wsb, st,
+                               stream)
+            moe.moe_dispatch(ids, T, k, E, counts, offsets, perm, inv, x if xp is not None else None, cfg.H, xp,
+                             wsx, wsb, st, stream)
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            moe.moe_expert_ffn_grouped(dc.struct, l, counts, offsets, perm, x, xp, T, k, None, mode, y, wsx, wsb, st,
+                                       stream)
+            b.record(stream)
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b) / 1e3)
+            active = int((counts > 0).sum().item())
+            byts.append(active * cfg.expert_bytes + R * cfg.H * 2 + R * cfg.H * 4)
+            flops.append(expert_ffn_flops(cfg))
+    t = float(np.mean(times))
+    if decode_like:
+        achieved = float(np.mean(byts)) / t / 1e9
+        peak = peaks["hbm_gbs"]
+        return {"kernel": "moe_expert_ffn_grouped (gate/up GEMV + down GEMV)", "bound": "hbm",
+                "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "traffic": None, "peak_source": peaks["source"] + " (burst copy bandwidth)",
+                "algorithmic_bytes_per_call": int(np.mean(byts)), "call_us": round(t * 1e6, 3)}
+    achieved = float(np.mean(flops)) / t / 1e12
+    peak = peaks["bf16_tflops"]
+    return {"kernel": "moe_expert_ffn_grouped", "bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+            "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+            "peak_source": peaks["source"] + " (burst cuBLAS bf16)", "flops_per_call": expert_ffn_flops(cfg),
+            "call_us": round(t * 1e6, 3)}
+
+
+def measure_e2e(cfg, dc, layers, decode_like, stream, args, moe, torch, ws, ws_bytes, status, stats):
+    """The public call with host buffers: pinned H2D of the step's tokens,
+    moe_layer_forward, D2H of the output, host waits for it; wall clock."""
+    dev = ws.device
+    T, H = cfg.T, cfg.H
+    n = args.steps
+    host_x = [torch.from_numpy(gen.x_bits(cfg, 0, (s if decode_like else 0)).view(np.int16)).view(torch.bfloat16)
+              .pin_memory() for s in range(n if decode_like else 1)]
+    host_out = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    dc.reset()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(n):
+            for l in range(cfg.n_layers):
+                hx = host_x[i] if decode_like else host_x[0]
+                x_dev.copy_(hx, non_blocking=True)
+                moe.moe_layer_forward(layers[l].struct, dc.struct, x_dev, T, out, cfg.phi_q16, cfg.min_fill,
+                                      cfg.fill_policy, 1000 + l, moe.MOE_FFN_AUTO, None, ws, ws_bytes, status, stats,
+                                      stream)
+                host_out.copy_(out, non_blocking=True)
+            stream.synchronize()
+    el = time.perf_counter() - t0
+    return {"value": round(n * T / el, 3), "unit": UNIT,
+            "h2d_bytes_per_step": T * H * 2 * cfg.n_layers, "d2h_bytes_per_step": T * H * 2 * cfg.n_layers,
+            "note": "moe_layer_forward per layer, not graph-captured; host waits for each step's output"}
+
+
+# ------------------------------------------------------------------ oracle arm
+def oracle_step(cfg, step, state, O):
+    """One step of the workload through the CPU fp64 oracle: router, top-k,
+    residency bind, dispatch, per-expert SwiGLU, combine."""
+    layers = range(cfg.n_layers)
+    for layer in layers:
+        s = step if cfg.steps > 1 else 0
+        x = gen.bf16_bits_to_f64(gen.x_bits(cfg, layer, s))
+        res = O.layer_forward(x, gen.w_router(cfg, layer), gen.bias(cfg, layer, s), cfg.k,
+                              lambda e: gen.expert_f64(cfg, layer, e), E=cfg.E)
+        state, _ = O.bind(state, layer, res["ids"], cfg.E, cfg.phi_q16, cfg.min_fill, cfg.fill_policy, 1000 + layer)
+    return state
+
+
+def oracle_tokens_per_step(cfg, sample_tokens):
+    return cfg.T if sample_tokens is None else sample_tokens
+
+
+def run_oracle_bounded(cfg, budget_s, max_steps=None):
+    """Time the oracle on a bounded sample of the workload (whole steps)."""
+    from oracle import moe_oracle as O
+    import dataclasses
+    sample = cfg
+    note = "whole decode steps"
+    if cfg.T > 64:
+        # a prefill block takes minutes in fp64: time a 64-token slice of it (same layer shape)
+        sample = dataclasses.replace(cfg, T=64)
+        note = f"64-token slices of the {cfg.T}-token block, {cfg.n_layers} layer(s) each"
+    state = gen.initial_cache(sample)
+    t0 = time.perf_counter()
+    steps = 0
+    while True:
+        state = oracle_step(sample, steps, state, O)
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or (max_steps and steps >= max_steps):
+            break
+    return {"value": round(steps * sample.T / el, 5), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{steps} step(s) of '{cfg.name}' ({note}) in {el:.1f} s, fp64 numpy, BLAS on all cores"}
+
+
+def run_reference(args, rank, world):
+    cfg = CONFIGS[args.workload]
+    if rank != 0:
+        return None
+    per_step_budget = max(0.5, args.reference_budget_s / max(1, args.steps + args.warmup))
+    run_oracle_bounded(cfg, 0.0, max_steps=max(1, min(args.warmup, 1)))
+    cb = run_oracle_bounded(cfg, per_step_budget * args.steps, max_steps=args.steps)
+    return {"metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": workload_config(cfg, world),
+            "impl": "reference", "cpu_baseline": cb,
+            "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=32)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="decode", choices=sorted(CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-baseline-s", type=float, default=15.0)
+    ap.add_argument("--reference-budget-s", type=float, default=120.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res))
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl")
+    res = run_ours(args, rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = run_oracle_bounded(CONFIGS[args.workload], args.cpu_baseline_s)
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

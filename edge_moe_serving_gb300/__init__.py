@@ -1,0 +1,192 @@
+"""Python binding of libmoe (include/moe.h): argument marshalling only.
+
+Every function has the C name and argument order.  Pointer arguments accept a
+torch tensor (its data pointer is passed), an int address, or None (NULL);
+``stream`` accepts a torch.cuda.Stream, an int handle or None (the current
+torch stream).  The structs mirror moe.h.  Nothing here computes any step of
+the layer: all of it runs in the library's CUDA kernels, and importing this
+package fails loudly when the library is missing.
+"""
+import ctypes
+import os
+
+from ctypes import c_int, c_int32, c_uint32, c_uint64, c_size_t, c_void_p, c_char_p, POINTER
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe.so")
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA = range(5)
+MOE_DEV_ERR_BAD_ID, MOE_DEV_ERR_UNBOUND, MOE_DEV_ERR_BAD_SLOT, MOE_DEV_ERR_TIMEOUT = 1, 2, 4, 8
+MOE_FILL_LOWEST_ID, MOE_FILL_RANDOM = 0, 1
+MOE_FFN_AUTO, MOE_FFN_GEMV, MOE_FFN_GEMM = 0, 1, 2
+MOE_STAGING_TAG = 1 << 30
+MOE_SLOT_MASK = (1 << 30) - 1
+
+
+class moe_pool(ctypes.Structure):
+    _fields_ = [("w_gate", c_void_p), ("w_up", c_void_p), ("w_down", c_void_p), ("n_slots", c_int32)]
+
+
+class moe_cache(ctypes.Structure):
+    _fields_ = [("cache", moe_pool), ("staging", moe_pool), ("slot_table", c_void_p), ("owner", c_void_p),
+                ("stamp", c_void_p), ("clock", c_void_p), ("n_layers", c_int32), ("E", c_int32),
+                ("H", c_int32), ("I", c_int32)]
+
+
+class moe_bind_stats(ctypes.Structure):
+    _fields_ = [("n_unique", c_int32), ("n_hit", c_int32), ("n_miss", c_int32), ("q", c_int32),
+                ("n_fill", c_int32), ("n_overflow", c_int32), ("n_staged", c_int32), ("clock", c_uint32)]
+
+
+class moe_layer(ctypes.Structure):
+    _fields_ = [("w_router", c_void_p), ("bias", c_void_p), ("layer", c_int32), ("E", c_int32),
+                ("k", c_int32), ("H", c_int32), ("I", c_int32)]
+
+
+class moe_layer_buffers(ctypes.Structure):
+    _fields_ = [("topk_ids", c_void_p), ("topk_w", c_void_p), ("counts", c_void_p), ("offsets", c_void_p),
+                ("perm", c_void_p), ("inv_perm", c_void_p), ("y_rows", c_void_p)]
+
+
+BIND_STATS_FIELDS = [f for f, _ in moe_bind_stats._fields_]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn, status):
+        super().__init__(f"{fn}: {moe_status_string(status)} (status {status})")
+        self.status = status
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libmoe.so is not built at {LIB_PATH}; run "
+                          "`python -m edge_moe_serving_gb300._build` (nvcc, sm_103a)")
+    lib = ctypes.CDLL(LIB_PATH)
+    P = c_void_p
+    sig = {
+        "moe_version": (c_int, []),
+        "moe_status_string": (c_char_p, [c_int]),
+        "moe_route_topk_workspace_size": (c_size_t, [c_int, c_int]),
+        "moe_route_topk": (c_int, [P, c_int, c_int, P, P, c_int, c_int, P, P, P, P, c_size_t, P, P]),
+        "moe_dispatch_workspace_size": (c_size_t, [c_int, c_int, c_int]),
+        "moe_dispatch": (c_int, [P, c_int, c_int, c_int, P, P, P, P, P, c_int, P, P, c_size_t, P, P]),
+        "moe_cache_bind_workspace_size": (c_size_t, [POINTER(moe_cache), c_int, c_int]),
+        "moe_cache_bind_slots": (c_int, [POINTER(moe_cache), c_int, P, c_int, c_int, c_uint32, c_int, c_int,
+                                         c_uint64, P, P, P, c_size_t, P, P]),
+        "moe_expert_ffn_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int, c_int]),
+        "moe_expert_ffn_grouped": (c_int, [POINTER(moe_cache), c_int, P, P, P, P, P, c_int, c_int, P, c_int,
+                                           P, P, c_size_t, P, P]),
+        "moe_combine": (c_int, [P, P, P, c_int, c_int, c_int, P, P, P, P]),
+        "moe_layer_workspace_size": (c_size_t, [POINTER(moe_layer), POINTER(moe_cache), c_int, c_int]),
+        "moe_layer_forward": (c_int, [POINTER(moe_layer), POINTER(moe_cache), P, c_int, P, c_uint32, c_int,
+                                      c_int, c_uint64, c_int, POINTER(moe_layer_buffers), P, c_size_t, P, P,
+                                      P]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = _load()
+EXPORTED = ["moe_version", "moe_status_string", "moe_route_topk_workspace_size", "moe_route_topk",
+            "moe_dispatch_workspace_size", "moe_dispatch", "moe_cache_bind_workspace_size",
+            "moe_cache_bind_slots", "moe_expert_ffn_workspace_size", "moe_expert_ffn_grouped", "moe_combine",
+            "moe_layer_workspace_size", "moe_layer_forward"]
+
+
+def lib():
+    return _lib
+
+
+def _p(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _s(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn, status):
+    if status != MOE_OK:
+        raise MoeError(fn, status)
+    return status
+
+
+def moe_version():
+    return _lib.moe_version()
+
+
+def moe_status_string(status):
+    return _lib.moe_status_string(status).decode()
+
+
+def moe_route_topk_workspace_size(T, E):
+    return _lib.moe_route_topk_workspace_size(T, E)
+
+
+def moe_route_topk(x, T, H, w_router, bias, E, k, topk_ids, topk_w, logits_opt, ws, ws_bytes, dev_status,
+                   stream=None):
+    return _check("moe_route_topk", _lib.moe_route_topk(
+        _p(x), T, H, _p(w_router), _p(bias), E, k, _p(topk_ids), _p(topk_w), _p(logits_opt), _p(ws), ws_bytes,
+        _p(dev_status), _s(stream)))
+
+
+def moe_dispatch_workspace_size(T, k, E):
+    return _lib.moe_dispatch_workspace_size(T, k, E)
+
+
+def moe_dispatch(topk_ids, T, k, E, counts, offsets, perm, inv_perm, x_opt, H, x_perm_opt, ws, ws_bytes,
+                 dev_status, stream=None):
+    return _check("moe_dispatch", _lib.moe_dispatch(
+        _p(topk_ids), T, k, E, _p(counts), _p(offsets), _p(perm), _p(inv_perm), _p(x_opt), H, _p(x_perm_opt),
+        _p(ws), ws_bytes, _p(dev_status), _s(stream)))
+
+
+def moe_cache_bind_workspace_size(cache, T, k):
+    return _lib.moe_cache_bind_workspace_size(ctypes.byref(cache), T, k)
+
+
+def moe_cache_bind_slots(cache, layer, topk_ids, T, k, phi_q16, min_fill, fill_policy, seed, stats_dev,
+                         fills_opt, ws, ws_bytes, dev_status, stream=None):
+    return _check("moe_cache_bind_slots", _lib.moe_cache_bind_slots(
+        ctypes.byref(cache), layer, _p(topk_ids), T, k, phi_q16, min_fill, fill_policy, seed, _p(stats_dev),
+        _p(fills_opt), _p(ws), ws_bytes, _p(dev_status), _s(stream)))
+
+
+def moe_expert_ffn_workspace_size(T, k, E, H, I, ffn_mode):
+    return _lib.moe_expert_ffn_workspace_size(T, k, E, H, I, ffn_mode)
+
+
+def moe_expert_ffn_grouped(cache, layer, counts, offsets, perm, x, x_perm_opt, T, k, expert_mask_opt,
+                           ffn_mode, y_rows, ws, ws_bytes, dev_status, stream=None):
+    return _check("moe_expert_ffn_grouped", _lib.moe_expert_ffn_grouped(
+        ctypes.byref(cache), layer, _p(counts), _p(offsets), _p(perm), _p(x), _p(x_perm_opt), T, k,
+        _p(expert_mask_opt), ffn_mode, _p(y_rows), _p(ws), ws_bytes, _p(dev_status), _s(stream)))
+
+
+def moe_combine(y_rows, inv_perm, topk_w, T, k, H, out, out_f32_opt, dev_status, stream=None):
+    return _check("moe_combine", _lib.moe_combine(
+        _p(y_rows), _p(inv_perm), _p(topk_w), T, k, H, _p(out), _p(out_f32_opt), _p(dev_status), _s(stream)))
+
+
+def moe_layer_workspace_size(layer, cache, T, ffn_mode):
+    return _lib.moe_layer_workspace_size(ctypes.byref(layer), ctypes.byref(cache), T, ffn_mode)
+
+
+def moe_layer_forward(layer, cache, x, T, out, phi_q16, min_fill, fill_policy, seed, ffn_mode, bufs_opt, ws,
+                      ws_bytes, dev_status, stats_dev, stream=None):
+    return _check("moe_layer_forward", _lib.moe_layer_forward(
+        ctypes.byref(layer), ctypes.byref(cache), _p(x), T, _p(out), phi_q16, min_fill, fill_policy, seed,
+        ffn_mode, ctypes.byref(bufs_opt) if bufs_opt is not None else None, _p(ws), ws_bytes, _p(dev_status),
+        _p(stats_dev), _s(stream)))

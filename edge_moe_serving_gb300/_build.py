@@ -1,0 +1,64 @@
+"""Build libmoe.so in-tree with nvcc for sm_103a (GB300).
+
+    python -m edge_moe_serving_gb300._build [--force] [--ptxas-verbose]
+"""
+import os
+import subprocess
+import sys
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+LIB = os.path.join(PKG, "libmoe.so")
+SOURCES = ["moe_api.cu", "route_topk.cu", "dispatch.cu", "bind.cu", "ffn.cu", "ffn_gemv.cu",
+           "combine.cu"]
+ARCH = "-gencode=arch=compute_103a,code=sm_103a"
+
+
+def cuda_home():
+    for cand in (os.environ.get("CUDA_HOME"), os.environ.get("CUDA_PATH"), "/usr/local/cuda"):
+        if cand and os.path.exists(os.path.join(cand, "bin", "nvcc")):
+            return cand
+    raise RuntimeError("nvcc not found (set CUDA_HOME)")
+
+
+def _inputs():
+    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
+    files.append(os.path.join(INCLUDE, "moe.h"))
+    files.append(os.path.abspath(__file__))
+    return files
+
+
+def up_to_date():
+    if not os.path.exists(LIB):
+        return False
+    t = os.path.getmtime(LIB)
+    return all(os.path.getmtime(f) <= t for f in _inputs())
+
+
+def build(force=False, ptxas_verbose=False, quiet=True):
+    """Compile every CUDA source into libmoe.so (one nvcc call, parallel TUs)."""
+    if not force and up_to_date():
+        return LIB
+    home = cuda_home()
+    tmp = LIB + f".tmp{os.getpid()}"
+    cmd = [os.path.join(home, "bin", "nvcc"), "-shared", "-Xcompiler", "-fPIC,-O2", "-std=c++17", "-O3",
+           "-lineinfo", ARCH, "--threads", "0", "-cudart", "shared", "-I", INCLUDE, "-I", CSRC,
+           "-Xlinker", "-rpath," + os.path.join(home, "lib64")]
+    if ptxas_verbose:
+        cmd += ["-Xptxas", "-v"]
+    cmd += [os.path.join(CSRC, s) for s in SOURCES] + ["-o", tmp]
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    if res.returncode != 0:
+        sys.stderr.write(res.stdout + res.stderr)
+        raise RuntimeError("nvcc failed building libmoe.so")
+    if not quiet or ptxas_verbose:
+        sys.stderr.write(res.stdout + res.stderr)
+    os.replace(tmp, LIB)
+    return LIB
+
+
+if __name__ == "__main__":
+    build(force="--force" in sys.argv, ptxas_verbose="--ptxas-verbose" in sys.argv, quiet=False)
+    print(LIB)

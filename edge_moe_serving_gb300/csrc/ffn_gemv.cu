@@ -1,0 +1,257 @@
+// Weight-streaming grouped GEMV for decode-sized expert groups (FreeToken
+// paper, section 3.2: grouped evaluation of the GPU execution set; section 3:
+// experts are reached through their (layer, expert) slot).
+//
+// Decode reads every routed expert's weights once per step, so these kernels
+// are HBM-bound: each CTA streams a contiguous range of weight rows with
+// 16-byte non-allocating loads, and every thread of the CTA works on every
+// row (a row is split across the CTA, not across warps), so all SMs keep the
+// same number of bytes in flight until the end and the grid is balanced to
+// within one row group.
+//
+//  gateup_kernel  h[pos, i]  = bf16( silu(W_gate[i,:] . x_t) * (W_up[i,:] . x_t) )
+//  down_kernel    y[pos, o]  = W_down[o,:] . h[pos,:]            (fp32)
+//
+// Work list: an "instance" is (expert e, chunk c of up to NT of its rows); an
+// instance has I (gate/up) or H (down) tasks, one per output neuron, and
+// consecutive tasks read consecutive weight rows.  CTA b owns tasks
+// [b*per, (b+1)*per) of the flattened list and processes them NG at a time.
+// Partial dot products are reduced with a warp reduce-scatter plus a fixed
+// order sum over warps, so results do not depend on the grid.
+#include "ffn_params.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kMaxThreads = 256;
+
+// Warp reduce-scatter of N (power of two >= 32) values: afterwards lane l
+// holds the warp totals of values [l*N/32, (l+1)*N/32) in v[0 .. N/32).
+template <int N>
+__device__ inline void warp_reduce_scatter(float (&v)[N]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 16, n = N; o > 0; o >>= 1, n >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int j = 0; j < n / 2; ++j) {
+      const float keep = upper ? v[j + n / 2] : v[j];
+      const float send = upper ? v[j] : v[j + n / 2];
+      v[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+}
+
+// Instances per expert (prefix over experts of ceil(rows / NT), eligible only).
+template <int NT>
+__device__ void build_prefix(const GemvParams& p, int* s_pref, int* s_warp) {
+  const int tid = threadIdx.x, nthreads = blockDim.x;
+  const int per_thread = (p.E + nthreads - 1) / nthreads;
+  const int e0 = tid * per_thread;
+  int local[kMaxE / 32];
+  int sum = 0;
+  for (int u = 0; u < per_thread; ++u) {
+    const int e = e0 + u;
+    int n = 0;
+    if (e < p.E) {
+      const int cnt = p.counts[e];
+      const bool ok = cnt > 0 && cnt <= p.max_rows && (p.mask == nullptr || p.mask[e] != 0);
+      n = ok ? (cnt + NT - 1) / NT : 0;
+    }
+    local[u] = n;
+    sum += n;
+  }
+  // exclusive scan of per-thread sums
+  const int lane = tid & 31, warp = tid >> 5;
+  int inc = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += n;
+  }
+  if (lane == 31) s_warp[warp] = inc;
+  __syncthreads();
+  if (tid == 0) {
+    int run = 0;
+    for (int w = 0; w < nthreads / 32; ++w) {
+      const int t = s_warp[w];
+      s_warp[w] = run;
+      run += t;
+    }
+    s_pref[p.E] = run;
+  }
+  __syncthreads();
+  int run = s_warp[warp] + inc - sum;
+  for (int u = 0; u < per_thread; ++u) {
+    const int e = e0 + u;
+    if (e < p.E) s_pref[e] = run;
+    run += local[u];
+  }
+  __syncthreads();
+}
+
+// largest e with s_pref[e] <= j < s_pref[e + 1]
+__device__ inline int find_expert(const int* s_pref, int E, int j) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_pref[mid] <= j) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+template <int NT, int NG, bool GATEUP>
+__global__ void __launch_bounds__(kMaxThreads)
+gemv_kernel(GemvParams p) {
+  constexpr int NR = GATEUP ? 2 : 1;
+  constexpr int NV = NG * NR * NT;
+  constexpr int NVP = NV < 32 ? 32 : NV;
+  constexpr int PER_LANE = NVP / 32;
+  __shared__ int s_pref[kMaxE + 1];
+  __shared__ int s_warp[kMaxThreads / 32];
+  __shared__ float red[2][kMaxThreads / 32][NVP];
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nthreads = blockDim.x, nwarps = nthreads >> 5;
+  const int K = GATEUP ? p.H : p.I;        // weight row length
+  const int NTASK = GATEUP ? p.I : p.H;    // output neurons per instance
+  const int KV = K >> 3;                   // 16-byte vectors per row
+  const int sweeps = (KV + nthreads - 1) / nthreads;
+
+  build_prefix<NT>(p, s_pref, s_warp);
+  const long long total = (long long)s_pref[p.E] * NTASK;
+  const long long per = (total + gridDim.x - 1) / gridDim.x;
+  const long long begin = (long long)blockIdx.x * per;
+  const long long end = begin + per < total ? begin + per : total;
+
+  int buf = 0;
+  for (long long tau = begin; tau < end;) {
+    const int j = (int)(tau / NTASK);
+    const int n0 = (int)(tau % NTASK);
+    int gsize = NTASK - n0;
+    if (gsize > NG) gsize = NG;
+    if (end - tau < gsize) gsize = (int)(end - tau);
+    const int e = find_expert(s_pref, p.E, j);
+    const int c = j - s_pref[e];
+    const int cnt = p.counts[e];
+    const int pos0 = p.offsets[e] + c * NT;
+    const int ntok = min(NT, cnt - c * NT);
+    BankSet bs;
+    const int32_t entry = p.c.slot_table[p.layer * p.E + e];
+    if (!resolve_slot(p.c, entry, p.H, p.I, &bs, tid == 0 ? p.status : nullptr)) {
+      tau += gsize;
+      continue;
+    }
+    const __nv_bfloat16* wrow0;
+    const __nv_bfloat16* wrow1;
+    if (GATEUP) {
+      wrow0 = bs.gate + (size_t)n0 * K;
+      wrow1 = bs.up + (size_t)n0 * K;
+    } else {
+      wrow0 = bs.down + (size_t)n0 * K;
+      wrow1 = wrow0;
+    }
+    const __nv_bfloat16* act[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const int pos = pos0 + (t < ntok ? t : 0);
+      if (GATEUP) {
+        act[t] = p.x_perm ? p.x_perm + (size_t)pos * p.H : p.x + (size_t)(p.perm[pos] / p.k) * p.H;
+      } else {
+        act[t] = p.h + (size_t)pos * p.I;
+      }
+    }
+
+    float acc[NVP];
+#pragma unroll
+    for (int q = 0; q < NVP; ++q) acc[q] = 0.0f;
+    for (int s = 0; s < sweeps; ++s) {
+      const int v = s * nthreads + tid;
+      if (v < KV) {
+        uint4 w[NG][NR];
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+          if (g < gsize) {
+            w[g][0] = ldg_stream(wrow0 + (size_t)g * K + (size_t)v * 8);
+            if (NR == 2) w[g][NR - 1] = ldg_stream(wrow1 + (size_t)g * K + (size_t)v * 8);
+          } else {
+            w[g][0] = make_uint4(0, 0, 0, 0);
+            w[g][NR - 1] = make_uint4(0, 0, 0, 0);
+          }
+        }
+        uint4 a[NT];
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+          a[t] = (t < ntok) ? ldg_cached(act[t] + (size_t)v * 8) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int g = 0; g < NG; ++g)
+#pragma unroll
+          for (int r = 0; r < NR; ++r)
+#pragma unroll
+            for (int t = 0; t < NT; ++t)
+              acc[(g * NR + r) * NT + t] = dot8(w[g][r], a[t], acc[(g * NR + r) * NT + t]);
+      }
+    }
+    warp_reduce_scatter<NVP>(acc);
+#pragma unroll
+    for (int u = 0; u < PER_LANE; ++u) red[buf][warp][lane * PER_LANE + u] = acc[u];
+    __syncthreads();
+    for (int qi = tid; qi < NG * NT; qi += nthreads) {
+      const int g = qi / NT, t = qi % NT;
+      if (g < gsize && t < ntok) {
+        if (GATEUP) {
+          float gs = 0.0f, us = 0.0f;
+          for (int w = 0; w < nwarps; ++w) {
+            gs += red[buf][w][(g * 2 + 0) * NT + t];
+            us += red[buf][w][(g * 2 + 1) * NT + t];
+          }
+          p.h[(size_t)(pos0 + t) * p.I + n0 + g] = __float2bfloat16_rn(silu(gs) * us);
+        } else {
+          float ys = 0.0f;
+          for (int w = 0; w < nwarps; ++w) ys += red[buf][w][g * NT + t];
+          p.y[(size_t)(pos0 + t) * p.H + n0 + g] = ys;
+        }
+      }
+    }
+    buf ^= 1;
+    tau += gsize;
+  }
+}
+
+template <typename Kern>
+int grid_for(Kern kern, int threads) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, 0) != cudaSuccess || per_sm < 1)
+    per_sm = 1;
+  return per_sm * num_sms();
+}
+
+template <int NT>
+cudaError_t launch_gemv_nt(const GemvParams& p, cudaStream_t s) {
+  constexpr int NG_UP = 4, NG_DOWN = 8;
+  const int thr_up = std::min(kMaxThreads, (int)align_up((size_t)(p.H / 8), 32));
+  const int thr_dn = std::min(kMaxThreads, (int)align_up((size_t)(p.I / 8), 32));
+  static int grid_up[kMaxThreads / 32 + 1] = {0};
+  static int grid_dn[kMaxThreads / 32 + 1] = {0};
+  if (!grid_up[thr_up / 32]) grid_up[thr_up / 32] = grid_for(gemv_kernel<NT, NG_UP, true>, thr_up);
+  if (!grid_dn[thr_dn / 32]) grid_dn[thr_dn / 32] = grid_for(gemv_kernel<NT, NG_DOWN, false>, thr_dn);
+  gemv_kernel<NT, NG_UP, true><<<grid_up[thr_up / 32], thr_up, 0, s>>>(p);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  gemv_kernel<NT, NG_DOWN, false><<<grid_dn[thr_dn / 32], thr_dn, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// Rows per pass: bounded by the tokens of the call (a group never exceeds T).
+cudaError_t launch_gemv(const GemvParams& p, cudaStream_t s) {
+  const int bound = std::min(p.T, p.max_rows);
+  if (bound <= 1) return launch_gemv_nt<1>(p, s);
+  if (bound <= 2) return launch_gemv_nt<2>(p, s);
+  if (bound <= 4) return launch_gemv_nt<4>(p, s);
+  return launch_gemv_nt<8>(p, s);
+}
+
+}  // namespace moe

@@ -1,0 +1,25 @@
+// Parameters of the weight-streaming expert GEMV kernels.
+#pragma once
+
+#include "moe_common.cuh"
+
+namespace moe {
+
+struct GemvParams {
+  moe_cache c;
+  int layer, E, H, I, k, T;
+  const int32_t* counts;
+  const int32_t* offsets;
+  const int32_t* perm;
+  const __nv_bfloat16* x;
+  const __nv_bfloat16* x_perm;
+  const uint8_t* mask;
+  int max_rows;       // experts with more rows are left to the GEMM kernel
+  __nv_bfloat16* h;   // [R, I]
+  float* y;           // [R, H]
+  uint32_t* status;
+};
+
+cudaError_t launch_gemv(const GemvParams& p, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,123 @@
+// Shared device helpers and internal launch declarations of libmoe.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+constexpr int kNumSMs = 152;          // GB300: 2 dies x 76 SMs (queried at run time too)
+constexpr int kMaxE = 1024;           // bind / dispatch limit
+constexpr int kMaxRouteE = 512;       // router top-k limit (16 logits per lane)
+constexpr int kMaxK = 16;
+constexpr int kMaxCacheSlots = 16384; // bind kernel keeps all (stamp, slot) keys in shared memory
+constexpr int kGemvMaxRows = 8;       // AUTO mode: groups up to this size use the GEMV path
+
+__host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// ---------------------------------------------------------------- device status
+__device__ inline void set_status(uint32_t* status, uint32_t bit) {
+  if (status) atomicOr(status, bit);
+}
+
+// ---------------------------------------------------------------- bf16 helpers
+// bf16 -> fp32 is exact: the bf16 bits are the high half of the fp32 bits.
+__device__ inline float bf16_lo(uint32_t packed) { return __uint_as_float(packed << 16); }
+__device__ inline float bf16_hi(uint32_t packed) { return __uint_as_float(packed & 0xFFFF0000u); }
+
+__device__ inline uint4 ldg_stream(const void* p) {
+  // 16-byte load that does not allocate in L1: weights are read once.
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ inline uint4 ldg_cached(const void* p) {
+  return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+// Dot product of 8 bf16 weights with 8 bf16 activations, accumulated in fp32.
+__device__ inline float dot8(const uint4& w, const uint4& a, float acc) {
+  acc = fmaf(bf16_lo(w.x), bf16_lo(a.x), acc);
+  acc = fmaf(bf16_hi(w.x), bf16_hi(a.x), acc);
+  acc = fmaf(bf16_lo(w.y), bf16_lo(a.y), acc);
+  acc = fmaf(bf16_hi(w.y), bf16_hi(a.y), acc);
+  acc = fmaf(bf16_lo(w.z), bf16_lo(a.z), acc);
+  acc = fmaf(bf16_hi(w.z), bf16_hi(a.z), acc);
+  acc = fmaf(bf16_lo(w.w), bf16_lo(a.w), acc);
+  acc = fmaf(bf16_hi(w.w), bf16_hi(a.w), acc);
+  return acc;
+}
+
+__device__ inline float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ inline float silu(float g) { return g / (1.0f + expf(-g)); }
+
+// Slot-table decoding: returns the bank base row pointer set for (pool, slot),
+// or false when the entry is unbound or out of range.
+struct BankSet {
+  const __nv_bfloat16* gate;
+  const __nv_bfloat16* up;
+  const __nv_bfloat16* down;
+};
+
+__device__ inline bool resolve_slot(const moe_cache& c, int32_t entry, int H, int I, BankSet* out,
+                                    uint32_t* status) {
+  if (entry < 0) {
+    set_status(status, MOE_DEV_ERR_UNBOUND);
+    return false;
+  }
+  const moe_pool* pool = (entry & MOE_STAGING_TAG) ? &c.staging : &c.cache;
+  const int32_t slot = entry & MOE_SLOT_MASK;
+  if ((entry & ~(MOE_STAGING_TAG | MOE_SLOT_MASK)) != 0 || slot >= pool->n_slots) {
+    set_status(status, MOE_DEV_ERR_BAD_SLOT);
+    return false;
+  }
+  const size_t per = (size_t)H * (size_t)I;
+  out->gate = reinterpret_cast<const __nv_bfloat16*>(pool->w_gate) + (size_t)slot * per;
+  out->up = reinterpret_cast<const __nv_bfloat16*>(pool->w_up) + (size_t)slot * per;
+  out->down = reinterpret_cast<const __nv_bfloat16*>(pool->w_down) + (size_t)slot * per;
+  return true;
+}
+
+// ---------------------------------------------------------------- internal launchers
+int num_sms();
+
+cudaError_t launch_route_topk(const __nv_bfloat16* x, int T, int H, const float* w_router,
+                              const float* bias, int E, int k, int32_t* topk_ids, float* topk_w,
+                              float* logits_opt, void* ws, uint32_t* status, cudaStream_t s);
+size_t route_ws_bytes(int T, int E);
+
+size_t dispatch_ws_bytes(int T, int k, int E);
+cudaError_t launch_dispatch(const int32_t* ids, int R, int k, int E, int32_t* counts,
+                            int32_t* offsets, int32_t* perm, int32_t* inv_perm,
+                            const __nv_bfloat16* x, int H, __nv_bfloat16* x_perm, void* ws,
+                            uint32_t* status, cudaStream_t s);
+
+size_t bind_ws_bytes(int T, int k, int E);
+size_t bind_smem_bytes(int n_slots, int E);
+cudaError_t launch_bind(const moe_cache& c, int layer, const int32_t* ids, int R,
+                        uint32_t phi_q16, int min_fill, int policy, uint64_t seed,
+                        moe_bind_stats* stats, int32_t* fills_opt, void* ws, uint32_t* status,
+                        cudaStream_t s);
+
+size_t ffn_ws_bytes(int T, int k, int E, int H, int I, int mode);
+cudaError_t launch_ffn(const moe_cache& c, int layer, const int32_t* counts, const int32_t* offsets,
+                       const int32_t* perm, const __nv_bfloat16* x, const __nv_bfloat16* x_perm,
+                       int T, int k, const uint8_t* mask, int mode, float* y_rows, void* ws,
+                       uint32_t* status, cudaStream_t s);
+
+cudaError_t launch_combine(const float* y_rows, const int32_t* inv_perm, const float* topk_w, int T,
+                           int k, int H, __nv_bfloat16* out, float* out_f32, uint32_t* status,
+                           cudaStream_t s);
+
+}  // namespace moe

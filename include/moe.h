@@ -1,0 +1,245 @@
+/*
+ * moe.h — C ABI of libmoe: one routed Mixture-of-Experts layer's forward pass
+ * on an NVIDIA GB300 (sm_103a), with an expert cache addressed through a
+ * (layer, expert) -> slot table.
+ *
+ * Source of the method: "FreeToken: Efficient Edge-Native MoE Serving with
+ * Bandwidth-Adaptive Execution" (arXiv 2608.16157), cited below as [P], and
+ * the write-up "FreeToken: bandwidth-adaptive edge MoE serving", cited as [W].
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Pointers.   Every tensor pointer is a DEVICE pointer unless stated, owned by
+ *             the caller; the library never allocates, frees or keeps a
+ *             pointer after the call returns.  Structs (moe_cache, moe_layer,
+ *             moe_layer_buffers) are HOST structs holding device pointers;
+ *             they are read during the call only.
+ * Layout.     Row-major, densely packed.  x, out: bf16 [T, H].  Expert banks:
+ *             W_gate, W_up bf16 [n_slots, I, H]; W_down bf16 [n_slots, H, I]
+ *             (nn.Linear out x in); the leading dimension is the slot, as in
+ *             [P] section 4.2 (banks share one expert -> slot mapping).  Router
+ *             weights fp32 [E, H], bias fp32 [E].  ids / indices int32.
+ *             Every device pointer must be 16-byte aligned; H and I must be
+ *             multiples of 8.
+ * Async.      Every call only enqueues work on `stream` (a cudaStream_t) and
+ *             returns; no call synchronises with the host, so a sequence of
+ *             calls may be captured into a CUDA graph.
+ * Errors.     The return value is a host status (MOE_OK or MOE_ERR_*), from
+ *             argument checks before any launch or from the launch itself.
+ *             Errors found on the device (bad expert id, unbound slot, a
+ *             bounded wait that ran out) are OR-ed into *dev_status (device
+ *             uint32, caller-zeroed) as MOE_DEV_ERR_* bits; the kernel skips
+ *             the offending work and returns, it never traps.
+ * Workspace.  Calls that need scratch take (ws, ws_bytes): a device buffer of
+ *             at least the size the matching *_workspace_size() reports,
+ *             256-byte aligned, with no content requirement.  A call that
+ *             gets a smaller ws returns MOE_ERR_WORKSPACE without launching.
+ *             Calls sharing one ws must not overlap on the GPU.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* same type as cudaStream_t; NULL = legacy default stream */
+
+/* host status codes */
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG 1  /* null pointer, negative size, k > E, layer out of range ... */
+#define MOE_ERR_UNSUPPORTED 2  /* shape or alignment outside what the kernels handle */
+#define MOE_ERR_WORKSPACE 3    /* ws_bytes below the reported workspace size */
+#define MOE_ERR_CUDA 4         /* a CUDA launch or API call failed */
+
+/* device status bits (OR-ed into *dev_status) */
+#define MOE_DEV_ERR_BAD_ID 1u     /* a routed expert id outside [0, E) was skipped */
+#define MOE_DEV_ERR_UNBOUND 2u    /* an expert's slot-table entry was -1; its rows were not written */
+#define MOE_DEV_ERR_BAD_SLOT 4u   /* a slot-table entry pointed outside its pool; treated as unbound */
+#define MOE_DEV_ERR_TIMEOUT 8u    /* a bounded wait in a pipelined kernel ran out; its tile was abandoned */
+
+/* fill policy of moe_cache_bind_slots: which q misses form the fill set F */
+#define MOE_FILL_LOWEST_ID 0  /* the q misses with the lowest expert ids */
+#define MOE_FILL_RANDOM 1     /* a seeded uniformly random q-subset (SplitMix64 keys) */
+
+/* expert-FFN kernel selection */
+#define MOE_FFN_AUTO 0  /* weight-streaming GEMV for groups of <= 8 rows, tensor-core GEMM above */
+#define MOE_FFN_GEMV 1  /* weight-streaming GEMV for every group */
+#define MOE_FFN_GEMM 2  /* tcgen05 grouped GEMM for every non-empty group */
+
+/* slot-table entry encoding: -1 unbound; s (0 <= s < cache.n_slots) = cache pool slot s;
+ * MOE_STAGING_TAG | p = staging pool slot p, where p = layer * E + expert. */
+#define MOE_STAGING_TAG (1 << 30)
+#define MOE_SLOT_MASK ((1 << 30) - 1)
+
+/* One pool of expert banks (bf16, see Layout above). */
+typedef struct moe_pool {
+  void* w_gate;   /* [n_slots, I, H] */
+  void* w_up;     /* [n_slots, I, H] */
+  void* w_down;   /* [n_slots, H, I] */
+  int32_t n_slots;
+} moe_pool;
+
+/* The expert cache of [P] section 3: one elastic slot pool shared by every
+ * MoE layer (pool A, `cache`), plus the staging pool (pool B, `staging`) that
+ * holds every (layer, expert) pair at slot layer*E + expert and stands in for
+ * the host-resident source-of-truth pool of [P] section 3.  A staging pool with
+ * fewer than n_layers*E slots is allowed only if no call ever needs it.
+ * Residency state (device arrays, read and written by moe_cache_bind_slots):
+ *   slot_table [n_layers*E] int32  entry per (layer, expert), encoding above
+ *   owner      [cache.n_slots] int32  layer*E+expert held by a slot, or -1
+ *   stamp      [cache.n_slots] uint32 clock value of the slot's last use (0 = never)
+ *   clock      [1] uint32           one LRU clock for all layers, +1 per bind call */
+typedef struct moe_cache {
+  moe_pool cache;
+  moe_pool staging;
+  int32_t* slot_table;
+  int32_t* owner;
+  uint32_t* stamp;
+  uint32_t* clock;
+  int32_t n_layers;
+  int32_t E;
+  int32_t H;
+  int32_t I;
+} moe_cache;
+
+/* Per-call counters written by moe_cache_bind_slots (device struct). */
+typedef struct moe_bind_stats {
+  int32_t n_unique;    /* distinct routed experts of the call */
+  int32_t n_hit;       /* |H|: resident in the cache pool */
+  int32_t n_miss;      /* m = |M| */
+  int32_t q;           /* fetch count from the q* rule */
+  int32_t n_fill;      /* fills performed (q minus overflow) */
+  int32_t n_overflow;  /* fills that found no victim and stayed in C */
+  int32_t n_staged;    /* |C|: misses served from the staging pool */
+  uint32_t clock;      /* stamp of this call */
+} moe_bind_stats;
+
+/* Router and shape of one MoE layer. */
+typedef struct moe_layer {
+  const float* w_router;  /* fp32 [E, H] */
+  const float* bias;      /* fp32 [E] added to the logits, or NULL */
+  int32_t layer;          /* layer index into the slot table */
+  int32_t E;
+  int32_t k;
+  int32_t H;
+  int32_t I;
+} moe_layer;
+
+/* Optional caller-owned destinations for the intermediates of
+ * moe_layer_forward; a NULL field is placed in the workspace instead. */
+typedef struct moe_layer_buffers {
+  int32_t* topk_ids;  /* [T, k] */
+  float* topk_w;      /* [T, k] */
+  int32_t* counts;    /* [E] */
+  int32_t* offsets;   /* [E + 1] */
+  int32_t* perm;      /* [T*k] */
+  int32_t* inv_perm;  /* [T*k] */
+  float* y_rows;      /* [T*k, H] */
+} moe_layer_buffers;
+
+int moe_version(void);
+const char* moe_status_string(int status);
+
+/* ---------------------------------------------------------------- router
+ * Router scoring and top-k with renormalisation ([P] section 3.2: at each
+ * MoE layer the router runs on the GPU and selects the active experts).
+ *   logits[t, e] = sum_h x[t, h] * w_router[e, h] + bias[e]   (fp32 accumulation)
+ *   topk_ids[t, :] = the k largest logits' ids (ties to the lower id), ascending
+ *   topk_w[t, j]  = exp(l_j - max_sel) / sum_sel exp(l - max_sel)
+ *                   (softmax over all E, renormalised over the k selected)
+ * x bf16 [T, H]; logits_opt fp32 [T, E] or NULL.  1 <= k <= 16, k <= E <= 512.
+ * T = 0 is a no-op. */
+size_t moe_route_topk_workspace_size(int T, int E);
+int moe_route_topk(const void* x, int T, int H, const float* w_router, const float* bias, int E,
+                   int k, int32_t* topk_ids, float* topk_w, float* logits_opt, void* ws,
+                   size_t ws_bytes, uint32_t* dev_status, moe_stream_t stream);
+
+/* ---------------------------------------------------------------- dispatch
+ * Token -> expert grouping for the grouped evaluation of [P] section 3.2.
+ * Stable counting sort of the flat routed rows i = t*k + j by expert id:
+ *   counts[e] = #{i : topk_ids[i] == e};  offsets[0] = 0, offsets[e+1] = offsets[e] + counts[e]
+ *   perm[pos] = i, inv_perm[i] = pos, with rows of one expert in increasing i.
+ * x_opt / x_perm_opt: if both non-NULL, x_perm[pos, :] = x[perm[pos] / k, :]
+ * (bf16, [T*k, H]).  Ids outside [0, E) set MOE_DEV_ERR_BAD_ID and are
+ * counted nowhere; their perm/inv_perm entries are left unwritten. */
+size_t moe_dispatch_workspace_size(int T, int k, int E);
+int moe_dispatch(const int32_t* topk_ids, int T, int k, int E, int32_t* counts, int32_t* offsets,
+                 int32_t* perm, int32_t* inv_perm, const void* x_opt, int H, void* x_perm_opt,
+                 void* ws, size_t ws_bytes, uint32_t* dev_status, moe_stream_t stream);
+
+/* ---------------------------------------------------------------- residency
+ * Device-side cache control of [P] section 4.1 for one MoE layer, followed by
+ * the fused batched fill copy.  One kernel: deduplicate the routed experts,
+ * classify them against the slot table into hits H and misses M (m = |M|),
+ * derive q = fill count of m at fetch fraction phi_q16 = B_P/B_H in Q16
+ * ([P] section 3.2, Eq. 1-4; integer rule of [W] "The split, and what it is
+ * actually optimising"; if min_fill != 0 and phi_q16 > 0 and m > 0 then
+ * q >= 1, the "at least one fill" floor of [P] section 3.2), choose F
+ * (fill_policy), find the q least-recently-used slots not hit by this call
+ * in one pass (victims, ordered by (stamp, slot)), rebind evicted pairs to
+ * the staging pool, admit F into the victims (F in ascending id order paired
+ * with victims in order), and bind the other misses C to the staging pool.
+ * Hits and fills take stamp = ++clock.  Then one fixed-shape copy launch,
+ * masked by the device fill count, copies every filled expert's three bank
+ * rows from the staging pool to its cache slot.
+ * fills_opt: int32 [min(T*k, E), 2] (src staging slot, dst cache slot) rows
+ * 0..n_fill-1, or NULL.  stats_dev: moe_bind_stats, or NULL.
+ * Limits: E <= 1024, cache.n_slots <= 16384. */
+size_t moe_cache_bind_workspace_size(const moe_cache* cache, int T, int k);
+int moe_cache_bind_slots(const moe_cache* cache, int layer, const int32_t* topk_ids, int T, int k,
+                         uint32_t phi_q16, int min_fill, int fill_policy, uint64_t seed,
+                         moe_bind_stats* stats_dev, int32_t* fills_opt, void* ws, size_t ws_bytes,
+                         uint32_t* dev_status, moe_stream_t stream);
+
+/* ---------------------------------------------------------------- expert FFN
+ * Grouped SwiGLU expert FFN over the combined execution set of [P] section
+ * 3.2, reading every expert's weights through the slot table ([P] section 3:
+ * lookup and execution on logical (layer, expert) ids).  For each expert e
+ * with counts[e] > 0 (and expert_mask_opt[e] != 0 if a mask is given), with
+ * rows pos in [offsets[e], offsets[e+1]) and x row t = perm[pos] / k:
+ *   g = x_t W_gate^T, u = x_t W_up^T (fp32 accumulation), h = bf16(silu(g) * u),
+ *   y_rows[pos, :] = h W_down^T (fp32 accumulation, stored fp32)
+ * where the banks are those of pool slot_table[layer*E + e].  x bf16 [T, H];
+ * x_perm_opt: bf16 [T*k, H] gathered rows (from moe_dispatch), required by
+ * the GEMM kernel and used by the GEMV kernel if given.  Rows of experts
+ * outside the mask are not written.  An unbound entry sets
+ * MOE_DEV_ERR_UNBOUND and leaves that expert's rows unwritten. */
+size_t moe_expert_ffn_workspace_size(int T, int k, int E, int H, int I, int ffn_mode);
+int moe_expert_ffn_grouped(const moe_cache* cache, int layer, const int32_t* counts,
+                           const int32_t* offsets, const int32_t* perm, const void* x,
+                           const void* x_perm_opt, int T, int k, const uint8_t* expert_mask_opt,
+                           int ffn_mode, float* y_rows, void* ws, size_t ws_bytes,
+                           uint32_t* dev_status, moe_stream_t stream);
+
+/* ---------------------------------------------------------------- combine
+ * Gate-weighted merge of the expert outputs ([P] section 3.2: the partial
+ * sums of the GPU set and the in-place set merge into the exact layer
+ * output).  out[t, :] = sum_{j=0}^{k-1} topk_w[t, j] * y_rows[inv_perm[t*k+j], :]
+ * summed in j order (ascending expert id) with fp32 FMAs, then rounded to
+ * bf16 (out) and/or stored fp32 (out_f32_opt).  The result does not depend
+ * on which pool any row's expert was read from.  out or out_f32_opt may be
+ * NULL, not both. */
+int moe_combine(const float* y_rows, const int32_t* inv_perm, const float* topk_w, int T, int k,
+                int H, void* out, float* out_f32_opt, uint32_t* dev_status, moe_stream_t stream);
+
+/* ---------------------------------------------------------------- whole layer
+ * moe_route_topk -> moe_cache_bind_slots -> moe_dispatch ->
+ * moe_expert_ffn_grouped -> moe_combine on one stream ([P] section 3.2 decode
+ * order: cache update, batch copy of F, grouped evaluation, merge).
+ * out bf16 [T, H].  bufs_opt may name caller buffers for intermediates.
+ * stats_dev: moe_bind_stats or NULL. */
+size_t moe_layer_workspace_size(const moe_layer* layer, const moe_cache* cache, int T,
+                                int ffn_mode);
+int moe_layer_forward(const moe_layer* layer, const moe_cache* cache, const void* x, int T,
+                      void* out, uint32_t phi_q16, int min_fill, int fill_policy, uint64_t seed,
+                      int ffn_mode, const moe_layer_buffers* bufs_opt, void* ws, size_t ws_bytes,
+                      uint32_t* dev_status, moe_bind_stats* stats_dev, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H_ */

@@ -1,0 +1,113 @@
+"""Upload the seeded inputs of ``moe_inputs.gen`` into CUDA tensors (torch).
+
+Plain copies only: expert banks are filled by slicing the uploaded pools at
+the generator's offsets, the cache pool by copying staging slots, and the
+residency state is uploaded as is.  No step of the layer is computed here.
+"""
+import numpy as np
+import torch
+
+import edge_moe_serving_gb300 as moe
+
+from . import gen
+from .configs import LayerConfig
+
+
+def to_dev_bf16(bits: np.ndarray, device) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
+
+
+def to_dev(a: np.ndarray, device) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+class DeviceCache:
+    """Cache pool (A), staging pool (B) and residency state on one device."""
+
+    def __init__(self, cfg: LayerConfig, device="cuda", staging_layers=None):
+        self.cfg = cfg
+        self.device = device
+        L, E, H, I = cfg.n_layers, cfg.E, cfg.H, cfg.I
+        LE = L * E
+        self.staging = [torch.empty((LE,) + gen.bank_shape(cfg, b), dtype=torch.bfloat16, device=device)
+                        for b in range(3)]
+        n = I * H
+        for layer in range(L):
+            for b in range(3):
+                pool = to_dev_bf16(gen.bank_pool(cfg, layer, b), device)
+                offs = gen.bank_offsets(cfg, layer, b)
+                dst = self.staging[b]
+                for e in range(E):
+                    o = int(offs[e])
+                    dst[layer * E + e].copy_(pool[o:o + n].view(gen.bank_shape(cfg, b)))
+                del pool
+        st = gen.initial_cache(cfg)
+        self.identity = cfg.cache_slots is None
+        if self.identity:
+            self.cache = self.staging
+        else:
+            owner = torch.from_numpy(st["owner"].astype(np.int64)).to(device)
+            self.cache = [self.staging[b].index_select(0, owner) for b in range(3)]
+        self.table = to_dev(st["table"].astype(np.int32), device)
+        self.owner = to_dev(st["owner"].astype(np.int32), device)
+        self.stamp = to_dev(st["stamp"].astype(np.uint32).view(np.int32), device)
+        self.clock = torch.zeros(1, dtype=torch.int32, device=device)
+        self.initial = st
+        self.struct = self._make_struct()
+
+    def n_cache_slots(self):
+        return self.cache[0].shape[0]
+
+    def _make_struct(self):
+        c = moe.moe_cache()
+        c.cache = moe.moe_pool(self.cache[0].data_ptr(), self.cache[1].data_ptr(), self.cache[2].data_ptr(),
+                               self.n_cache_slots())
+        c.staging = moe.moe_pool(self.staging[0].data_ptr(), self.staging[1].data_ptr(),
+                                 self.staging[2].data_ptr(), self.staging[0].shape[0])
+        c.slot_table = self.table.data_ptr()
+        c.owner = self.owner.data_ptr()
+        c.stamp = self.stamp.data_ptr()
+        c.clock = self.clock.data_ptr()
+        c.n_layers, c.E, c.H, c.I = self.cfg.n_layers, self.cfg.E, self.cfg.H, self.cfg.I
+        return c
+
+    def state(self):
+        """Residency state as numpy, in the oracle's format."""
+        return {"table": self.table.cpu().numpy().astype(np.int64),
+                "owner": self.owner.cpu().numpy().astype(np.int64),
+                "stamp": self.stamp.cpu().numpy().view(np.uint32).astype(np.int64),
+                "clock": int(self.clock.cpu().numpy().view(np.uint32)[0])}
+
+    def reset(self):
+        """Restore the initial residency state and the cache pool contents."""
+        st = self.initial
+        self.table.copy_(to_dev(st["table"].astype(np.int32), self.device))
+        self.owner.copy_(to_dev(st["owner"].astype(np.int32), self.device))
+        self.stamp.zero_()
+        self.clock.zero_()
+        if not self.identity:
+            owner = torch.from_numpy(st["owner"].astype(np.int64)).to(self.device)
+            for b in range(3):
+                self.cache[b].copy_(self.staging[b].index_select(0, owner))
+
+
+class DeviceLayer:
+    """Router weights, bias and struct of one layer of a workload."""
+
+    def __init__(self, cfg: LayerConfig, layer: int, device="cuda", step: int = 0):
+        self.cfg = cfg
+        self.layer = layer
+        self.w_router = to_dev(gen.w_router(cfg, layer), device)
+        b = gen.bias(cfg, layer, step)
+        self.bias = None if b is None else to_dev(b, device)
+        self.struct = moe.moe_layer(self.w_router.data_ptr(), None if self.bias is None else self.bias.data_ptr(),
+                                    layer, cfg.E, cfg.k, cfg.H, cfg.I)
+
+    def set_bias(self, step: int):
+        b = gen.bias(self.cfg, self.layer, step)
+        if b is not None:
+            self.bias.copy_(to_dev(b, self.bias.device))
+
+
+def x_dev(cfg: LayerConfig, layer: int, step: int, device="cuda") -> torch.Tensor:
+    return to_dev_bf16(gen.x_bits(cfg, layer, step), device)

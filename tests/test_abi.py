@@ -1,0 +1,75 @@
+"""The C-ABI library loads and exports every entry point include/moe.h
+declares; host-side argument checks answer without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import edge_moe_serving_gb300 as moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "moe.h")) as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_symbols_exported():
+    names = _declared()
+    assert len(names) >= 13
+    lib = ctypes.CDLL(moe.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(moe.EXPORTED)
+
+
+def test_struct_layouts_match_header():
+    assert ctypes.sizeof(moe.moe_pool) == 32
+    assert ctypes.sizeof(moe.moe_bind_stats) == 32
+    assert ctypes.sizeof(moe.moe_layer) == 40
+    assert ctypes.sizeof(moe.moe_layer_buffers) == 56
+    assert ctypes.sizeof(moe.moe_cache) == 2 * 32 + 4 * 8 + 16
+
+
+def test_status_strings_and_version():
+    assert moe.moe_version() >= 100
+    assert moe.moe_status_string(moe.MOE_OK) == "ok"
+    assert "workspace" in moe.moe_status_string(moe.MOE_ERR_WORKSPACE)
+
+
+def test_workspace_sizes_are_host_arithmetic():
+    assert moe.moe_route_topk_workspace_size(1, 256) >= 1024
+    assert moe.moe_route_topk_workspace_size(8192, 256) == 0
+    assert moe.moe_dispatch_workspace_size(1, 6, 256) == 0
+    assert moe.moe_dispatch_workspace_size(8192, 6, 256) >= 48 * 256 * 4
+    assert moe.moe_expert_ffn_workspace_size(32, 8, 128, 2048, 768, moe.MOE_FFN_GEMV) >= 256 * 768 * 2
+
+
+def test_invalid_arguments_rejected_before_launch():
+    L = moe.lib()
+    # k > E, negative T, null outputs: rejected on the host
+    assert L.moe_route_topk(None, 4, 64, None, None, 4, 5, None, None, None, None, 0, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_route_topk(None, -1, 64, None, None, 8, 2, None, None, None, None, 0, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_route_topk(None, 0, 64, None, None, 8, 2, None, None, None, None, 0, None, None) == moe.MOE_OK
+    assert L.moe_dispatch(None, 4, 2, 8, None, None, None, None, None, 0, None, None, 0, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_combine(None, None, None, 4, 2, 64, None, None, None, None) == moe.MOE_ERR_INVALID_ARG
+    c = moe.moe_cache()
+    assert L.moe_cache_bind_slots(ctypes.byref(c), 0, None, 1, 1, 0, 1, 0, 0, None, None, None, 0, None, None) == moe.MOE_ERR_INVALID_ARG
+    # unsupported shape: H not a multiple of 8 (fake non-null pointers: never dereferenced)
+    c.cache = moe.moe_pool(16, 16, 16, 4)
+    c.slot_table, c.owner, c.stamp, c.clock = 16, 16, 16, 16
+    c.n_layers, c.E, c.H, c.I = 1, 4, 12, 8
+    assert L.moe_cache_bind_slots(ctypes.byref(c), 0, None, 0, 1, 0, 1, 0, 0, None, None, None, 0, None, None) == moe.MOE_ERR_UNSUPPORTED
+    c.H = 16
+    # phi > 0 with no staging pool cannot fill
+    assert L.moe_cache_bind_slots(ctypes.byref(c), 0, None, 0, 1, 100, 1, 0, 0, None, None, None, 0, None, None) == moe.MOE_ERR_INVALID_ARG
+    # workspace too small
+    assert L.moe_cache_bind_slots(ctypes.byref(c), 0, None, 0, 1, 0, 1, 0, 0, None, None, None, 0, None, None) == moe.MOE_ERR_WORKSPACE
+    # bad policy / phi above 1.0 / layer out of range
+    assert L.moe_cache_bind_slots(ctypes.byref(c), 0, None, 0, 1, 0, 1, 7, 0, None, None, None, 0, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_cache_bind_slots(ctypes.byref(c), 0, None, 0, 1, 70000, 1, 0, 0, None, None, None, 0, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_cache_bind_slots(ctypes.byref(c), 1, None, 0, 1, 0, 1, 0, 0, None, None, None, 0, None, None) == moe.MOE_ERR_INVALID_ARG
