@@ -60,7 +60,7 @@ class MoeError(RuntimeError):
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"libmoe.so is not built at {LIB_PATH}; run "
-                          "`python -m edge_moe_serving_gb300._build` (nvcc, sm_103a)")
+                          "`python edge_moe_serving_gb300/csrc/build.py` (nvcc, sm_103a)")
     lib = ctypes.CDLL(LIB_PATH)
     P = c_void_p
     sig = {

@@ -1,18 +1,21 @@
 """Build libmoe.so in-tree with nvcc for sm_103a (GB300).
 
-    python -m edge_moe_serving_gb300._build [--force] [--ptxas-verbose]
+    python edge_moe_serving_gb300/csrc/build.py [--force] [--ptxas-verbose]
+
+A plain script (not imported through the package, whose import needs the
+library that this script builds).
 """
 import os
 import subprocess
 import sys
 
-PKG = os.path.dirname(os.path.abspath(__file__))
+CSRC = os.path.dirname(os.path.abspath(__file__))
+PKG = os.path.dirname(CSRC)
 ROOT = os.path.dirname(PKG)
-CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libmoe.so")
 SOURCES = ["moe_api.cu", "route_topk.cu", "dispatch.cu", "bind.cu", "ffn.cu", "ffn_gemv.cu",
-           "combine.cu"]
+           "ffn_gemm.cu", "combine.cu"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 
@@ -24,9 +27,8 @@ def cuda_home():
 
 
 def _inputs():
-    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
+    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cu", ".cuh", ".h", ".py"))]
     files.append(os.path.join(INCLUDE, "moe.h"))
-    files.append(os.path.abspath(__file__))
     return files
 
 

@@ -20,26 +20,41 @@ cudaError_t launch_ffn(const moe_cache& c, int layer, const int32_t* counts, con
                        int T, int k, const uint8_t* mask, int mode, float* y_rows, void* ws,
                        uint32_t* status, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  if (mode == MOE_FFN_GEMM) return cudaErrorNotSupported;
-  GemvParams p;
-  p.c = c;
-  p.layer = layer;
-  p.E = c.E;
-  p.H = c.H;
-  p.I = c.I;
-  p.k = k;
-  p.T = T;
-  p.counts = counts;
-  p.offsets = offsets;
-  p.perm = perm;
-  p.x = x;
-  p.x_perm = x_perm;
-  p.mask = mask;
-  p.max_rows = INT_MAX;
-  p.h = reinterpret_cast<__nv_bfloat16*>(ws);
-  p.y = y_rows;
-  p.status = status;
-  return launch_gemv(p, s);
+  const int R = T * k;
+  __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(ws);
+  // groups above gemv_max run on the tensor-core GEMM; the rest on the GEMV
+  int gemv_max = INT_MAX;
+  if (mode == MOE_FFN_GEMM) {
+    if (!gemm_shape_ok(c.H, c.I) || !x_perm) return cudaErrorNotSupported;
+    gemv_max = 0;
+  } else if (mode == MOE_FFN_AUTO && x_perm && gemm_shape_ok(c.H, c.I) && T > kGemvMaxRows) {
+    gemv_max = kGemvMaxRows;
+  }
+  if (gemv_max > 0) {
+    GemvParams p;
+    p.c = c;
+    p.layer = layer;
+    p.E = c.E;
+    p.H = c.H;
+    p.I = c.I;
+    p.k = k;
+    p.T = T;
+    p.counts = counts;
+    p.offsets = offsets;
+    p.perm = perm;
+    p.x = x;
+    p.x_perm = x_perm;
+    p.mask = mask;
+    p.max_rows = gemv_max;
+    p.h = h;
+    p.y = y_rows;
+    p.status = status;
+    cudaError_t err = launch_gemv(p, s);
+    if (err != cudaSuccess) return err;
+  }
+  if (gemv_max != INT_MAX)
+    return launch_gemm(c, layer, counts, offsets, mask, gemv_max, x_perm, R, h, y_rows, status, s);
+  return cudaSuccess;
 }
 
 }  // namespace moe

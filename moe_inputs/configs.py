@@ -80,4 +80,11 @@ PREFILL = LayerConfig("prefill", T=8192, H=4096, E=256, k=6, I=2048, seed=3)
 LONG_PREFILL = LayerConfig("long_prefill", T=16384, H=4096, E=256, k=6, I=2048, seed=500,
                            n_layers=4, cache_slots=113, phi_q16=0, min_fill=1, bias="zipf")
 
-CONFIGS = {c.name: c for c in (TINY, DECODE, BATCHED_DECODE, PREFILL, LONG_PREFILL)}
+# Profiling case for ncu captures: the decode layer shape (one expert = 50 MB,
+# six routed per token) with 32 experts so that the whole device footprint
+# stays near 2 GB.  Not a benchmark workload.
+DECODE_PROFILE = LayerConfig("decode_profile", T=1, H=4096, E=32, k=6, I=2048, seed=11, steps=32,
+                             cache_slots=12, phi_q16=Q16, fill_policy=FILL_LOWEST_ID, min_fill=1,
+                             bias="zipf")
+
+CONFIGS = {c.name: c for c in (TINY, DECODE, BATCHED_DECODE, PREFILL, LONG_PREFILL, DECODE_PROFILE)}
