@@ -76,6 +76,8 @@ def _load():
         "moe_expert_ffn_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int, c_int]),
         "moe_expert_ffn_grouped": (c_int, [POINTER(moe_cache), c_int, P, P, P, P, P, c_int, c_int, P, c_int,
                                            P, P, c_size_t, P, P]),
+        "moe_expert_ffn_grouped_noalloc": (c_int, [POINTER(moe_cache), c_int, P, P, P, P, P, c_int, c_int, P,
+                                                   c_int, P, P, P]),
         "moe_combine": (c_int, [P, P, P, c_int, c_int, c_int, P, P, P, P]),
         "moe_layer_workspace_size": (c_size_t, [POINTER(moe_layer), POINTER(moe_cache), c_int, c_int]),
         "moe_layer_forward": (c_int, [POINTER(moe_layer), POINTER(moe_cache), P, c_int, P, c_uint32, c_int,
@@ -92,7 +94,8 @@ def _load():
 _lib = _load()
 EXPORTED = ["moe_version", "moe_status_string", "moe_route_topk_workspace_size", "moe_route_topk",
             "moe_dispatch_workspace_size", "moe_dispatch", "moe_cache_bind_workspace_size",
-            "moe_cache_bind_slots", "moe_expert_ffn_workspace_size", "moe_expert_ffn_grouped", "moe_combine",
+            "moe_cache_bind_slots", "moe_expert_ffn_workspace_size", "moe_expert_ffn_grouped",
+            "moe_expert_ffn_grouped_noalloc", "moe_combine",
             "moe_layer_workspace_size", "moe_layer_forward"]
 
 
@@ -173,6 +176,18 @@ def moe_expert_ffn_grouped(cache, layer, counts, offsets, perm, x, x_perm_opt, T
     return _check("moe_expert_ffn_grouped", _lib.moe_expert_ffn_grouped(
         ctypes.byref(cache), layer, _p(counts), _p(offsets), _p(perm), _p(x), _p(x_perm_opt), T, k,
         _p(expert_mask_opt), ffn_mode, _p(y_rows), _p(ws), ws_bytes, _p(dev_status), _s(stream)))
+
+
+MOE_NOALLOC_FFN_SCRATCH_BYTES = 4 << 20
+
+
+def moe_expert_ffn_grouped_noalloc(cache, layer, counts, offsets, perm, x, x_perm_opt, T, k, expert_mask_opt,
+                                   ffn_mode, y_rows, dev_status, stream=None):
+    """moe_expert_ffn_grouped for callers that cannot allocate device memory:
+    the scratch is a static array inside the library (see include/moe.h)."""
+    return _check("moe_expert_ffn_grouped_noalloc", _lib.moe_expert_ffn_grouped_noalloc(
+        ctypes.byref(cache), layer, _p(counts), _p(offsets), _p(perm), _p(x), _p(x_perm_opt), T, k,
+        _p(expert_mask_opt), ffn_mode, _p(y_rows), _p(dev_status), _s(stream)))
 
 
 def moe_combine(y_rows, inv_perm, topk_w, T, k, H, out, out_f32_opt, dev_status, stream=None):

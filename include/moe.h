@@ -215,6 +215,30 @@ int moe_expert_ffn_grouped(const moe_cache* cache, int layer, const int32_t* cou
                            int ffn_mode, float* y_rows, void* ws, size_t ws_bytes,
                            uint32_t* dev_status, moe_stream_t stream);
 
+/* Size of the scratch array built into the library for
+ * moe_expert_ffn_grouped_noalloc (4 MiB per device that loads the library). */
+#define MOE_NOALLOC_FFN_SCRATCH_BYTES (4u << 20)
+
+/* moe_expert_ffn_grouped without a workspace argument, for callers that cannot
+ * allocate device memory: a host framework that owns all device memory and
+ * offers no allocator, a service running on a memory budget fixed at load
+ * time, or a serving loop that must not call cudaMalloc/cudaFree because they
+ * can synchronise the device.  The paper has no counterpart to this call.
+ * Same arguments, results and errors as moe_expert_ffn_grouped; the scratch
+ * is a static array of MOE_NOALLOC_FFN_SCRATCH_BYTES inside the library, held
+ * by every device that loads it until the process exits.  Returns
+ * MOE_ERR_WORKSPACE when the call would need more than that
+ * (moe_expert_ffn_workspace_size(T, k, E, H, I, ffn_mode) bytes).  The first
+ * call on a device looks up the array's device address with that device
+ * current; make that first call before any stream capture.  All calls on a
+ * device share the array, so calls that overlap on the GPU race; the array
+ * needs no clearing between calls.  Allocates nothing. */
+int moe_expert_ffn_grouped_noalloc(const moe_cache* cache, int layer, const int32_t* counts,
+                                   const int32_t* offsets, const int32_t* perm, const void* x,
+                                   const void* x_perm_opt, int T, int k,
+                                   const uint8_t* expert_mask_opt, int ffn_mode, float* y_rows,
+                                   uint32_t* dev_status, moe_stream_t stream);
+
 /* ---------------------------------------------------------------- combine
  * Gate-weighted merge of the expert outputs ([P] section 3.2: the partial
  * sums of the GPU set and the in-place set merge into the exact layer
