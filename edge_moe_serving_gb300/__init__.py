@@ -78,7 +78,7 @@ def _load():
                                            P, P, c_size_t, P, P]),
         "moe_expert_ffn_grouped_noalloc": (c_int, [POINTER(moe_cache), c_int, P, P, P, P, P, c_int, c_int, P,
                                                    c_int, P, P, P]),
-        "moe_combine": (c_int, [P, P, P, c_int, c_int, c_int, P, P, P, P]),
+        "moe_combine": (c_int, [P, P, c_int, c_int, c_int, P, P, P, P]),
         "moe_layer_workspace_size": (c_size_t, [POINTER(moe_layer), POINTER(moe_cache), c_int, c_int]),
         "moe_layer_forward": (c_int, [POINTER(moe_layer), POINTER(moe_cache), P, c_int, P, c_uint32, c_int,
                                       c_int, c_uint64, c_int, POINTER(moe_layer_buffers), P, c_size_t, P, P,
@@ -190,9 +190,9 @@ def moe_expert_ffn_grouped_noalloc(cache, layer, counts, offsets, perm, x, x_per
         _p(expert_mask_opt), ffn_mode, _p(y_rows), _p(dev_status), _s(stream)))
 
 
-def moe_combine(y_rows, inv_perm, topk_w, T, k, H, out, out_f32_opt, dev_status, stream=None):
+def moe_combine(y_rows, topk_w, T, k, H, out, out_f32_opt, dev_status, stream=None):
     return _check("moe_combine", _lib.moe_combine(
-        _p(y_rows), _p(inv_perm), _p(topk_w), T, k, H, _p(out), _p(out_f32_opt), _p(dev_status), _s(stream)))
+        _p(y_rows), _p(topk_w), T, k, H, _p(out), _p(out_f32_opt), _p(dev_status), _s(stream)))
 
 
 def moe_layer_workspace_size(layer, cache, T, ffn_mode):

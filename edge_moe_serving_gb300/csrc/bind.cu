@@ -96,6 +96,8 @@ bind_kernel(moe_cache c, int layer, const int32_t* __restrict__ ids, int R, uint
   const int tid = threadIdx.x;
   const int base = layer * E;
   const int n_slots = c.cache.n_slots;
+  pdl_wait();
+  pdl_trigger();
 
   if (tid == 0) {
     s_now = *c.clock + 1u;
@@ -166,37 +168,38 @@ bind_kernel(moe_cache c, int layer, const int32_t* __restrict__ ids, int R, uint
     if (tid < q) Flist[tid] = Mlist[tid];
   }
   // 6. victims: one pass over the recency state, then a shared-memory sort
-  //    (stamps written above are visible after the barrier inside scan1024 /
-  //    the one below)
+  //    (skipped when nothing is filled; q is uniform across the block)
   __syncthreads();
-  int local_cand = 0;
-  for (int v = tid; v < np2; v += kBindThreads) {
-    unsigned long long key = ~0ull;
-    if (v < n_slots) {
-      const uint32_t sv = c.stamp[v];
-      if (sv != now) {
-        key = ((unsigned long long)sv << 32) | (unsigned long long)v;
-        ++local_cand;
-      }
-    }
-    vkeys[v] = key;
-  }
-  if (local_cand) atomicAdd(&s_ncand, local_cand);
-  __syncthreads();
-  for (int kk = 2; kk <= np2; kk <<= 1) {
-    for (int j = kk >> 1; j > 0; j >>= 1) {
-      for (int i = tid; i < np2; i += kBindThreads) {
-        const int ixj = i ^ j;
-        if (ixj > i) {
-          const unsigned long long a = vkeys[i], b = vkeys[ixj];
-          const bool up = (i & kk) == 0;
-          if ((a > b) == up) {
-            vkeys[i] = b;
-            vkeys[ixj] = a;
-          }
+  if (q > 0) {
+    int local_cand = 0;
+    for (int v = tid; v < np2; v += kBindThreads) {
+      unsigned long long key = ~0ull;
+      if (v < n_slots) {
+        const uint32_t sv = c.stamp[v];
+        if (sv != now) {
+          key = ((unsigned long long)sv << 32) | (unsigned long long)v;
+          ++local_cand;
         }
       }
-      __syncthreads();
+      vkeys[v] = key;
+    }
+    if (local_cand) atomicAdd(&s_ncand, local_cand);
+    __syncthreads();
+    for (int kk = 2; kk <= np2; kk <<= 1) {
+      for (int j = kk >> 1; j > 0; j >>= 1) {
+        for (int i = tid; i < np2; i += kBindThreads) {
+          const int ixj = i ^ j;
+          if (ixj > i) {
+            const unsigned long long a = vkeys[i], b = vkeys[ixj];
+            const bool up = (i & kk) == 0;
+            if ((a > b) == up) {
+              vkeys[i] = b;
+              vkeys[ixj] = a;
+            }
+          }
+        }
+        __syncthreads();
+      }
     }
   }
   const int n_fill = min(q, s_ncand);
@@ -242,6 +245,8 @@ bind_kernel(moe_cache c, int layer, const int32_t* __restrict__ ids, int R, uint
 __global__ void __launch_bounds__(kCopyThreads)
 fill_copy_kernel(moe_pool src, moe_pool dst, size_t bank_bytes, const int32_t* __restrict__ fills,
                  const int32_t* __restrict__ n_fill_p, uint32_t* status) {
+  pdl_wait();
+  pdl_trigger();
   const int n_fill = *n_fill_p;
   const size_t chunks = (bank_bytes + kCopyChunk - 1) / kCopyChunk;
   const size_t items = (size_t)n_fill * 3 * chunks;
@@ -298,7 +303,7 @@ size_t bind_ws_bytes(int T, int k, int E) {
 cudaError_t launch_bind(const moe_cache& c, int layer, const int32_t* ids, int R,
                         uint32_t phi_q16, int min_fill, int policy, uint64_t seed,
                         moe_bind_stats* stats, int32_t* fills_opt, void* ws, uint32_t* status,
-                        cudaStream_t s) {
+                        cudaStream_t s, bool do_copy) {
   static size_t attr_bytes = 0;
   const size_t smem = bind_smem_bytes(c.cache.n_slots, c.E);
   if (smem > attr_bytes) {
@@ -311,15 +316,13 @@ cudaError_t launch_bind(const moe_cache& c, int layer, const int32_t* ids, int R
   int32_t* fills = n_fill + 4;
   (void)kmax;
   const int np2 = next_pow2(c.cache.n_slots < 1 ? 1 : c.cache.n_slots);
-  bind_kernel<<<1, kBindThreads, smem, s>>>(c, layer, ids, R, phi_q16, min_fill, policy,
-                                            (unsigned long long)seed, np2, stats, fills, n_fill,
-                                            fills_opt, status);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = launch_k(bind_kernel, 1, kBindThreads, smem, s, c, layer, ids, R, phi_q16, min_fill, policy,
+                             (unsigned long long)seed, np2, stats, fills, n_fill, fills_opt, status);
   if (err != cudaSuccess) return err;
-  if (c.staging.w_gate == nullptr) return cudaSuccess;   // no staging pool: nothing can be filled
+  if (!do_copy || c.staging.w_gate == nullptr) return cudaSuccess;   // copy fused elsewhere / no staging pool
   const size_t bank_bytes = (size_t)c.H * c.I * sizeof(__nv_bfloat16);
-  fill_copy_kernel<<<num_sms() * 4, kCopyThreads, 0, s>>>(c.staging, c.cache, bank_bytes, fills, n_fill, status);
-  return cudaGetLastError();
+  return launch_k(fill_copy_kernel, num_sms() * 4, kCopyThreads, 0, s, c.staging, c.cache, bank_bytes,
+                  (const int32_t*)fills, (const int32_t*)n_fill, status);
 }
 
 }  // namespace moe

@@ -1,37 +1,52 @@
 // Gate-weighted combine (FreeToken paper, section 3.2: the partial sums of
 // the GPU execution set and of the in-place set merge into the exact layer
-// output; Figure 2).  Every routed row's expert output sits in one y_rows
-// buffer at its dispatch position, whichever pool served the expert, so the
-// merge is one fixed-order sum per token:
-//   out[t, :] = sum_{j = 0..k-1} w[t, j] * y_rows[inv_perm[t*k + j], :]
+// output; Figure 2).  Every routed row's expert output sits in one
+// token-major y_rows buffer (row t*k + j), whichever pool served the expert,
+// so the merge is one fixed-order sum per token over k contiguous rows:
+//   out[t, :] = sum_{j = 0..k-1} w[t, j] * y_rows[t*k + j, :]
 // in ascending expert order, sequential fp32 FMAs, no atomics.  HBM-bound:
-// each thread owns 4 consecutive columns (16-byte loads of y).
+// a work item is (token, 1024 columns); each thread owns 4 consecutive
+// columns and has the k row loads (16 bytes each) in flight together.
 #include "moe_common.cuh"
 
 namespace moe {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kChunk4 = kThreads;   // float4 columns per work item
 
+template <int KM>
 __global__ void __launch_bounds__(kThreads)
-combine_kernel(const float* __restrict__ y_rows, const int32_t* __restrict__ inv_perm,
-               const float* __restrict__ topk_w, int T, int k, int H, __nv_bfloat16* __restrict__ out,
-               float* __restrict__ out_f32) {
+combine_kernel(const float* __restrict__ y_rows, const float* __restrict__ topk_w, int T, int k, int H,
+               __nv_bfloat16* __restrict__ out, float* __restrict__ out_f32) {
+  pdl_wait();
+  pdl_trigger();
   const int H4 = H >> 2;
-  const long long total = (long long)T * H4;
-  for (long long idx = (long long)blockIdx.x * kThreads + threadIdx.x; idx < total;
-       idx += (long long)gridDim.x * kThreads) {
-    const int t = (int)(idx / H4);
-    const int c4 = (int)(idx % H4);
+  const int chunks = (H4 + kChunk4 - 1) / kChunk4;
+  const long long items = (long long)T * chunks;
+  for (long long it = blockIdx.x; it < items; it += gridDim.x) {
+    const int t = (int)(it / chunks);
+    const int c4 = (int)(it % chunks) * kChunk4 + threadIdx.x;
+    if (c4 >= H4) continue;
+    const float4* rows = reinterpret_cast<const float4*>(y_rows + (size_t)t * k * H) + c4;
+    float wv[KM];
+    float4 yv[KM];
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+      if (j < k) {
+        wv[j] = __ldg(topk_w + (size_t)t * k + j);
+        yv[j] = __ldcs(rows + (size_t)j * H4);
+      }
+    }
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < k; ++j) {
-      const float w = __ldg(topk_w + (size_t)t * k + j);
-      const int pos = __ldg(inv_perm + (size_t)t * k + j);
-      const float4 y = __ldcs(reinterpret_cast<const float4*>(y_rows + (size_t)pos * H) + c4);
-      acc.x = fmaf(w, y.x, acc.x);
-      acc.y = fmaf(w, y.y, acc.y);
-      acc.z = fmaf(w, y.z, acc.z);
-      acc.w = fmaf(w, y.w, acc.w);
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+      if (j < k) {
+        acc.x = fmaf(wv[j], yv[j].x, acc.x);
+        acc.y = fmaf(wv[j], yv[j].y, acc.y);
+        acc.z = fmaf(wv[j], yv[j].z, acc.z);
+        acc.w = fmaf(wv[j], yv[j].w, acc.w);
+      }
     }
     if (out) {
       __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
@@ -47,17 +62,16 @@ combine_kernel(const float* __restrict__ y_rows, const int32_t* __restrict__ inv
 
 }  // namespace
 
-cudaError_t launch_combine(const float* y_rows, const int32_t* inv_perm, const float* topk_w, int T,
-                           int k, int H, __nv_bfloat16* out, float* out_f32, uint32_t* status,
-                           cudaStream_t s) {
+cudaError_t launch_combine(const float* y_rows, const float* topk_w, int T, int k, int H, __nv_bfloat16* out,
+                           float* out_f32, uint32_t* status, cudaStream_t s) {
   (void)status;
   if (T == 0) return cudaSuccess;
-  const long long total = (long long)T * (H / 4);
-  long long blocks = (total + kThreads - 1) / kThreads;
+  const long long items = (long long)T * ((H / 4 + kChunk4 - 1) / kChunk4);
+  long long blocks = items;
   const long long cap = (long long)num_sms() * 8;
   if (blocks > cap) blocks = cap;
-  combine_kernel<<<(int)blocks, kThreads, 0, s>>>(y_rows, inv_perm, topk_w, T, k, H, out, out_f32);
-  return cudaGetLastError();
+  if (k <= 8) return launch_k(combine_kernel<8>, (int)blocks, kThreads, 0, s, y_rows, topk_w, T, k, H, out, out_f32);
+  return launch_k(combine_kernel<kMaxK>, (int)blocks, kThreads, 0, s, y_rows, topk_w, T, k, H, out, out_f32);
 }
 
 }  // namespace moe

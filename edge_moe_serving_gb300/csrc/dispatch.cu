@@ -99,6 +99,8 @@ dispatch_single_kernel(const int32_t* __restrict__ ids, int R, int E, int32_t* _
   __shared__ int warp_tot[32];
   __shared__ int total;
   const int tid = threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
   for (int j = tid; j < E * 33; j += kTile) sm[j] = 0;
   __syncthreads();
   bool bad = false;
@@ -130,6 +132,8 @@ tile_hist_kernel(const int32_t* __restrict__ ids, int R, int E, int32_t* __restr
                  uint32_t* status) {
   extern __shared__ int hist[];
   const int tid = threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
   for (int j = tid; j < E; j += kTile) hist[j] = 0;
   __syncthreads();
   const int i = blockIdx.x * kTile + tid;
@@ -148,6 +152,8 @@ tile_scan_kernel(int32_t* __restrict__ tile_counts, int ntiles, int E, int32_t* 
   __shared__ int warp_tot[32];
   __shared__ int total;
   const int e = threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
   int run = 0;
   if (e < E) {
     // tile counts -> exclusive prefix over tiles (the tile's base before offsets are added);
@@ -180,6 +186,8 @@ tile_scatter_kernel(const int32_t* __restrict__ ids, int R, int E,
   int* cursor = sm;
   int* wcnt = cursor + E;
   const int tid = threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
   for (int j = tid; j < E * 32; j += kTile) wcnt[j] = 0;
   for (int j = tid; j < E; j += kTile) cursor[j] = tile_base[(size_t)blockIdx.x * E + j];
   __syncthreads();
@@ -193,6 +201,8 @@ gather_rows_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, int k,
                    int R, __nv_bfloat16* __restrict__ x_perm) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
+  pdl_wait();
+  pdl_trigger();
   // rows past offsets[E] exist only when some ids were invalid: nothing to gather
   if (warp >= R || warp >= offsets[E]) return;
   const int t = perm[warp] / k;
@@ -227,21 +237,22 @@ cudaError_t launch_dispatch(const int32_t* ids, int R, int k, int E, int32_t* co
     if (err != cudaSuccess) return err;
     attr_bytes = (int)(sizeof(int) * 33 * kMaxE);
   }
+  cudaError_t err;
   if (R <= kSingleMaxR) {
-    dispatch_single_kernel<<<1, kTile, need, s>>>(ids, R, E, counts, offsets, perm, inv_perm, status);
+    err = launch_k(dispatch_single_kernel, 1, kTile, need, s, ids, R, E, counts, offsets, perm, inv_perm, status);
   } else {
     const int ntiles = (R + kTile - 1) / kTile;
     int32_t* tile_counts = reinterpret_cast<int32_t*>(ws);
-    tile_hist_kernel<<<ntiles, kTile, sizeof(int) * E, s>>>(ids, R, E, tile_counts, status);
-    tile_scan_kernel<<<1, kTile, 0, s>>>(tile_counts, ntiles, E, counts, offsets);
-    tile_scatter_kernel<<<ntiles, kTile, need, s>>>(ids, R, E, tile_counts, perm, inv_perm);
+    err = launch_k(tile_hist_kernel, ntiles, kTile, sizeof(int) * E, s, ids, R, E, tile_counts, status);
+    if (err == cudaSuccess) err = launch_k(tile_scan_kernel, 1, kTile, 0, s, tile_counts, ntiles, E, counts, offsets);
+    if (err == cudaSuccess)
+      err = launch_k(tile_scatter_kernel, ntiles, kTile, need, s, ids, R, E, (const int32_t*)tile_counts, perm, inv_perm);
   }
-  cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   if (x && x_perm && R > 0) {
     const int blocks = (R + 7) / 8;
-    gather_rows_kernel<<<blocks, 256, 0, s>>>(x, R / k, H, k, perm, offsets, E, R, x_perm);
-    err = cudaGetLastError();
+    err = launch_k(gather_rows_kernel, blocks, 256, 0, s, x, R / k, H, k, (const int32_t*)perm,
+                   (const int32_t*)offsets, E, R, x_perm);
   }
   return err;
 }

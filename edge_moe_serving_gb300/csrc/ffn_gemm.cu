@@ -56,8 +56,9 @@ struct GemmParams {
   int K;                   // reduction length (H for gate/up, I for down)
   int has_staging;
   int32_t cache_slots, staging_slots;
-  __nv_bfloat16* h;        // gate/up output [R, I]
-  float* y;                // down output [R, H]
+  const int32_t* perm;     // dispatch position -> token-major row
+  __nv_bfloat16* h;        // gate/up output [R, I] (dispatch order)
+  float* y;                // down output [R, H] (token-major)
   uint32_t* status;
 };
 
@@ -283,6 +284,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
                  "r"(kTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
+  pdl_wait();
   build_mpair_prefix(p, s_pref, s_warp);   // contains __syncthreads
   tc_fence_before();
   __syncthreads();
@@ -425,7 +427,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
             }
           }
         } else {
-          float* dst = p.y + (size_t)(tl.r0 + row) * p.H + tl.n0;
+          // token-major output row of this dispatch row
+          const int yrow = valid ? p.perm[tl.r0 + row] : 0;
+          float* dst = p.y + (size_t)yrow * p.H + tl.n0;
 #pragma unroll 1
           for (int c = 0; c < 256; c += 32) {
             uint32_t v[32];
@@ -446,6 +450,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ C
       tphase ^= 1u;
     }
   }
+  pdl_trigger();
   __syncthreads();
   if (*abort_flag && tid == 0) set_status(p.status, MOE_DEV_ERR_TIMEOUT);
   tc_fence_after();
@@ -486,8 +491,8 @@ bool gemm_shape_ok(int H, int I) { return H % 256 == 0 && I % 128 == 0 && H >= 2
 
 // Grouped GEMM over the experts with more than min_rows rows (gate/up, then down).
 cudaError_t launch_gemm(const moe_cache& c, int layer, const int32_t* counts, const int32_t* offsets,
-                        const uint8_t* mask, int min_rows, const __nv_bfloat16* x_perm, int R,
-                        __nv_bfloat16* h, float* y, uint32_t* status, cudaStream_t s) {
+                        const int32_t* perm, const uint8_t* mask, int min_rows, const __nv_bfloat16* x_perm,
+                        int R, __nv_bfloat16* h, float* y, uint32_t* status, cudaStream_t s) {
   if (!gemm_shape_ok(c.H, c.I)) return cudaErrorNotSupported;
   static bool attr = false;
   if (!attr) {
@@ -503,6 +508,7 @@ cudaError_t launch_gemm(const moe_cache& c, int layer, const int32_t* counts, co
   p.counts = counts;
   p.offsets = offsets;
   p.mask = mask;
+  p.perm = perm;
   p.slot_table = c.slot_table;
   p.layer = layer;
   p.E = c.E;
@@ -532,8 +538,7 @@ cudaError_t launch_gemm(const moe_cache& c, int layer, const int32_t* counts, co
   p.K = c.H;
   p.n_tiles = c.I / 128;
   const int grid = num_sms();
-  gemm_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(a, g0, u0, g1, u1, p);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = launch_k(gemm_kernel<true>, grid, kThreads, kSmemBytes, s, a, g0, u0, g1, u1, p);
   if (err != cudaSuccess) return err;
 
   CUtensorMap ha, d0, d1;
@@ -547,8 +552,7 @@ cudaError_t launch_gemm(const moe_cache& c, int layer, const int32_t* counts, co
   }
   p.K = c.I;
   p.n_tiles = c.H / 256;
-  gemm_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(ha, d0, d0, d1, d1, p);
-  return cudaGetLastError();
+  return launch_k(gemm_kernel<false>, grid, kThreads, kSmemBytes, s, ha, d0, d0, d1, d1, p);
 }
 
 }  // namespace moe

@@ -18,13 +18,18 @@ struct GemvParams {
   __nv_bfloat16* h;   // [R, I]
   float* y;           // [R, H]
   uint32_t* status;
+  // Fused fill (optional): experts admitted to the cache by this call's bind
+  // are read from the staging pool and written to their cache slot on the fly.
+  const int32_t* fills;     // [n][2]: (staging slot l*E+e, cache slot)
+  const int32_t* n_fill;    // device count of valid rows of `fills`
+  unsigned int* grid_count; // workspace word for the fused kernel's grid barrier
 };
 
 cudaError_t launch_gemv(const GemvParams& p, cudaStream_t s);
 
 bool gemm_shape_ok(int H, int I);
 cudaError_t launch_gemm(const moe_cache& c, int layer, const int32_t* counts, const int32_t* offsets,
-                        const uint8_t* mask, int min_rows, const __nv_bfloat16* x_perm, int R,
-                        __nv_bfloat16* h, float* y, uint32_t* status, cudaStream_t s);
+                        const int32_t* perm, const uint8_t* mask, int min_rows, const __nv_bfloat16* x_perm,
+                        int R, __nv_bfloat16* h, float* y, uint32_t* status, cudaStream_t s);
 
 }  // namespace moe

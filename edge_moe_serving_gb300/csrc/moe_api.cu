@@ -43,6 +43,21 @@ int check_cache(const moe_cache* c) {
   return check_pool(c->staging, false);
 }
 
+int check_bind_args(const moe_cache* cache, int layer, int T, int k, uint32_t phi_q16, int fill_policy) {
+  int st = check_cache(cache);
+  if (st != MOE_OK) return st;
+  if (!cache->owner || !cache->stamp || !cache->clock) return MOE_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= cache->n_layers || T < 0 || k < 1 || k > cache->E) return MOE_ERR_INVALID_ARG;
+  if (phi_q16 > 65536u) return MOE_ERR_INVALID_ARG;
+  if (fill_policy != MOE_FILL_LOWEST_ID && fill_policy != MOE_FILL_RANDOM) return MOE_ERR_INVALID_ARG;
+  if (cache->cache.n_slots > kMaxCacheSlots) return MOE_ERR_UNSUPPORTED;
+  // any fill copies from the staging pool, which must then hold every (layer, expert) pair
+  if (phi_q16 > 0 && (cache->staging.w_gate == nullptr ||
+                      (long long)cache->staging.n_slots < (long long)cache->n_layers * cache->E))
+    return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
 struct Carve {
   char* base;
   size_t off = 0;
@@ -66,6 +81,7 @@ struct LayerWs {
   int32_t* inv_perm;
   float* y_rows;
   __nv_bfloat16* x_perm;
+  void* bind_ws;     // fill count + fill list, alive until the FFN has run
   void* scratch;
   size_t bytes;
 };
@@ -88,6 +104,7 @@ LayerWs layer_ws(void* ws, const moe_layer_buffers* b, int T, int k, int E, int 
   L.inv_perm = cv.take<int32_t>(R);
   L.y_rows = cv.take<float>(R * H);
   L.x_perm = needs_x_perm(mode, T) ? cv.take<__nv_bfloat16>(R * H) : nullptr;
+  L.bind_ws = cv.take<char>(bind_ws_bytes(T, k, E));
   if (b) {
     if (b->topk_ids) L.ids = b->topk_ids;
     if (b->topk_w) L.w = b->topk_w;
@@ -97,7 +114,7 @@ LayerWs layer_ws(void* ws, const moe_layer_buffers* b, int T, int k, int E, int 
     if (b->inv_perm) L.inv_perm = b->inv_perm;
     if (b->y_rows) L.y_rows = b->y_rows;
   }
-  const size_t scratch = std::max({route_ws_bytes(T, E), dispatch_ws_bytes(T, k, E), bind_ws_bytes(T, k, E),
+  const size_t scratch = std::max({route_ws_bytes(T, E), dispatch_ws_bytes(T, k, E),
                                    ffn_ws_bytes(T, k, E, H, I, mode)});
   L.scratch = cv.take<char>(scratch);
   L.bytes = cv.off;
@@ -174,18 +191,9 @@ int moe_cache_bind_slots(const moe_cache* cache, int layer, const int32_t* topk_
                          uint32_t phi_q16, int min_fill, int fill_policy, uint64_t seed,
                          moe_bind_stats* stats_dev, int32_t* fills_opt, void* ws, size_t ws_bytes,
                          uint32_t* dev_status, moe_stream_t stream) {
-  int st = check_cache(cache);
+  int st = check_bind_args(cache, layer, T, k, phi_q16, fill_policy);
   if (st != MOE_OK) return st;
-  if (!cache->owner || !cache->stamp || !cache->clock) return MOE_ERR_INVALID_ARG;
-  if (layer < 0 || layer >= cache->n_layers || T < 0 || k < 1 || k > cache->E) return MOE_ERR_INVALID_ARG;
   if (T > 0 && !topk_ids) return MOE_ERR_INVALID_ARG;
-  if (phi_q16 > 65536u) return MOE_ERR_INVALID_ARG;
-  if (fill_policy != MOE_FILL_LOWEST_ID && fill_policy != MOE_FILL_RANDOM) return MOE_ERR_INVALID_ARG;
-  if (cache->cache.n_slots > kMaxCacheSlots) return MOE_ERR_UNSUPPORTED;
-  // any fill copies from the staging pool, which must then hold every (layer, expert) pair
-  if (phi_q16 > 0 && (cache->staging.w_gate == nullptr ||
-                      (long long)cache->staging.n_slots < (long long)cache->n_layers * cache->E))
-    return MOE_ERR_INVALID_ARG;
   const size_t need = bind_ws_bytes(T, k, cache->E);
   if (!ws || ws_bytes < need) return MOE_ERR_WORKSPACE;
   return cuda_status(launch_bind(*cache, layer, topk_ids, T * k, phi_q16, min_fill, fill_policy, seed,
@@ -218,15 +226,15 @@ int moe_expert_ffn_grouped(const moe_cache* cache, int layer, const int32_t* cou
   return cuda_status(err);
 }
 
-int moe_combine(const float* y_rows, const int32_t* inv_perm, const float* topk_w, int T, int k, int H,
-                void* out, float* out_f32_opt, uint32_t* dev_status, moe_stream_t stream) {
-  if (T < 0 || k < 1 || H < 8) return MOE_ERR_INVALID_ARG;
+int moe_combine(const float* y_rows, const float* topk_w, int T, int k, int H, void* out, float* out_f32_opt,
+                uint32_t* dev_status, moe_stream_t stream) {
+  if (T < 0 || k < 1 || k > kMaxK || H < 8) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
-  if (!y_rows || !inv_perm || !topk_w || (!out && !out_f32_opt)) return MOE_ERR_INVALID_ARG;
+  if (!y_rows || !topk_w || (!out && !out_f32_opt)) return MOE_ERR_INVALID_ARG;
   if ((H % 8) || !aligned16(y_rows) || (out && !aligned16(out)) || (out_f32_opt && !aligned16(out_f32_opt)))
     return MOE_ERR_UNSUPPORTED;
-  return cuda_status(launch_combine(y_rows, inv_perm, topk_w, T, k, H, reinterpret_cast<__nv_bfloat16*>(out),
-                                    out_f32_opt, dev_status, reinterpret_cast<cudaStream_t>(stream)));
+  return cuda_status(launch_combine(y_rows, topk_w, T, k, H, reinterpret_cast<__nv_bfloat16*>(out), out_f32_opt,
+                                    dev_status, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t moe_layer_workspace_size(const moe_layer* layer, const moe_cache* cache, int T, int ffn_mode) {
@@ -253,16 +261,36 @@ int moe_layer_forward(const moe_layer* layer, const moe_cache* cache, const void
   st = moe_route_topk(x, T, H, layer->w_router, layer->bias, E, k, L.ids, L.w, nullptr, L.scratch, scratch_bytes,
                       dev_status, stream);
   if (st != MOE_OK) return st;
-  st = moe_cache_bind_slots(cache, layer->layer, L.ids, T, k, phi_q16, min_fill, fill_policy, seed, stats_dev,
-                            nullptr, L.scratch, scratch_bytes, dev_status, stream);
-  if (st != MOE_OK) return st;
+  // Decode-sized calls run every group on the GEMV kernels, which copy each
+  // admitted expert into its cache slot while they stream it (one read of the
+  // staging copy instead of two); other calls copy in the bind step.
+  const bool fuse_fill = ffn_mode != MOE_FFN_GEMM && !L.x_perm;
+  if (fuse_fill) {
+    st = check_bind_args(cache, layer->layer, T, k, phi_q16, fill_policy);
+    if (st != MOE_OK) return st;
+    if (cuda_status(launch_bind(*cache, layer->layer, L.ids, T * k, phi_q16, min_fill, fill_policy, seed, stats_dev,
+                                nullptr, L.bind_ws, dev_status, reinterpret_cast<cudaStream_t>(stream), false)) != MOE_OK)
+      return MOE_ERR_CUDA;
+  } else {
+    st = moe_cache_bind_slots(cache, layer->layer, L.ids, T, k, phi_q16, min_fill, fill_policy, seed, stats_dev,
+                              nullptr, L.bind_ws, bind_ws_bytes(T, k, E), dev_status, stream);
+    if (st != MOE_OK) return st;
+  }
   st = moe_dispatch(L.ids, T, k, E, L.counts, L.offsets, L.perm, L.inv_perm, L.x_perm ? x : nullptr, H, L.x_perm,
                     L.scratch, scratch_bytes, dev_status, stream);
   if (st != MOE_OK) return st;
-  st = moe_expert_ffn_grouped(cache, layer->layer, L.counts, L.offsets, L.perm, x, L.x_perm, T, k, nullptr,
-                              ffn_mode, L.y_rows, L.scratch, scratch_bytes, dev_status, stream);
-  if (st != MOE_OK) return st;
-  return moe_combine(L.y_rows, L.inv_perm, L.w, T, k, H, out, nullptr, dev_status, stream);
+  if (fuse_fill) {
+    const int32_t* n_fill = reinterpret_cast<const int32_t*>(L.bind_ws);
+    cudaError_t err = launch_ffn(*cache, layer->layer, L.counts, L.offsets, L.perm,
+                                 reinterpret_cast<const __nv_bfloat16*>(x), nullptr, T, k, nullptr, ffn_mode, L.y_rows,
+                                 L.scratch, dev_status, reinterpret_cast<cudaStream_t>(stream), n_fill + 4, n_fill);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+  } else {
+    st = moe_expert_ffn_grouped(cache, layer->layer, L.counts, L.offsets, L.perm, x, L.x_perm, T, k, nullptr,
+                                ffn_mode, L.y_rows, L.scratch, scratch_bytes, dev_status, stream);
+    if (st != MOE_OK) return st;
+  }
+  return moe_combine(L.y_rows, L.w, T, k, H, out, nullptr, dev_status, stream);
 }
 
 }  // extern "C"

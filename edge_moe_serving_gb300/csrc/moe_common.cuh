@@ -14,9 +14,35 @@ constexpr int kMaxE = 1024;           // bind / dispatch limit
 constexpr int kMaxRouteE = 512;       // router top-k limit (16 logits per lane)
 constexpr int kMaxK = 16;
 constexpr int kMaxCacheSlots = 16384; // bind kernel keeps all (stamp, slot) keys in shared memory
-constexpr int kGemvMaxRows = 8;       // AUTO mode: groups up to this size use the GEMV path
+constexpr int kGemvMaxRows = 2;       // AUTO mode: groups up to this size use the GEMV path
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// ---------------------------------------------------------------- launch chaining
+// Every kernel of the library is launched with programmatic stream
+// serialization: the next kernel on the stream may start its prologue while
+// this one drains.  Each kernel calls pdl_wait() before it reads anything a
+// previous kernel wrote (on every path, so completion stays transitive), and
+// pdl_trigger() once its dependents may be scheduled.  Without the launch
+// attribute both are no-ops.
+__device__ inline void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ inline void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                            Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 // ---------------------------------------------------------------- device status
 __device__ inline void set_status(uint32_t* status, uint32_t bit) {
@@ -105,19 +131,21 @@ cudaError_t launch_dispatch(const int32_t* ids, int R, int k, int E, int32_t* co
 
 size_t bind_ws_bytes(int T, int k, int E);
 size_t bind_smem_bytes(int n_slots, int E);
+// ws holds the fill count (int32 at offset 0) and the fill list (from int32 offset 4).
+// do_copy = false leaves the copy to a fused-fill FFN launch.
 cudaError_t launch_bind(const moe_cache& c, int layer, const int32_t* ids, int R,
                         uint32_t phi_q16, int min_fill, int policy, uint64_t seed,
                         moe_bind_stats* stats, int32_t* fills_opt, void* ws, uint32_t* status,
-                        cudaStream_t s);
+                        cudaStream_t s, bool do_copy = true);
 
 size_t ffn_ws_bytes(int T, int k, int E, int H, int I, int mode);
 cudaError_t launch_ffn(const moe_cache& c, int layer, const int32_t* counts, const int32_t* offsets,
                        const int32_t* perm, const __nv_bfloat16* x, const __nv_bfloat16* x_perm,
                        int T, int k, const uint8_t* mask, int mode, float* y_rows, void* ws,
-                       uint32_t* status, cudaStream_t s);
+                       uint32_t* status, cudaStream_t s, const int32_t* fused_fills = nullptr,
+                       const int32_t* fused_n_fill = nullptr);
 
-cudaError_t launch_combine(const float* y_rows, const int32_t* inv_perm, const float* topk_w, int T,
-                           int k, int H, __nv_bfloat16* out, float* out_f32, uint32_t* status,
-                           cudaStream_t s);
+cudaError_t launch_combine(const float* y_rows, const float* topk_w, int T, int k, int H,
+                           __nv_bfloat16* out, float* out_f32, uint32_t* status, cudaStream_t s);
 
 }  // namespace moe

@@ -88,6 +88,8 @@ route_small_kernel(const __nv_bfloat16* __restrict__ x, int T, int H,
                    int32_t* __restrict__ topk_ids, float* __restrict__ topk_w) {
   __shared__ float red[kSmallThreads / 32][NT];
   __shared__ bool is_last;
+  pdl_wait();
+  pdl_trigger();
   const int e = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float4* wrow = reinterpret_cast<const float4*>(w_router + (size_t)e * H);
@@ -159,6 +161,8 @@ route_large_kernel(const __nv_bfloat16* __restrict__ x, int T, int H,
                    int k, float* __restrict__ logits_opt, int32_t* __restrict__ topk_ids,
                    float* __restrict__ topk_w) {
   extern __shared__ float smem[];
+  pdl_wait();
+  pdl_trigger();
   float* xs = smem;                          // [kLK][kLT]
   float* wsm = xs + kLK * kLT;               // [kLK][kLE + 4]
   float* lg = wsm + kLK * (kLE + 4);         // [kLT][E + 1]
@@ -261,12 +265,13 @@ cudaError_t launch_route_topk(const __nv_bfloat16* x, int T, int H, const float*
     cudaError_t err = cudaMemsetAsync(ticket, 0, sizeof(unsigned int), s);
     if (err != cudaSuccess) return err;
     if (T <= 1)
-      route_small_kernel<1><<<E, kSmallThreads, 0, s>>>(x, T, H, w_router, bias, E, k, logits, ticket, topk_ids, topk_w);
-    else if (T <= 4)
-      route_small_kernel<4><<<E, kSmallThreads, 0, s>>>(x, T, H, w_router, bias, E, k, logits, ticket, topk_ids, topk_w);
-    else
-      route_small_kernel<8><<<E, kSmallThreads, 0, s>>>(x, T, H, w_router, bias, E, k, logits, ticket, topk_ids, topk_w);
-    return cudaGetLastError();
+      return launch_k(route_small_kernel<1>, E, kSmallThreads, 0, s, x, T, H, w_router, bias, E, k, logits, ticket,
+                      topk_ids, topk_w);
+    if (T <= 4)
+      return launch_k(route_small_kernel<4>, E, kSmallThreads, 0, s, x, T, H, w_router, bias, E, k, logits, ticket,
+                      topk_ids, topk_w);
+    return launch_k(route_small_kernel<8>, E, kSmallThreads, 0, s, x, T, H, w_router, bias, E, k, logits, ticket,
+                    topk_ids, topk_w);
   }
   const size_t smem = large_smem(E);
   static bool attr_set = false;
@@ -277,8 +282,8 @@ cudaError_t launch_route_topk(const __nv_bfloat16* x, int T, int H, const float*
     attr_set = true;
   }
   const int grid = (T + kLT - 1) / kLT;
-  route_large_kernel<<<grid, kLThreads, smem, s>>>(x, T, H, w_router, bias, E, k, logits_opt, topk_ids, topk_w);
-  return cudaGetLastError();
+  return launch_k(route_large_kernel, grid, kLThreads, smem, s, x, T, H, w_router, bias, E, k, logits_opt, topk_ids,
+                  topk_w);
 }
 
 }  // namespace moe

@@ -66,7 +66,7 @@ typedef struct CUstream_st* moe_stream_t; /* same type as cudaStream_t; NULL = l
 #define MOE_FILL_RANDOM 1     /* a seeded uniformly random q-subset (SplitMix64 keys) */
 
 /* expert-FFN kernel selection */
-#define MOE_FFN_AUTO 0  /* weight-streaming GEMV for groups of <= 8 rows, tensor-core GEMM above */
+#define MOE_FFN_AUTO 0  /* weight-streaming GEMV for groups of <= 2 rows, tensor-core GEMM above */
 #define MOE_FFN_GEMV 1  /* weight-streaming GEMV for every group */
 #define MOE_FFN_GEMM 2  /* tcgen05 grouped GEMM for every non-empty group */
 
@@ -138,7 +138,7 @@ typedef struct moe_layer_buffers {
   int32_t* offsets;   /* [E + 1] */
   int32_t* perm;      /* [T*k] */
   int32_t* inv_perm;  /* [T*k] */
-  float* y_rows;      /* [T*k, H] */
+  float* y_rows;      /* [T*k, H], row t*k+j = output of token t's j-th expert */
 } moe_layer_buffers;
 
 int moe_version(void);
@@ -202,7 +202,9 @@ int moe_cache_bind_slots(const moe_cache* cache, int layer, const int32_t* topk_
  * with counts[e] > 0 (and expert_mask_opt[e] != 0 if a mask is given), with
  * rows pos in [offsets[e], offsets[e+1]) and x row t = perm[pos] / k:
  *   g = x_t W_gate^T, u = x_t W_up^T (fp32 accumulation), h = bf16(silu(g) * u),
- *   y_rows[pos, :] = h W_down^T (fp32 accumulation, stored fp32)
+ *   y_rows[perm[pos], :] = h W_down^T (fp32 accumulation, stored fp32)
+ * i.e. y_rows is token-major: row t*k + j holds the output of token t's j-th
+ * routed expert, so the combine reads each token's k rows contiguously.
  * where the banks are those of pool slot_table[layer*E + e].  x bf16 [T, H];
  * x_perm_opt: bf16 [T*k, H] gathered rows (from moe_dispatch), required by
  * the GEMM kernel and used by the GEMV kernel if given.  Rows of experts
@@ -242,13 +244,13 @@ int moe_expert_ffn_grouped_noalloc(const moe_cache* cache, int layer, const int3
 /* ---------------------------------------------------------------- combine
  * Gate-weighted merge of the expert outputs ([P] section 3.2: the partial
  * sums of the GPU set and the in-place set merge into the exact layer
- * output).  out[t, :] = sum_{j=0}^{k-1} topk_w[t, j] * y_rows[inv_perm[t*k+j], :]
+ * output).  out[t, :] = sum_{j=0}^{k-1} topk_w[t, j] * y_rows[t*k + j, :]
  * summed in j order (ascending expert id) with fp32 FMAs, then rounded to
  * bf16 (out) and/or stored fp32 (out_f32_opt).  The result does not depend
  * on which pool any row's expert was read from.  out or out_f32_opt may be
  * NULL, not both. */
-int moe_combine(const float* y_rows, const int32_t* inv_perm, const float* topk_w, int T, int k,
-                int H, void* out, float* out_f32_opt, uint32_t* dev_status, moe_stream_t stream);
+int moe_combine(const float* y_rows, const float* topk_w, int T, int k, int H, void* out,
+                float* out_f32_opt, uint32_t* dev_status, moe_stream_t stream);
 
 /* ---------------------------------------------------------------- whole layer
  * moe_route_topk -> moe_cache_bind_slots -> moe_dispatch ->

@@ -87,4 +87,10 @@ DECODE_PROFILE = LayerConfig("decode_profile", T=1, H=4096, E=32, k=6, I=2048, s
                              cache_slots=12, phi_q16=Q16, fill_policy=FILL_LOWEST_ID, min_fill=1,
                              bias="zipf")
 
-CONFIGS = {c.name: c for c in (TINY, DECODE, BATCHED_DECODE, PREFILL, LONG_PREFILL, DECODE_PROFILE)}
+# Profiling case for ncu captures of the prefill kernels: the prefill layer
+# shape with 32 experts and 2048 tokens (about 2 GB on the device, ~384 rows per
+# expert).  Not a benchmark workload.
+PREFILL_PROFILE = LayerConfig("prefill_profile", T=2048, H=4096, E=32, k=6, I=2048, seed=12)
+
+CONFIGS = {c.name: c for c in (TINY, DECODE, BATCHED_DECODE, PREFILL, LONG_PREFILL, DECODE_PROFILE,
+                               PREFILL_PROFILE)}

@@ -67,6 +67,12 @@ def status_bits(s):
     return int(s.cpu().numpy().view(np.uint32)[0])
 
 
+def token_major(ref):
+    """The oracle's expert rows (dispatch order) in the token-major order the
+    library writes: row t*k + j = output of token t's j-th expert."""
+    return ref["y_rows"][ref["inv_perm"]]
+
+
 def oracle_layer(cfg, layer, step, wcache, x_bits=None, tokens=None):
     """Oracle forward of (layer, step) on the workload's inputs."""
     xb = gen.x_bits(cfg, layer, step) if x_bits is None else x_bits

@@ -56,7 +56,8 @@ def test_invalid_arguments_rejected_before_launch():
     assert L.moe_route_topk(None, -1, 64, None, None, 8, 2, None, None, None, None, 0, None, None) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_route_topk(None, 0, 64, None, None, 8, 2, None, None, None, None, 0, None, None) == moe.MOE_OK
     assert L.moe_dispatch(None, 4, 2, 8, None, None, None, None, None, 0, None, None, 0, None, None) == moe.MOE_ERR_INVALID_ARG
-    assert L.moe_combine(None, None, None, 4, 2, 64, None, None, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_combine(None, None, 4, 2, 64, None, None, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_combine(None, None, 4, 17, 64, None, None, None, None) == moe.MOE_ERR_INVALID_ARG
     c = moe.moe_cache()
     assert L.moe_cache_bind_slots(ctypes.byref(c), 0, None, 1, 1, 0, 1, 0, 0, None, None, None, 0, None, None) == moe.MOE_ERR_INVALID_ARG
     # unsupported shape: H not a multiple of 8 (fake non-null pointers: never dereferenced)

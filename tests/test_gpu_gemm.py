@@ -10,7 +10,7 @@ import edge_moe_serving_gb300 as moe
 from moe_inputs import CONFIGS, gen
 from moe_inputs.device import DeviceCache, to_dev_bf16, x_dev
 from oracle import moe_oracle as O
-from gpu_helpers import DEV, ExpertCache, assert_close, oracle_layer, status, status_bits, ws
+from gpu_helpers import DEV, ExpertCache, assert_close, oracle_layer, status, status_bits, token_major, ws
 
 pytestmark = pytest.mark.gpu
 
@@ -48,7 +48,7 @@ def test_gemm_forced_tiny():
     ref = oracle_layer(cfg, 0, 0, ExpertCache(cfg))
     y, st = _ffn(cfg, dc, ref, x_dev(cfg, 0, 0), moe.MOE_FFN_GEMM)
     assert st == 0
-    assert_close(y, ref["y_rows"], what="tiny GEMM y_rows")
+    assert_close(y, token_major(ref), what="tiny GEMM y_rows")
 
 
 @pytest.mark.parametrize("T", [300, 1000])
@@ -70,7 +70,7 @@ def test_gemm_auto_mixed_groups(T):
     for mode in (moe.MOE_FFN_AUTO, moe.MOE_FFN_GEMM, moe.MOE_FFN_GEMV):
         y, st = _ffn(cfg, dc, ref, to_dev_bf16(xb, DEV), mode)
         assert st == 0
-        assert_close(y, ref["y_rows"], what=f"T={T} mode {mode}")
+        assert_close(y, token_major(ref), what=f"T={T} mode {mode}")
 
 
 def test_gemm_mask_split_is_bitwise():
@@ -84,7 +84,7 @@ def test_gemm_mask_split_is_bitwise():
     mask = (np.arange(cfg.E) % 3 == 0).astype(np.uint8)
     y1, _ = _ffn(cfg, dc, ref, xd, moe.MOE_FFN_GEMM, torch.from_numpy(mask).to(DEV))
     y2, _ = _ffn(cfg, dc, ref, xd, moe.MOE_FFN_GEMM, torch.from_numpy(1 - mask).to(DEV))
-    rows_m = mask[ref["ids"].reshape(-1)[ref["perm"]]].astype(bool)
+    rows_m = mask[ref["ids"].reshape(-1)].astype(bool)        # token-major rows
     assert np.array_equal(np.where(rows_m[:, None], y1, y2), full)
 
 
@@ -98,4 +98,4 @@ def test_gemv_general_shape():
     for mode in (moe.MOE_FFN_AUTO, moe.MOE_FFN_GEMV):
         y, st = _ffn(cfg, dc, ref, to_dev_bf16(xb, DEV), mode)
         assert st == 0
-        assert_close(y, ref["y_rows"], what=f"odd shape mode {mode}")
+        assert_close(y, token_major(ref), what=f"odd shape mode {mode}")

@@ -14,7 +14,7 @@ from moe_inputs import CONFIGS, gen
 from moe_inputs.device import DeviceCache, DeviceLayer, to_dev, to_dev_bf16, x_dev
 from oracle import moe_oracle as O
 from gpu_helpers import (DEV, ExpertCache, assert_close, bf16_to_f64, oracle_layer, run_layer, status,
-                         status_bits, ws)
+                         status_bits, token_major, ws)
 
 pytestmark = pytest.mark.gpu
 
@@ -245,7 +245,7 @@ def test_expert_ffn_gemv_rows(name, steps):
                                    moe.MOE_FFN_GEMV, y, ws(nb), nb, st)
         torch.cuda.synchronize()
         assert status_bits(st) == 0
-        assert_close(y.cpu().numpy(), ref["y_rows"], what=f"{name} step {step} y_rows")
+        assert_close(y.cpu().numpy(), token_major(ref), what=f"{name} step {step} y_rows")
 
 
 def test_expert_ffn_mask_split_is_bitwise():
@@ -297,11 +297,10 @@ def test_expert_ffn_unbound_slot_is_reported():
     torch.cuda.synchronize()
     assert status_bits(st) & moe.MOE_DEV_ERR_UNBOUND
     yc = y.cpu().numpy()
-    lo, hi = ref["offsets"][e_bad], ref["offsets"][e_bad + 1]
-    assert np.all(yc[lo:hi] == 123.0)
-    keep = np.ones(R, bool)
-    keep[lo:hi] = False
-    assert_close(yc[keep], ref["y_rows"][keep], what="other experts")
+    bad_rows = ref["ids"].reshape(-1) == e_bad            # token-major rows of the unbound expert
+    assert bad_rows.sum() == ref["counts"][e_bad] > 0
+    assert np.all(yc[bad_rows] == 123.0)
+    assert_close(yc[~bad_rows], token_major(ref)[~bad_rows], what="other experts")
 
 
 # ------------------------------------------------------------------ combine
@@ -309,14 +308,13 @@ def test_combine_matches_oracle_definition():
     rng = np.random.default_rng(3)
     for T, k, H in ((1, 6, 4096), (37, 3, 64), (513, 8, 2048)):
         R = T * k
-        y = rng.standard_normal((R, H)).astype(np.float32)
-        inv = np.argsort(rng.random(R)).astype(np.int32)
+        y = rng.standard_normal((R, H)).astype(np.float32)        # token-major rows
         w = rng.random((T, k)).astype(np.float32)
         out = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
         o32 = torch.empty((T, H), dtype=torch.float32, device=DEV)
-        moe.moe_combine(to_dev(y, DEV), to_dev(inv, DEV), to_dev(w, DEV), T, k, H, out, o32, status())
+        moe.moe_combine(to_dev(y, DEV), to_dev(w, DEV), T, k, H, out, o32, status())
         torch.cuda.synchronize()
-        ref = O.combine(y.astype(np.float64), inv, w.astype(np.float64), k)
+        ref = O.combine(y.astype(np.float64), np.arange(R), w.astype(np.float64), k)
         got32 = o32.cpu().numpy()
         assert np.abs(got32 - ref).max() <= 1e-5 * max(1.0, np.abs(ref).max())
         # the bf16 output is the fp32 result rounded to nearest even
@@ -434,7 +432,8 @@ def _prefill_sampled(name, layer, n_experts=4, n_tokens=8, ffn_mode=moe.MOE_FFN_
     pick |= set(int(e) for e in rng.choice(active, n_experts, replace=False))
     for e in sorted(pick):
         rows = O.expert_rows(x, ids_ref, offsets, perm, lambda ee: wc(layer, ee), [e], cfg.k)[e]
-        assert_close(y[offsets[e]:offsets[e + 1]], rows, what=f"{name} layer {layer} expert {e}")
+        got_rows = y[perm[offsets[e]:offsets[e + 1]]]        # token-major rows of the expert's dispatch rows
+        assert_close(got_rows, rows, what=f"{name} layer {layer} expert {e}")
     # layer output of sampled tokens, one by one
     toks = rng.choice(cfg.T, n_tokens, replace=False)
     out = bf16_to_f64(got["out"])

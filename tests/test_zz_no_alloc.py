@@ -12,7 +12,7 @@ import torch
 import edge_moe_serving_gb300 as moe
 from moe_inputs import CONFIGS
 from moe_inputs.device import DeviceCache, x_dev
-from gpu_helpers import DEV, ExpertCache, assert_close, oracle_layer, status, status_bits, ws
+from gpu_helpers import DEV, ExpertCache, assert_close, oracle_layer, status, status_bits, token_major, ws
 
 pytestmark = pytest.mark.gpu
 
@@ -63,7 +63,7 @@ def test_noalloc_matches_workspace_entry_point_twice():
         a, b = y_na.cpu().numpy(), y_ws.cpu().numpy()
         assert np.isfinite(a).all()
         assert_close(a, b, what=f"no-alloc vs workspace entry point, call {step}")
-        assert_close(a, ref["y_rows"], what=f"no-alloc vs oracle, call {step}")
+        assert_close(a, token_major(ref), what=f"no-alloc vs oracle, call {step}")
 
 
 def test_noalloc_rejects_calls_beyond_its_scratch():
