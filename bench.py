@@ -223,15 +223,17 @@ def run_ours(args, rank, world):
 
 
 def kernels_per_call(cfg):
-    """Kernels one moe_layer_forward call launches for this workload."""
+    """Kernels one moe_layer_forward call launches for this workload (AUTO mode)."""
     R = cfg.T * cfg.k
-    route = 1
-    bind = 2                      # bind + fill copy
-    dispatch = 1 if R <= 4096 else 3
-    gather = 1 if cfg.T > 8 else 0
-    ffn = 2
-    combine = 1
-    return route + bind + dispatch + gather + ffn + combine
+    n = 1                                   # router + top-k
+    n += 1                                  # residency bind (+ dispatch when R <= 4096)
+    if R > 4096:
+        n += 3                              # multi-CTA dispatch: histogram, scan, scatter
+    if cfg.T <= 2:
+        n += 1                              # fused GEMV: gate/up, down, fill copy, combine
+    else:
+        n += 1 + 1 + 1 + 2 + 1              # fill copy, gather, GEMV (small groups), GEMM x2, combine
+    return n
 
 
 def workload_config(cfg, world):

@@ -21,7 +21,9 @@
 //      when fewer than q victims exist) are bound to the staging pool.
 // fill_copy_kernel: one fixed-shape persistent launch applies the device fill
 // list to all three banks, masked by the device fill count.
-#include "moe_common.cuh"
+#include <algorithm>
+
+#include "dispatch_block.cuh"
 
 namespace moe {
 namespace {
@@ -78,20 +80,34 @@ __device__ int scan1024(int v, int* warp_tot, int* total) {
 
 enum : int { kNotRouted = 0, kHit = 1, kMiss = 2, kFilled = 3 };
 
+// Outputs of the optional fused dispatch (see dispatch_block.cuh).
+struct DispatchOut {
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* perm;
+  int32_t* inv_perm;
+};
+
+// The kernel reads all the state it needs in one batch of independent loads
+// (clock, routed ids, this layer's slot-table entries, every slot's stamp),
+// decides everything in shared memory, then writes: two dependent round
+// trips to memory instead of one per step of the algorithm.
+template <bool DISPATCH>
 __global__ void __launch_bounds__(kBindThreads)
 bind_kernel(moe_cache c, int layer, const int32_t* __restrict__ ids, int R, uint32_t phi_q16,
             int min_fill, int policy, unsigned long long seed, int np2, moe_bind_stats* stats,
             int32_t* __restrict__ fills, int32_t* __restrict__ n_fill_out,
-            int32_t* __restrict__ fills_opt, uint32_t* status) {
+            int32_t* __restrict__ fills_opt, uint32_t* status, DispatchOut dout) {
   extern __shared__ unsigned long long sm64[];
   const int E = c.E;
-  unsigned long long* vkeys = sm64;                       // [np2] victim keys
+  unsigned long long* vkeys = sm64;                       // [np2] (stamp << 32 | slot) of candidate victims
   unsigned long long* mkeys = vkeys + np2;                // [E] random-policy keys of M
   int* st = reinterpret_cast<int*>(mkeys + E);            // [E] per-expert state
-  int* Mlist = st + E;                                    // [E] misses ascending
+  int* ent = st + E;                                      // [E] this layer's slot-table entries
+  int* Mlist = ent + E;                                   // [E] misses ascending
   int* Flist = Mlist + E;                                 // [E] fill set ascending
   __shared__ int warp_tot[32];
-  __shared__ int s_total, s_m, s_q, s_nU, s_ncand, s_nF;
+  __shared__ int s_total, s_m, s_q, s_nU, s_ncand;
   __shared__ uint32_t s_now;
   const int tid = threadIdx.x;
   const int base = layer * E;
@@ -99,15 +115,26 @@ bind_kernel(moe_cache c, int layer, const int32_t* __restrict__ ids, int R, uint
   pdl_wait();
   pdl_trigger();
 
+  // 1. independent loads
   if (tid == 0) {
     s_now = *c.clock + 1u;
-    *c.clock = s_now;
     s_ncand = 0;
   }
-  for (int e = tid; e < E; e += kBindThreads) st[e] = kNotRouted;
+  for (int e = tid; e < E; e += kBindThreads) {
+    st[e] = kNotRouted;
+    ent[e] = c.slot_table[base + e];
+  }
+  int local_cand = 0;
+  for (int v = tid; v < np2; v += kBindThreads) {
+    unsigned long long key = ~0ull;
+    if (v < n_slots) {
+      key = ((unsigned long long)c.stamp[v] << 32) | (unsigned long long)v;
+      ++local_cand;
+    }
+    vkeys[v] = key;
+  }
   __syncthreads();
   const uint32_t now = s_now;
-  // 2. dedup
   bool bad = false;
   for (int i = tid; i < R; i += kBindThreads) {
     const int e = ids[i];
@@ -116,22 +143,25 @@ bind_kernel(moe_cache c, int layer, const int32_t* __restrict__ ids, int R, uint
   }
   if (bad) set_status(status, MOE_DEV_ERR_BAD_ID);
   __syncthreads();
-  // 3. classify (thread e owns expert e; E <= 1024)
+  // 2. classify (thread e owns expert e; E <= 1024); a hit's slot leaves the victim candidates
   const int e = tid;
-  bool routed = (e < E) && st[e] != kNotRouted;
+  const bool routed = (e < E) && st[e] != kNotRouted;
   bool miss = false;
+  int my_slot = -1;
   if (routed) {
-    const int32_t ent = c.slot_table[base + e];
-    if (ent >= 0 && ent < n_slots) {
-      c.stamp[ent] = now;
+    const int32_t en = ent[e];
+    if (en >= 0 && en < n_slots) {
+      my_slot = en;
+      vkeys[en] = ~0ull;
+      --local_cand;   // the thread that loaded the slot's key may differ: fixed below by the count
       st[e] = kHit;
     } else {
-      if (ent >= 0 && ent < MOE_STAGING_TAG) set_status(status, MOE_DEV_ERR_BAD_SLOT);
+      if (en >= 0 && en < MOE_STAGING_TAG) set_status(status, MOE_DEV_ERR_BAD_SLOT);
       miss = true;
     }
   }
-  const int n_routed_before = scan1024(routed ? 1 : 0, warp_tot, &s_total);
-  (void)n_routed_before;
+  atomicAdd(&s_ncand, local_cand);
+  scan1024(routed ? 1 : 0, warp_tot, &s_total);
   if (tid == 0) s_nU = s_total;
   __syncthreads();
   const int mpos = scan1024(miss ? 1 : 0, warp_tot, &s_total);
@@ -142,7 +172,7 @@ bind_kernel(moe_cache c, int layer, const int32_t* __restrict__ ids, int R, uint
   }
   __syncthreads();
   const int m = s_m, q = s_q;
-  // 5. fill set F (ascending ids)
+  // 3. fill set F (ascending ids)
   if (policy == MOE_FILL_RANDOM) {
     if (tid < m) {
       const int me = Mlist[tid];
@@ -167,24 +197,10 @@ bind_kernel(moe_cache c, int layer, const int32_t* __restrict__ ids, int R, uint
   } else {
     if (tid < q) Flist[tid] = Mlist[tid];
   }
-  // 6. victims: one pass over the recency state, then a shared-memory sort
-  //    (skipped when nothing is filled; q is uniform across the block)
   __syncthreads();
+  // 4. victims: the q least (stamp, slot) candidates (one pass over the state, then a
+  //    shared-memory bitonic sort; skipped when nothing is filled)
   if (q > 0) {
-    int local_cand = 0;
-    for (int v = tid; v < np2; v += kBindThreads) {
-      unsigned long long key = ~0ull;
-      if (v < n_slots) {
-        const uint32_t sv = c.stamp[v];
-        if (sv != now) {
-          key = ((unsigned long long)sv << 32) | (unsigned long long)v;
-          ++local_cand;
-        }
-      }
-      vkeys[v] = key;
-    }
-    if (local_cand) atomicAdd(&s_ncand, local_cand);
-    __syncthreads();
     for (int kk = 2; kk <= np2; kk <<= 1) {
       for (int j = kk >> 1; j > 0; j >>= 1) {
         for (int i = tid; i < np2; i += kBindThreads) {
@@ -203,7 +219,7 @@ bind_kernel(moe_cache c, int layer, const int32_t* __restrict__ ids, int R, uint
     }
   }
   const int n_fill = min(q, s_ncand);
-  // 7. admit F[i] into victim i
+  // 5. writes: admit F[i] into victim i, refresh hits, bind C to the staging pool
   if (tid < n_fill) {
     const int fe = Flist[tid];
     const int v = (int)(vkeys[tid] & 0xFFFFFFFFull);
@@ -220,13 +236,14 @@ bind_kernel(moe_cache c, int layer, const int32_t* __restrict__ ids, int R, uint
       fills_opt[2 * tid + 1] = v;
     }
   }
+  if (my_slot >= 0) c.stamp[my_slot] = now;
   __syncthreads();
-  // misses not filled (C, with any overflow) are served from the staging pool
   if (tid < m) {
     const int me = Mlist[tid];
     if (st[me] != kFilled) c.slot_table[base + me] = MOE_STAGING_TAG | (base + me);
   }
   if (tid == 0) {
+    *c.clock = now;
     *n_fill_out = n_fill;
     if (stats) {
       stats->n_unique = s_nU;
@@ -238,6 +255,12 @@ bind_kernel(moe_cache c, int layer, const int32_t* __restrict__ ids, int R, uint
       stats->n_staged = m - n_fill;
       stats->clock = now;
     }
+  }
+  if (DISPATCH) {
+    // the routed rows' grouping for the expert FFN, in the same launch
+    __syncthreads();
+    blk::dispatch_block(ids, R, E, dout.counts, dout.offsets, dout.perm, dout.inv_perm, nullptr,
+                        reinterpret_cast<int*>(sm64));
   }
 }
 
@@ -292,7 +315,7 @@ int next_pow2(int v) {
 
 size_t bind_smem_bytes(int n_slots, int E) {
   const size_t np2 = (size_t)next_pow2(n_slots < 1 ? 1 : n_slots);
-  return np2 * 8 + (size_t)E * 8 + (size_t)E * 4 * 3;
+  return np2 * 8 + (size_t)E * 8 + (size_t)E * 4 * 4;
 }
 
 size_t bind_ws_bytes(int T, int k, int E) {
@@ -300,24 +323,32 @@ size_t bind_ws_bytes(int T, int k, int E) {
   return align_up(kmax * 2 * sizeof(int32_t) + 16, 256);
 }
 
+// Fused residency + dispatch is used when one CTA can sort the routed rows.
+bool bind_dispatch_fusable(int R, int E) { return R <= 4096 && E <= kMaxE; }
+
 cudaError_t launch_bind(const moe_cache& c, int layer, const int32_t* ids, int R,
                         uint32_t phi_q16, int min_fill, int policy, uint64_t seed,
                         moe_bind_stats* stats, int32_t* fills_opt, void* ws, uint32_t* status,
-                        cudaStream_t s, bool do_copy) {
-  static size_t attr_bytes = 0;
-  const size_t smem = bind_smem_bytes(c.cache.n_slots, c.E);
-  if (smem > attr_bytes) {
-    cudaError_t err = cudaFuncSetAttribute(bind_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+                        cudaStream_t s, bool do_copy, int32_t* counts, int32_t* offsets, int32_t* perm,
+                        int32_t* inv_perm) {
+  const bool fused = counts != nullptr;
+  size_t smem = bind_smem_bytes(c.cache.n_slots, c.E);
+  if (fused) smem = std::max(smem, (size_t)c.E * 33 * sizeof(int));
+  static size_t attr_bytes[2] = {0, 0};
+  if (smem > attr_bytes[fused]) {
+    cudaError_t err = fused ? cudaFuncSetAttribute(bind_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
+                            : cudaFuncSetAttribute(bind_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    attr_bytes = smem;
+    attr_bytes[fused] = smem;
   }
-  const int kmax = (int)std::min((long long)R, (long long)c.E);
   int32_t* n_fill = reinterpret_cast<int32_t*>(ws);
   int32_t* fills = n_fill + 4;
-  (void)kmax;
   const int np2 = next_pow2(c.cache.n_slots < 1 ? 1 : c.cache.n_slots);
-  cudaError_t err = launch_k(bind_kernel, 1, kBindThreads, smem, s, c, layer, ids, R, phi_q16, min_fill, policy,
-                             (unsigned long long)seed, np2, stats, fills, n_fill, fills_opt, status);
+  DispatchOut d = {counts, offsets, perm, inv_perm};
+  cudaError_t err = fused ? launch_k(bind_kernel<true>, 1, kBindThreads, smem, s, c, layer, ids, R, phi_q16, min_fill,
+                                     policy, (unsigned long long)seed, np2, stats, fills, n_fill, fills_opt, status, d)
+                          : launch_k(bind_kernel<false>, 1, kBindThreads, smem, s, c, layer, ids, R, phi_q16, min_fill,
+                                     policy, (unsigned long long)seed, np2, stats, fills, n_fill, fills_opt, status, d);
   if (err != cudaSuccess) return err;
   if (!do_copy || c.staging.w_gate == nullptr) return cudaSuccess;   // copy fused elsewhere / no staging pool
   const size_t bank_bytes = (size_t)c.H * c.I * sizeof(__nv_bfloat16);

@@ -15,7 +15,8 @@ ROOT = os.path.dirname(PKG)
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libmoe.so")
 SOURCES = ["moe_api.cu", "route_topk.cu", "dispatch.cu", "bind.cu", "ffn.cu", "ffn_gemv.cu",
-           "ffn_gemm.cu", "combine.cu", "ffn_noalloc.cu"]
+           "ffn_gemm.cu", "combine.cu", "ffn_noalloc.cu",
+           "front_small.cu"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 

@@ -13,118 +13,24 @@
 //    bases and the offsets, (C) one CTA per tile scatters.
 // The optional gather x_perm[pos] = x[perm[pos] / k] is a separate
 // bandwidth-bound kernel (one warp per row).
-#include "moe_common.cuh"
+#include "dispatch_block.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kTile = 1024;
+using blk::kTile;
+using blk::block_exclusive_scan;
+using blk::scatter_tile;
 constexpr int kSingleMaxR = 4096;
-
-__device__ inline unsigned lanemask_lt() {
-  unsigned m;
-  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
-  return m;
-}
-
-// Exclusive scan over a 1024-thread block; returns this thread's prefix and
-// writes the block total to *total.
-__device__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int inc = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int n = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += n;
-  }
-  if (lane == 31) warp_tot[warp] = inc;
-  __syncthreads();
-  if (warp == 0) {
-    int w = warp_tot[lane];
-    int winc = w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(0xffffffffu, winc, o);
-      if (lane >= o) winc += n;
-    }
-    warp_tot[lane] = winc - w;
-    if (lane == 31) *total = winc;
-  }
-  __syncthreads();
-  const int res = warp_tot[warp] + inc - v;
-  __syncthreads();
-  return res;
-}
-
-// Scatter one tile of rows [base, base + 1024).  cursor[e] holds the next free
-// position of expert e; wcnt is a zeroed [32][E] table (left zeroed on exit).
-__device__ void scatter_tile(const int32_t* __restrict__ ids, int R, int E, int base, int* cursor,
-                             int* wcnt, int32_t* __restrict__ perm, int32_t* __restrict__ inv_perm) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int i = base + tid;
-  const int e = (i < R) ? ids[i] : -1;
-  const bool valid = (e >= 0 && e < E);
-  const int key = valid ? e : -1;
-  const unsigned mask = __match_any_sync(0xffffffffu, key);
-  const unsigned lt = lanemask_lt();
-  const int rank = __popc(mask & lt);
-  const bool leader = (mask & lt) == 0;
-  const int nwarps = blockDim.x >> 5;
-  if (valid && leader) wcnt[warp * E + e] = __popc(mask);
-  __syncthreads();
-  int pos = 0;
-  bool last = false;
-  if (valid) {
-    int pre = 0, later = 0;
-    for (int w = 0; w < warp; ++w) pre += wcnt[w * E + e];
-    for (int w = warp + 1; w < nwarps; ++w) later += wcnt[w * E + e];
-    pos = cursor[e] + pre + rank;
-    last = (later == 0) && (rank == __popc(mask) - 1);
-    perm[pos] = i;
-    inv_perm[i] = pos;
-  }
-  __syncthreads();
-  if (valid && last) cursor[e] = pos + 1;
-  if (valid && leader) wcnt[warp * E + e] = 0;
-  __syncthreads();
-}
 
 __global__ void __launch_bounds__(kTile)
 dispatch_single_kernel(const int32_t* __restrict__ ids, int R, int E, int32_t* __restrict__ counts,
                        int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
                        int32_t* __restrict__ inv_perm, uint32_t* status) {
   extern __shared__ int sm[];
-  int* cursor = sm;              // [E]
-  int* wcnt = cursor + E;        // [32][E]
-  __shared__ int warp_tot[32];
-  __shared__ int total;
-  const int tid = threadIdx.x;
   pdl_wait();
   pdl_trigger();
-  for (int j = tid; j < E * 33; j += kTile) sm[j] = 0;
-  __syncthreads();
-  bool bad = false;
-  for (int i = tid; i < R; i += kTile) {
-    const int e = ids[i];
-    if (e >= 0 && e < E) atomicAdd(&cursor[e], 1);
-    else bad = true;
-  }
-  if (bad) set_status(status, MOE_DEV_ERR_BAD_ID);
-  __syncthreads();
-  for (int e0 = 0; e0 < E; e0 += kTile) {
-    // E <= 1024 = kTile: one pass
-    const int e = e0 + tid;
-    const int c = (e < E) ? cursor[e] : 0;
-    const int off = block_exclusive_scan(c, warp_tot, &total);
-    if (e < E) {
-      counts[e] = c;
-      offsets[e] = off;
-      cursor[e] = off;
-    }
-    if (tid == 0) offsets[E] = total;
-  }
-  __syncthreads();
-  for (int base = 0; base < R; base += kTile) scatter_tile(ids, R, E, base, cursor, wcnt, perm, inv_perm);
+  blk::dispatch_block(ids, R, E, counts, offsets, perm, inv_perm, status, sm);
 }
 
 __global__ void __launch_bounds__(kTile)
@@ -249,12 +155,14 @@ cudaError_t launch_dispatch(const int32_t* ids, int R, int k, int E, int32_t* co
       err = launch_k(tile_scatter_kernel, ntiles, kTile, need, s, ids, R, E, (const int32_t*)tile_counts, perm, inv_perm);
   }
   if (err != cudaSuccess) return err;
-  if (x && x_perm && R > 0) {
-    const int blocks = (R + 7) / 8;
-    err = launch_k(gather_rows_kernel, blocks, 256, 0, s, x, R / k, H, k, (const int32_t*)perm,
-                   (const int32_t*)offsets, E, R, x_perm);
-  }
+  if (x && x_perm && R > 0) err = launch_gather(x, H, k, perm, offsets, E, R, x_perm, s);
   return err;
+}
+
+cudaError_t launch_gather(const __nv_bfloat16* x, int H, int k, const int32_t* perm, const int32_t* offsets, int E,
+                          int R, __nv_bfloat16* x_perm, cudaStream_t s) {
+  const int blocks = (R + 7) / 8;
+  return launch_k(gather_rows_kernel, blocks, 256, 0, s, x, R / k, H, k, perm, offsets, E, R, x_perm);
 }
 
 }  // namespace moe

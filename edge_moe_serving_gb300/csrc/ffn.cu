@@ -12,14 +12,14 @@ size_t ffn_ws_bytes(int T, int k, int E, int H, int I, int mode) {
   (void)H;
   (void)mode;
   const size_t R = (size_t)T * k;
-  return align_up(R * I * sizeof(__nv_bfloat16), 256) + 256;   // h, then the grid-barrier word
+  return align_up(R * I * sizeof(__nv_bfloat16), 256) + 256;   // h, then the grid-barrier words
 }
 
 cudaError_t launch_ffn(const moe_cache& c, int layer, const int32_t* counts, const int32_t* offsets,
                        const int32_t* perm, const __nv_bfloat16* x, const __nv_bfloat16* x_perm,
                        int T, int k, const uint8_t* mask, int mode, float* y_rows, void* ws,
                        uint32_t* status, cudaStream_t s, const int32_t* fused_fills,
-                       const int32_t* fused_n_fill) {
+                       const int32_t* fused_n_fill, const float* combine_w, __nv_bfloat16* combine_out) {
   if (T == 0) return cudaSuccess;
   const int R = T * k;
   __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(ws);
@@ -31,8 +31,9 @@ cudaError_t launch_ffn(const moe_cache& c, int layer, const int32_t* counts, con
   } else if (mode == MOE_FFN_AUTO && x_perm && gemm_shape_ok(c.H, c.I) && T > kGemvMaxRows) {
     gemv_max = kGemvMaxRows;
   }
-  // a fused fill is only done by the GEMV kernels
-  if (fused_fills != nullptr && gemv_max != INT_MAX) return cudaErrorNotSupported;
+  // a fused fill or combine is only done by the fused GEMV kernel
+  if ((fused_fills != nullptr || combine_out != nullptr) && gemv_max != INT_MAX) return cudaErrorNotSupported;
+  if (combine_out != nullptr && !gemv_fused_ok(c.H, c.I)) return cudaErrorNotSupported;
   if (gemv_max > 0) {
     GemvParams p;
     p.c = c;
@@ -54,6 +55,8 @@ cudaError_t launch_ffn(const moe_cache& c, int layer, const int32_t* counts, con
     p.status = status;
     p.fills = fused_fills;
     p.n_fill = fused_n_fill;
+    p.combine_w = combine_w;
+    p.combine_out = combine_out;
     p.grid_count = reinterpret_cast<unsigned int*>(reinterpret_cast<char*>(ws) +
                                                    align_up((size_t)R * c.I * sizeof(__nv_bfloat16), 256));
     cudaError_t err = launch_gemv(p, s);

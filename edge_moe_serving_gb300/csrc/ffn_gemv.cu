@@ -613,8 +613,50 @@ gemv_fused_kernel(GemvParams p, unsigned int* grid_count) {
       volatile int no_abort = 0;
       for (int q = st.armed_last; q >= 0 && q > st.armed_last - kRingStages; --q)
         ring_wait(&full_bar[q % kRingStages], (uint32_t)(q / kRingStages) & 1u, &no_abort);
-    } else if (st.stored && lane == 0) {
-      bulk_wait_all();   // fused-fill writes complete before exit
+    } else {
+      if (st.stored && lane == 0) bulk_wait_all();   // fused-fill writes complete before exit
+      if (p.combine_out != nullptr) {
+        // second grid-wide barrier: every y row is written; then the gate-weighted
+        // combine in fixed expert order, spread over all CTAs
+        __threadfence();
+        asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+        if (tid == 0) {
+          __threadfence();
+          atomicAdd(grid_count + 1, 1u);
+          const unsigned long long t0 = gtimer();
+          while (*reinterpret_cast<volatile unsigned int*>(grid_count + 1) < gridDim.x) {
+            if (*abort_flag) break;
+            if (gtimer() - t0 > kGridWaitNs) {
+              *abort_flag = 1;
+              break;
+            }
+          }
+          __threadfence();
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+        if (!*abort_flag) {
+          const int H4 = p.H >> 2;
+          const int items = p.T * H4;
+          for (int it = blockIdx.x * (kConsumerWarps * 32) + tid; it < items; it += gridDim.x * (kConsumerWarps * 32)) {
+            const int t = it / H4, c4 = it - t * H4;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int jj = 0; jj < p.k; ++jj) {
+              const float w = p.combine_w[t * p.k + jj];
+              const float4 y = __ldcg(reinterpret_cast<const float4*>(p.y + (size_t)(t * p.k + jj) * p.H) + c4);
+              acc.x = fmaf(w, y.x, acc.x);
+              acc.y = fmaf(w, y.y, acc.y);
+              acc.z = fmaf(w, y.z, acc.z);
+              acc.w = fmaf(w, y.w, acc.w);
+            }
+            __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+            uint2 packed;
+            packed.x = *reinterpret_cast<uint32_t*>(&lo);
+            packed.y = *reinterpret_cast<uint32_t*>(&hi);
+            reinterpret_cast<uint2*>(p.combine_out + (size_t)t * p.H)[c4] = packed;
+          }
+        }
+      }
     }
   }
   pdl_trigger();
@@ -633,7 +675,7 @@ cudaError_t launch_fused_one(const GemvParams& p, unsigned int* grid_count, cuda
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  cudaError_t err = cudaMemsetAsync(grid_count, 0, sizeof(unsigned int), s);
+  cudaError_t err = cudaMemsetAsync(grid_count, 0, 2 * sizeof(unsigned int), s);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms());
@@ -690,8 +732,7 @@ cudaError_t launch_gemv_nt(const GemvParams& p, cudaStream_t s) {
 // Row lengths that are multiples of 256 take the fused TMA-ring kernel.
 cudaError_t launch_gemv(const GemvParams& p, cudaStream_t s) {
   const int bound = std::min(p.T, p.max_rows);
-  // a unit (one gate row + one up row, or one down row) must fit one 16 KB stage
-  if (p.H % 256 == 0 && p.I % 256 == 0 && 2 * p.H * 2 <= kUnitBytes && p.I * 2 <= kUnitBytes) {
+  if (gemv_fused_ok(p.H, p.I)) {
     unsigned int* grid_count = p.grid_count;
     if (bound <= 1) return launch_ring_nt<1>(p, grid_count, s);
     if (bound <= 2) return launch_ring_nt<2>(p, grid_count, s);

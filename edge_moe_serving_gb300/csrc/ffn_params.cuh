@@ -22,8 +22,12 @@ struct GemvParams {
   // are read from the staging pool and written to their cache slot on the fly.
   const int32_t* fills;     // [n][2]: (staging slot l*E+e, cache slot)
   const int32_t* n_fill;    // device count of valid rows of `fills`
-  unsigned int* grid_count; // workspace word for the fused kernel's grid barrier
+  unsigned int* grid_count; // workspace words for the fused kernel's grid barriers
+  // Fused combine (optional): out[t] = sum_j combine_w[t*k+j] * y[t*k+j] after the FFN.
+  const float* combine_w;
+  __nv_bfloat16* combine_out;
 };
+
 
 cudaError_t launch_gemv(const GemvParams& p, cudaStream_t s);
 

@@ -258,38 +258,64 @@ int moe_layer_forward(const moe_layer* layer, const moe_cache* cache, const void
   if (!ws || ws_bytes < need.bytes) return MOE_ERR_WORKSPACE;
   const LayerWs L = layer_ws(ws, bufs_opt, T, k, E, H, I, ffn_mode);
   const size_t scratch_bytes = ws_bytes - (size_t)(reinterpret_cast<char*>(L.scratch) - reinterpret_cast<char*>(ws));
+  const bool fuse_fill = ffn_mode != MOE_FFN_GEMM && !L.x_perm && gemv_fused_ok(H, I);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (fuse_fill && T <= 32 && E <= kMaxRouteE && front_small_ok(T, k, E, cache->cache.n_slots) &&
+      k <= kMaxK && layer->w_router && aligned16(x) && aligned16(layer->w_router)) {
+    // Decode: router logits over all SMs, then one warp selects, binds and
+    // dispatches, then one fused FFN launch (gate/up, down, fills, combine).
+    st = check_bind_args(cache, layer->layer, T, k, phi_q16, fill_policy);
+    if (st != MOE_OK) return st;
+    float* logits = reinterpret_cast<float*>(L.scratch);
+    if (launch_route_logits(reinterpret_cast<const __nv_bfloat16*>(x), T, H, layer->w_router, layer->bias, E, logits,
+                            s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    if (launch_front_small(logits, T, k, *cache, layer->layer, phi_q16, min_fill, fill_policy, seed, stats_dev, L.ids,
+                           L.w, L.counts, L.offsets, L.perm, L.inv_perm, L.bind_ws, dev_status, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    const int32_t* n_fill = reinterpret_cast<const int32_t*>(L.bind_ws);
+    cudaError_t err = launch_ffn(*cache, layer->layer, L.counts, L.offsets, L.perm,
+                                 reinterpret_cast<const __nv_bfloat16*>(x), nullptr, T, k, nullptr, ffn_mode, L.y_rows,
+                                 L.scratch, dev_status, s, n_fill + 4, n_fill, L.w,
+                                 reinterpret_cast<__nv_bfloat16*>(out));
+    return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  }
   st = moe_route_topk(x, T, H, layer->w_router, layer->bias, E, k, L.ids, L.w, nullptr, L.scratch, scratch_bytes,
                       dev_status, stream);
   if (st != MOE_OK) return st;
-  // Decode-sized calls run every group on the GEMV kernels, which copy each
-  // admitted expert into its cache slot while they stream it (one read of the
-  // staging copy instead of two); other calls copy in the bind step.
-  const bool fuse_fill = ffn_mode != MOE_FFN_GEMM && !L.x_perm;
-  if (fuse_fill) {
-    st = check_bind_args(cache, layer->layer, T, k, phi_q16, fill_policy);
-    if (st != MOE_OK) return st;
-    if (cuda_status(launch_bind(*cache, layer->layer, L.ids, T * k, phi_q16, min_fill, fill_policy, seed, stats_dev,
-                                nullptr, L.bind_ws, dev_status, reinterpret_cast<cudaStream_t>(stream), false)) != MOE_OK)
-      return MOE_ERR_CUDA;
-  } else {
-    st = moe_cache_bind_slots(cache, layer->layer, L.ids, T, k, phi_q16, min_fill, fill_policy, seed, stats_dev,
-                              nullptr, L.bind_ws, bind_ws_bytes(T, k, E), dev_status, stream);
-    if (st != MOE_OK) return st;
-  }
-  st = moe_dispatch(L.ids, T, k, E, L.counts, L.offsets, L.perm, L.inv_perm, L.x_perm ? x : nullptr, H, L.x_perm,
-                    L.scratch, scratch_bytes, dev_status, stream);
+  // Decode-sized calls run every group on the fused GEMV kernel, which copies
+  // each admitted expert into its cache slot while it streams it (one read of
+  // the staging copy instead of two) and ends with the combine; other calls
+  // copy in the bind step and combine in their own launch.  Calls with few
+  // enough routed rows get the dispatch in the bind launch.
+  const int R = T * k;
+  const bool fuse_dispatch = bind_dispatch_fusable(R, E);
+  st = check_bind_args(cache, layer->layer, T, k, phi_q16, fill_policy);
   if (st != MOE_OK) return st;
+  if (launch_bind(*cache, layer->layer, L.ids, R, phi_q16, min_fill, fill_policy, seed, stats_dev, nullptr,
+                  L.bind_ws, dev_status, s, !fuse_fill, fuse_dispatch ? L.counts : nullptr, L.offsets, L.perm,
+                  L.inv_perm) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (!fuse_dispatch) {
+    st = moe_dispatch(L.ids, T, k, E, L.counts, L.offsets, L.perm, L.inv_perm, L.x_perm ? x : nullptr, H, L.x_perm,
+                      L.scratch, scratch_bytes, dev_status, stream);
+    if (st != MOE_OK) return st;
+  } else if (L.x_perm) {
+    if (launch_gather(reinterpret_cast<const __nv_bfloat16*>(x), H, k, L.perm, L.offsets, E, R, L.x_perm, s) !=
+        cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
   if (fuse_fill) {
     const int32_t* n_fill = reinterpret_cast<const int32_t*>(L.bind_ws);
     cudaError_t err = launch_ffn(*cache, layer->layer, L.counts, L.offsets, L.perm,
                                  reinterpret_cast<const __nv_bfloat16*>(x), nullptr, T, k, nullptr, ffn_mode, L.y_rows,
-                                 L.scratch, dev_status, reinterpret_cast<cudaStream_t>(stream), n_fill + 4, n_fill);
-    if (err != cudaSuccess) return MOE_ERR_CUDA;
-  } else {
-    st = moe_expert_ffn_grouped(cache, layer->layer, L.counts, L.offsets, L.perm, x, L.x_perm, T, k, nullptr,
-                                ffn_mode, L.y_rows, L.scratch, scratch_bytes, dev_status, stream);
-    if (st != MOE_OK) return st;
+                                 L.scratch, dev_status, s, n_fill + 4, n_fill, L.w,
+                                 reinterpret_cast<__nv_bfloat16*>(out));
+    return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
   }
+  st = moe_expert_ffn_grouped(cache, layer->layer, L.counts, L.offsets, L.perm, x, L.x_perm, T, k, nullptr, ffn_mode,
+                              L.y_rows, L.scratch, scratch_bytes, dev_status, stream);
+  if (st != MOE_OK) return st;
   return moe_combine(L.y_rows, L.w, T, k, H, out, nullptr, dev_status, stream);
 }
 

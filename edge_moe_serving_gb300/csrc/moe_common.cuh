@@ -18,6 +18,12 @@ constexpr int kGemvMaxRows = 2;       // AUTO mode: groups up to this size use t
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// The fused TMA-ring GEMV handles row lengths that are multiples of 256 whose
+// units (one gate row + one up row, or one down row) fit a 16 KB stage.
+inline bool gemv_fused_ok(int H, int I) {
+  return H % 256 == 0 && I % 256 == 0 && 2 * H * 2 <= 16384 && I * 2 <= 16384;
+}
+
 // ---------------------------------------------------------------- launch chaining
 // Every kernel of the library is launched with programmatic stream
 // serialization: the next kernel on the stream may start its prologue while
@@ -122,6 +128,13 @@ cudaError_t launch_route_topk(const __nv_bfloat16* x, int T, int H, const float*
                               const float* bias, int E, int k, int32_t* topk_ids, float* topk_w,
                               float* logits_opt, void* ws, uint32_t* status, cudaStream_t s);
 size_t route_ws_bytes(int T, int E);
+cudaError_t launch_route_logits(const __nv_bfloat16* x, int T, int H, const float* w_router, const float* bias,
+                                int E, float* logits, cudaStream_t s);
+bool front_small_ok(int T, int k, int E, int n_slots);
+cudaError_t launch_front_small(const float* logits, int T, int k, const moe_cache& c, int layer, uint32_t phi_q16,
+                               int min_fill, int policy, uint64_t seed, moe_bind_stats* stats, int32_t* topk_ids,
+                               float* topk_w, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv_perm,
+                               void* bind_ws, uint32_t* status, cudaStream_t s);
 
 size_t dispatch_ws_bytes(int T, int k, int E);
 cudaError_t launch_dispatch(const int32_t* ids, int R, int k, int E, int32_t* counts,
@@ -129,21 +142,28 @@ cudaError_t launch_dispatch(const int32_t* ids, int R, int k, int E, int32_t* co
                             const __nv_bfloat16* x, int H, __nv_bfloat16* x_perm, void* ws,
                             uint32_t* status, cudaStream_t s);
 
+cudaError_t launch_gather(const __nv_bfloat16* x, int H, int k, const int32_t* perm, const int32_t* offsets, int E,
+                          int R, __nv_bfloat16* x_perm, cudaStream_t s);
+
 size_t bind_ws_bytes(int T, int k, int E);
 size_t bind_smem_bytes(int n_slots, int E);
 // ws holds the fill count (int32 at offset 0) and the fill list (from int32 offset 4).
 // do_copy = false leaves the copy to a fused-fill FFN launch.
+// counts != nullptr: the same single-CTA launch also does the dispatch (R <= 4096).
+bool bind_dispatch_fusable(int R, int E);
 cudaError_t launch_bind(const moe_cache& c, int layer, const int32_t* ids, int R,
                         uint32_t phi_q16, int min_fill, int policy, uint64_t seed,
                         moe_bind_stats* stats, int32_t* fills_opt, void* ws, uint32_t* status,
-                        cudaStream_t s, bool do_copy = true);
+                        cudaStream_t s, bool do_copy = true, int32_t* counts = nullptr,
+                        int32_t* offsets = nullptr, int32_t* perm = nullptr, int32_t* inv_perm = nullptr);
 
 size_t ffn_ws_bytes(int T, int k, int E, int H, int I, int mode);
 cudaError_t launch_ffn(const moe_cache& c, int layer, const int32_t* counts, const int32_t* offsets,
                        const int32_t* perm, const __nv_bfloat16* x, const __nv_bfloat16* x_perm,
                        int T, int k, const uint8_t* mask, int mode, float* y_rows, void* ws,
                        uint32_t* status, cudaStream_t s, const int32_t* fused_fills = nullptr,
-                       const int32_t* fused_n_fill = nullptr);
+                       const int32_t* fused_n_fill = nullptr, const float* combine_w = nullptr,
+                       __nv_bfloat16* combine_out = nullptr);
 
 cudaError_t launch_combine(const float* y_rows, const float* topk_w, int T, int k, int H,
                            __nv_bfloat16* out, float* out_f32, uint32_t* status, cudaStream_t s);

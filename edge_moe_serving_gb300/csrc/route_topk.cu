@@ -80,7 +80,8 @@ __device__ void warp_topk(const float* row, int E, int k, int32_t* ids_out, floa
 }
 
 // ---------------------------------------------------------------- decode path
-template <int NT>
+// TOPK = false: only the logits are written (the decode front end selects).
+template <int NT, bool TOPK>
 __global__ void __launch_bounds__(kSmallThreads)
 route_small_kernel(const __nv_bfloat16* __restrict__ x, int T, int H,
                    const float* __restrict__ w_router, const float* __restrict__ bias, int E,
@@ -128,6 +129,7 @@ route_small_kernel(const __nv_bfloat16* __restrict__ x, int T, int H,
     }
     __syncthreads();
   }
+  if (!TOPK) return;
   // last CTA to finish runs the top-k for every token
   __threadfence();
   if (tid == 0) {
@@ -265,12 +267,12 @@ cudaError_t launch_route_topk(const __nv_bfloat16* x, int T, int H, const float*
     cudaError_t err = cudaMemsetAsync(ticket, 0, sizeof(unsigned int), s);
     if (err != cudaSuccess) return err;
     if (T <= 1)
-      return launch_k(route_small_kernel<1>, E, kSmallThreads, 0, s, x, T, H, w_router, bias, E, k, logits, ticket,
-                      topk_ids, topk_w);
+      return launch_k(route_small_kernel<1, true>, E, kSmallThreads, 0, s, x, T, H, w_router, bias, E, k, logits,
+                      ticket, topk_ids, topk_w);
     if (T <= 4)
-      return launch_k(route_small_kernel<4>, E, kSmallThreads, 0, s, x, T, H, w_router, bias, E, k, logits, ticket,
-                      topk_ids, topk_w);
-    return launch_k(route_small_kernel<8>, E, kSmallThreads, 0, s, x, T, H, w_router, bias, E, k, logits, ticket,
+      return launch_k(route_small_kernel<4, true>, E, kSmallThreads, 0, s, x, T, H, w_router, bias, E, k, logits,
+                      ticket, topk_ids, topk_w);
+    return launch_k(route_small_kernel<8, true>, E, kSmallThreads, 0, s, x, T, H, w_router, bias, E, k, logits, ticket,
                     topk_ids, topk_w);
   }
   const size_t smem = large_smem(E);
@@ -284,6 +286,19 @@ cudaError_t launch_route_topk(const __nv_bfloat16* x, int T, int H, const float*
   const int grid = (T + kLT - 1) / kLT;
   return launch_k(route_large_kernel, grid, kLThreads, smem, s, x, T, H, w_router, bias, E, k, logits_opt, topk_ids,
                   topk_w);
+}
+
+// Logits only, T <= 32 (the decode front end does the selection).
+cudaError_t launch_route_logits(const __nv_bfloat16* x, int T, int H, const float* w_router, const float* bias,
+                                int E, float* logits, cudaStream_t s) {
+  if (T <= 1)
+    return launch_k(route_small_kernel<1, false>, E, kSmallThreads, 0, s, x, T, H, w_router, bias, E, 1, logits,
+                    (unsigned int*)nullptr, (int32_t*)nullptr, (float*)nullptr);
+  if (T <= 4)
+    return launch_k(route_small_kernel<4, false>, E, kSmallThreads, 0, s, x, T, H, w_router, bias, E, 1, logits,
+                    (unsigned int*)nullptr, (int32_t*)nullptr, (float*)nullptr);
+  return launch_k(route_small_kernel<8, false>, E, kSmallThreads, 0, s, x, T, H, w_router, bias, E, 1, logits,
+                  (unsigned int*)nullptr, (int32_t*)nullptr, (float*)nullptr);
 }
 
 }  // namespace moe
