@@ -189,14 +189,7 @@ def run_ours(args, rank, world):
     total_s = sum(step_ms) / 1e3
     dev_status = int(status.cpu().numpy().view(np.uint32)[0])
 
-    # max over ranks
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_s], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_s = float(t.item())
-    tokens_per_step = T * (1 if decode_like else 1)
-    value = world * args.steps * tokens_per_step / total_s
+    total_s, value = aggregate_replicas(total_s, args.steps, T, world, dev)
 
     # ---- dominant kernel: the expert FFN call, events on its stream (eager pass)
     roof = measure_ffn_roofline(cfg, dc, layers, xs, decode_like, stream, peaks, args, moe, torch)
@@ -220,6 +213,20 @@ def run_ours(args, rank, world):
         "gpu_launches": launches_per_call * cfg.n_layers * args.steps,
     }
     return result
+
+
+def aggregate_replicas(local_s, steps, tokens_per_step, world, device="cpu"):
+    """Whole-job throughput of N independent replicas (no data-path exchange):
+    every rank processes `steps` steps of `tokens_per_step` tokens; the job time
+    is the slowest rank's (max over ranks).  Returns (job seconds, tokens/s)."""
+    job_s = local_s
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([local_s], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        job_s = float(t.item())
+    return job_s, world * steps * tokens_per_step / job_s
 
 
 def kernels_per_call(cfg):

@@ -66,6 +66,7 @@ def _load():
     sig = {
         "moe_version": (c_int, []),
         "moe_status_string": (c_char_p, [c_int]),
+        "moe_check_bounded_wait": (c_int, [P, P]),
         "moe_route_topk_workspace_size": (c_size_t, [c_int, c_int]),
         "moe_route_topk": (c_int, [P, c_int, c_int, P, P, c_int, c_int, P, P, P, P, c_size_t, P, P]),
         "moe_dispatch_workspace_size": (c_size_t, [c_int, c_int, c_int]),
@@ -92,7 +93,8 @@ def _load():
 
 
 _lib = _load()
-EXPORTED = ["moe_version", "moe_status_string", "moe_route_topk_workspace_size", "moe_route_topk",
+EXPORTED = ["moe_version", "moe_status_string", "moe_check_bounded_wait", "moe_route_topk_workspace_size",
+            "moe_route_topk",
             "moe_dispatch_workspace_size", "moe_dispatch", "moe_cache_bind_workspace_size",
             "moe_cache_bind_slots", "moe_expert_ffn_workspace_size", "moe_expert_ffn_grouped",
             "moe_expert_ffn_grouped_noalloc", "moe_combine",
@@ -132,6 +134,10 @@ def moe_version():
 
 def moe_status_string(status):
     return _lib.moe_status_string(status).decode()
+
+
+def moe_check_bounded_wait(dev_status, stream=None):
+    return _check("moe_check_bounded_wait", _lib.moe_check_bounded_wait(_p(dev_status), _s(stream)))
 
 
 def moe_route_topk_workspace_size(T, E):

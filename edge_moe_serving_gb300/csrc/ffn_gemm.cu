@@ -43,7 +43,6 @@ constexpr int kStageBytes = 2 * kATile + kBBytes;   // 64 KB
 constexpr int kSmemBytes = kStages * kStageBytes + 1024;
 constexpr int kThreads = 192;
 constexpr int kTmemCols = 512;
-constexpr unsigned long long kWaitNs = 1000000000ull;   // bounded waits: 1 s
 
 struct GemmParams {
   const int32_t* counts;
@@ -86,32 +85,8 @@ __device__ inline void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-__device__ inline bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait for the phase of `bar` with the given parity.  Returns false
-// when the CTA aborted (here or elsewhere).
 __device__ inline bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-  unsigned long long start = 0;
-  for (uint32_t it = 0;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63) == 63) {
-      if (*abort_flag) return false;
-      const unsigned long long now = globaltimer();
-      if (start == 0) start = now;
-      else if (now - start > kWaitNs) {
-        *abort_flag = 1;
-        return false;
-      }
-    }
-  }
+  return bounded_wait(bar, parity, abort_flag);
 }
 
 __device__ inline void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1) {

@@ -241,7 +241,6 @@ constexpr int kConsumerWarps = 6;
 // divides the stage count.
 static_assert(kRingStages % kConsumerWarps == 0, "each ring stage must have one consumer warp");
 constexpr int kRingThreads = (kConsumerWarps + 1) * 32;
-constexpr unsigned long long kRingWaitNs = 1000000000ull;
 
 __device__ inline uint32_t smem_addr(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
 
@@ -251,30 +250,8 @@ __device__ inline unsigned long long gtimer() {
   return t;
 }
 
-__device__ inline bool ring_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 __device__ inline bool ring_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-  unsigned long long start = 0;
-  for (uint32_t it = 0;; ++it) {
-    if (ring_try_wait(bar, parity)) return true;
-    if ((it & 63) == 63) {
-      if (*abort_flag) return false;
-      const unsigned long long now = gtimer();
-      if (start == 0) start = now;
-      else if (now - start > kRingWaitNs) {
-        *abort_flag = 1;
-        return false;
-      }
-    }
-  }
+  return bounded_wait(bar, parity, abort_flag);
 }
 
 __device__ inline void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {

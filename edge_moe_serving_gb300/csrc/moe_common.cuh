@@ -50,6 +50,46 @@ inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, siz
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// ---------------------------------------------------------------- bounded waits
+// Every wait of a pipelined kernel on an mbarrier goes through bounded_wait:
+// it gives up after about one second of %globaltimer, raises the CTA's abort
+// flag and returns false; the caller then winds down (drains its copies,
+// frees TMEM) and the kernel reports MOE_DEV_ERR_TIMEOUT.
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+
+__device__ inline unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ inline bool mbar_try_wait_parity(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  const uint32_t addr = static_cast<uint32_t>(__cvta_generic_to_shared(bar));
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ inline bool bounded_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  unsigned long long start = 0;
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait_parity(bar, parity)) return true;
+    if ((it & 63) == 63) {
+      if (*abort_flag) return false;
+      const unsigned long long now = globaltimer_ns();
+      if (start == 0) start = now;
+      else if (now - start > kWaitLimitNs) {
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------- device status
 __device__ inline void set_status(uint32_t* status, uint32_t bit) {
   if (status) atomicOr(status, bit);

@@ -144,6 +144,13 @@ typedef struct moe_layer_buffers {
 int moe_version(void);
 const char* moe_status_string(int status);
 
+/* Diagnostic of the failure path of the pipelined kernels (no counterpart in
+ * the paper): one launch waits, with the same bounded wait the expert-FFN
+ * kernels use, on a barrier that nothing completes; after the wait limit
+ * (about one second) it ORs MOE_DEV_ERR_TIMEOUT into *dev_status and returns.
+ * The context stays usable. */
+int moe_check_bounded_wait(uint32_t* dev_status, moe_stream_t stream);
+
 /* ---------------------------------------------------------------- router
  * Router scoring and top-k with renormalisation ([P] section 3.2: at each
  * MoE layer the router runs on the GPU and selects the active experts).
