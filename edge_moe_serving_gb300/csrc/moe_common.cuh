@@ -134,6 +134,11 @@ __device__ inline float warp_sum(float v) {
 
 __device__ inline float silu(float g) { return g / (1.0f + expf(-g)); }
 
+// silu with CUDA's fast exponential and division intrinsics, for epilogues
+// whose result is rounded to bf16.  As g -> -inf the divisor overflows and the
+// intrinsic division returns 0, the limit of silu.
+__device__ inline float silu_fast(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+
 // Slot-table decoding: returns the bank base row pointer set for (pool, slot),
 // or false when the entry is unbound or out of range.
 struct BankSet {
