@@ -10,7 +10,7 @@ package fails loudly when the library is missing.
 import ctypes
 import os
 
-from ctypes import c_int, c_int32, c_uint32, c_uint64, c_size_t, c_void_p, c_char_p, POINTER
+from ctypes import c_int, c_int32, c_uint32, c_uint64, c_ulonglong, c_size_t, c_void_p, c_char_p, POINTER
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe.so")
@@ -67,7 +67,8 @@ def _load():
         "moe_version": (c_int, []),
         "moe_status_string": (c_char_p, [c_int]),
         "moe_check_bounded_wait": (c_int, [P, P]),
-        "moe_route_topk_workspace_size": (c_size_t, [c_int, c_int]),
+        "moe_kernel_launch_count": (c_ulonglong, []),
+        "moe_route_topk_workspace_size": (c_size_t, [c_int, c_int, c_int]),
         "moe_route_topk": (c_int, [P, c_int, c_int, P, P, c_int, c_int, P, P, P, P, c_size_t, P, P]),
         "moe_dispatch_workspace_size": (c_size_t, [c_int, c_int, c_int]),
         "moe_dispatch": (c_int, [P, c_int, c_int, c_int, P, P, P, P, P, c_int, P, P, c_size_t, P, P]),
@@ -93,7 +94,7 @@ def _load():
 
 
 _lib = _load()
-EXPORTED = ["moe_version", "moe_status_string", "moe_check_bounded_wait", "moe_route_topk_workspace_size",
+EXPORTED = ["moe_version", "moe_status_string", "moe_check_bounded_wait", "moe_kernel_launch_count", "moe_route_topk_workspace_size",
             "moe_route_topk",
             "moe_dispatch_workspace_size", "moe_dispatch", "moe_cache_bind_workspace_size",
             "moe_cache_bind_slots", "moe_expert_ffn_workspace_size", "moe_expert_ffn_grouped",
@@ -140,8 +141,12 @@ def moe_check_bounded_wait(dev_status, stream=None):
     return _check("moe_check_bounded_wait", _lib.moe_check_bounded_wait(_p(dev_status), _s(stream)))
 
 
-def moe_route_topk_workspace_size(T, E):
-    return _lib.moe_route_topk_workspace_size(T, E)
+def moe_kernel_launch_count():
+    return int(_lib.moe_kernel_launch_count())
+
+
+def moe_route_topk_workspace_size(T, H, E):
+    return _lib.moe_route_topk_workspace_size(T, H, E)
 
 
 def moe_route_topk(x, T, H, w_router, bias, E, k, topk_ids, topk_w, logits_opt, ws, ws_bytes, dev_status,

@@ -664,7 +664,7 @@ cudaError_t launch_fused_one(const GemvParams& p, unsigned int* grid_count, cuda
   attrs[0].val.cooperative = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemv_fused_kernel<NT, VA, VB>, p, grid_count);
+  return counted(cudaLaunchKernelEx(&cfg, gemv_fused_kernel<NT, VA, VB>, p, grid_count));
 }
 
 // Single-token calls with rows of 4096 (gate/up) and 2048 (down) elements,

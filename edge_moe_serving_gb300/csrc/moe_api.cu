@@ -114,7 +114,7 @@ LayerWs layer_ws(void* ws, const moe_layer_buffers* b, int T, int k, int E, int 
     if (b->inv_perm) L.inv_perm = b->inv_perm;
     if (b->y_rows) L.y_rows = b->y_rows;
   }
-  const size_t scratch = std::max({route_ws_bytes(T, E), dispatch_ws_bytes(T, k, E),
+  const size_t scratch = std::max({route_ws_bytes(T, H, E), dispatch_ws_bytes(T, k, E),
                                    ffn_ws_bytes(T, k, E, H, I, mode)});
   L.scratch = cv.take<char>(scratch);
   L.bytes = cv.off;
@@ -130,6 +130,8 @@ extern "C" {
 
 int moe_version(void) { return kVersion; }
 
+unsigned long long moe_kernel_launch_count(void) { return launch_counter().load(std::memory_order_relaxed); }
+
 const char* moe_status_string(int status) {
   switch (status) {
     case MOE_OK: return "ok";
@@ -141,9 +143,9 @@ const char* moe_status_string(int status) {
   }
 }
 
-size_t moe_route_topk_workspace_size(int T, int E) {
-  if (T < 0 || E < 1) return 0;
-  return route_ws_bytes(T, E);
+size_t moe_route_topk_workspace_size(int T, int H, int E) {
+  if (T < 0 || H < 1 || E < 1) return 0;
+  return route_ws_bytes(T, H, E);
 }
 
 int moe_route_topk(const void* x, int T, int H, const float* w_router, const float* bias, int E, int k,
@@ -153,7 +155,7 @@ int moe_route_topk(const void* x, int T, int H, const float* w_router, const flo
   if (T == 0) return MOE_OK;
   if (!x || !w_router || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
   if (E > kMaxRouteE || (H % 8) || !aligned16(x) || !aligned16(w_router)) return MOE_ERR_UNSUPPORTED;
-  const size_t need = route_ws_bytes(T, E);
+  const size_t need = route_ws_bytes(T, H, E);
   if (need && (!ws || ws_bytes < need)) return MOE_ERR_WORKSPACE;
   return cuda_status(launch_route_topk(reinterpret_cast<const __nv_bfloat16*>(x), T, H, w_router, bias, E, k,
                                        topk_ids, topk_w, logits_opt, ws, dev_status,

@@ -1,6 +1,8 @@
 // Shared device helpers and internal launch declarations of libmoe.
 #pragma once
 
+#include <atomic>
+
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -34,6 +36,18 @@ inline bool gemv_fused_ok(int H, int I) {
 __device__ inline void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ inline void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Kernels this library has launched or captured into a graph in this process
+// (host-side count, one per launch call that the runtime accepted).
+inline std::atomic<unsigned long long>& launch_counter() {
+  static std::atomic<unsigned long long> n{0};
+  return n;
+}
+
+inline cudaError_t counted(cudaError_t e) {
+  if (e == cudaSuccess) launch_counter().fetch_add(1, std::memory_order_relaxed);
+  return e;
+}
+
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                             Args&&... args) {
@@ -47,7 +61,7 @@ inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, siz
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+  return counted(cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...));
 }
 
 // ---------------------------------------------------------------- bounded waits
@@ -139,6 +153,66 @@ __device__ inline float silu(float g) { return g / (1.0f + expf(-g)); }
 // intrinsic division returns 0, the limit of silu.
 __device__ inline float silu_fast(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
+// One warp selects the top-k of one token's logits (E <= 512) and writes
+// ascending ids with softmax weights renormalised over the selection.
+__device__ inline void warp_topk(const float* row, int E, int k, int32_t* ids_out, float* w_out) {
+  const int lane = threadIdx.x & 31;
+  constexpr int kPer = kMaxRouteE / 32;
+  float v[kPer];
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int e = lane + 32 * j;
+    v[j] = (e < E) ? row[e] : -INFINITY;
+  }
+  uint32_t taken = 0;
+  float sel_v = -INFINITY;
+  int sel_id = 0x7fffffff;
+  for (int r = 0; r < k; ++r) {
+    // best untaken candidate of this lane
+    float bv = -INFINITY;
+    int bid = 0x7fffffff;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int e = lane + 32 * j;
+      if (e < E && !((taken >> j) & 1u)) {
+        if (v[j] > bv || (v[j] == bv && e < bid)) {
+          bv = v[j];
+          bid = e;
+        }
+      }
+    }
+    // warp arg-max on (value desc, id asc)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oid = __shfl_xor_sync(0xffffffffu, bid, o);
+      if (ov > bv || (ov == bv && oid < bid)) {
+        bv = ov;
+        bid = oid;
+      }
+    }
+    if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
+    if (lane == r) {
+      sel_v = bv;
+      sel_id = bid;
+    }
+  }
+  // lane 0 holds the largest selected logit
+  const float vmax = __shfl_sync(0xffffffffu, sel_v, 0);
+  const float ex = (lane < k) ? expf(sel_v - vmax) : 0.0f;
+  const float denom = warp_sum(ex);
+  // rank of this lane's id among the selected ids -> ascending output order
+  int rank = 0;
+  for (int j = 0; j < k; ++j) {
+    const int other = __shfl_sync(0xffffffffu, sel_id, j);
+    rank += (other < sel_id) ? 1 : 0;
+  }
+  if (lane < k) {
+    ids_out[rank] = sel_id;
+    w_out[rank] = ex / denom;
+  }
+}
+
 // Slot-table decoding: returns the bank base row pointer set for (pool, slot),
 // or false when the entry is unbound or out of range.
 struct BankSet {
@@ -172,7 +246,12 @@ int num_sms();
 cudaError_t launch_route_topk(const __nv_bfloat16* x, int T, int H, const float* w_router,
                               const float* bias, int E, int k, int32_t* topk_ids, float* topk_w,
                               float* logits_opt, void* ws, uint32_t* status, cudaStream_t s);
-size_t route_ws_bytes(int T, int E);
+size_t route_ws_bytes(int T, int H, int E);
+bool route_tc_ok(int T, int H, int E);
+size_t route_tc_ws_bytes(int T, int H, int E);
+cudaError_t launch_route_tc(const __nv_bfloat16* x, int T, int H, const float* w_router, const float* bias, int E,
+                            int k, int32_t* topk_ids, float* topk_w, float* logits_opt, void* ws, uint32_t* status,
+                            cudaStream_t s);
 cudaError_t launch_route_logits(const __nv_bfloat16* x, int T, int H, const float* w_router, const float* bias,
                                 int E, float* logits, cudaStream_t s);
 bool front_small_ok(int T, int k, int E, int n_slots);

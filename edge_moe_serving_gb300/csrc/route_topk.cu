@@ -6,9 +6,10 @@
 //    row once and dots it with every token (the router weights are the only
 //    bytes of the step besides the experts).  The last CTA to finish (ticket
 //    counter) runs the top-k for all tokens.
-//  * T > 32 (prefill): a register-blocked fp32 SIMT GEMM; a CTA owns 32
-//    tokens x all E experts, so the top-k runs in its epilogue from shared
-//    memory.
+//  * T > 32 (prefill): the tensor-core router of route_tc.cu when H is a
+//    multiple of 64; otherwise a register-blocked fp32 SIMT GEMM where a CTA
+//    owns 32 tokens x all E experts, so the top-k runs in its epilogue from
+//    shared memory.
 // Accumulation is fp32 (bf16 x is exact in fp32).  Top-k order is (logit
 // descending, id ascending); ids are written ascending.
 #include "moe_common.cuh"
@@ -18,66 +19,6 @@ namespace {
 
 constexpr int kSmallT = 32;
 constexpr int kSmallThreads = 256;
-
-// One warp selects the top-k of one token's logits (E <= 512) and writes
-// ascending ids with softmax weights renormalised over the selection.
-__device__ void warp_topk(const float* row, int E, int k, int32_t* ids_out, float* w_out) {
-  const int lane = threadIdx.x & 31;
-  constexpr int kPer = kMaxRouteE / 32;
-  float v[kPer];
-#pragma unroll
-  for (int j = 0; j < kPer; ++j) {
-    const int e = lane + 32 * j;
-    v[j] = (e < E) ? row[e] : -INFINITY;
-  }
-  uint32_t taken = 0;
-  float sel_v = -INFINITY;
-  int sel_id = 0x7fffffff;
-  for (int r = 0; r < k; ++r) {
-    // best untaken candidate of this lane
-    float bv = -INFINITY;
-    int bid = 0x7fffffff;
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      const int e = lane + 32 * j;
-      if (e < E && !((taken >> j) & 1u)) {
-        if (v[j] > bv || (v[j] == bv && e < bid)) {
-          bv = v[j];
-          bid = e;
-        }
-      }
-    }
-    // warp arg-max on (value desc, id asc)
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oid = __shfl_xor_sync(0xffffffffu, bid, o);
-      if (ov > bv || (ov == bv && oid < bid)) {
-        bv = ov;
-        bid = oid;
-      }
-    }
-    if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
-    if (lane == r) {
-      sel_v = bv;
-      sel_id = bid;
-    }
-  }
-  // lane 0 holds the largest selected logit
-  const float vmax = __shfl_sync(0xffffffffu, sel_v, 0);
-  const float ex = (lane < k) ? expf(sel_v - vmax) : 0.0f;
-  const float denom = warp_sum(ex);
-  // rank of this lane's id among the selected ids -> ascending output order
-  int rank = 0;
-  for (int j = 0; j < k; ++j) {
-    const int other = __shfl_sync(0xffffffffu, sel_id, j);
-    rank += (other < sel_id) ? 1 : 0;
-  }
-  if (lane < k) {
-    ids_out[rank] = sel_id;
-    w_out[rank] = ex / denom;
-  }
-}
 
 // ---------------------------------------------------------------- decode path
 // TOPK = false: only the logits are written (the decode front end selects).
@@ -250,8 +191,9 @@ size_t large_smem(int E) {
 
 }  // namespace
 
-size_t route_ws_bytes(int T, int E) {
+size_t route_ws_bytes(int T, int H, int E) {
   if (T <= kSmallT) return align_up((size_t)T * E * sizeof(float), 256) + 256;
+  if (route_tc_ok(T, H, E)) return route_tc_ws_bytes(T, H, E);
   return 0;
 }
 
@@ -275,6 +217,8 @@ cudaError_t launch_route_topk(const __nv_bfloat16* x, int T, int H, const float*
     return launch_k(route_small_kernel<8, true>, E, kSmallThreads, 0, s, x, T, H, w_router, bias, E, k, logits, ticket,
                     topk_ids, topk_w);
   }
+  if (route_tc_ok(T, H, E))
+    return launch_route_tc(x, T, H, w_router, bias, E, k, topk_ids, topk_w, logits_opt, ws, status, s);
   const size_t smem = large_smem(E);
   static bool attr_set = false;
   if (!attr_set) {

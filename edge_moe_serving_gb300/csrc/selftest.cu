@@ -28,5 +28,5 @@ __global__ void __launch_bounds__(32) bounded_wait_check_kernel(uint32_t* status
 extern "C" int moe_check_bounded_wait(uint32_t* dev_status, moe_stream_t stream) {
   if (!dev_status) return MOE_ERR_INVALID_ARG;
   moe::bounded_wait_check_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(dev_status);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  return moe::counted(cudaGetLastError()) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -151,6 +151,12 @@ const char* moe_status_string(int status);
  * The context stays usable. */
 int moe_check_bounded_wait(uint32_t* dev_status, moe_stream_t stream);
 
+/* Number of kernels this library has launched, or captured into a CUDA graph,
+ * in this process: a host-side counter, incremented once per launch that the
+ * CUDA runtime accepted (no counterpart in the paper).  The difference across
+ * a graph capture is the number of kernels one replay runs. */
+unsigned long long moe_kernel_launch_count(void);
+
 /* ---------------------------------------------------------------- router
  * Router scoring and top-k with renormalisation ([P] section 3.2: at each
  * MoE layer the router runs on the GPU and selects the active experts).
@@ -159,8 +165,13 @@ int moe_check_bounded_wait(uint32_t* dev_status, moe_stream_t stream);
  *   topk_w[t, j]  = exp(l_j - max_sel) / sum_sel exp(l - max_sel)
  *                   (softmax over all E, renormalised over the k selected)
  * x bf16 [T, H]; logits_opt fp32 [T, E] or NULL.  1 <= k <= 16, k <= E <= 512.
- * T = 0 is a no-op. */
-size_t moe_route_topk_workspace_size(int T, int E);
+ * T = 0 is a no-op.
+ * For T > 32 and H a multiple of 64 the products run on the tensor cores:
+ * each fp32 router weight is split exactly into three bf16 parts
+ * (hi + mid + lo == w) and the bf16 products are accumulated in fp32 over
+ * K = 3H.  The workspace then holds the split weights (E x 3H bf16) and,
+ * when logits_opt is NULL, the logits (T x E fp32); its size depends on H. */
+size_t moe_route_topk_workspace_size(int T, int H, int E);
 int moe_route_topk(const void* x, int T, int H, const float* w_router, const float* bias, int E,
                    int k, int32_t* topk_ids, float* topk_w, float* logits_opt, void* ws,
                    size_t ws_bytes, uint32_t* dev_status, moe_stream_t stream);

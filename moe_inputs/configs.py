@@ -88,9 +88,10 @@ DECODE_PROFILE = LayerConfig("decode_profile", T=1, H=4096, E=32, k=6, I=2048, s
                              bias="zipf")
 
 # Profiling case for ncu captures of the prefill kernels: the prefill layer
-# shape with 32 experts and 2048 tokens (about 2 GB on the device, ~384 rows per
-# expert).  Not a benchmark workload.
-PREFILL_PROFILE = LayerConfig("prefill_profile", T=2048, H=4096, E=32, k=6, I=2048, seed=12)
+# shape with 64 experts and 2048 tokens, so each expert gets ~192 rows as in
+# the 8192-token block over 256 experts (about 3.5 GB on the device).  Not a
+# benchmark workload.
+PREFILL_PROFILE = LayerConfig("prefill_profile", T=2048, H=4096, E=64, k=6, I=2048, seed=12)
 
 CONFIGS = {c.name: c for c in (TINY, DECODE, BATCHED_DECODE, PREFILL, LONG_PREFILL, DECODE_PROFILE,
                                PREFILL_PROFILE)}

@@ -42,8 +42,10 @@ def test_status_strings_and_version():
 
 
 def test_workspace_sizes_are_host_arithmetic():
-    assert moe.moe_route_topk_workspace_size(1, 256) >= 1024
-    assert moe.moe_route_topk_workspace_size(8192, 256) == 0
+    assert moe.moe_route_topk_workspace_size(1, 4096, 256) >= 1024
+    assert moe.moe_route_topk_workspace_size(8192, 40, 256) == 0
+    # tensor-core router: the 3-way bf16 split of the router weights + fp32 logits
+    assert moe.moe_route_topk_workspace_size(8192, 4096, 256) >= 256 * 3 * 4096 * 2 + 8192 * 256 * 4
     assert moe.moe_dispatch_workspace_size(1, 6, 256) == 0
     assert moe.moe_dispatch_workspace_size(8192, 6, 256) >= 48 * 256 * 4
     assert moe.moe_expert_ffn_workspace_size(32, 8, 128, 2048, 768, moe.MOE_FFN_GEMV) >= 256 * 768 * 2

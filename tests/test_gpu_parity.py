@@ -35,7 +35,7 @@ def _route(cfg, layer, step, x_bits=None, want_logits=True):
     ids = torch.empty((T, cfg.k), dtype=torch.int32, device=DEV)
     w = torch.empty((T, cfg.k), dtype=torch.float32, device=DEV)
     lg = torch.empty((T, cfg.E), dtype=torch.float32, device=DEV) if want_logits else None
-    nb = moe.moe_route_topk_workspace_size(T, cfg.E)
+    nb = moe.moe_route_topk_workspace_size(T, cfg.H, cfg.E)
     st = status()
     moe.moe_route_topk(x, T, cfg.H, wr, bd, cfg.E, cfg.k, ids, w, lg, ws(nb), nb, st)
     torch.cuda.synchronize()
@@ -62,27 +62,36 @@ def test_route_topk_bit_exact(name, steps):
 def test_route_topk_small_shapes_and_ties():
     """Ragged E and T, all-equal logits (ties go to the lower id)."""
     rng = np.random.default_rng(0)
-    for T, H, E, k in ((1, 8, 3, 1), (5, 24, 33, 4), (33, 64, 100, 7), (70, 40, 512, 16), (31, 16, 64, 16)):
+    # (T > 32, H % 64 == 0) runs on the tensor cores: ragged expert tiles
+    # (E = 100, 130), ragged token tiles (T = 200, 129, 300), E = 512, tiny E.
+    for T, H, E, k in ((1, 8, 3, 1), (5, 24, 33, 4), (33, 64, 100, 7), (70, 40, 512, 16), (31, 16, 64, 16),
+                       (200, 128, 130, 6), (129, 192, 512, 16), (300, 64, 8, 2)):
         xb = gen.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
         wr = (rng.standard_normal((E, H)) * 0.1).astype(np.float32)
+        b = (rng.standard_normal(E) * 0.05).astype(np.float32)
         x = to_dev_bf16(xb, DEV)
         ids = torch.empty((T, k), dtype=torch.int32, device=DEV)
         w = torch.empty((T, k), dtype=torch.float32, device=DEV)
-        nb = moe.moe_route_topk_workspace_size(T, E)
-        moe.moe_route_topk(x, T, H, to_dev(wr, DEV), None, E, k, ids, w, None, ws(nb), nb, status())
-        ref_lg = O.router_logits(gen.bf16_bits_to_f64(xb), wr)
+        lg = torch.empty((T, E), dtype=torch.float32, device=DEV)
+        nb = moe.moe_route_topk_workspace_size(T, H, E)
+        st = status()
+        moe.moe_route_topk(x, T, H, to_dev(wr, DEV), to_dev(b, DEV), E, k, ids, w, lg, ws(nb), nb, st)
+        ref_lg = O.router_logits(gen.bf16_bits_to_f64(xb), wr, b)
         gaps = O.topk_gap(ref_lg, k) if k < E else np.full(T, np.inf)
         ref_ids, ref_w = O.select_topk(ref_lg, k)
         ok = gaps >= 1e-3
-        assert np.array_equal(ids.cpu().numpy()[ok], ref_ids[ok])
+        assert status_bits(st) == 0
+        assert np.abs(lg.cpu().numpy() - ref_lg).max() < 1e-4, (T, H, E)
+        assert np.array_equal(ids.cpu().numpy()[ok], ref_ids[ok]), (T, H, E)
+        assert np.abs(w.cpu().numpy()[ok] - ref_w[ok]).max() < 1e-5, (T, H, E)
     # ties: zero router weights -> every logit equal -> ids 0..k-1, weights 1/k
-    for T in (1, 40):
-        x = to_dev_bf16(np.zeros((T, 16), np.uint16), DEV)
-        wr = torch.zeros((10, 16), dtype=torch.float32, device=DEV)
+    for T, H in ((1, 16), (40, 16), (40, 64), (257, 128)):
+        x = to_dev_bf16(np.zeros((T, H), np.uint16), DEV)
+        wr = torch.zeros((10, H), dtype=torch.float32, device=DEV)
         ids = torch.empty((T, 3), dtype=torch.int32, device=DEV)
         w = torch.empty((T, 3), dtype=torch.float32, device=DEV)
-        nb = moe.moe_route_topk_workspace_size(T, 10)
-        moe.moe_route_topk(x, T, 16, wr, None, 10, 3, ids, w, None, ws(nb), nb, status())
+        nb = moe.moe_route_topk_workspace_size(T, H, 10)
+        moe.moe_route_topk(x, T, H, wr, None, 10, 3, ids, w, None, ws(nb), nb, status())
         assert (ids.cpu().numpy() == np.array([0, 1, 2])).all()
         assert np.allclose(w.cpu().numpy(), 1.0 / 3, atol=1e-7)
 
