@@ -1,0 +1,339 @@
+// The whole routed MoE layer for a decode-sized call in one cooperative
+// launch (FreeToken paper, section 3.2: router, cache lookup and q* split,
+// grouped expert evaluation, combine; section 4.1: device-side cache
+// control).  One CTA per SM:
+//
+//   phase R   every CTA scores its router rows (fp32 rows fetched with
+//             cp.async.bulk into the weight ring's shared memory, the token
+//             rows converted to fp32 next to them) and writes the logits
+//   barrier   bounded grid-wide barrier: every logit is written
+//   decide    warp 0 of every CTA runs the same top-k, dispatch and
+//             residency decision (front_decide) on the pre-call cache state,
+//             so no CTA waits for another to publish it
+//   FFN       the fused weight-streaming gate/up + down phases, admitted
+//             experts copied into their cache slots while they stream, then
+//             the gate-weighted combine (fused_ffn_body)
+//   commit    CTA 0 writes the routing outputs and applies the decision to
+//             the slot table, owners, stamps and clock (every other CTA read
+//             the pre-call state before the first grid barrier of the FFN)
+//
+// It computes exactly what the router, bind, dispatch, FFN and combine
+// launches compute for such calls; it replaces their four kernel boundaries
+// by two grid barriers.
+#include <algorithm>
+
+#include "front_warp.cuh"
+#include "ring_gemv.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kDecMaxT = 8;        // token rows converted to fp32 in shared memory
+constexpr int kDecMaxRows = 4;     // router rows per CTA
+
+struct DecodeParams {
+  GemvParams g;                    // counts / perm / combine_w are pointed at shared memory in the kernel
+  const float* w_router;           // [E, H] fp32
+  const float* bias;               // [E] or null
+  uint32_t phi_q16;
+  int min_fill, policy;
+  unsigned long long seed;
+  moe_bind_stats* stats;
+  float* logits;                   // [T, E] workspace
+  int32_t* topk_ids;
+  float* topk_w;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* perm;
+  int32_t* inv_perm;
+  int rows_per_cta;                // ceil(E / grid)
+  size_t state_off;                // ring offset of the cache-state copy
+};
+
+constexpr size_t kKeysBytes = (size_t)kMaxCacheSlots / 4 * 8 + kMaxCacheSlots / 4 / 8;   // victim keys + hit bitmap
+
+size_t state_offset(int T, int E, int H) {
+  const int G = num_sms();
+  const size_t rows = (size_t)(E + G - 1) / G;
+  return align_up(std::max(rows * H * 4 + (size_t)T * H * 2, kKeysBytes), 16);
+}
+
+__device__ inline bool grid_barrier(unsigned int* count, volatile int* abort_flag) {
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    atomicAdd(count, 1u);
+    const unsigned long long t0 = gtimer();
+    while (*reinterpret_cast<volatile unsigned int*>(count) < gridDim.x) {
+      if (*abort_flag) break;
+      if (gtimer() - t0 > kGridWaitNs) {
+        *abort_flag = 1;
+        break;
+      }
+    }
+    __threadfence();
+  }
+  __syncthreads();
+  return !*abort_flag;
+}
+
+template <int NT, int VA, int VB>
+__global__ void __launch_bounds__(kRingThreads, 1)
+decode_layer_kernel(DecodeParams d, unsigned int* grid_count) {
+  extern __shared__ uint8_t ring_raw[];
+  __shared__ __align__(16) FusedShared fs;
+  __shared__ __align__(16) FrontDecision fr;
+  __shared__ __align__(8) uint64_t rbar;
+  __shared__ float red[kRingThreads / 32][kDecMaxRows][kDecMaxT];
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ring_raw) + 127) & ~uintptr_t(127));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  GemvParams p = d.g;
+  const int E = p.E, H = p.H, T = p.T, G = gridDim.x, b = blockIdx.x;
+  const int n_my = b < E ? (E - 1 - b) / G + 1 : 0;
+  // ring bytes during the prologue: router rows (fp32) | token rows (bf16) | state copy;
+  // after the first barrier: victim keys | hit bitmap (below the state copy)
+  const int n_slots = p.c.cache.n_slots, base = p.layer * E;
+  float* wrow = reinterpret_cast<float*>(ring);                                    // [n_my][H]
+  __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(wrow + (size_t)d.rows_per_cta * H);   // [T][H]
+  int32_t* s_table = reinterpret_cast<int32_t*>(ring + d.state_off);               // [E]
+  uint32_t* s_stamp = reinterpret_cast<uint32_t*>(s_table + align_up((size_t)E, 4));
+  int32_t* s_owner = reinterpret_cast<int32_t*>(s_stamp + align_up((size_t)n_slots, 4));
+  __shared__ uint32_t s_clock;
+  __shared__ float s_bias[kDecMaxRows];
+
+  if (tid == 0) {
+    ring_init(fs);
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&rbar)));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  pdl_wait();
+  // ---------------------------------------------------------------- phase R
+  // One round of bulk copies brings everything the prologue reads: this CTA's
+  // router rows, the token rows, and the cache state the decision reads (this
+  // layer's slot-table row, the pool's stamps and owners); 16-byte tails and
+  // misaligned rows take plain loads.
+  const bool table_bulk = (reinterpret_cast<uintptr_t>(p.c.slot_table + base) & 15) == 0;
+  const bool slot_bulk = ((reinterpret_cast<uintptr_t>(p.c.stamp) | reinterpret_cast<uintptr_t>(p.c.owner)) & 15) == 0;
+  const int table_bulk_n = table_bulk ? (E & ~3) : 0;
+  const int slot_bulk_n = slot_bulk ? (n_slots & ~3) : 0;
+  if (tid == 0) {
+    const uint32_t row_bytes = (uint32_t)H * 4u;
+    const uint32_t x_bytes = (uint32_t)T * H * 2u;
+    const uint32_t bytes = row_bytes * (uint32_t)n_my + x_bytes + 4u * (uint32_t)table_bulk_n + 8u * (uint32_t)slot_bulk_n;
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(&rbar)), "r"(bytes)
+                 : "memory");
+    for (int i = 0; i < n_my; ++i)
+      bulk_g2s(wrow + (size_t)i * H, d.w_router + (size_t)(b + i * G) * H, row_bytes, &rbar);
+    bulk_g2s(xs, p.x, x_bytes, &rbar);
+    if (table_bulk_n > 0) bulk_g2s(s_table, p.c.slot_table + base, 4u * table_bulk_n, &rbar);
+    if (slot_bulk_n > 0) {
+      bulk_g2s(s_stamp, p.c.stamp, 4u * slot_bulk_n, &rbar);
+      bulk_g2s(s_owner, p.c.owner, 4u * slot_bulk_n, &rbar);
+    }
+  } else if (warp == kConsumerWarps) {
+    for (int e = table_bulk_n + lane; e < E; e += 32) s_table[e] = __ldcg(p.c.slot_table + base + e);
+    for (int v = slot_bulk_n + lane; v < n_slots; v += 32) {
+      s_stamp[v] = __ldcg(p.c.stamp + v);
+      s_owner[v] = __ldcg(p.c.owner + v);
+    }
+    if (lane == 0) s_clock = __ldcg(p.c.clock);
+  } else if (warp == 1 && lane < n_my) {
+    s_bias[lane] = d.bias ? __ldg(d.bias + b + lane * G) : 0.0f;
+  }
+  if (!bounded_wait(&rbar, 0u, &fs.abort)) fs.abort = 1;
+  __syncthreads();
+  if (n_my > 0 && !fs.abort) {
+    float acc[kDecMaxRows][kDecMaxT];
+#pragma unroll
+    for (int i = 0; i < kDecMaxRows; ++i)
+#pragma unroll
+      for (int t = 0; t < kDecMaxT; ++t) acc[i][t] = 0.0f;
+    const int H4 = H >> 2;
+    for (int q = tid; q < H4; q += blockDim.x) {
+      float4 xv[kDecMaxT];
+#pragma unroll
+      for (int t = 0; t < kDecMaxT; ++t) {
+        if (t < T) {
+          const uint2 u = reinterpret_cast<const uint2*>(xs + (size_t)t * H)[q];
+          xv[t] = make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kDecMaxRows; ++i) {
+        if (i < n_my) {
+          const float4 w = reinterpret_cast<const float4*>(wrow + (size_t)i * H)[q];
+#pragma unroll
+          for (int t = 0; t < kDecMaxT; ++t) {
+            if (t < T) {
+              float a = acc[i][t];
+              a = fmaf(w.x, xv[t].x, a);
+              a = fmaf(w.y, xv[t].y, a);
+              a = fmaf(w.z, xv[t].z, a);
+              a = fmaf(w.w, xv[t].w, a);
+              acc[i][t] = a;
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kDecMaxRows; ++i)
+#pragma unroll
+      for (int t = 0; t < kDecMaxT; ++t) {
+        if (i < n_my && t < T) {
+          const float s = warp_sum(acc[i][t]);
+          if (lane == 0) red[warp][i][t] = s;
+        }
+      }
+    __syncthreads();
+    if (tid < n_my * T) {
+      const int i = tid / T, t = tid - (tid / T) * T;
+      float s = 0.0f;
+      for (int w = 0; w < kRingThreads / 32; ++w) s += red[w][i][t];
+      d.logits[(size_t)t * E + b + i * G] = s + s_bias[i];
+    }
+  }
+  // ---------------------------------------------------------------- decide
+  if (grid_barrier(grid_count + 2, &fs.abort)) {
+    if (warp == 0) {
+      unsigned long long* keys = reinterpret_cast<unsigned long long*>(ring);
+      uint32_t* hitmap = reinterpret_cast<uint32_t*>(ring + (size_t)kMaxCacheSlots / 4 * 8);
+      front_decide(d.logits, T, p.k, E, p.c.cache.n_slots, p.layer, s_table, s_stamp, s_owner, s_clock, d.phi_q16,
+                   d.min_fill, d.policy, d.seed, fr, keys, hitmap);
+    }
+    __syncthreads();
+    const int R = T * p.k;
+    front_counts(fr, E, R);
+    __syncthreads();
+    for (int e = tid; e < E; e += blockDim.x) {
+      fs.off[e] = fr.offsets[e];
+      fs.fill[e] = -1;
+      fs.ent[e] = -1;
+    }
+    __syncthreads();
+    if (tid < R) {
+      const int kind = fr.u_kind[tid], e = fr.u_e[tid];
+      if (kind == kFrontHit) fs.ent[e] = fr.u_slot[tid];
+      if (kind == kFrontFill) fs.fill[e] = fr.u_slot[tid];
+      if (kind == kFrontFill || kind == kFrontStage) fs.ent[e] = MOE_STAGING_TAG | (base + e);
+    }
+    if (b == 0) {
+      for (int e = tid; e <= E; e += blockDim.x) {
+        d.offsets[e] = fr.offsets[e];
+        if (e < E) d.counts[e] = fr.counts[e];
+      }
+      if (tid < R) {
+        d.topk_ids[tid] = fr.ids[tid];
+        d.topk_w[tid] = fr.w[tid];
+        d.perm[tid] = fr.perm[tid];
+        d.inv_perm[tid] = fr.inv_perm[tid];
+      }
+    }
+    __syncthreads();
+    // ---------------------------------------------------------------- FFN
+    p.counts = fr.counts;
+    p.offsets = fr.offsets;
+    p.perm = fr.perm;
+    p.combine_w = fr.w;
+    p.fills = nullptr;
+    fused_ffn_body<NT, VA, VB>(p, grid_count, fs, ring);
+    __syncthreads();
+    // ---------------------------------------------------------------- commit
+    if (b == 0 && warp == 0 && !fs.abort) front_commit(fr, p.c, p.layer, d.stats, p.status);
+  }
+  pdl_trigger();
+  __syncthreads();
+  if (fs.abort && tid == 0) set_status(p.status, MOE_DEV_ERR_TIMEOUT);
+}
+
+template <int NT, int VA, int VB>
+cudaError_t launch_one(const DecodeParams& d, unsigned int* grid_count, int grid, cudaStream_t s) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(decode_layer_kernel<NT, VA, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kRingSmem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const size_t words = 4 + (size_t)d.g.T * d.g.k;   // barrier words, then one counter per instance
+  cudaError_t err = cudaMemsetAsync(grid_count, 0, words * sizeof(unsigned int), s);
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kRingThreads);
+  cfg.dynamicSmemBytes = kRingSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attrs[1];
+  attrs[0].id = cudaLaunchAttributeCooperative;   // all CTAs resident: the grid barriers can complete
+  attrs[0].val.cooperative = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 1;
+  return counted(cudaLaunchKernelEx(&cfg, decode_layer_kernel<NT, VA, VB>, d, grid_count));
+}
+
+}  // namespace
+
+bool decode_layer_ok(int T, int k, int E, int H, int I, int n_slots) {
+  const int G = num_sms();
+  const int rows = (E + G - 1) / G;
+  return T >= 1 && T <= kDecMaxT && T * k <= 32 && E <= kMaxRouteE && rows <= kDecMaxRows && gemv_fused_ok(H, I) &&
+         n_slots >= 1 && n_slots <= kMaxCacheSlots / 4 &&
+         state_offset(T, E, H) + 4 * (align_up((size_t)E, 4) + 2 * align_up((size_t)n_slots, 4)) <=
+             (size_t)kRingStages * kUnitBytes;
+}
+
+cudaError_t launch_decode_layer(const moe_cache& c, int layer, const __nv_bfloat16* x, int T, int k,
+                                const float* w_router, const float* bias, uint32_t phi_q16, int min_fill, int policy,
+                                uint64_t seed, moe_bind_stats* stats, float* logits, int32_t* topk_ids, float* topk_w,
+                                int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv_perm, float* y_rows,
+                                __nv_bfloat16* h, unsigned int* grid_count, __nv_bfloat16* out, uint32_t* status,
+                                cudaStream_t s) {
+  DecodeParams d = {};
+  GemvParams& p = d.g;
+  p.c = c;
+  p.layer = layer;
+  p.E = c.E;
+  p.H = c.H;
+  p.I = c.I;
+  p.k = k;
+  p.T = T;
+  p.x = x;
+  p.x_perm = nullptr;
+  p.mask = nullptr;
+  p.max_rows = T;
+  p.h = h;
+  p.y = y_rows;
+  p.status = status;
+  p.combine_out = out;
+  p.grid_count = grid_count;
+  p.inst_done = grid_count + 4;
+  d.w_router = w_router;
+  d.bias = bias;
+  d.phi_q16 = phi_q16;
+  d.min_fill = min_fill;
+  d.policy = policy;
+  d.seed = seed;
+  d.stats = stats;
+  d.logits = logits;
+  d.topk_ids = topk_ids;
+  d.topk_w = topk_w;
+  d.counts = counts;
+  d.offsets = offsets;
+  d.perm = perm;
+  d.inv_perm = inv_perm;
+  const int G = num_sms();
+  d.rows_per_cta = (c.E + G - 1) / G;
+  d.state_off = state_offset(T, c.E, c.H);
+  if (T <= 1) {
+    const bool va = c.H == 4096 && ring_rows(c.H, true) == 1;
+    const bool vb = c.I == 2048;
+    if (va && vb) return launch_one<1, 16, 8>(d, grid_count, G, s);
+    return launch_one<1, 0, 0>(d, grid_count, G, s);
+  }
+  if (T <= 2) return launch_one<2, 0, 0>(d, grid_count, G, s);
+  if (T <= 4) return launch_one<4, 0, 0>(d, grid_count, G, s);
+  return launch_one<8, 0, 0>(d, grid_count, G, s);
+}
+
+}  // namespace moe

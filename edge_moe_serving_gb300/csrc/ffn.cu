@@ -12,7 +12,8 @@ size_t ffn_ws_bytes(int T, int k, int E, int H, int I, int mode) {
   (void)H;
   (void)mode;
   const size_t R = (size_t)T * k;
-  return align_up(R * I * sizeof(__nv_bfloat16), 256) + 256;   // h, then the grid-barrier words
+  // h, then the grid-barrier words and the per-instance counters of the fused GEMV
+  return align_up(R * I * sizeof(__nv_bfloat16), 256) + align_up((4 + R) * sizeof(unsigned int), 256);
 }
 
 cudaError_t launch_ffn(const moe_cache& c, int layer, const int32_t* counts, const int32_t* offsets,
@@ -59,6 +60,7 @@ cudaError_t launch_ffn(const moe_cache& c, int layer, const int32_t* counts, con
     p.combine_out = combine_out;
     p.grid_count = reinterpret_cast<unsigned int*>(reinterpret_cast<char*>(ws) +
                                                    align_up((size_t)R * c.I * sizeof(__nv_bfloat16), 256));
+    p.inst_done = R <= kMaxFusedInst ? p.grid_count + 4 : nullptr;
     cudaError_t err = launch_gemv(p, s);
     if (err != cudaSuccess) return err;
   }

@@ -18,7 +18,7 @@
 // [b*per, (b+1)*per) of the flattened list and processes them NG at a time.
 // Partial dot products are reduced with a warp reduce-scatter plus a fixed
 // order sum over warps, so results do not depend on the grid.
-#include "ffn_params.cuh"
+#include "ring_gemv.cuh"
 
 namespace moe {
 namespace {
@@ -40,65 +40,6 @@ __device__ inline void warp_reduce_scatter(float (&v)[N]) {
       v[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
     }
   }
-}
-
-// Instances per expert (prefix over experts of ceil(rows / NT), eligible only).
-template <int NT>
-__device__ void build_prefix(const GemvParams& p, int* s_pref, int* s_warp) {
-  const int tid = threadIdx.x, nthreads = blockDim.x;
-  const int per_thread = (p.E + nthreads - 1) / nthreads;
-  const int e0 = tid * per_thread;
-  int local[kMaxE / 32];
-  int sum = 0;
-  for (int u = 0; u < per_thread; ++u) {
-    const int e = e0 + u;
-    int n = 0;
-    if (e < p.E) {
-      const int cnt = p.counts[e];
-      const bool ok = cnt > 0 && cnt <= p.max_rows && (p.mask == nullptr || p.mask[e] != 0);
-      n = ok ? (cnt + NT - 1) / NT : 0;
-    }
-    local[u] = n;
-    sum += n;
-  }
-  // exclusive scan of per-thread sums
-  const int lane = tid & 31, warp = tid >> 5;
-  int inc = sum;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int n = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += n;
-  }
-  if (lane == 31) s_warp[warp] = inc;
-  __syncthreads();
-  if (tid == 0) {
-    int run = 0;
-    for (int w = 0; w < nthreads / 32; ++w) {
-      const int t = s_warp[w];
-      s_warp[w] = run;
-      run += t;
-    }
-    s_pref[p.E] = run;
-  }
-  __syncthreads();
-  int run = s_warp[warp] + inc - sum;
-  for (int u = 0; u < per_thread; ++u) {
-    const int e = e0 + u;
-    if (e < p.E) s_pref[e] = run;
-    run += local[u];
-  }
-  __syncthreads();
-}
-
-// largest e with s_pref[e] <= j < s_pref[e + 1]
-__device__ inline int find_expert(const int* s_pref, int E, int j) {
-  int lo = 0, hi = E - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (s_pref[mid] <= j) lo = mid;
-    else hi = mid - 1;
-  }
-  return lo;
 }
 
 template <int NT, int NG, bool GATEUP>
@@ -222,426 +163,36 @@ gemv_kernel(GemvParams p) {
 }
 
 
-// ---------------------------------------------------------------- TMA-ring variant
-// Used when the weight row length K is a multiple of 256 (every lane then owns
-// K/256 16-byte vectors of each row).  One producer thread streams "units" of
-// consecutive weight rows (about 16 KB: U gate rows + U up rows, or U down rows)
-// into a ring of shared-memory stages with cp.async.bulk, so each SM keeps
-// ~160 KB of weight reads in flight regardless of how long the reductions
-// take; four consumer warps each take every fourth unit, reduce each row with
-// warp shuffles and write the outputs.  One CTA per SM; a CTA owns a
-// contiguous range of units, so the grid is balanced to within one unit.
-constexpr int kRingStages = 12;
-constexpr int kUnitBytes = 16384;
-constexpr int kConsumerWarps = 6;
-// Unit i lives in stage i % kRingStages and is consumed by warp i % kConsumerWarps.
-// A parity wait tells only two phases of a stage apart, so a consumer may wait
-// for use n+1 of a stage only after use n has completed; that holds when every
-// stage is always consumed by the same warp, i.e. when the consumer count
-// divides the stage count.
-static_assert(kRingStages % kConsumerWarps == 0, "each ring stage must have one consumer warp");
-constexpr int kRingThreads = (kConsumerWarps + 1) * 32;
-
-__device__ inline uint32_t smem_addr(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
-
-__device__ inline unsigned long long gtimer() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ inline bool ring_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-  return bounded_wait(bar, parity, abort_flag);
-}
-
-__device__ inline void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-               ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
-               : "memory");
-}
-
-__device__ inline void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
-               ::"l"(dst), "r"(smem_addr(src)), "r"(bytes)
-               : "memory");
-}
-__device__ inline void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ inline void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ inline void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
-// 8 bf16 products into two partial sums (shorter dependency chains).
-__device__ inline void dot8x2(const uint4& w, const uint4& a, float& s0, float& s1) {
-  s0 = fmaf(bf16_lo(w.x), bf16_lo(a.x), s0);
-  s1 = fmaf(bf16_hi(w.x), bf16_hi(a.x), s1);
-  s0 = fmaf(bf16_lo(w.y), bf16_lo(a.y), s0);
-  s1 = fmaf(bf16_hi(w.y), bf16_hi(a.y), s1);
-  s0 = fmaf(bf16_lo(w.z), bf16_lo(a.z), s0);
-  s1 = fmaf(bf16_hi(w.z), bf16_hi(a.z), s1);
-  s0 = fmaf(bf16_lo(w.w), bf16_lo(a.w), s0);
-  s1 = fmaf(bf16_hi(w.w), bf16_hi(a.w), s1);
-}
-
-// Source and (for a fused fill) destination banks of the instance's expert.
-struct RingSrc {
-  BankSet src;
-  __nv_bfloat16* dst_gate;
-  __nv_bfloat16* dst_up;
-  __nv_bfloat16* dst_down;
-  bool ok, fill;
-};
-
-__device__ inline RingSrc ring_source(const GemvParams& p, int e, int entry, int fill_dst, uint32_t* status) {
-  RingSrc r;
-  r.fill = false;
-  r.dst_gate = r.dst_up = r.dst_down = nullptr;
-  if (fill_dst >= 0) {
-    // admitted by this call: read the staging copy, write the cache slot
-    r.ok = resolve_slot(p.c, MOE_STAGING_TAG | (p.layer * p.E + e), p.H, p.I, &r.src, status);
-    const size_t per = (size_t)p.H * p.I;
-    r.dst_gate = reinterpret_cast<__nv_bfloat16*>(p.c.cache.w_gate) + (size_t)fill_dst * per;
-    r.dst_up = reinterpret_cast<__nv_bfloat16*>(p.c.cache.w_up) + (size_t)fill_dst * per;
-    r.dst_down = reinterpret_cast<__nv_bfloat16*>(p.c.cache.w_down) + (size_t)fill_dst * per;
-    r.fill = r.ok;
-  } else {
-    r.ok = resolve_slot(p.c, entry, p.H, p.I, &r.src, status);
-  }
-  return r;
-}
-
-// Rows per unit (per bank) for a weight row length K: units of ~16 KB, at most 4 rows.
-__host__ __device__ inline int ring_rows(int K, bool gateup) {
-  const int nb = gateup ? 2 : 1;
-  const int u = kUnitBytes / (nb * K * 2);
-  return u >= 4 ? 4 : (u >= 2 ? 2 : 1);
-}
-
-constexpr unsigned long long kGridWaitNs = 1000000000ull;
-
-// Ring bookkeeping shared by the two phases of one CTA.  Ring index = the
-// CTA's running unit count over both phases; unit i sits in stage i % S and
-// belongs to consumer warp i % C.  Units of an unbound expert still take a
-// ring slot (the producer completes it without data), so every role can
-// compute ring indices without seeing the other roles' decisions.
-struct RingState {
-  int base;               // ring index of the current phase's first unit
-  int armed_last;         // producer: last ring index with copies in flight
-  bool stored;            // a consumer issued fused-fill stores
-};
-
-// Number of this CTA's units among `total` grid-strided units.
-__device__ inline int local_units(int total) {
-  const int b = blockIdx.x, G = gridDim.x;
-  return b < total ? (total - 1 - b) / G + 1 : 0;
-}
-
-// One phase of the fused GEMV: phase A (GATEUP) streams gate and up rows and
-// writes h; phase B streams down rows and writes y.  Units are grid-strided:
-// CTA b takes units b, b + G, b + 2G, ...  VC > 0: the single token's
-// activation row (K = 256*VC) is held in registers.
-template <int NT, bool GATEUP, int VC>
-__device__ inline void ring_phase(const GemvParams& p, const int* s_pref, const int* s_off, const int* s_ent,
-                                  const int* s_fill, uint8_t* ring, uint64_t* full_bar, uint64_t* empty_bar,
-                                  volatile int* abort_flag, RingState& st, bool producer) {
-  constexpr int NB = GATEUP ? 2 : 1;
-  constexpr int PS = (NT == 1) ? 2 : 1;
-  constexpr int XR = (NT == 1 && VC > 0) ? VC : 1;
-  constexpr bool x_in_regs = (NT == 1) && VC > 0;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int K = GATEUP ? p.H : p.I;
-  const int NTASK = GATEUP ? p.I : p.H;
-  const int row_bytes = K * 2;
-  const int U = ring_rows(K, GATEUP);
-  const int upi = (NTASK + U - 1) / U;
-  const int bank_stride = kUnitBytes / NB;
-  const int VPL = K / 256;
-  const int total = s_pref[p.E] * upi;
-  const int G = gridDim.x;
-  const int n_local = local_units(total);
-  const int base = st.base;
-  st.base += n_local;
-
-  if (producer) {
-    int cur_j = -1;
-    RingSrc rs;
-    rs.ok = false;
-    for (int i = 0; i < n_local && !*abort_flag; ++i) {
-      const int u = blockIdx.x + i * G;
-      const int j = u / upi;
-      const int n0 = (u - j * upi) * U;
-      if (j != cur_j) {
-        cur_j = j;
-        const int e = find_expert(s_pref, p.E, j);
-        rs = ring_source(p, e, s_ent[e], s_fill[e], nullptr);
-      }
-      const int ri = base + i;
-      const int stage = ri % kRingStages;
-      const uint32_t use = (uint32_t)(ri / kRingStages);
-      if (!ring_wait(&empty_bar[stage], (use & 1u) ^ 1u, abort_flag)) break;
-      if (!rs.ok) {
-        // nothing to stream: complete the slot's phase without data
-        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&full_bar[stage])) : "memory");
-        continue;
-      }
-      uint8_t* dst = ring + stage * kUnitBytes;
-      const int rows = min(U, NTASK - n0);
-      const uint32_t bytes = (uint32_t)(rows * row_bytes);
-      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(&full_bar[stage])),
-                   "r"(bytes * NB)
-                   : "memory");
-      if (GATEUP) {
-        bulk_g2s(dst, rs.src.gate + (size_t)n0 * K, bytes, &full_bar[stage]);
-        bulk_g2s(dst + bank_stride, rs.src.up + (size_t)n0 * K, bytes, &full_bar[stage]);
-      } else {
-        bulk_g2s(dst, rs.src.down + (size_t)n0 * K, bytes, &full_bar[stage]);
-      }
-      st.armed_last = ri;
-    }
-    return;
-  }
-
-  int cur_j = -1;
-  RingSrc rs;
-  rs.ok = false;
-  int pos0 = 0, ntok = 0;
-  const __nv_bfloat16* act[NT];
-  int yrow[NT];
-  uint4 xr[XR];
-  // this warp's units: ring index ri = base + i with ri % C == warp
-  const int i0 = ((warp - base) % kConsumerWarps + kConsumerWarps) % kConsumerWarps;
-  for (int i = i0; i < n_local; i += kConsumerWarps) {
-    const int u = blockIdx.x + i * G;
-    const int j = u / upi;
-    const int n0 = (u - j * upi) * U;
-    if (j != cur_j) {
-      cur_j = j;
-      const int e = find_expert(s_pref, p.E, j);
-      // any warp that meets an unbound expert reports it (units are spread over warps)
-      rs = ring_source(p, e, s_ent[e], s_fill[e], (lane == 0) ? p.status : nullptr);
-      const int c = j - s_pref[e];
-      pos0 = s_off[e] + c * NT;
-      ntok = min(NT, p.counts[e] - c * NT);
-#pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        const int pos = pos0 + (t < ntok ? t : 0);
-        if (GATEUP)
-          act[t] = p.x_perm ? p.x_perm + (size_t)pos * p.H : p.x + (size_t)(p.perm[pos] / p.k) * p.H;
-        else
-          act[t] = p.h + (size_t)pos * p.I;
-        yrow[t] = GATEUP ? 0 : p.perm[pos];
-      }
-      if (x_in_regs && rs.ok) {
-        // phase B reads h written by other CTAs of this launch: through L2, not the read-only path
-#pragma unroll
-        for (int c2 = 0; c2 < XR; ++c2)
-          xr[c2] = GATEUP ? ldg_cached(act[0] + (size_t)(lane + 32 * c2) * 8)
-                          : __ldcg(reinterpret_cast<const uint4*>(act[0] + (size_t)(lane + 32 * c2) * 8));
-      }
-    }
-    const int ri = base + i;
-    const int stage = ri % kRingStages;
-    const uint32_t use = (uint32_t)(ri / kRingStages);
-    if (!ring_wait(&full_bar[stage], use & 1u, abort_flag)) break;
-    const uint8_t* sw = ring + stage * kUnitBytes;
-    const int rows = min(U, NTASK - n0);
-    if (rs.ok) {
-      if (rs.fill && lane == 0) {
-        // this expert is being admitted to the cache: write the unit to its slot
-        const uint32_t bytes = (uint32_t)(rows * row_bytes);
-        if (GATEUP) {
-          bulk_s2g(rs.dst_gate + (size_t)n0 * K, sw, bytes);
-          bulk_s2g(rs.dst_up + (size_t)n0 * K, sw + bank_stride, bytes);
-        } else {
-          bulk_s2g(rs.dst_down + (size_t)n0 * K, sw, bytes);
-        }
-        bulk_commit();
-        st.stored = true;
-      }
-      const uint8_t* wbase = sw + (size_t)lane * 16;
-      for (int r = 0; r < rows; ++r) {
-        float acc[NB][NT][PS];
-#pragma unroll
-        for (int b = 0; b < NB; ++b)
-#pragma unroll
-          for (int t = 0; t < NT; ++t)
-#pragma unroll
-            for (int q = 0; q < PS; ++q) acc[b][t][q] = 0.0f;
-        const uint8_t* wr = wbase + (size_t)r * row_bytes;
-        if (x_in_regs) {
-#pragma unroll
-          for (int c = 0; c < XR; ++c)
-#pragma unroll
-            for (int b = 0; b < NB; ++b) {
-              const uint4 w = *reinterpret_cast<const uint4*>(wr + b * bank_stride + c * 512);
-              dot8x2(w, xr[c], acc[b][0][0], acc[b][0][PS - 1]);
-            }
-        } else {
-#pragma unroll 4
-          for (int c = 0; c < VPL; ++c) {
-            const int v = lane + 32 * c;
-            uint4 a[NT];
-#pragma unroll
-            for (int t = 0; t < NT; ++t)
-              a[t] = (t < ntok) ? (GATEUP ? ldg_cached(act[t] + (size_t)v * 8)
-                                          : __ldcg(reinterpret_cast<const uint4*>(act[t] + (size_t)v * 8)))
-                                : make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int b = 0; b < NB; ++b) {
-              const uint4 w = *reinterpret_cast<const uint4*>(wr + b * bank_stride + c * 512);
-#pragma unroll
-              for (int t = 0; t < NT; ++t) acc[b][t][0] = dot8(w, a[t], acc[b][t][0]);
-            }
-          }
-        }
-#pragma unroll
-        for (int b = 0; b < NB; ++b)
-#pragma unroll
-          for (int t = 0; t < NT; ++t) {
-            float v = acc[b][t][0];
-            if (PS == 2) v += acc[b][t][PS - 1];
-            acc[b][t][0] = warp_sum(v);
-          }
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          if (lane == t && t < ntok) {
-            if (GATEUP)
-              p.h[(size_t)(pos0 + t) * p.I + n0 + r] = __float2bfloat16_rn(silu(acc[0][t][0]) * acc[NB - 1][t][0]);
-            else
-              p.y[(size_t)yrow[t] * p.H + n0 + r] = acc[0][t][0];
-          }
-        }
-      }
-      if (rs.fill && lane == 0) bulk_wait_read_all();   // the store has read the stage
-    }
-    __syncwarp();
-    if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&empty_bar[stage])) : "memory");
-  }
-}
-
-// One persistent cooperative launch (one CTA per SM) does both projections:
-// phase A (gate/up -> h) and phase B (down -> y) share one weight ring, so
-// the producer keeps streaming down rows while the consumers wait at a
-// bounded grid-wide barrier for every h row of phase A.
+// One persistent cooperative launch (one CTA per SM) does both projections;
+// see fused_ffn_body.
 template <int NT, int VA, int VB>
 __global__ void __launch_bounds__(kRingThreads, 1)
 gemv_fused_kernel(GemvParams p, unsigned int* grid_count) {
   extern __shared__ uint8_t ring_raw[];
-  __shared__ int s_pref[kMaxE + 1];
-  __shared__ int s_warp[kRingThreads / 32];
-  __shared__ int s_off[kMaxE];
-  __shared__ int s_ent[kMaxE];
-  __shared__ int s_fill[kMaxE];
-  __shared__ __align__(8) uint64_t full_bar[kRingStages], empty_bar[kRingStages];
-  __shared__ int s_abort;
+  __shared__ __align__(16) FusedShared fs;
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ring_raw) + 127) & ~uintptr_t(127));
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-  if (tid == 0) {
-    for (int s = 0; s < kRingStages; ++s) {
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&full_bar[s])));
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&empty_bar[s])));
-    }
-    s_abort = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
+  const int tid = threadIdx.x, lane = tid & 31;
+  if (tid == 0) ring_init(fs);
   pdl_wait();
   for (int e = tid; e < p.E; e += blockDim.x) {
-    s_off[e] = p.offsets[e];
-    s_ent[e] = p.c.slot_table[p.layer * p.E + e];
-    s_fill[e] = -1;
+    fs.off[e] = p.offsets[e];
+    fs.ent[e] = p.c.slot_table[p.layer * p.E + e];
+    fs.fill[e] = -1;
   }
   __syncthreads();
   if (p.fills != nullptr && tid < 32) {
     const int nf = *p.n_fill;
     for (int f = lane; f < nf; f += 32) {
       const int e = p.fills[2 * f] - p.layer * p.E;
-      if (e >= 0 && e < p.E) s_fill[e] = p.fills[2 * f + 1];
+      if (e >= 0 && e < p.E) fs.fill[e] = p.fills[2 * f + 1];
     }
   }
-  build_prefix<NT>(p, s_pref, s_warp);   // ends with __syncthreads
-  volatile int* abort_flag = &s_abort;
-  RingState st = {0, -1, false};
-  const bool producer = warp == kConsumerWarps;
-
-  if (!producer || lane == 0) {
-    ring_phase<NT, true, VA>(p, s_pref, s_off, s_ent, s_fill, ring, full_bar, empty_bar, abort_flag, st, producer);
-    if (!producer) {
-      // grid-wide barrier: every h row of phase A is written before any is read
-      __threadfence();
-      asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
-      if (tid == 0) {
-        __threadfence();
-        atomicAdd(grid_count, 1u);
-        const unsigned long long t0 = gtimer();
-        while (*reinterpret_cast<volatile unsigned int*>(grid_count) < gridDim.x) {
-          if (*abort_flag) break;
-          if (gtimer() - t0 > kGridWaitNs) {
-            *abort_flag = 1;
-            break;
-          }
-        }
-        __threadfence();
-      }
-      asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
-    }
-    if (!*abort_flag)
-      ring_phase<NT, false, VB>(p, s_pref, s_off, s_ent, s_fill, ring, full_bar, empty_bar, abort_flag, st, producer);
-    if (producer) {
-      // drain: the copies of the last ring round land before the CTA exits
-      volatile int no_abort = 0;
-      for (int q = st.armed_last; q >= 0 && q > st.armed_last - kRingStages; --q)
-        ring_wait(&full_bar[q % kRingStages], (uint32_t)(q / kRingStages) & 1u, &no_abort);
-    } else {
-      if (st.stored && lane == 0) bulk_wait_all();   // fused-fill writes complete before exit
-      if (p.combine_out != nullptr) {
-        // second grid-wide barrier: every y row is written; then the gate-weighted
-        // combine in fixed expert order, spread over all CTAs
-        __threadfence();
-        asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
-        if (tid == 0) {
-          __threadfence();
-          atomicAdd(grid_count + 1, 1u);
-          const unsigned long long t0 = gtimer();
-          while (*reinterpret_cast<volatile unsigned int*>(grid_count + 1) < gridDim.x) {
-            if (*abort_flag) break;
-            if (gtimer() - t0 > kGridWaitNs) {
-              *abort_flag = 1;
-              break;
-            }
-          }
-          __threadfence();
-        }
-        asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
-        if (!*abort_flag) {
-          const int H4 = p.H >> 2;
-          const int items = p.T * H4;
-          for (int it = blockIdx.x * (kConsumerWarps * 32) + tid; it < items; it += gridDim.x * (kConsumerWarps * 32)) {
-            const int t = it / H4, c4 = it - t * H4;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int jj = 0; jj < p.k; ++jj) {
-              const float w = p.combine_w[t * p.k + jj];
-              const float4 y = __ldcg(reinterpret_cast<const float4*>(p.y + (size_t)(t * p.k + jj) * p.H) + c4);
-              acc.x = fmaf(w, y.x, acc.x);
-              acc.y = fmaf(w, y.y, acc.y);
-              acc.z = fmaf(w, y.z, acc.z);
-              acc.w = fmaf(w, y.w, acc.w);
-            }
-            __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-            __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-            uint2 packed;
-            packed.x = *reinterpret_cast<uint32_t*>(&lo);
-            packed.y = *reinterpret_cast<uint32_t*>(&hi);
-            reinterpret_cast<uint2*>(p.combine_out + (size_t)t * p.H)[c4] = packed;
-          }
-        }
-      }
-    }
-  }
+  fused_ffn_body<NT, VA, VB>(p, grid_count, fs, ring);
   pdl_trigger();
   __syncthreads();
-  if (*abort_flag && tid == 0) set_status(p.status, MOE_DEV_ERR_TIMEOUT);
+  if (fs.abort && tid == 0) set_status(p.status, MOE_DEV_ERR_TIMEOUT);
 }
 
-constexpr int kRingSmem = kRingStages * kUnitBytes + 128;
 
 template <int NT, int VA, int VB>
 cudaError_t launch_fused_one(const GemvParams& p, unsigned int* grid_count, cudaStream_t s) {
@@ -652,7 +203,8 @@ cudaError_t launch_fused_one(const GemvParams& p, unsigned int* grid_count, cuda
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  cudaError_t err = cudaMemsetAsync(grid_count, 0, 2 * sizeof(unsigned int), s);
+  const size_t words = p.inst_done != nullptr ? 4 + (size_t)p.T * p.k : 2;
+  cudaError_t err = cudaMemsetAsync(grid_count, 0, words * sizeof(unsigned int), s);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms());

@@ -5,6 +5,8 @@
 
 namespace moe {
 
+constexpr int kMaxFusedInst = 1024;   // fused launches with at most this many routed rows track instances
+
 struct GemvParams {
   moe_cache c;
   int layer, E, H, I, k, T;
@@ -23,6 +25,10 @@ struct GemvParams {
   const int32_t* fills;     // [n][2]: (staging slot l*E+e, cache slot)
   const int32_t* n_fill;    // device count of valid rows of `fills`
   unsigned int* grid_count; // workspace words for the fused kernel's grid barriers
+  // Per-instance phase-A completion counters (zero at launch, one word per
+  // instance), or null: the fused kernel then separates its phases with a
+  // grid barrier.
+  unsigned int* inst_done;
   // Fused combine (optional): out[t] = sum_j combine_w[t*k+j] * y[t*k+j] after the FFN.
   const float* combine_w;
   __nv_bfloat16* combine_out;

@@ -9,98 +9,12 @@
 // calls, with warp shuffles instead of block barriers: lane r holds routed
 // row r (r = t*k + j).  Used by moe_layer_forward on decode-sized calls,
 // after a router launch that only writes the logits.
-#include "moe_common.cuh"
+#include "front_warp.cuh"
 
 namespace moe {
 namespace {
 
 constexpr int kMaxSlotsPerLane = 128;   // cache pools up to 4096 slots
-
-__device__ inline unsigned long long mix64(unsigned long long z) {
-  // SplitMix64 output function (Steele, Lea & Flood 2014)
-  z += 0x9E3779B97F4A7C15ull;
-  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
-  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
-  return z ^ (z >> 31);
-}
-
-__device__ inline int fill_rule(int m, uint32_t phi, int min_fill) {
-  const long long mm = m, p = phi;
-  const long long lo = (mm * p) >> 16;
-  const long long c_lo = max(lo * (65536 - p), (mm - lo) * p);
-  const long long c_hi = max((lo + 1) * (65536 - p), (mm - lo - 1) * p);
-  long long q = (c_hi < c_lo) ? lo + 1 : lo;
-  if (q > mm) q = mm;
-  if (min_fill && p > 0 && mm > 0 && q < 1) q = 1;
-  return (int)q;
-}
-
-__device__ inline unsigned lane_lt() {
-  unsigned m;
-  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
-  return m;
-}
-
-// One token's top-k over E <= 512 logits; every lane returns the selected ids
-// (ascending) and weights through its first k lanes' registers.
-__device__ inline void topk_lanes(const float* row, int E, int k, int& id_out, float& w_out) {
-  const int lane = threadIdx.x & 31;
-  constexpr int kPer = kMaxRouteE / 32;
-  float v[kPer];
-#pragma unroll
-  for (int j = 0; j < kPer; ++j) {
-    const int e = lane + 32 * j;
-    v[j] = (e < E) ? __ldcg(row + e) : -INFINITY;
-  }
-  uint32_t taken = 0;
-  float sel_v = -INFINITY;
-  int sel_id = 0x7fffffff;
-  for (int r = 0; r < k; ++r) {
-    float bv = -INFINITY;
-    int bid = 0x7fffffff;
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      const int e = lane + 32 * j;
-      if (e < E && !((taken >> j) & 1u) && (v[j] > bv || (v[j] == bv && e < bid))) {
-        bv = v[j];
-        bid = e;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oid = __shfl_xor_sync(0xffffffffu, bid, o);
-      if (ov > bv || (ov == bv && oid < bid)) {
-        bv = ov;
-        bid = oid;
-      }
-    }
-    if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
-    if (lane == r) {
-      sel_v = bv;
-      sel_id = bid;
-    }
-  }
-  const float vmax = __shfl_sync(0xffffffffu, sel_v, 0);
-  const float ex = (lane < k) ? expf(sel_v - vmax) : 0.0f;
-  const float denom = warp_sum(ex);
-  int rank = 0;
-  for (int j = 0; j < k; ++j) rank += (__shfl_sync(0xffffffffu, sel_id, j) < sel_id) ? 1 : 0;
-  // lane `rank` receives the id of rank `rank`
-  int out_id = 0x7fffffff;
-  float out_w = 0.0f;
-  for (int j = 0; j < k; ++j) {
-    const int rj = __shfl_sync(0xffffffffu, rank, j);
-    const int ij = __shfl_sync(0xffffffffu, sel_id, j);
-    const float wj = __shfl_sync(0xffffffffu, ex, j);
-    if (lane == rj) {
-      out_id = ij;
-      out_w = wj / denom;
-    }
-  }
-  id_out = out_id;
-  w_out = out_w;
-}
 
 struct FrontOut {
   int32_t* topk_ids;

@@ -81,6 +81,7 @@ struct LayerWs {
   int32_t* inv_perm;
   float* y_rows;
   __nv_bfloat16* x_perm;
+  float* logits;     // decode-sized calls: router logits of the one-launch layer
   void* bind_ws;     // fill count + fill list, alive until the FFN has run
   void* scratch;
   size_t bytes;
@@ -104,6 +105,7 @@ LayerWs layer_ws(void* ws, const moe_layer_buffers* b, int T, int k, int E, int 
   L.inv_perm = cv.take<int32_t>(R);
   L.y_rows = cv.take<float>(R * H);
   L.x_perm = needs_x_perm(mode, T) ? cv.take<__nv_bfloat16>(R * H) : nullptr;
+  L.logits = R <= 32 ? cv.take<float>((size_t)T * E) : nullptr;
   L.bind_ws = cv.take<char>(bind_ws_bytes(T, k, E));
   if (b) {
     if (b->topk_ids) L.ids = b->topk_ids;
@@ -262,6 +264,21 @@ int moe_layer_forward(const moe_layer* layer, const moe_cache* cache, const void
   const size_t scratch_bytes = ws_bytes - (size_t)(reinterpret_cast<char*>(L.scratch) - reinterpret_cast<char*>(ws));
   const bool fuse_fill = ffn_mode != MOE_FFN_GEMM && !L.x_perm && gemv_fused_ok(H, I);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (fuse_fill && L.logits && decode_layer_ok(T, k, E, H, I, cache->cache.n_slots) && layer->w_router &&
+      aligned16(x) && aligned16(layer->w_router)) {
+    // Decode: the whole layer in one cooperative launch (router, selection,
+    // residency decision, fused FFN with fills, combine, state commit).
+    st = check_bind_args(cache, layer->layer, T, k, phi_q16, fill_policy);
+    if (st != MOE_OK) return st;
+    unsigned int* grid_count = reinterpret_cast<unsigned int*>(
+        reinterpret_cast<char*>(L.scratch) + align_up((size_t)T * k * I * sizeof(__nv_bfloat16), 256));
+    cudaError_t err = launch_decode_layer(*cache, layer->layer, reinterpret_cast<const __nv_bfloat16*>(x), T, k,
+                                          layer->w_router, layer->bias, phi_q16, min_fill, fill_policy, seed, stats_dev,
+                                          L.logits, L.ids, L.w, L.counts, L.offsets, L.perm, L.inv_perm, L.y_rows,
+                                          reinterpret_cast<__nv_bfloat16*>(L.scratch), grid_count,
+                                          reinterpret_cast<__nv_bfloat16*>(out), dev_status, s);
+    return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  }
   if (fuse_fill && T <= 32 && E <= kMaxRouteE && front_small_ok(T, k, E, cache->cache.n_slots) &&
       k <= kMaxK && layer->w_router && aligned16(x) && aligned16(layer->w_router)) {
     // Decode: router logits over all SMs, then one warp selects, binds and

@@ -254,6 +254,13 @@ cudaError_t launch_route_tc(const __nv_bfloat16* x, int T, int H, const float* w
                             cudaStream_t s);
 cudaError_t launch_route_logits(const __nv_bfloat16* x, int T, int H, const float* w_router, const float* bias,
                                 int E, float* logits, cudaStream_t s);
+bool decode_layer_ok(int T, int k, int E, int H, int I, int n_slots);
+cudaError_t launch_decode_layer(const moe_cache& c, int layer, const __nv_bfloat16* x, int T, int k,
+                                const float* w_router, const float* bias, uint32_t phi_q16, int min_fill, int policy,
+                                uint64_t seed, moe_bind_stats* stats, float* logits, int32_t* topk_ids, float* topk_w,
+                                int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv_perm, float* y_rows,
+                                __nv_bfloat16* h, unsigned int* grid_count, __nv_bfloat16* out, uint32_t* status,
+                                cudaStream_t s);
 bool front_small_ok(int T, int k, int E, int n_slots);
 cudaError_t launch_front_small(const float* logits, int T, int k, const moe_cache& c, int layer, uint32_t phi_q16,
                                int min_fill, int policy, uint64_t seed, moe_bind_stats* stats, int32_t* topk_ids,
