@@ -98,10 +98,20 @@ def router_flops(cfg):
     return 2.0 * cfg.T * cfg.H * cfg.E
 
 
-# DRAM bytes (read + write) per launch of the expert-FFN call, from the ncu
-# captures summarised under profiles/; a workload whose kernels changed since
-# their capture has no entry (null in the JSON line).
-FFN_TRAFFIC = {}
+# DRAM bytes (read + write) per launch of the dominant kernel, from the ncu
+# captures summarised under profiles/ (a workload without an entry, or whose
+# kernels changed since their capture, reports null).
+#  decode: decode_layer_kernel captured on decode_profile (same six 50.3 MB
+#    experts per step, one cache fill; profiles/decode_layer_kernel_profile.md)
+#    plus the 224 extra 16 KB router rows of the 256-expert layer.
+#  prefill: the two gemm_kernel launches captured on prefill_profile (64
+#    experts x ~192 rows; profiles/gemm_prefill_profile.md) scaled by the
+#    units processed (4x the experts, 4x the rows): traffic there is each
+#    weight byte once plus the activations, both proportional.
+FFN_TRAFFIC = {"decode": 302683392 + 45722624 + 224 * 16384,
+               "prefill": 4 * (2254040000 + 48339456 + 1127092000 + 181571840)}
+TRAFFIC_NOTE = {"decode": "ncu capture of decode_layer_kernel on decode_profile (1 fill) + 224 router rows",
+                "prefill": "ncu capture of the two gemm_kernel launches on prefill_profile, x4 (units processed)"}
 
 
 # ------------------------------------------------------------------ our arm
@@ -168,6 +178,7 @@ def run_ours(args, rank, world):
 
     # warm-up steps (untimed), then K timed steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    stats_host = torch.zeros((args.steps, 8), dtype=torch.int32).pin_memory()
     with torch.cuda.stream(stream):
         for s in range(args.warmup):
             if decode_like:
@@ -188,6 +199,7 @@ def run_ours(args, rank, world):
             ev[i][0].record(stream)
             graph.replay()
             ev[i][1].record(stream)
+            stats_host[i].copy_(stats, non_blocking=True)   # residency counts of the step, outside the events
             flush.zero_()
     torch.cuda.synchronize()
     barrier()
@@ -199,8 +211,12 @@ def run_ours(args, rank, world):
 
     total_s, value = aggregate_replicas(total_s, args.steps, T, world, dev)
 
-    # ---- dominant kernel: the expert FFN call, events on its stream (eager pass)
-    roof = measure_ffn_roofline(cfg, dc, layers, xs, decode_like, stream, peaks, args, moe, torch)
+    # ---- dominant kernel: decode-sized calls run the whole layer as one kernel (the timed
+    # step itself); otherwise the expert-FFN call, timed alone
+    if kernels_per_step == cfg.n_layers:
+        roof = decode_step_roofline(cfg, step_ms, stats_host.numpy(), peaks)
+    else:
+        roof = measure_ffn_roofline(cfg, dc, layers, xs, decode_like, stream, peaks, args, moe, torch)
 
     # ---- end to end through the public call with host buffers
     e2e = measure_e2e(cfg, dc, layers, decode_like, stream, args, moe, torch, ws, ws_bytes, status, stats)
@@ -244,6 +260,37 @@ def workload_config(cfg, world):
             "phi_q16": cfg.phi_q16, "fill_policy": "random" if cfg.fill_policy else "lowest_id",
             "routing_bias": cfg.bias, "l2": "flushed between steps (256 MB write)",
             "parallelism": f"replicas x{world}", "graph": "one CUDA graph replay per step"}
+
+
+def decode_step_roofline(cfg, step_ms, stats, peaks):
+    """Decode-sized steps are one kernel (router, residency decision, fused
+    gate/up + down weight streaming with cache fills, combine).  Algorithmic
+    bytes per step: every distinct routed expert's weights once, one more
+    expert write per cache fill, the router weights, and the activations
+    (token row, h, y rows, output).  Duration: the CUDA events around the
+    step's graph replay (the kernel and its 4 + T*k word counter reset)."""
+    T, k, E, H, I = cfg.T, cfg.k, cfg.E, cfg.H, cfg.I
+    R = T * k
+    n_unique, n_fill = stats[:, 0].astype(np.float64), stats[:, 4].astype(np.float64)
+    act = T * H * 2 + R * I * 2 * 2 + R * H * 4 * 2 + T * H * 2
+    byts = (n_unique + n_fill) * cfg.expert_bytes + E * H * 4 + act
+    t = float(np.sum(step_ms)) / 1e3
+    achieved = float(np.sum(byts)) / t / 1e9
+    peak = peaks["hbm_gbs"]
+    return {"kernel": "decode_layer_kernel (whole layer in one cooperative launch)", "bound": "hbm",
+            "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "traffic": FFN_TRAFFIC.get(cfg.name), "traffic_note": TRAFFIC_NOTE.get(cfg.name),
+            "peak_source": peaks["source"] + " (burst copy bandwidth)",
+            "algorithmic_bytes_per_step": int(np.mean(byts)), "step_us": round(t / len(step_ms) * 1e6, 3),
+            "fills_per_step": round(float(np.mean(n_fill)), 3),
+            "timing": "CUDA events around each timed step (the kernel is the whole step)"}
+
+
+def ffn_bytes(cfg, active):
+    """Algorithmic HBM bytes of one expert-FFN call: each active expert's
+    weights once, the gathered token rows, h written and read, y rows written."""
+    R = cfg.T * cfg.k
+    return active * cfg.expert_bytes + R * cfg.H * 2 + R * cfg.I * 2 * 2 + R * cfg.H * 4
 
 
 def measure_ffn_roofline(cfg, dc, layers, xs, decode_like, stream, peaks, args, moe, torch):
@@ -311,25 +358,29 @@ def measure_ffn_roofline(cfg, dc, layers, xs, decode_like, stream, peaks, args, 
             torch.cuda.synchronize()
             times.append(a.elapsed_time(b) / 1e3)
             active = int((counts > 0).sum().item())
-            byts.append(active * cfg.expert_bytes + R * cfg.H * 2 + R * cfg.H * 4)
+            byts.append(ffn_bytes(cfg, active))
             flops.append(expert_ffn_flops(cfg))
     t = float(np.mean(times))
     traffic = FFN_TRAFFIC.get(cfg.name)
-    if decode_like:
-        achieved = float(np.mean(byts)) / t / 1e9
-        peak = peaks["hbm_gbs"]
-        return {"kernel": "moe_expert_ffn_grouped (fused gate/up + down GEMV, one launch)", "bound": "hbm",
-                "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                "traffic": traffic, "peak_source": peaks["source"] + " (burst copy bandwidth)",
-                "algorithmic_bytes_per_call": int(np.mean(byts)), "call_us": round(t * 1e6, 3),
-                "timing": "graph replay of the FFN call, L2 flushed before each"}
-    achieved = float(np.mean(flops)) / t / 1e12
-    peak = peaks["bf16_tflops"]
-    return {"kernel": "moe_expert_ffn_grouped (tcgen05 gate/up + down GEMM)", "bound": "tensor",
-            "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-            "traffic": traffic, "peak_source": peaks["source"] + " (burst cuBLAS bf16)",
-            "flops_per_call": expert_ffn_flops(cfg), "call_us": round(t * 1e6, 3),
-            "timing": "graph replay of the FFN call, L2 flushed before each"}
+    # both rooflines; the one whose time at peak is longer binds
+    hbm = float(np.mean(byts)) / t / 1e9
+    tc = float(np.mean(flops)) / t / 1e12
+    t_hbm = float(np.mean(byts)) / (peaks["hbm_gbs"] * 1e9)
+    t_tc = float(np.mean(flops)) / (peaks["bf16_tflops"] * 1e12)
+    hbm_part = {"bound": "hbm", "achieved": round(hbm, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(hbm / peaks["hbm_gbs"], 4), "peak_source": peaks["source"] + " (burst copy bandwidth)",
+                "algorithmic_bytes_per_call": int(np.mean(byts))}
+    tc_part = {"bound": "tensor", "achieved": round(tc, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+               "frac": round(tc / peaks["bf16_tflops"], 4), "peak_source": peaks["source"] + " (burst cuBLAS bf16)",
+               "flops_per_call": float(np.mean(flops))}
+    main, other = (hbm_part, tc_part) if t_hbm >= t_tc else (tc_part, hbm_part)
+    kernel = ("moe_expert_ffn_grouped (fused gate/up + down GEMV, one launch)" if decode_like and cfg.T <= 8
+              else "moe_expert_ffn_grouped (tcgen05 gate/up + down GEMM, GEMV for groups of <= 2 rows)")
+    out = {"kernel": kernel, **main, "traffic": traffic, "traffic_note": TRAFFIC_NOTE.get(cfg.name),
+           "call_us": round(t * 1e6, 3),
+           "timing": "graph replay of the FFN call, L2 flushed before each",
+           "other_roofline": other}
+    return out
 
 
 def measure_e2e(cfg, dc, layers, decode_like, stream, args, moe, torch, ws, ws_bytes, status, stats):
