@@ -114,6 +114,9 @@ TRAFFIC_NOTE = {"decode": "ncu capture of decode_layer_kernel on decode_profile 
                 "prefill": "ncu capture of the two gemm_kernel launches on prefill_profile, x4 (units processed)"}
 
 
+FFN_MODES = {"auto": lambda m: m.MOE_FFN_AUTO, "gemv": lambda m: m.MOE_FFN_GEMV, "gemm": lambda m: m.MOE_FFN_GEMM}
+
+
 # ------------------------------------------------------------------ our arm
 def run_ours(args, rank, world):
     import torch
@@ -136,7 +139,7 @@ def run_ours(args, rank, world):
     else:
         xs = [to_dev_bf16(gen.x_bits(cfg, l, 0), dev) for l in range(cfg.n_layers)]
     T, H = cfg.T, cfg.H
-    mode = moe.MOE_FFN_AUTO
+    mode = FFN_MODES[args.ffn_mode](moe)
     ws_bytes = moe.moe_layer_workspace_size(layers[0].struct, dc.struct, T, mode)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
@@ -314,7 +317,7 @@ def measure_ffn_roofline(cfg, dc, layers, xs, decode_like, stream, peaks, args, 
     xp = torch.empty((R, cfg.H), dtype=torch.bfloat16, device=dev) if T > 8 else None
     x_cur = torch.empty((T, cfg.H), dtype=torch.bfloat16, device=dev)
     layer_cur = torch.zeros(1, dtype=torch.int32)      # host value read at capture time only
-    mode = moe.MOE_FFN_AUTO
+    mode = FFN_MODES[args.ffn_mode](moe)
     wsb = max(moe.moe_route_topk_workspace_size(T, cfg.H, E), moe.moe_dispatch_workspace_size(T, k, E),
               moe.moe_expert_ffn_workspace_size(T, k, E, cfg.H, cfg.I, mode))
     wsx = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
@@ -403,7 +406,7 @@ def measure_e2e(cfg, dc, layers, decode_like, stream, args, moe, torch, ws, ws_b
                 hx = host_x[i] if decode_like else host_x[0]
                 x_dev.copy_(hx, non_blocking=True)
                 moe.moe_layer_forward(layers[l].struct, dc.struct, x_dev, T, out, cfg.phi_q16, cfg.min_fill,
-                                      cfg.fill_policy, 1000 + l, moe.MOE_FFN_AUTO, None, ws, ws_bytes, status, stats,
+                                      cfg.fill_policy, 1000 + l, FFN_MODES[args.ffn_mode](moe), None, ws, ws_bytes, status, stats,
                                       stream)
                 host_out.copy_(out, non_blocking=True)
             stream.synchronize()
@@ -477,6 +480,8 @@ def main():
     ap.add_argument("--cpu-baseline-s", type=float, default=15.0)
     ap.add_argument("--reference-budget-s", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ffn-mode", default="auto", choices=sorted(FFN_MODES),
+                    help="expert-FFN kernel choice passed to moe_layer_forward (default: auto)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -30,7 +30,8 @@ cudaError_t launch_ffn(const moe_cache& c, int layer, const int32_t* counts, con
     if (!gemm_shape_ok(c.H, c.I) || !x_perm) return cudaErrorNotSupported;
     gemv_max = 0;
   } else if (mode == MOE_FFN_AUTO && x_perm && gemm_shape_ok(c.H, c.I) && T > kGemvMaxRows) {
-    gemv_max = kGemvMaxRows;
+    // the GEMM pads a group only to 16 token rows, so it takes small groups too
+    gemv_max = 0;
   }
   // a fused fill or combine is only done by the fused GEMV kernel
   if ((fused_fills != nullptr || combine_out != nullptr) && gemv_max != INT_MAX) return cudaErrorNotSupported;

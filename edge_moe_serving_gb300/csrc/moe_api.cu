@@ -87,7 +87,7 @@ struct LayerWs {
   size_t bytes;
 };
 
-// gathered rows feed the GEMM kernel, which runs on groups above kGemvMaxRows
+// gathered rows feed the GEMM kernel, which AUTO uses for calls of more than kGemvMaxRows tokens
 bool needs_x_perm(int mode, int T) {
   return mode == MOE_FFN_GEMM || (mode == MOE_FFN_AUTO && T > kGemvMaxRows);
 }

@@ -16,7 +16,7 @@ constexpr int kMaxE = 1024;           // bind / dispatch limit
 constexpr int kMaxRouteE = 512;       // router top-k limit (16 logits per lane)
 constexpr int kMaxK = 16;
 constexpr int kMaxCacheSlots = 16384; // bind kernel keeps all (stamp, slot) keys in shared memory
-constexpr int kGemvMaxRows = 2;       // AUTO mode: groups up to this size use the GEMV path
+constexpr int kGemvMaxRows = 2;       // AUTO mode: calls of up to this many tokens use the GEMV path
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 

@@ -66,7 +66,8 @@ typedef struct CUstream_st* moe_stream_t; /* same type as cudaStream_t; NULL = l
 #define MOE_FILL_RANDOM 1     /* a seeded uniformly random q-subset (SplitMix64 keys) */
 
 /* expert-FFN kernel selection */
-#define MOE_FFN_AUTO 0  /* weight-streaming GEMV for groups of <= 2 rows, tensor-core GEMM above */
+#define MOE_FFN_AUTO 0  /* calls of <= 2 tokens (or without gathered rows): the fused weight-streaming
+                           GEMV; larger calls: the tensor-core grouped GEMM for every group */
 #define MOE_FFN_GEMV 1  /* weight-streaming GEMV for every group */
 #define MOE_FFN_GEMM 2  /* tcgen05 grouped GEMM for every non-empty group */
 

@@ -53,8 +53,8 @@ def test_gemm_forced_tiny():
 
 @pytest.mark.parametrize("T", [300, 1000])
 def test_gemm_auto_mixed_groups(T):
-    """Groups above and below the GEMV threshold, groups over 256 rows, ragged
-    tails, and experts served from both pools."""
+    """Groups of a few rows and of over 256 rows, ragged tails, and experts
+    served from both pools, in every FFN mode."""
     cfg = dataclasses.replace(CONFIGS["batched_decode"], name="mixed", T=T, bias="none", cache_slots=40)
     dc = DeviceCache(cfg, DEV)
     xb = gen.f32_to_bf16_bits(np.random.default_rng(T).standard_normal((T, cfg.H)).astype(np.float32))
