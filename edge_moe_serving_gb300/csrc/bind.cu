@@ -30,7 +30,7 @@ namespace {
 
 constexpr int kBindThreads = 1024;
 constexpr int kCopyThreads = 256;
-constexpr size_t kCopyChunk = 64 * 1024;  // bytes per work item of the fill copy
+constexpr size_t kCopyChunk = 16 * 1024;  // bytes per work item of the fill copy (one load round per CTA)
 
 __device__ inline unsigned long long splitmix64(unsigned long long z) {
   // SplitMix64 output function (Steele, Lea & Flood 2014)

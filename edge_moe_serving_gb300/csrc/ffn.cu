@@ -66,7 +66,7 @@ cudaError_t launch_ffn(const moe_cache& c, int layer, const int32_t* counts, con
     if (err != cudaSuccess) return err;
   }
   if (gemv_max != INT_MAX)
-    return launch_gemm(c, layer, counts, offsets, perm, mask, gemv_max, x_perm, R, h, y_rows, status, s);
+    return launch_gemm(c, layer, counts, offsets, perm, mask, gemv_max, x_perm, T, R, h, y_rows, status, s);
   return cudaSuccess;
 }
 

@@ -24,7 +24,8 @@
 // owner), warps 2..9 = epilogue (TMEM lanes 32*(warp%4) .. +31; the two warps
 // on one lane quarter take alternate 32-column chunks).  Shared memory holds
 // 3 stages of {2 weight tiles 128x64, token tile <=256x64} bf16 in the
-// 128-byte swizzled K-major layout TMA writes.  The two accumulators use TMEM
+// 128-byte swizzled K-major layout TMA writes (calls of at most 32 tokens:
+// 6 stages with a token tile of <= 32 rows).  The two accumulators use TMEM
 // columns [0, N) and [256, 256 + N).  Every mbarrier wait is bounded (about
 // one second of %globaltimer); on expiry the CTA sets MOE_DEV_ERR_TIMEOUT,
 // drains its in-flight copies and MMAs, frees TMEM and returns.
@@ -39,12 +40,21 @@ namespace {
 using namespace tc;
 
 constexpr int kBM = 128;                            // weight rows of one MMA
-constexpr int kChunk = 256;                         // token rows of one tile at most
-constexpr int kStages = 3;
 constexpr int kATile = kBM * kBK * 2;               // 16 KB
-constexpr int kBTileMax = kChunk * kBK * 2;         // 32 KB
-constexpr int kStageBytes = 2 * kATile + kBTileMax; // 64 KB
-constexpr int kSmemBytes = kStages * kStageBytes + 1024;
+
+// Pipeline shape by the largest token chunk of a tile: 256-row chunks with
+// three 64 KB stages, or (calls of at most 32 tokens, where the tiles are
+// weight streams with a thin token operand) 32-row chunks with six 36 KB
+// stages, twice the bytes in flight.
+template <int CHUNK>
+struct Shape {
+  static constexpr int kChunk = CHUNK;                            // token rows of one tile at most
+  static constexpr int kStages = CHUNK <= 32 ? 6 : 3;
+  static constexpr int kBTileMax = CHUNK * kBK * 2;
+  static constexpr int kStageBytes = 2 * kATile + kBTileMax;
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024;
+};
+static_assert(Shape<256>::kSmemBytes <= 227 * 1024 && Shape<32>::kSmemBytes <= 227 * 1024, "shared memory");
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kTmemCols = 512;
@@ -68,6 +78,7 @@ struct GemmParams {
 
 // ---------------------------------------------------------------- tile list
 // s_pref[e] = first chunk index of expert e; s_pref[E] = number of chunks.
+template <int kChunk>
 __device__ void build_chunk_prefix(const GemmParams& p, int* s_pref, int* s_warp) {
   const int tid = threadIdx.x, nthreads = blockDim.x;
   const int per_thread = (p.E + nthreads - 1) / nthreads;
@@ -129,6 +140,7 @@ struct Tile {
   bool ok;
 };
 
+template <int kChunk>
 __device__ inline Tile decode_tile(const GemmParams& p, const int* s_pref, int t) {
   Tile tl;
   const int ci = t / p.n_fb;
@@ -152,12 +164,14 @@ __device__ inline Tile decode_tile(const GemmParams& p, const int* s_pref, int t
 // map_w{0,1}_{cache,stage}: weight banks [n_slots * rows_per_slot, K] with a
 // 128-row box (gate/up: w0 = gate, w1 = up; down: w0 = w1 = down).
 // map_b64 / map_b16: the token operand [R, K] with 64- and 16-row boxes.
-template <bool GATEUP>
+template <bool GATEUP, int CHUNK>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap map_b64, const __grid_constant__ CUtensorMap map_b16,
             const __grid_constant__ CUtensorMap map_w0_cache, const __grid_constant__ CUtensorMap map_w1_cache,
             const __grid_constant__ CUtensorMap map_w0_stage, const __grid_constant__ CUtensorMap map_w1_stage,
             const GemmParams p) {
+  using S = Shape<CHUNK>;
+  constexpr int kStages = S::kStages, kStageBytes = S::kStageBytes;
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_pref[kMaxE + 1];
   __shared__ int s_warp[kThreads / 32];
@@ -185,7 +199,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_b64, const __grid_constant__
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   pdl_wait();
-  build_chunk_prefix(p, s_pref, s_warp);   // contains __syncthreads
+  build_chunk_prefix<CHUNK>(p, s_pref, s_warp);   // contains __syncthreads
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -200,10 +214,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_b64, const __grid_constant__
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      bool armed[kStages] = {false, false, false};
-      uint32_t armed_parity[kStages] = {0, 0, 0};
+      bool armed[kStages] = {};
+      uint32_t armed_parity[kStages] = {};
       for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
-        const Tile tl = decode_tile(p, s_pref, t);
+        const Tile tl = decode_tile<CHUNK>(p, s_pref, t);
         if (!tl.ok) continue;
         const CUtensorMap* mw0 = tl.pool ? &map_w0_stage : &map_w0_cache;
         const CUtensorMap* mw1 = tl.pool ? &map_w1_stage : &map_w1_cache;
@@ -245,7 +259,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_b64, const __grid_constant__
       uint32_t phase = 0, tphase = 0;
       bool issued = false;
       for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
-        const Tile tl = decode_tile(p, s_pref, t);
+        const Tile tl = decode_tile<CHUNK>(p, s_pref, t);
         if (!tl.ok) continue;
         const uint32_t idesc = make_idesc(kBM, tl.N);
         if (!mbar_wait(&tmem_empty, tphase ^ 1u, abort_flag)) break;
@@ -292,7 +306,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_b64, const __grid_constant__
     const uint32_t lane_addr = tmem_base + ((uint32_t)(quarter * 32) << 16);
     uint32_t tphase = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const Tile tl = decode_tile(p, s_pref, t);
+      const Tile tl = decode_tile<CHUNK>(p, s_pref, t);
       if (!tl.ok) {
         if (tid == 64) set_status(p.status, tl.entry < 0 ? MOE_DEV_ERR_UNBOUND : MOE_DEV_ERR_BAD_SLOT);
         continue;
@@ -350,6 +364,20 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_b64, const __grid_constant__
   if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols));
 }
 
+template <bool GATEUP, int CHUNK>
+cudaError_t launch_one(int grid, cudaStream_t s, const CUtensorMap& b64, const CUtensorMap& b16, const CUtensorMap& w0c,
+                       const CUtensorMap& w1c, const CUtensorMap& w0s, const CUtensorMap& w1s, const GemmParams& p) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<GATEUP, CHUNK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Shape<CHUNK>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  return launch_k(gemm_kernel<GATEUP, CHUNK>, grid, kThreads, Shape<CHUNK>::kSmemBytes, s, b64, b16, w0c, w1c, w0s,
+                  w1s, p);
+}
+
 }  // namespace
 
 bool gemm_shape_ok(int H, int I) { return H % 256 == 0 && I % 128 == 0 && H >= 256 && I >= 128; }
@@ -357,16 +385,8 @@ bool gemm_shape_ok(int H, int I) { return H % 256 == 0 && I % 128 == 0 && H >= 2
 // Grouped GEMM over the experts with more than min_rows rows (gate/up, then down).
 cudaError_t launch_gemm(const moe_cache& c, int layer, const int32_t* counts, const int32_t* offsets,
                         const int32_t* perm, const uint8_t* mask, int min_rows, const __nv_bfloat16* x_perm,
-                        int R, __nv_bfloat16* h, float* y, uint32_t* status, cudaStream_t s) {
+                        int T, int R, __nv_bfloat16* h, float* y, uint32_t* status, cudaStream_t s) {
   if (!gemm_shape_ok(c.H, c.I)) return cudaErrorNotSupported;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e1 = cudaFuncSetAttribute(gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    cudaError_t e2 = cudaFuncSetAttribute(gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e1 != cudaSuccess) return e1;
-    if (e2 != cudaSuccess) return e2;
-    attr = true;
-  }
   const bool has_stage = c.staging.w_gate != nullptr;
   const uint64_t H = (uint64_t)c.H, I = (uint64_t)c.I;
   GemmParams p;
@@ -403,7 +423,9 @@ cudaError_t launch_gemm(const moe_cache& c, int layer, const int32_t* counts, co
   p.K = c.H;
   p.n_fb = c.I / kBM;
   const int grid = num_sms();
-  cudaError_t err = launch_k(gemm_kernel<true>, grid, kThreads, kSmemBytes, s, x64, x16, g0, u0, g1, u1, p);
+  const bool thin = T <= 32;   // a group has at most T rows (one per token)
+  cudaError_t err = thin ? launch_one<true, 32>(grid, s, x64, x16, g0, u0, g1, u1, p)
+                         : launch_one<true, 256>(grid, s, x64, x16, g0, u0, g1, u1, p);
   if (err != cudaSuccess) return err;
 
   CUtensorMap h64, h16, d0, d1;
@@ -417,7 +439,8 @@ cudaError_t launch_gemm(const moe_cache& c, int layer, const int32_t* counts, co
   }
   p.K = c.I;
   p.n_fb = c.H / (2 * kBM);
-  return launch_k(gemm_kernel<false>, grid, kThreads, kSmemBytes, s, h64, h16, d0, d0, d1, d1, p);
+  return thin ? launch_one<false, 32>(grid, s, h64, h16, d0, d0, d1, d1, p)
+              : launch_one<false, 256>(grid, s, h64, h16, d0, d0, d1, d1, p);
 }
 
 }  // namespace moe

@@ -36,78 +36,9 @@ __device__ inline unsigned lane_lt() {
   return m;
 }
 
-// Order-preserving map of a float to 32 unsigned bits (larger float, larger
-// key; equal floats, equal keys); its inverse.
-__device__ inline uint32_t ord_key(float v) {
-  const uint32_t u = __float_as_uint(v == 0.0f ? 0.0f : v);   // -0 and +0 compare equal
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-__device__ inline float ord_val(uint32_t k) { return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k); }
-
-// One token's top-k over E <= 512 logits (order: logit descending, id
-// ascending); every lane returns the selected ids (ascending) and weights
-// through its first k lanes' registers.  Lane l holds experts l + 32 j and its
-// best untaken candidate; each round is two warp reductions (largest key,
-// then the lowest id among lanes holding it), and only the lane that owned
-// the winner rescans its candidates.
+// One token's top-k through L2 (the logits come from other CTAs of the launch).
 __device__ inline void topk_lanes(const float* row, int E, int k, int& id_out, float& w_out) {
-  const int lane = threadIdx.x & 31;
-  constexpr int kPer = kMaxRouteE / 32;
-  uint32_t key[kPer];
-#pragma unroll
-  for (int j = 0; j < kPer; ++j) {
-    const int e = lane + 32 * j;
-    key[j] = (e < E) ? ord_key(__ldcg(row + e)) : 0u;   // 0: no expert (every logit maps above 0)
-  }
-  uint32_t taken = 0;
-  auto rescan = [&](uint32_t& bk, int& bj) {
-    bk = 0u;
-    bj = -1;
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      if (lane + 32 * j < E && !((taken >> j) & 1u) && (bj < 0 || key[j] > bk)) {
-        bk = key[j];
-        bj = j;
-      }
-    }
-  };
-  uint32_t bk;
-  int bj;
-  rescan(bk, bj);
-  float sel_v = -INFINITY;
-  int sel_id = 0x7fffffff;
-  for (int r = 0; r < k; ++r) {
-    const uint32_t m = __reduce_max_sync(0xffffffffu, bj >= 0 ? bk : 0u);
-    const uint32_t cand = (bj >= 0 && bk == m) ? (uint32_t)(lane + 32 * bj) : 0xffffffffu;
-    const int id = (int)__reduce_min_sync(0xffffffffu, cand);
-    if ((id & 31) == lane) {
-      taken |= 1u << (id >> 5);
-      rescan(bk, bj);
-    }
-    if (lane == r) {
-      sel_v = ord_val(m);
-      sel_id = id;
-    }
-  }
-  const float vmax = __shfl_sync(0xffffffffu, sel_v, 0);
-  const float ex = (lane < k) ? expf(sel_v - vmax) : 0.0f;
-  const float denom = warp_sum(ex);
-  int rank = 0;
-  for (int j = 0; j < k; ++j) rank += (__shfl_sync(0xffffffffu, sel_id, j) < sel_id) ? 1 : 0;
-  // lane `rank` receives the id of rank `rank`
-  int out_id = 0x7fffffff;
-  float out_w = 0.0f;
-  for (int j = 0; j < k; ++j) {
-    const int rj = __shfl_sync(0xffffffffu, rank, j);
-    const int ij = __shfl_sync(0xffffffffu, sel_id, j);
-    const float wj = __shfl_sync(0xffffffffu, ex, j);
-    if (lane == rj) {
-      out_id = ij;
-      out_w = wj / denom;
-    }
-  }
-  id_out = out_id;
-  w_out = out_w;
+  topk_core<true>(row, E, k, id_out, w_out);
 }
 
 // The decision of one decode-sized call (at most 32 routed rows), computed by

@@ -153,63 +153,93 @@ __device__ inline float silu(float g) { return g / (1.0f + expf(-g)); }
 // intrinsic division returns 0, the limit of silu.
 __device__ inline float silu_fast(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
-// One warp selects the top-k of one token's logits (E <= 512) and writes
-// ascending ids with softmax weights renormalised over the selection.
-__device__ inline void warp_topk(const float* row, int E, int k, int32_t* ids_out, float* w_out) {
+// Order-preserving map of a float to 32 unsigned bits (larger float, larger
+// key; equal floats, equal keys); its inverse.
+__device__ inline uint32_t ord_key(float v) {
+  const uint32_t u = __float_as_uint(v == 0.0f ? 0.0f : v);   // -0 and +0 compare equal
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ inline float ord_val(uint32_t k) { return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k); }
+
+// One warp selects the top-k of one token's logits (E <= 512; order: logit
+// descending, id ascending) and renormalises the softmax over the selection.
+// On return lane r < k holds the r-th selected id in ascending order and its
+// weight.  Lane l holds experts l + 32 j and its best untaken candidate; a
+// round is two warp reductions (largest key, then the lowest id among the
+// lanes holding it), and only the lane that owned the winner rescans.
+// L2_ONLY: read the row through L2 (rows written by other CTAs of the launch).
+template <bool L2_ONLY>
+__device__ inline void topk_core(const float* row, int E, int k, int& id_out, float& w_out) {
   const int lane = threadIdx.x & 31;
   constexpr int kPer = kMaxRouteE / 32;
-  float v[kPer];
+  uint32_t key[kPer];
 #pragma unroll
   for (int j = 0; j < kPer; ++j) {
     const int e = lane + 32 * j;
-    v[j] = (e < E) ? row[e] : -INFINITY;
+    float v = 0.0f;
+    if (e < E) v = L2_ONLY ? __ldcg(row + e) : row[e];
+    key[j] = (e < E) ? ord_key(v) : 0u;   // 0: no expert (every logit maps above 0)
   }
   uint32_t taken = 0;
+  uint32_t bk = 0u;
+  int bj = -1;
+  auto rescan = [&]() {
+    bk = 0u;
+    bj = -1;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      if (lane + 32 * j < E && !((taken >> j) & 1u) && (bj < 0 || key[j] > bk)) {
+        bk = key[j];
+        bj = j;
+      }
+    }
+  };
+  rescan();
   float sel_v = -INFINITY;
   int sel_id = 0x7fffffff;
   for (int r = 0; r < k; ++r) {
-    // best untaken candidate of this lane
-    float bv = -INFINITY;
-    int bid = 0x7fffffff;
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      const int e = lane + 32 * j;
-      if (e < E && !((taken >> j) & 1u)) {
-        if (v[j] > bv || (v[j] == bv && e < bid)) {
-          bv = v[j];
-          bid = e;
-        }
-      }
+    const uint32_t m = __reduce_max_sync(0xffffffffu, bj >= 0 ? bk : 0u);
+    const uint32_t cand = (bj >= 0 && bk == m) ? (uint32_t)(lane + 32 * bj) : 0xffffffffu;
+    const int id = (int)__reduce_min_sync(0xffffffffu, cand);
+    if ((id & 31) == lane) {
+      taken |= 1u << (id >> 5);
+      rescan();
     }
-    // warp arg-max on (value desc, id asc)
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oid = __shfl_xor_sync(0xffffffffu, bid, o);
-      if (ov > bv || (ov == bv && oid < bid)) {
-        bv = ov;
-        bid = oid;
-      }
-    }
-    if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
     if (lane == r) {
-      sel_v = bv;
-      sel_id = bid;
+      sel_v = ord_val(m);
+      sel_id = id;
     }
   }
-  // lane 0 holds the largest selected logit
   const float vmax = __shfl_sync(0xffffffffu, sel_v, 0);
   const float ex = (lane < k) ? expf(sel_v - vmax) : 0.0f;
   const float denom = warp_sum(ex);
-  // rank of this lane's id among the selected ids -> ascending output order
   int rank = 0;
+  for (int j = 0; j < k; ++j) rank += (__shfl_sync(0xffffffffu, sel_id, j) < sel_id) ? 1 : 0;
+  // lane `rank` receives the id of rank `rank`
+  int out_id = 0x7fffffff;
+  float out_w = 0.0f;
   for (int j = 0; j < k; ++j) {
-    const int other = __shfl_sync(0xffffffffu, sel_id, j);
-    rank += (other < sel_id) ? 1 : 0;
+    const int rj = __shfl_sync(0xffffffffu, rank, j);
+    const int ij = __shfl_sync(0xffffffffu, sel_id, j);
+    const float wj = __shfl_sync(0xffffffffu, ex, j);
+    if (lane == rj) {
+      out_id = ij;
+      out_w = wj / denom;
+    }
   }
+  id_out = out_id;
+  w_out = out_w;
+}
+
+// topk_core writing the selection: ids_out[0..k) ascending, w_out[0..k).
+__device__ inline void warp_topk(const float* row, int E, int k, int32_t* ids_out, float* w_out) {
+  int id;
+  float w;
+  topk_core<false>(row, E, k, id, w);
+  const int lane = threadIdx.x & 31;
   if (lane < k) {
-    ids_out[rank] = sel_id;
-    w_out[rank] = ex / denom;
+    ids_out[lane] = id;
+    w_out[lane] = w;
   }
 }
 
@@ -248,6 +278,9 @@ cudaError_t launch_route_topk(const __nv_bfloat16* x, int T, int H, const float*
                               float* logits_opt, void* ws, uint32_t* status, cudaStream_t s);
 size_t route_ws_bytes(int T, int H, int E);
 bool route_tc_ok(int T, int H, int E);
+// One warp per token: logits (+ bias, written back when asked) -> top-k ids and weights.
+cudaError_t launch_topk(float* logits, const float* bias, int T, int E, int k, bool write_back, int32_t* topk_ids,
+                        float* topk_w, cudaStream_t s);
 size_t route_tc_ws_bytes(int T, int H, int E);
 cudaError_t launch_route_tc(const __nv_bfloat16* x, int T, int H, const float* w_router, const float* bias, int E,
                             int k, int32_t* topk_ids, float* topk_w, float* logits_opt, void* ws, uint32_t* status,

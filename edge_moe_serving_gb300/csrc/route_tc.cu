@@ -290,8 +290,13 @@ cudaError_t launch_route_tc(const __nv_bfloat16* x, int T, int H, const float* w
   p.status = status;
   err = launch_k(logits_kernel, std::min(p.n_tiles, sms), kRThreads, kRSmem, s, mw, mx, p);
   if (err != cudaSuccess) return err;
-  const int tgrid = std::min((T + kTopkWarps - 1) / kTopkWarps, sms * 8);
-  return launch_k(topk_kernel, tgrid, 32 * kTopkWarps, 0, s, logits, bias, T, E, k, logits_opt ? 1 : 0, topk_ids,
+  return launch_topk(logits, bias, T, E, k, logits_opt != nullptr, topk_ids, topk_w, s);
+}
+
+cudaError_t launch_topk(float* logits, const float* bias, int T, int E, int k, bool write_back, int32_t* topk_ids,
+                        float* topk_w, cudaStream_t s) {
+  const int tgrid = std::min((T + kTopkWarps - 1) / kTopkWarps, num_sms() * 8);
+  return launch_k(topk_kernel, tgrid, 32 * kTopkWarps, 0, s, logits, bias, T, E, k, write_back ? 1 : 0, topk_ids,
                   topk_w);
 }
 

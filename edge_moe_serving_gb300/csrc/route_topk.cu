@@ -206,16 +206,22 @@ cudaError_t launch_route_topk(const __nv_bfloat16* x, int T, int H, const float*
     float* logits = logits_opt ? logits_opt : reinterpret_cast<float*>(ws);
     unsigned int* ticket = reinterpret_cast<unsigned int*>(
         reinterpret_cast<char*>(ws) + align_up((size_t)T * E * sizeof(float), 256));
-    cudaError_t err = cudaMemsetAsync(ticket, 0, sizeof(unsigned int), s);
-    if (err != cudaSuccess) return err;
+    cudaError_t err = cudaSuccess;
+    if (T <= 4) {
+      err = cudaMemsetAsync(ticket, 0, sizeof(unsigned int), s);
+      if (err != cudaSuccess) return err;
+    }
     if (T <= 1)
       return launch_k(route_small_kernel<1, true>, E, kSmallThreads, 0, s, x, T, H, w_router, bias, E, k, logits,
                       ticket, topk_ids, topk_w);
     if (T <= 4)
       return launch_k(route_small_kernel<4, true>, E, kSmallThreads, 0, s, x, T, H, w_router, bias, E, k, logits,
                       ticket, topk_ids, topk_w);
-    return launch_k(route_small_kernel<8, true>, E, kSmallThreads, 0, s, x, T, H, w_router, bias, E, k, logits, ticket,
-                    topk_ids, topk_w);
+    // more tokens: logits only, then one warp per token selects
+    err = launch_k(route_small_kernel<8, false>, E, kSmallThreads, 0, s, x, T, H, w_router, bias, E, k, logits,
+                   (unsigned int*)nullptr, (int32_t*)nullptr, (float*)nullptr);
+    if (err != cudaSuccess) return err;
+    return launch_topk(logits, nullptr, T, E, k, false, topk_ids, topk_w, s);
   }
   if (route_tc_ok(T, H, E))
     return launch_route_tc(x, T, H, w_router, bias, E, k, topk_ids, topk_w, logits_opt, ws, status, s);

@@ -73,6 +73,27 @@ def test_gemm_auto_mixed_groups(T):
         assert_close(y, token_major(ref), what=f"T={T} mode {mode}")
 
 
+@pytest.mark.parametrize("T,concentrated", [(32, True), (32, False), (7, False), (19, True)])
+def test_gemm_thin_tiles(T, concentrated):
+    """Calls of at most 32 tokens run the GEMM with 32-row chunks and a deeper
+    pipeline: full 32-row groups (every token routed to the same k experts),
+    ragged groups of 1..T rows, and both pools."""
+    cfg = dataclasses.replace(CONFIGS["batched_decode"], name="thin", T=T, bias="none", cache_slots=40)
+    dc = DeviceCache(cfg, DEV)
+    xb = gen.f32_to_bf16_bits(np.random.default_rng(100 + T).standard_normal((T, cfg.H)).astype(np.float32))
+    wc = ExpertCache(cfg, cap=128)
+    x = gen.bf16_bits_to_f64(xb)
+    b = np.zeros(cfg.E, np.float32)
+    if concentrated:
+        b[40:40 + cfg.k] = 50.0            # every token takes the same k experts
+    ref = O.layer_forward(x, gen.w_router(cfg), b, cfg.k, lambda e: wc(0, e), E=cfg.E)
+    if concentrated:
+        assert (ref["counts"][40:40 + cfg.k] == T).all()
+    y, st = _ffn(cfg, dc, ref, to_dev_bf16(xb, DEV), moe.MOE_FFN_GEMM)
+    assert st == 0
+    assert_close(y, token_major(ref), what=f"thin GEMM T={T}")
+
+
 def test_gemm_mask_split_is_bitwise():
     cfg = dataclasses.replace(CONFIGS["batched_decode"], name="mixed", T=400, bias="none")
     dc = DeviceCache(cfg, DEV)
