@@ -416,7 +416,7 @@ __device__ inline void ring_phase(const GemvParams& p, const int* s_pref, const 
 // Shared memory of a fused-GEMV CTA besides the ring itself.
 struct FusedShared {
   int pref[kMaxE + 1];
-  int warp[kRingThreads / 32];
+  int warp[32];               // per-warp scan partials of build_prefix: any block of up to 1024 threads
   int off[kMaxE];
   int ent[kMaxE];
   int fill[kMaxE];
