@@ -187,6 +187,7 @@ constexpr unsigned long long kGridWaitNs = 1000000000ull;
 struct RingState {
   int base;               // ring index of the current phase's first unit
   int armed_last;         // producer: last ring index with copies in flight
+  int last_issued;        // producer: last ring index it completed or armed (data or not)
   bool stored;            // a consumer issued fused-fill stores
 };
 
@@ -195,6 +196,147 @@ __device__ inline int local_units(int total) {
   const int b = blockIdx.x, G = gridDim.x;
   return b < total ? (total - 1 - b) / G + 1 : 0;
 }
+
+// Per-warp consumer of ring units: the state of the current instance and the
+// reduction of one unit in shared memory (gate/up: h rows; down: y rows).  An
+// admitted expert's unit is also written to its cache slot from the stage.
+template <int NT, bool GATEUP, int VC>
+struct UnitWorker {
+  static constexpr int NB = GATEUP ? 2 : 1;
+  static constexpr int PS = (NT == 1) ? 2 : 1;
+  static constexpr int XR = (NT == 1 && VC > 0) ? VC : 1;
+  static constexpr bool x_in_regs = (NT == 1) && VC > 0;
+  int cur_j = -1, pos0 = 0, ntok = 0;
+  RingSrc rs;
+  const __nv_bfloat16* act[NT];
+  int yrow[NT];
+  uint4 xr[XR];
+
+  // New instance j.  Down rows wait (bounded) until p.inst_done[j] >= need:
+  // h of the instance is then complete.  Returns false on abort.
+  __device__ inline bool begin(const GemvParams& p, int j, const int* s_pref, const int* s_off, const int* s_ent,
+                               const int* s_fill, unsigned need, volatile int* abort_flag) {
+    const int lane = threadIdx.x & 31;
+    cur_j = j;
+    if (!GATEUP && p.inst_done != nullptr) {
+      if (lane == 0) {
+        const unsigned long long t0 = gtimer();
+        while (ld_acquire_u32(p.inst_done + j) < need) {
+          if (*abort_flag) break;
+          if (gtimer() - t0 > kGridWaitNs) {
+            *abort_flag = 1;
+            break;
+          }
+        }
+      }
+      __syncwarp();
+      if (*abort_flag) return false;
+    }
+    const int e = find_expert(s_pref, p.E, j);
+    // any warp that meets an unbound expert reports it (units are spread over warps)
+    rs = ring_source(p, e, s_ent[e], s_fill[e], (lane == 0) ? p.status : nullptr);
+    const int c = j - s_pref[e];
+    pos0 = s_off[e] + c * NT;
+    ntok = min(NT, p.counts[e] - c * NT);
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const int pos = pos0 + (t < ntok ? t : 0);
+      if (GATEUP)
+        act[t] = p.x_perm ? p.x_perm + (size_t)pos * p.H : p.x + (size_t)(p.perm[pos] / p.k) * p.H;
+      else
+        act[t] = p.h + (size_t)pos * p.I;
+      yrow[t] = GATEUP ? 0 : p.perm[pos];
+    }
+    if (x_in_regs && rs.ok) {
+      // phase B reads h written by other CTAs of this launch: through L2, not the read-only path
+#pragma unroll
+      for (int c2 = 0; c2 < XR; ++c2)
+        xr[c2] = GATEUP ? ldg_cached(act[0] + (size_t)(lane + 32 * c2) * 8)
+                        : __ldcg(reinterpret_cast<const uint4*>(act[0] + (size_t)(lane + 32 * c2) * 8));
+    }
+    return true;
+  }
+
+  // Reduce the unit in stage sw: rows n0 .. n0 + U - 1 of the instance's expert.
+  __device__ inline void run(const GemvParams& p, const uint8_t* sw, int n0, RingState& st) {
+    const int lane = threadIdx.x & 31;
+    const int K = GATEUP ? p.H : p.I;
+    const int NTASK = GATEUP ? p.I : p.H;
+    const int row_bytes = K * 2;
+    const int U = ring_rows(K, GATEUP);
+    const int bank_stride = kUnitBytes / NB;
+    const int VPL = K / 256;
+    const int rows = min(U, NTASK - n0);
+    if (!rs.ok) return;
+    if (rs.fill && lane == 0) {
+      // this expert is being admitted to the cache: write the unit to its slot
+      const uint32_t bytes = (uint32_t)(rows * row_bytes);
+      if (GATEUP) {
+        bulk_s2g(rs.dst_gate + (size_t)n0 * K, sw, bytes);
+        bulk_s2g(rs.dst_up + (size_t)n0 * K, sw + bank_stride, bytes);
+      } else {
+        bulk_s2g(rs.dst_down + (size_t)n0 * K, sw, bytes);
+      }
+      bulk_commit();
+      st.stored = true;
+    }
+    const uint8_t* wbase = sw + (size_t)lane * 16;
+    for (int r = 0; r < rows; ++r) {
+      float acc[NB][NT][PS];
+#pragma unroll
+      for (int b = 0; b < NB; ++b)
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+#pragma unroll
+          for (int q = 0; q < PS; ++q) acc[b][t][q] = 0.0f;
+      const uint8_t* wr = wbase + (size_t)r * row_bytes;
+      if (x_in_regs) {
+#pragma unroll
+        for (int c = 0; c < XR; ++c)
+#pragma unroll
+          for (int b = 0; b < NB; ++b) {
+            const uint4 w = *reinterpret_cast<const uint4*>(wr + b * bank_stride + c * 512);
+            dot8x2(w, xr[c], acc[b][0][0], acc[b][0][PS - 1]);
+          }
+      } else {
+#pragma unroll 4
+        for (int c = 0; c < VPL; ++c) {
+          const int v = lane + 32 * c;
+          uint4 a[NT];
+#pragma unroll
+          for (int t = 0; t < NT; ++t)
+            a[t] = (t < ntok) ? (GATEUP ? ldg_cached(act[t] + (size_t)v * 8)
+                                        : __ldcg(reinterpret_cast<const uint4*>(act[t] + (size_t)v * 8)))
+                              : make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int b = 0; b < NB; ++b) {
+            const uint4 w = *reinterpret_cast<const uint4*>(wr + b * bank_stride + c * 512);
+#pragma unroll
+            for (int t = 0; t < NT; ++t) acc[b][t][0] = dot8(w, a[t], acc[b][t][0]);
+          }
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < NB; ++b)
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          float v = acc[b][t][0];
+          if (PS == 2) v += acc[b][t][PS - 1];
+          acc[b][t][0] = warp_sum(v);
+        }
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        if (lane == t && t < ntok) {
+          if (GATEUP)
+            p.h[(size_t)(pos0 + t) * p.I + n0 + r] = __float2bfloat16_rn(silu(acc[0][t][0]) * acc[NB - 1][t][0]);
+          else
+            p.y[(size_t)yrow[t] * p.H + n0 + r] = acc[0][t][0];
+        }
+      }
+    }
+    if (rs.fill && lane == 0) bulk_wait_read_all();   // the store has read the stage
+  }
+};
 
 // One phase of the fused GEMV: phase A (GATEUP) streams gate and up rows and
 // writes h; phase B streams down rows and writes y.  Units are grid-strided:
@@ -205,9 +347,6 @@ __device__ inline void ring_phase(const GemvParams& p, const int* s_pref, const 
                                   const int* s_fill, int* s_cnt, uint8_t* ring, uint64_t* full_bar,
                                   uint64_t* empty_bar, volatile int* abort_flag, RingState& st, bool producer) {
   constexpr int NB = GATEUP ? 2 : 1;
-  constexpr int PS = (NT == 1) ? 2 : 1;
-  constexpr int XR = (NT == 1 && VC > 0) ? VC : 1;
-  constexpr bool x_in_regs = (NT == 1) && VC > 0;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int K = GATEUP ? p.H : p.I;
   const int NTASK = GATEUP ? p.I : p.H;
@@ -215,7 +354,6 @@ __device__ inline void ring_phase(const GemvParams& p, const int* s_pref, const 
   const int U = ring_rows(K, GATEUP);
   const int upi = (NTASK + U - 1) / U;
   const int bank_stride = kUnitBytes / NB;
-  const int VPL = K / 256;
   const int total = s_pref[p.E] * upi;
   const int G = gridDim.x;
   const int n_local = local_units(total);
@@ -239,6 +377,7 @@ __device__ inline void ring_phase(const GemvParams& p, const int* s_pref, const 
       const int stage = ri % kRingStages;
       const uint32_t use = (uint32_t)(ri / kRingStages);
       if (!ring_wait(&empty_bar[stage], (use & 1u) ^ 1u, abort_flag)) break;
+      st.last_issued = ri;
       if (!rs.ok) {
         // nothing to stream: complete the slot's phase without data
         asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&full_bar[stage])) : "memory");
@@ -261,136 +400,21 @@ __device__ inline void ring_phase(const GemvParams& p, const int* s_pref, const 
     return;
   }
 
-  int cur_j = -1;
-  RingSrc rs;
-  rs.ok = false;
-  int pos0 = 0, ntok = 0;
-  const __nv_bfloat16* act[NT];
-  int yrow[NT];
-  uint4 xr[XR];
+  UnitWorker<NT, GATEUP, VC> wk;
+  const int ua = ring_rows(p.H, true);
+  const unsigned need = (unsigned)min(G, (p.I + ua - 1) / ua);   // CTAs holding gate/up units of an instance
   // this warp's units: ring index ri = base + i with ri % C == warp
   const int i0 = ((warp - base) % kConsumerWarps + kConsumerWarps) % kConsumerWarps;
   for (int i = i0; i < n_local; i += kConsumerWarps) {
     const int u = blockIdx.x + i * G;
     const int j = u / upi;
     const int n0 = (u - j * upi) * U;
-    if (j != cur_j) {
-      cur_j = j;
-      if (!GATEUP && p.inst_done != nullptr) {
-        // h of this instance is read only after every CTA's gate/up units of it are done
-        const int ua = ring_rows(p.H, true);
-        const unsigned need = (unsigned)min(G, (p.I + ua - 1) / ua);
-        if (lane == 0) {
-          const unsigned long long t0 = gtimer();
-          while (ld_acquire_u32(p.inst_done + j) < need) {
-            if (*abort_flag) break;
-            if (gtimer() - t0 > kGridWaitNs) {
-              *abort_flag = 1;
-              break;
-            }
-          }
-        }
-        __syncwarp();
-        if (*abort_flag) break;
-      }
-      const int e = find_expert(s_pref, p.E, j);
-      // any warp that meets an unbound expert reports it (units are spread over warps)
-      rs = ring_source(p, e, s_ent[e], s_fill[e], (lane == 0) ? p.status : nullptr);
-      const int c = j - s_pref[e];
-      pos0 = s_off[e] + c * NT;
-      ntok = min(NT, p.counts[e] - c * NT);
-#pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        const int pos = pos0 + (t < ntok ? t : 0);
-        if (GATEUP)
-          act[t] = p.x_perm ? p.x_perm + (size_t)pos * p.H : p.x + (size_t)(p.perm[pos] / p.k) * p.H;
-        else
-          act[t] = p.h + (size_t)pos * p.I;
-        yrow[t] = GATEUP ? 0 : p.perm[pos];
-      }
-      if (x_in_regs && rs.ok) {
-        // phase B reads h written by other CTAs of this launch: through L2, not the read-only path
-#pragma unroll
-        for (int c2 = 0; c2 < XR; ++c2)
-          xr[c2] = GATEUP ? ldg_cached(act[0] + (size_t)(lane + 32 * c2) * 8)
-                          : __ldcg(reinterpret_cast<const uint4*>(act[0] + (size_t)(lane + 32 * c2) * 8));
-      }
-    }
+    if (j != wk.cur_j && !wk.begin(p, j, s_pref, s_off, s_ent, s_fill, need, abort_flag)) break;
     const int ri = base + i;
     const int stage = ri % kRingStages;
     const uint32_t use = (uint32_t)(ri / kRingStages);
     if (!ring_wait(&full_bar[stage], use & 1u, abort_flag)) break;
-    const uint8_t* sw = ring + stage * kUnitBytes;
-    const int rows = min(U, NTASK - n0);
-    if (rs.ok) {
-      if (rs.fill && lane == 0) {
-        // this expert is being admitted to the cache: write the unit to its slot
-        const uint32_t bytes = (uint32_t)(rows * row_bytes);
-        if (GATEUP) {
-          bulk_s2g(rs.dst_gate + (size_t)n0 * K, sw, bytes);
-          bulk_s2g(rs.dst_up + (size_t)n0 * K, sw + bank_stride, bytes);
-        } else {
-          bulk_s2g(rs.dst_down + (size_t)n0 * K, sw, bytes);
-        }
-        bulk_commit();
-        st.stored = true;
-      }
-      const uint8_t* wbase = sw + (size_t)lane * 16;
-      for (int r = 0; r < rows; ++r) {
-        float acc[NB][NT][PS];
-#pragma unroll
-        for (int b = 0; b < NB; ++b)
-#pragma unroll
-          for (int t = 0; t < NT; ++t)
-#pragma unroll
-            for (int q = 0; q < PS; ++q) acc[b][t][q] = 0.0f;
-        const uint8_t* wr = wbase + (size_t)r * row_bytes;
-        if (x_in_regs) {
-#pragma unroll
-          for (int c = 0; c < XR; ++c)
-#pragma unroll
-            for (int b = 0; b < NB; ++b) {
-              const uint4 w = *reinterpret_cast<const uint4*>(wr + b * bank_stride + c * 512);
-              dot8x2(w, xr[c], acc[b][0][0], acc[b][0][PS - 1]);
-            }
-        } else {
-#pragma unroll 4
-          for (int c = 0; c < VPL; ++c) {
-            const int v = lane + 32 * c;
-            uint4 a[NT];
-#pragma unroll
-            for (int t = 0; t < NT; ++t)
-              a[t] = (t < ntok) ? (GATEUP ? ldg_cached(act[t] + (size_t)v * 8)
-                                          : __ldcg(reinterpret_cast<const uint4*>(act[t] + (size_t)v * 8)))
-                                : make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int b = 0; b < NB; ++b) {
-              const uint4 w = *reinterpret_cast<const uint4*>(wr + b * bank_stride + c * 512);
-#pragma unroll
-              for (int t = 0; t < NT; ++t) acc[b][t][0] = dot8(w, a[t], acc[b][t][0]);
-            }
-          }
-        }
-#pragma unroll
-        for (int b = 0; b < NB; ++b)
-#pragma unroll
-          for (int t = 0; t < NT; ++t) {
-            float v = acc[b][t][0];
-            if (PS == 2) v += acc[b][t][PS - 1];
-            acc[b][t][0] = warp_sum(v);
-          }
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          if (lane == t && t < ntok) {
-            if (GATEUP)
-              p.h[(size_t)(pos0 + t) * p.I + n0 + r] = __float2bfloat16_rn(silu(acc[0][t][0]) * acc[NB - 1][t][0]);
-            else
-              p.y[(size_t)yrow[t] * p.H + n0 + r] = acc[0][t][0];
-          }
-        }
-      }
-      if (rs.fill && lane == 0) bulk_wait_read_all();   // the store has read the stage
-    }
+    wk.run(p, ring + stage * kUnitBytes, n0, st);
     if (GATEUP && p.inst_done != nullptr) {
       // Publish the instance once this CTA's units of it are all done: each
       // warp counts its unit with a CTA-scope acquire-release add (ordering
@@ -455,8 +479,8 @@ __device__ void fused_ffn_body(const GemvParams& p, unsigned int* grid_count, Fu
     for (int i = tid; i < fs.pref[p.E] && i < kMaxFusedInst; i += blockDim.x) fs.cnt[i] = 0;
     __syncthreads();
   }
-  RingState st = {0, -1, false};
   const bool producer = warp == kConsumerWarps;
+  RingState st = {0, -1, -1, false};
 
   if (!producer || lane == 0) {
     ring_phase<NT, true, VA>(p, fs.pref, fs.off, fs.ent, fs.fill, fs.cnt, ring, fs.full_bar, fs.empty_bar, abort_flag, st,
@@ -484,10 +508,12 @@ __device__ void fused_ffn_body(const GemvParams& p, unsigned int* grid_count, Fu
       ring_phase<NT, false, VB>(p, fs.pref, fs.off, fs.ent, fs.fill, fs.cnt, ring, fs.full_bar, fs.empty_bar, abort_flag,
                                 st, producer);
     if (producer) {
-      // drain: the copies of the last ring round land before the CTA exits
+      // drain: the copies of the last ring round land before the CTA exits (the last
+      // kRingStages slots issued: each stage's latest use, whatever it carried)
       volatile int no_abort = 0;
-      for (int q = st.armed_last; q >= 0 && q > st.armed_last - kRingStages; --q)
-        ring_wait(&fs.full_bar[q % kRingStages], (uint32_t)(q / kRingStages) & 1u, &no_abort);
+      if (st.armed_last >= 0)
+        for (int q = st.last_issued; q >= 0 && q > st.last_issued - kRingStages; --q)
+          ring_wait(&fs.full_bar[q % kRingStages], (uint32_t)(q / kRingStages) & 1u, &no_abort);
     } else {
       if (st.stored && lane == 0) bulk_wait_all();   // fused-fill writes complete before exit
       if (p.combine_out != nullptr) {
