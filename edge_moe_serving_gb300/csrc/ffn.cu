@@ -20,7 +20,8 @@ cudaError_t launch_ffn(const moe_cache& c, int layer, const int32_t* counts, con
                        const int32_t* perm, const __nv_bfloat16* x, const __nv_bfloat16* x_perm,
                        int T, int k, const uint8_t* mask, int mode, float* y_rows, void* ws,
                        uint32_t* status, cudaStream_t s, const int32_t* fused_fills,
-                       const int32_t* fused_n_fill, const float* combine_w, __nv_bfloat16* combine_out) {
+                       const int32_t* fused_n_fill, const float* combine_w, __nv_bfloat16* combine_out,
+                       __nv_bfloat16* y_rows_bf16) {
   if (T == 0) return cudaSuccess;
   const int R = T * k;
   __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(ws);
@@ -33,6 +34,8 @@ cudaError_t launch_ffn(const moe_cache& c, int layer, const int32_t* counts, con
     // the GEMM pads a group only to 16 token rows, so it takes small groups too
     gemv_max = 0;
   }
+  // bf16 expert rows are written by the GEMM only
+  if (y_rows_bf16 != nullptr && gemv_max != 0) return cudaErrorNotSupported;
   // a fused fill or combine is only done by the fused GEMV kernel
   if ((fused_fills != nullptr || combine_out != nullptr) && gemv_max != INT_MAX) return cudaErrorNotSupported;
   if (combine_out != nullptr && !gemv_fused_ok(c.H, c.I)) return cudaErrorNotSupported;
@@ -66,7 +69,8 @@ cudaError_t launch_ffn(const moe_cache& c, int layer, const int32_t* counts, con
     if (err != cudaSuccess) return err;
   }
   if (gemv_max != INT_MAX)
-    return launch_gemm(c, layer, counts, offsets, perm, mask, gemv_max, x_perm, T, R, h, y_rows, status, s);
+    return launch_gemm(c, layer, counts, offsets, perm, mask, gemv_max, x_perm, T, R, h, y_rows, y_rows_bf16, status,
+                       s);
   return cudaSuccess;
 }
 

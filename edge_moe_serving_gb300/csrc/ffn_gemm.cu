@@ -18,7 +18,7 @@
 //   gate/up kernel  D_g = W_gate[f0:f0+128] X_c^T, D_u = W_up[f0:f0+128] X_c^T
 //                   epilogue h[c, f] = bf16(silu(D_g) * D_u)  (one thread per f)
 //   down kernel     D_m = W_down[f0+128m : +128] H_c^T (m = 0, 1)
-//                   epilogue y[perm[c], f] = D  (fp32, token-major rows)
+//                   epilogue y[perm[c], f] = D  (token-major rows, fp32 or bf16)
 //
 // Roles (320 threads): warp 0 = TMA producer, warp 1 = MMA issuer (and TMEM
 // owner), warps 2..9 = epilogue (TMEM lanes 32*(warp%4) .. +31; the two warps
@@ -72,7 +72,8 @@ struct GemmParams {
   int32_t cache_slots, staging_slots;
   const int32_t* perm;     // dispatch position -> token-major row
   __nv_bfloat16* h;        // gate/up output [R, I] (dispatch order)
-  float* y;                // down output [R, H] (token-major)
+  float* y;                // down output [R, H] (token-major), fp32
+  __nv_bfloat16* y16;      // or bf16 when non-null
   uint32_t* status;
 };
 
@@ -347,7 +348,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_b64, const __grid_constant__
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               const int yrow = __shfl_sync(0xffffffffu, prow, j);
-              if (j < nv) p.y[(size_t)yrow * p.H + f] = __uint_as_float(v[j]);
+              if (j < nv) {
+                if (p.y16 != nullptr)
+                  p.y16[(size_t)yrow * p.H + f] = __float2bfloat16_rn(__uint_as_float(v[j]));
+                else
+                  p.y[(size_t)yrow * p.H + f] = __uint_as_float(v[j]);
+              }
             }
           }
         }
@@ -385,7 +391,8 @@ bool gemm_shape_ok(int H, int I) { return H % 256 == 0 && I % 128 == 0 && H >= 2
 // Grouped GEMM over the experts with more than min_rows rows (gate/up, then down).
 cudaError_t launch_gemm(const moe_cache& c, int layer, const int32_t* counts, const int32_t* offsets,
                         const int32_t* perm, const uint8_t* mask, int min_rows, const __nv_bfloat16* x_perm,
-                        int T, int R, __nv_bfloat16* h, float* y, uint32_t* status, cudaStream_t s) {
+                        int T, int R, __nv_bfloat16* h, float* y, __nv_bfloat16* y16, uint32_t* status,
+                        cudaStream_t s) {
   if (!gemm_shape_ok(c.H, c.I)) return cudaErrorNotSupported;
   const bool has_stage = c.staging.w_gate != nullptr;
   const uint64_t H = (uint64_t)c.H, I = (uint64_t)c.I;
@@ -405,6 +412,7 @@ cudaError_t launch_gemm(const moe_cache& c, int layer, const int32_t* counts, co
   p.staging_slots = has_stage ? c.staging.n_slots : 0;
   p.h = h;
   p.y = y;
+  p.y16 = y16;
   p.status = status;
 
   CUtensorMap x64, x16, g0, u0, g1, u1;

@@ -40,6 +40,7 @@ cudaError_t launch_gemv(const GemvParams& p, cudaStream_t s);
 bool gemm_shape_ok(int H, int I);
 cudaError_t launch_gemm(const moe_cache& c, int layer, const int32_t* counts, const int32_t* offsets,
                         const int32_t* perm, const uint8_t* mask, int min_rows, const __nv_bfloat16* x_perm,
-                        int T, int R, __nv_bfloat16* h, float* y, uint32_t* status, cudaStream_t s);
+                        int T, int R, __nv_bfloat16* h, float* y, __nv_bfloat16* y16, uint32_t* status,
+                        cudaStream_t s);
 
 }  // namespace moe

@@ -332,6 +332,16 @@ int moe_layer_forward(const moe_layer* layer, const moe_cache* cache, const void
                                  reinterpret_cast<__nv_bfloat16*>(out));
     return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
   }
+  if (L.x_perm && gemm_shape_ok(H, I) && !(bufs_opt && bufs_opt->y_rows)) {
+    // Every group runs on the GEMM and nobody reads the expert rows but the
+    // combine: keep them in bf16 (half the bytes written and read back).
+    __nv_bfloat16* y16 = reinterpret_cast<__nv_bfloat16*>(L.y_rows);
+    cudaError_t err = launch_ffn(*cache, layer->layer, L.counts, L.offsets, L.perm,
+                                 reinterpret_cast<const __nv_bfloat16*>(x), L.x_perm, T, k, nullptr, ffn_mode, nullptr,
+                                 L.scratch, dev_status, s, nullptr, nullptr, nullptr, nullptr, y16);
+    if (err != cudaSuccess) return err == cudaErrorNotSupported ? MOE_ERR_UNSUPPORTED : MOE_ERR_CUDA;
+    return cuda_status(launch_combine(y16, L.w, T, k, H, reinterpret_cast<__nv_bfloat16*>(out), nullptr, dev_status, s));
+  }
   st = moe_expert_ffn_grouped(cache, layer->layer, L.counts, L.offsets, L.perm, x, L.x_perm, T, k, nullptr, ffn_mode,
                               L.y_rows, L.scratch, scratch_bytes, dev_status, stream);
   if (st != MOE_OK) return st;

@@ -322,14 +322,17 @@ cudaError_t launch_bind(const moe_cache& c, int layer, const int32_t* ids, int R
                         int32_t* offsets = nullptr, int32_t* perm = nullptr, int32_t* inv_perm = nullptr);
 
 size_t ffn_ws_bytes(int T, int k, int E, int H, int I, int mode);
+bool gemm_shape_ok(int H, int I);
 cudaError_t launch_ffn(const moe_cache& c, int layer, const int32_t* counts, const int32_t* offsets,
                        const int32_t* perm, const __nv_bfloat16* x, const __nv_bfloat16* x_perm,
                        int T, int k, const uint8_t* mask, int mode, float* y_rows, void* ws,
                        uint32_t* status, cudaStream_t s, const int32_t* fused_fills = nullptr,
                        const int32_t* fused_n_fill = nullptr, const float* combine_w = nullptr,
-                       __nv_bfloat16* combine_out = nullptr);
+                       __nv_bfloat16* combine_out = nullptr, __nv_bfloat16* y_rows_bf16 = nullptr);
 
 cudaError_t launch_combine(const float* y_rows, const float* topk_w, int T, int k, int H,
+                           __nv_bfloat16* out, float* out_f32, uint32_t* status, cudaStream_t s);
+cudaError_t launch_combine(const __nv_bfloat16* y_rows, const float* topk_w, int T, int k, int H,
                            __nv_bfloat16* out, float* out_f32, uint32_t* status, cudaStream_t s);
 
 }  // namespace moe

@@ -346,6 +346,36 @@ def test_layer_tiny():
         assert_close(bf16_to_f64(got["out"]), ref["out"], what=f"tiny out mode {mode}")
 
 
+def _layer_without_buffers(dc, dl, x, T, mode):
+    """moe_layer_forward with no caller buffers: calls whose groups all run on
+    the GEMM keep the expert rows internally in bf16."""
+    cfg = dc.cfg
+    nbytes = moe.moe_layer_workspace_size(dl.struct, dc.struct, T, mode)
+    out = torch.empty((T, cfg.H), dtype=torch.bfloat16, device=DEV)
+    st = status()
+    moe.moe_layer_forward(dl.struct, dc.struct, x, T, out, 0, 1, 0, 0, mode, None, ws(nbytes), nbytes, st, None)
+    torch.cuda.synchronize()
+    return out, status_bits(st)
+
+
+@pytest.mark.parametrize("name", ["tiny", "batched_decode"])
+def test_layer_bf16_expert_rows(name):
+    """Without caller buffers the GEMM path keeps the expert rows in bf16; the
+    output stays within the tolerance of the oracle and of the fp32-rows path."""
+    cfg = CONFIGS[name]
+    dc = DeviceCache(cfg, DEV)
+    dl = DeviceLayer(cfg, 0, DEV)
+    ref = oracle_layer(cfg, 0, 0, ExpertCache(cfg, cap=64))
+    for mode in (moe.MOE_FFN_AUTO, moe.MOE_FFN_GEMM):
+        dc.reset()
+        out, st = _layer_without_buffers(dc, dl, x_dev(cfg, 0, 0), cfg.T, mode)
+        assert st == 0
+        assert_close(bf16_to_f64(out), ref["out"], what=f"{name} mode {mode} bf16 rows")
+        dc.reset()
+        got = run_layer(dc, dl, x_dev(cfg, 0, 0), cfg.T, 0, 1, 0, ffn_mode=mode)
+        assert_close(bf16_to_f64(out), bf16_to_f64(got["out"]), what=f"{name} bf16 rows vs fp32 rows")
+
+
 def _decode_trace(name, out_steps):
     cfg = CONFIGS[name]
     dc = DeviceCache(cfg, DEV)
