@@ -5,6 +5,8 @@ permutations must be bit-exact; residency state after every bind call must
 equal the oracle's; expert outputs and layer outputs must meet relative
 Frobenius error <= 1e-2 and max-abs error <= 2e-2.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -404,6 +406,52 @@ def _decode_trace(name, out_steps):
             assert_close(bf16_to_f64(got["out"]), ref["out"], what=f"{name} step {step}")
         outs.append(got["out"].clone())
     return outs
+
+
+def _gap_safe_x_bits(cfg, step):
+    """x of (layer 0, step) with every token's k-th/(k+1)-th logit gap >= 1e-3
+    (rows redrawn from the seeded stream until they are), for configurations
+    that have no stored redraw map."""
+    xb = gen.x_bits(cfg, 0, step, redraws={})
+    wr, b = gen.w_router(cfg, 0), gen.bias(cfg, 0, step)
+    for t in range(cfg.T):
+        r = 0
+        while O.topk_gap(O.router_logits(gen.bf16_bits_to_f64(xb[t:t + 1]), wr, b), cfg.k)[0] < 1e-3:
+            xb[t] = gen.x_row_redraw(cfg, 0, step, t, r)
+            r += 1
+    return xb
+
+
+@pytest.mark.parametrize("base,T,mode", [("decode", 2, moe.MOE_FFN_AUTO), ("decode", 3, moe.MOE_FFN_GEMV),
+                                         ("decode", 5, moe.MOE_FFN_GEMV), ("batched_decode", 4, moe.MOE_FFN_GEMV)])
+def test_layer_one_launch_multi_token(base, T, mode):
+    """The one-launch decode layer for 2..5 tokens (instances of 2, 4 and 8
+    rows): ids and residency state bit-exact over a short trace with fills,
+    outputs within tolerance."""
+    cfg = dataclasses.replace(CONFIGS[base], name=f"{base}_t{T}", T=T, steps=6)
+    assert cfg.T * cfg.k <= 32
+    dc = DeviceCache(cfg, DEV)
+    dl = DeviceLayer(cfg, 0, DEV)
+    wc = ExpertCache(cfg, cap=32)
+    ref_state = gen.initial_cache(cfg)
+    for step in range(cfg.steps):
+        dl.set_bias(step)
+        seed = 300 + step
+        xb = _gap_safe_x_bits(cfg, step)
+        got = run_layer(dc, dl, to_dev_bf16(xb, DEV), cfg.T, cfg.phi_q16, cfg.min_fill, cfg.fill_policy, seed,
+                        ffn_mode=mode)
+        assert got["status"] == 0
+        ref = oracle_layer(cfg, 0, step, wc, x_bits=xb)
+        assert np.array_equal(got["topk_ids"].cpu().numpy().reshape(cfg.T, cfg.k), ref["ids"]), step
+        assert np.array_equal(got["perm"].cpu().numpy(), ref["perm"]), step
+        ref_state, res = O.bind(ref_state, 0, ref["ids"], cfg.E, cfg.phi_q16, cfg.min_fill, cfg.fill_policy, seed)
+        st = dc.state()
+        for key in ("table", "owner", "stamp"):
+            assert np.array_equal(st[key], np.asarray(ref_state[key])), (step, key)
+        for kk, v in res["stats"].items():
+            assert got["stats"][kk] == v, (step, kk)
+        assert_close(bf16_to_f64(got["out"]), ref["out"], what=f"{cfg.name} step {step}")
+        assert_close(got["y_rows"].cpu().numpy(), token_major(ref), what=f"{cfg.name} step {step} y_rows")
 
 
 def test_layer_decode_trace():
