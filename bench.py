@@ -108,10 +108,11 @@ def router_flops(cfg):
 #    experts x ~192 rows; profiles/gemm_prefill_profile.md) scaled by the
 #    units processed (4x the experts, 4x the rows): traffic there is each
 #    weight byte once plus the activations, both proportional.
-FFN_TRAFFIC = {"decode": 302683392 + 45722624 + 224 * 16384,
-               "prefill": 4 * (2254040000 + 48339456 + 1127092000 + 181571840)}
+FFN_TRAFFIC = {"decode": 302706176 + 45393664 + 224 * 16384,
+               "prefill": 4 * (2254268928 + 48164096 + 1126688256 + 92484608)}
 TRAFFIC_NOTE = {"decode": "ncu capture of decode_layer_kernel on decode_profile (1 fill) + 224 router rows",
-                "prefill": "ncu capture of the two gemm_kernel launches on prefill_profile, x4 (units processed)"}
+                "prefill": ("ncu capture of the layer call's two gemm_kernel launches on prefill_profile (bf16 expert "
+                            "rows), x4 (units processed); the timed public call writes fp32 rows: +T*k*H*2 B")}
 
 
 FFN_MODES = {"auto": lambda m: m.MOE_FFN_AUTO, "gemv": lambda m: m.MOE_FFN_GEMV, "gemm": lambda m: m.MOE_FFN_GEMM}
@@ -349,7 +350,7 @@ def measure_ffn_roofline(cfg, dc, layers, xs, decode_like, stream, peaks, args, 
                 ffn(l)
             graphs[l] = g
     torch.cuda.synchronize()
-    times, byts, flops = [], [], []
+    times, byts, flops, t_mixed = [], [], [], []
     with torch.cuda.stream(stream):
         for i in range(n):
             l = prep(i)
@@ -360,9 +361,16 @@ def measure_ffn_roofline(cfg, dc, layers, xs, decode_like, stream, peaks, args, 
             b.record(stream)
             torch.cuda.synchronize()
             times.append(a.elapsed_time(b) / 1e3)
-            active = int((counts > 0).sum().item())
+            cnt = counts.cpu().numpy().astype(np.float64)
+            active = int((cnt > 0).sum())
             byts.append(ffn_bytes(cfg, active))
             flops.append(expert_ffn_flops(cfg))
+            # per-expert roofline: each group takes the longer of its bytes at the HBM peak and its
+            # FLOPs at the tensor peak (weights once + its rows' activations; 2*3*H*I FLOP per row)
+            g_bytes = (cnt > 0) * cfg.expert_bytes + cnt * (cfg.H * 2 + cfg.I * 2 * 2 + cfg.H * 4)
+            g_flops = cnt * 2.0 * 3 * cfg.H * cfg.I
+            t_mixed.append(float(np.sum(np.maximum(g_bytes / (peaks["hbm_gbs"] * 1e9),
+                                                   g_flops / (peaks["bf16_tflops"] * 1e12)))))
     t = float(np.mean(times))
     traffic = FFN_TRAFFIC.get(cfg.name)
     # both rooflines; the one whose time at peak is longer binds
@@ -381,6 +389,9 @@ def measure_ffn_roofline(cfg, dc, layers, xs, decode_like, stream, peaks, args, 
               else "moe_expert_ffn_grouped (tcgen05 gate/up + down GEMM, GEMV for groups of <= 2 rows)")
     out = {"kernel": kernel, **main, "traffic": traffic, "traffic_note": TRAFFIC_NOTE.get(cfg.name),
            "call_us": round(t * 1e6, 3),
+           "mixed_roofline": {"min_us": round(float(np.mean(t_mixed)) * 1e6, 3),
+                              "frac": round(float(np.mean(t_mixed)) / t, 4),
+                              "note": "sum over experts of max(bytes / HBM peak, FLOP / bf16 peak)"},
            "timing": "graph replay of the FFN call, L2 flushed before each",
            "other_roofline": other}
     return out

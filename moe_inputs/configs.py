@@ -93,5 +93,10 @@ DECODE_PROFILE = LayerConfig("decode_profile", T=1, H=4096, E=32, k=6, I=2048, s
 # benchmark workload.
 PREFILL_PROFILE = LayerConfig("prefill_profile", T=2048, H=4096, E=64, k=6, I=2048, seed=12)
 
+# Profiling case for ncu captures of the tensor-bound GEMM regime of long
+# prefill: ~768 rows per expert (three 256-row chunks) over 16 experts, about
+# 1.5 GB on the device.  Not a benchmark workload.
+GEMM_PROFILE = LayerConfig("gemm_profile", T=2048, H=4096, E=16, k=6, I=2048, seed=13)
+
 CONFIGS = {c.name: c for c in (TINY, DECODE, BATCHED_DECODE, PREFILL, LONG_PREFILL, DECODE_PROFILE,
-                               PREFILL_PROFILE)}
+                               PREFILL_PROFILE, GEMM_PROFILE)}
