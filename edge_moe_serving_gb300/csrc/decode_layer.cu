@@ -5,17 +5,23 @@
 //
 //   phase R   every CTA scores its router rows (fp32 rows fetched with
 //             cp.async.bulk into the weight ring's shared memory, the token
-//             rows converted to fp32 next to them) and writes the logits
+//             rows converted to fp32 next to them) and writes the logits; the
+//             cache state the decision reads (this layer's slot-table row,
+//             the pool's stamps, owners and clock) is copied into shared
+//             memory in the same round of copies
 //   barrier   bounded grid-wide barrier: every logit is written
-//   decide    warp 0 of every CTA runs the same top-k, dispatch and
-//             residency decision (front_decide) on the pre-call cache state,
-//             so no CTA waits for another to publish it
+//   route     warp 0 of every CTA runs the same top-k and dispatch on the
+//             logits and looks up which routed experts the cache pool holds;
+//             that fixes every expert's weight source, so the producer warp
+//             starts streaming here
+//   residency warp 0 then decides q, the fill set and the victim slots
+//             (front_residency) while the first weights are in flight; the
+//             consumer warps start once it is done.  CTA 0 commits the
+//             decision to the cache state at once: every CTA read the
+//             pre-call state before the barrier
 //   FFN       the fused weight-streaming gate/up + down phases, admitted
 //             experts copied into their cache slots while they stream, then
-//             the gate-weighted combine (fused_ffn_body)
-//   commit    CTA 0 writes the routing outputs and applies the decision to
-//             the slot table, owners, stamps and clock (every other CTA read
-//             the pre-call state before the first grid barrier of the FFN)
+//             the gate-weighted combine (fused_phases)
 //
 // It computes exactly what the router, bind, dispatch, FFN and combine
 // launches compute for such calls; it replaces their four kernel boundaries
@@ -30,9 +36,10 @@ namespace {
 
 constexpr int kDecMaxT = 8;        // token rows converted to fp32 in shared memory
 constexpr int kDecMaxRows = 4;     // router rows per CTA
+constexpr int kDecMaxSlots = 1024; // cache-pool slots whose state the decision copies
 
 struct DecodeParams {
-  GemvParams g;                    // counts / perm / combine_w are pointed at shared memory in the kernel
+  GemvParams g;                    // perm / combine_w are pointed at shared memory in the kernel
   const float* w_router;           // [E, H] fp32
   const float* bias;               // [E] or null
   uint32_t phi_q16;
@@ -47,16 +54,25 @@ struct DecodeParams {
   int32_t* perm;
   int32_t* inv_perm;
   int rows_per_cta;                // ceil(E / grid)
-  size_t state_off;                // ring offset of the cache-state copy
 };
 
-constexpr size_t kKeysBytes = (size_t)kMaxCacheSlots / 4 * 8 + kMaxCacheSlots / 4 / 8;   // victim keys + hit bitmap
-
-size_t state_offset(int T, int E, int H) {
-  const int G = num_sms();
-  const size_t rows = (size_t)(E + G - 1) / G;
-  return align_up(std::max(rows * H * 4 + (size_t)T * H * 2, kKeysBytes), 16);
-}
+// Shared memory of a decode CTA besides the ring.  The state copies are
+// targets of bulk copies: 16-byte aligned, first.
+struct __align__(16) DecodeShared {
+  int32_t table[kMaxRouteE];       // this layer's slot-table row
+  uint32_t stamp[kDecMaxSlots];    // the cache pool's stamps
+  int32_t owner[kDecMaxSlots];     // and owners
+  uint32_t hitmap[kDecMaxSlots / 32];
+  FrontDecision fr;
+  DecInst inst[32];                // one instance per distinct routed expert, in dispatch order
+  int cnt[32];                     // per instance: this CTA's finished gate/up units
+  float red[kRingThreads / 32][kDecMaxRows][kDecMaxT];
+  float bias[kDecMaxRows];
+  uint64_t rbar;
+  RingShared r;
+  uint32_t clock;
+  int n_inst;
+};
 
 __device__ inline bool grid_barrier(unsigned int* count, volatile int* abort_flag) {
   __threadfence();
@@ -77,35 +93,32 @@ __device__ inline bool grid_barrier(unsigned int* count, volatile int* abort_fla
   return !*abort_flag;
 }
 
+// Named barriers besides __syncthreads (0) and the consumers' barrier inside
+// fused_phases (1, also used here once the decision is complete).
+constexpr int kBarConsumers = 1;
+constexpr int kBarStream = 2;      // warp 0 -> producer warp: the weight sources are known
+
 template <int NT, int VA, int VB>
 __global__ void __launch_bounds__(kRingThreads, 1)
 decode_layer_kernel(DecodeParams d, unsigned int* grid_count) {
   extern __shared__ uint8_t ring_raw[];
-  __shared__ __align__(16) FusedShared fs;
-  __shared__ __align__(16) FrontDecision fr;
-  __shared__ __align__(8) uint64_t rbar;
-  __shared__ float red[kRingThreads / 32][kDecMaxRows][kDecMaxT];
+  __shared__ DecodeShared sh;
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ring_raw) + 127) & ~uintptr_t(127));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   GemvParams p = d.g;
   const int E = p.E, H = p.H, T = p.T, G = gridDim.x, b = blockIdx.x;
   const int n_my = b < E ? (E - 1 - b) / G + 1 : 0;
-  // ring bytes during the prologue: router rows (fp32) | token rows (bf16) | state copy;
-  // after the first barrier: victim keys | hit bitmap (below the state copy)
+  // ring bytes during the prologue: router rows (fp32) | token rows (bf16)
   const int n_slots = p.c.cache.n_slots, base = p.layer * E;
   float* wrow = reinterpret_cast<float*>(ring);                                    // [n_my][H]
   __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(wrow + (size_t)d.rows_per_cta * H);   // [T][H]
-  int32_t* s_table = reinterpret_cast<int32_t*>(ring + d.state_off);               // [E]
-  uint32_t* s_stamp = reinterpret_cast<uint32_t*>(s_table + align_up((size_t)E, 4));
-  int32_t* s_owner = reinterpret_cast<int32_t*>(s_stamp + align_up((size_t)n_slots, 4));
-  __shared__ uint32_t s_clock;
-  __shared__ float s_bias[kDecMaxRows];
 
   if (tid == 0) {
-    ring_init(fs);
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&rbar)));
+    ring_init(sh.r);
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sh.rbar)));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  if (tid < 32) sh.cnt[tid] = 0;
   __syncthreads();
   pdl_wait();
   // ---------------------------------------------------------------- phase R
@@ -121,29 +134,29 @@ decode_layer_kernel(DecodeParams d, unsigned int* grid_count) {
     const uint32_t row_bytes = (uint32_t)H * 4u;
     const uint32_t x_bytes = (uint32_t)T * H * 2u;
     const uint32_t bytes = row_bytes * (uint32_t)n_my + x_bytes + 4u * (uint32_t)table_bulk_n + 8u * (uint32_t)slot_bulk_n;
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(&rbar)), "r"(bytes)
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(&sh.rbar)), "r"(bytes)
                  : "memory");
     for (int i = 0; i < n_my; ++i)
-      bulk_g2s(wrow + (size_t)i * H, d.w_router + (size_t)(b + i * G) * H, row_bytes, &rbar);
-    bulk_g2s(xs, p.x, x_bytes, &rbar);
-    if (table_bulk_n > 0) bulk_g2s(s_table, p.c.slot_table + base, 4u * table_bulk_n, &rbar);
+      bulk_g2s(wrow + (size_t)i * H, d.w_router + (size_t)(b + i * G) * H, row_bytes, &sh.rbar);
+    bulk_g2s(xs, p.x, x_bytes, &sh.rbar);
+    if (table_bulk_n > 0) bulk_g2s(sh.table, p.c.slot_table + base, 4u * table_bulk_n, &sh.rbar);
     if (slot_bulk_n > 0) {
-      bulk_g2s(s_stamp, p.c.stamp, 4u * slot_bulk_n, &rbar);
-      bulk_g2s(s_owner, p.c.owner, 4u * slot_bulk_n, &rbar);
+      bulk_g2s(sh.stamp, p.c.stamp, 4u * slot_bulk_n, &sh.rbar);
+      bulk_g2s(sh.owner, p.c.owner, 4u * slot_bulk_n, &sh.rbar);
     }
   } else if (warp == kConsumerWarps) {
-    for (int e = table_bulk_n + lane; e < E; e += 32) s_table[e] = __ldcg(p.c.slot_table + base + e);
+    for (int e = table_bulk_n + lane; e < E; e += 32) sh.table[e] = __ldcg(p.c.slot_table + base + e);
     for (int v = slot_bulk_n + lane; v < n_slots; v += 32) {
-      s_stamp[v] = __ldcg(p.c.stamp + v);
-      s_owner[v] = __ldcg(p.c.owner + v);
+      sh.stamp[v] = __ldcg(p.c.stamp + v);
+      sh.owner[v] = __ldcg(p.c.owner + v);
     }
-    if (lane == 0) s_clock = __ldcg(p.c.clock);
+    if (lane == 0) sh.clock = __ldcg(p.c.clock);
   } else if (warp == 1 && lane < n_my) {
-    s_bias[lane] = d.bias ? __ldg(d.bias + b + lane * G) : 0.0f;
+    sh.bias[lane] = d.bias ? __ldg(d.bias + b + lane * G) : 0.0f;
   }
-  if (!bounded_wait(&rbar, 0u, &fs.abort)) fs.abort = 1;
+  if (!bounded_wait(&sh.rbar, 0u, &sh.r.abort)) sh.r.abort = 1;
   __syncthreads();
-  if (n_my > 0 && !fs.abort) {
+  if (n_my > 0 && !sh.r.abort) {
     float acc[kDecMaxRows][kDecMaxT];
 #pragma unroll
     for (int i = 0; i < kDecMaxRows; ++i)
@@ -183,68 +196,72 @@ decode_layer_kernel(DecodeParams d, unsigned int* grid_count) {
       for (int t = 0; t < kDecMaxT; ++t) {
         if (i < n_my && t < T) {
           const float s = warp_sum(acc[i][t]);
-          if (lane == 0) red[warp][i][t] = s;
+          if (lane == 0) sh.red[warp][i][t] = s;
         }
       }
     __syncthreads();
     if (tid < n_my * T) {
       const int i = tid / T, t = tid - (tid / T) * T;
       float s = 0.0f;
-      for (int w = 0; w < kRingThreads / 32; ++w) s += red[w][i][t];
-      d.logits[(size_t)t * E + b + i * G] = s + s_bias[i];
+      for (int w = 0; w < kRingThreads / 32; ++w) s += sh.red[w][i][t];
+      d.logits[(size_t)t * E + b + i * G] = s + sh.bias[i];
     }
   }
-  // ---------------------------------------------------------------- decide
-  if (grid_barrier(grid_count + 2, &fs.abort)) {
-    if (warp == 0) {
-      unsigned long long* keys = reinterpret_cast<unsigned long long*>(ring);
-      uint32_t* hitmap = reinterpret_cast<uint32_t*>(ring + (size_t)kMaxCacheSlots / 4 * 8);
-      front_decide(d.logits, T, p.k, E, p.c.cache.n_slots, p.layer, s_table, s_stamp, s_owner, s_clock, d.phi_q16,
-                   d.min_fill, d.policy, d.seed, fr, keys, hitmap);
-    }
-    __syncthreads();
+  // ---------------------------------------------------------------- route, residency
+  if (grid_barrier(grid_count + 2, &sh.r.abort)) {
     const int R = T * p.k;
-    front_counts(fr, E, R);
-    __syncthreads();
-    for (int e = tid; e < E; e += blockDim.x) {
-      fs.off[e] = fr.offsets[e];
-      fs.fill[e] = -1;
-      fs.ent[e] = -1;
-    }
-    __syncthreads();
-    if (tid < R) {
-      const int kind = fr.u_kind[tid], e = fr.u_e[tid];
-      if (kind == kFrontHit) fs.ent[e] = fr.u_slot[tid];
-      if (kind == kFrontFill) fs.fill[e] = fr.u_slot[tid];
-      if (kind == kFrontFill || kind == kFrontStage) fs.ent[e] = MOE_STAGING_TAG | (base + e);
-    }
-    if (b == 0) {
-      for (int e = tid; e <= E; e += blockDim.x) {
-        d.offsets[e] = fr.offsets[e];
-        if (e < E) d.counts[e] = fr.counts[e];
+    if (warp == 0) {
+      const FrontLane fl = front_route(d.logits, T, p.k, E, n_slots, sh.table, sh.fr);
+      // one instance per distinct expert, in dispatch order; a hit streams
+      // from its cache slot, a miss (filled or not) from its staging slot
+      const unsigned um = __ballot_sync(0xffffffffu, fl.uniq);
+      const int j = __popc(um & lane_lt());
+      if (fl.uniq) {
+        const unsigned later = lane == 31 ? 0u : (um & (0xffffffffu << (lane + 1)));
+        sh.inst[j].e = fl.e;
+        sh.inst[j].src = fl.hit ? fl.entry : (int)(MOE_STAGING_TAG | (base + fl.e));
+        sh.inst[j].pos0 = lane;
+        sh.inst[j].ntok = (later ? __ffs(later) - 1 : R) - lane;
       }
-      if (tid < R) {
-        d.topk_ids[tid] = fr.ids[tid];
-        d.topk_w[tid] = fr.w[tid];
-        d.perm[tid] = fr.perm[tid];
-        d.inv_perm[tid] = fr.inv_perm[tid];
-      }
+      if (lane == 0) sh.n_inst = __popc(um);
+      __syncwarp();
+      asm volatile("bar.arrive %0, %1;" ::"n"(kBarStream), "n"(64) : "memory");   // the producer may stream
+      front_residency(fl, n_slots, p.layer, sh.stamp, sh.owner, sh.clock, d.phi_q16, d.min_fill, d.policy, d.seed,
+                      sh.fr, sh.hitmap);
+      if (fl.uniq) sh.inst[j].fill = sh.fr.u_kind[lane] == kFrontFill ? sh.fr.u_slot[lane] : -1;
+      __syncwarp();
     }
-    __syncthreads();
+    if (warp == kConsumerWarps) {
+      asm volatile("bar.sync %0, %1;" ::"n"(kBarStream), "n"(64) : "memory");
+    } else {
+      asm volatile("bar.sync %0, %1;" ::"n"(kBarConsumers), "n"(kConsumerWarps * 32) : "memory");
+      // routing outputs, spread over the CTAs; CTA 0 commits the decision
+      for (int e = b + tid * G; e <= E; e += G * kConsumerWarps * 32) {
+        int lo, hi;
+        dispatch_range(sh.fr.sorted, R, e, lo, hi);
+        d.offsets[e] = lo;
+        if (e < E) d.counts[e] = hi - lo;
+      }
+      if (b == (G > 1 ? 1 : 0) && tid < R) {
+        d.topk_ids[tid] = sh.fr.ids[tid];
+        d.topk_w[tid] = sh.fr.w[tid];
+        d.perm[tid] = sh.fr.perm[tid];
+        d.inv_perm[tid] = sh.fr.inv_perm[tid];
+      }
+      if (b == 0 && warp == 0) front_commit(sh.fr, p.c, p.layer, d.stats, p.status);
+    }
     // ---------------------------------------------------------------- FFN
-    p.counts = fr.counts;
-    p.offsets = fr.offsets;
-    p.perm = fr.perm;
-    p.combine_w = fr.w;
+    p.counts = nullptr;
+    p.offsets = nullptr;
+    p.perm = sh.fr.perm;
+    p.combine_w = sh.fr.w;
     p.fills = nullptr;
-    fused_ffn_body<NT, VA, VB>(p, grid_count, fs, ring);
-    __syncthreads();
-    // ---------------------------------------------------------------- commit
-    if (b == 0 && warp == 0 && !fs.abort) front_commit(fr, p.c, p.layer, d.stats, p.status);
+    const TableInsts v = {sh.inst, sh.n_inst};
+    fused_phases<NT, VA, VB>(p, v, grid_count, sh.r, sh.cnt, ring);
   }
   pdl_trigger();
   __syncthreads();
-  if (fs.abort && tid == 0) set_status(p.status, MOE_DEV_ERR_TIMEOUT);
+  if (sh.r.abort && tid == 0) set_status(p.status, MOE_DEV_ERR_TIMEOUT);
 }
 
 template <int NT, int VA, int VB>
@@ -278,9 +295,8 @@ bool decode_layer_ok(int T, int k, int E, int H, int I, int n_slots) {
   const int G = num_sms();
   const int rows = (E + G - 1) / G;
   return T >= 1 && T <= kDecMaxT && T * k <= 32 && E <= kMaxRouteE && rows <= kDecMaxRows && gemv_fused_ok(H, I) &&
-         n_slots >= 1 && n_slots <= kMaxCacheSlots / 4 &&
-         state_offset(T, E, H) + 4 * (align_up((size_t)E, 4) + 2 * align_up((size_t)n_slots, 4)) <=
-             (size_t)kRingStages * kUnitBytes;
+         n_slots >= 1 && n_slots <= kDecMaxSlots &&
+         (size_t)rows * H * 4 + (size_t)T * H * 2 <= (size_t)kRingStages * kUnitBytes;
 }
 
 cudaError_t launch_decode_layer(const moe_cache& c, int layer, const __nv_bfloat16* x, int T, int k,
@@ -324,7 +340,6 @@ cudaError_t launch_decode_layer(const moe_cache& c, int layer, const __nv_bfloat
   d.inv_perm = inv_perm;
   const int G = num_sms();
   d.rows_per_cta = (c.E + G - 1) / G;
-  d.state_off = state_offset(T, c.E, c.H);
   if (T <= 1) {
     const bool va = c.H == 4096 && ring_rows(c.H, true) == 1;
     const bool vb = c.I == 2048;

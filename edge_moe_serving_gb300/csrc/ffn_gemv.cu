@@ -172,7 +172,7 @@ gemv_fused_kernel(GemvParams p, unsigned int* grid_count) {
   __shared__ __align__(16) FusedShared fs;
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ring_raw) + 127) & ~uintptr_t(127));
   const int tid = threadIdx.x, lane = tid & 31;
-  if (tid == 0) ring_init(fs);
+  if (tid == 0) ring_init(fs.r);
   pdl_wait();
   for (int e = tid; e < p.E; e += blockDim.x) {
     fs.off[e] = p.offsets[e];
@@ -190,7 +190,7 @@ gemv_fused_kernel(GemvParams p, unsigned int* grid_count) {
   fused_ffn_body<NT, VA, VB>(p, grid_count, fs, ring);
   pdl_trigger();
   __syncthreads();
-  if (fs.abort && tid == 0) set_status(p.status, MOE_DEV_ERR_TIMEOUT);
+  if (fs.r.abort && tid == 0) set_status(p.status, MOE_DEV_ERR_TIMEOUT);
 }
 
 

@@ -47,7 +47,11 @@ __device__ inline void topk_lanes(const float* row, int E, int k, int& id_out, f
 // and front_commit applies it once.  Same rules as the one-warp front end:
 // top-k, stable dispatch by (expert, row), hits / misses, q from the Q16 rule,
 // the fill set F (lowest ids or seeded SplitMix64 ranks), victims = the q
-// least (stamp, slot) cache slots not used by a hit of this call.
+// least (stamp, slot) cache slots not used by a hit of this call.  It comes in
+// two parts: front_route (routing, dispatch, which experts hit) and
+// front_residency (F and the victims), so that a caller can start streaming
+// the routed experts' weights, whose pools the first part already fixes,
+// while the second part runs.
 enum { kFrontNone = 0, kFrontHit = 1, kFrontFill = 2, kFrontStage = 3 };
 
 struct FrontDecision {
@@ -56,8 +60,6 @@ struct FrontDecision {
   int perm[32];
   int inv_perm[32];
   int sorted[32];               // routed rows' expert ids in dispatch order (0x7fffffff past R)
-  int counts[kMaxRouteE];       // filled from `sorted` by front_counts
-  int offsets[kMaxRouteE + 1];
   int u_e[32];                  // per sorted position: the expert, where u_kind != kFrontNone
   int u_kind[32];
   int u_slot[32];               // hit: its cache slot; fill: the victim slot
@@ -66,15 +68,18 @@ struct FrontDecision {
   uint32_t now;
 };
 
-// The cache state comes in as copies: table = this layer's slot-table row
-// (E entries), stamp / owner = the cache pool's (n_slots entries), clock.
-// keys: >= 32 * ceil(n_slots / 32) 64-bit words of shared memory; hitmap:
-// >= ceil(n_slots / 32) words.  T * k <= 32, E <= kMaxRouteE.
-__device__ inline void front_decide(const float* logits, int T, int k, int E, int n_slots, int layer,
-                                    const int32_t* table, const uint32_t* stamp, const int32_t* owner,
-                                    uint32_t clock, uint32_t phi_q16, int min_fill, int policy,
-                                    unsigned long long seed, FrontDecision& d, unsigned long long* keys,
-                                    uint32_t* hitmap) {
+// What lane r (sorted dispatch position r) hands from front_route to front_residency.
+struct FrontLane {
+  int e;          // expert at this position (0x7fffffff past R)
+  int entry;      // its slot-table entry, where uniq
+  bool uniq;      // first position of its expert
+  bool hit, miss;
+};
+
+// Part 1: top-k of each token, the dispatch permutation, and which distinct
+// experts the cache pool holds.  table = this layer's slot-table row (E entries).
+__device__ inline FrontLane front_route(const float* logits, int T, int k, int E, int n_slots,
+                                        const int32_t* table, FrontDecision& d) {
   const int lane = threadIdx.x & 31;
   const int R = T * k;
   // 1. top-k per token: lane r ends up with routed row r = t*k + j
@@ -115,12 +120,27 @@ __device__ inline void front_decide(const float* logits, int T, int k, int E, in
   d.sorted[lane] = sorted_id;
   // 3. residency of the distinct experts (first occurrence in sorted order)
   const int prev_id = __shfl_up_sync(0xffffffffu, sorted_id, 1);
-  const bool uniq = lane < R && (lane == 0 || prev_id != sorted_id);
-  const int e = sorted_id;
-  const int entry = uniq ? table[e] : -1;
+  FrontLane fl;
+  fl.e = sorted_id;
+  fl.uniq = lane < R && (lane == 0 || prev_id != sorted_id);
+  fl.entry = fl.uniq ? table[sorted_id] : -1;
+  fl.hit = fl.uniq && fl.entry >= 0 && fl.entry < n_slots;
+  fl.miss = fl.uniq && !fl.hit;
+  return fl;
+}
+
+// Part 2: q, the fill set F and its victims.  stamp / owner = the cache pool's
+// (n_slots entries), clock = the pool's clock.  hitmap: ceil(n_slots / 32)
+// words of scratch (word l, bit b: slot 32 l + b is used by a hit of this call
+// or already taken as a victim).
+__device__ inline void front_residency(const FrontLane& fl, int n_slots, int layer, const uint32_t* stamp,
+                                       const int32_t* owner, uint32_t clock, uint32_t phi_q16, int min_fill,
+                                       int policy, unsigned long long seed, FrontDecision& d, uint32_t* hitmap) {
+  const int lane = threadIdx.x & 31;
+  const int e = fl.e;
+  const bool uniq = fl.uniq, hit = fl.hit, miss = fl.miss;
+  const int entry = fl.entry;
   const uint32_t now = clock + 1u;
-  const bool hit = uniq && entry >= 0 && entry < n_slots;
-  const bool miss = uniq && !hit;
   const int bad = __any_sync(0xffffffffu, miss && entry >= 0 && entry < MOE_STAGING_TAG) ? 1 : 0;
   const int map_words = (n_slots + 31) / 32;
   for (int w = lane; w < map_words; w += 32) hitmap[w] = 0u;
@@ -149,40 +169,34 @@ __device__ inline void front_decide(const float* logits, int T, int k, int E, in
   }
   const unsigned f_mask = __ballot_sync(0xffffffffu, inF);
   const int f_idx = __popc(f_mask & lane_lt());
-  // victims: the q least (stamp, slot) cache slots not used by a hit of this call
+  // victims: the q least (stamp, slot) cache slots not used by a hit of this
+  // call; lane b scans slots b, b + 32, ... each round, and the round's victim
+  // is marked in the hitmap so that the next round skips it
   int n_fill = 0;
   int my_victim = -1;
-  if (q > 0) {
-    int local = 0;
-    for (int v = lane; v < n_slots; v += 32, ++local) {
-      const uint32_t sv = stamp[v];
-      const bool used = ((hitmap[v >> 5] >> (v & 31)) & 1u) != 0 || sv == now;
-      keys[local * 32 + lane] = used ? ~0ull : (((unsigned long long)sv << 32) | (unsigned long long)v);
-    }
-    __syncwarp();
-    const int per_lane = (n_slots + 31) / 32;
-    for (int i = 0; i < q; ++i) {
-      unsigned long long best = ~0ull;
-      int best_at = -1;
-      for (int l = 0; l < per_lane; ++l) {
-        const unsigned long long kk = keys[l * 32 + lane];
-        if (lane + 32 * l < n_slots && kk < best) {
-          best = kk;
-          best_at = l;
-        }
+  const int per_lane = map_words;
+  for (int i = 0; i < q; ++i) {
+    unsigned long long best = ~0ull;
+    for (int l = 0; l < per_lane; ++l) {
+      const int v = lane + 32 * l;
+      if (v < n_slots) {
+        const uint32_t sv = stamp[v];
+        const bool used = ((hitmap[l] >> lane) & 1u) != 0 || sv == now;
+        const unsigned long long kk = used ? ~0ull : (((unsigned long long)sv << 32) | (unsigned long long)v);
+        best = kk < best ? kk : best;
       }
-      unsigned long long wmin = best;
+    }
 #pragma unroll
-      for (int o2 = 16; o2 > 0; o2 >>= 1) {
-        const unsigned long long ov = __shfl_xor_sync(0xffffffffu, wmin, o2);
-        wmin = ov < wmin ? ov : wmin;
-      }
-      if (wmin == ~0ull) break;   // no candidate left: the rest of F overflows to C
-      if (best == wmin && best_at >= 0) keys[best_at * 32 + lane] = ~0ull;
-      if (inF && f_idx == i) my_victim = (int)(wmin & 0xFFFFFFFFull);
-      ++n_fill;
-      __syncwarp();
+    for (int o2 = 16; o2 > 0; o2 >>= 1) {
+      const unsigned long long ov = __shfl_xor_sync(0xffffffffu, best, o2);
+      best = ov < best ? ov : best;
     }
+    if (best == ~0ull) break;   // no candidate left: the rest of F overflows to C
+    const int vv = (int)(best & 0xFFFFFFFFull);
+    if (lane == (vv & 31)) hitmap[vv >> 5] |= 1u << (vv & 31);
+    if (inF && f_idx == i) my_victim = vv;
+    ++n_fill;
+    __syncwarp();
   }
   const bool filled = inF && f_idx < n_fill;
   d.u_e[lane] = e;
@@ -200,25 +214,22 @@ __device__ inline void front_decide(const float* logits, int T, int k, int E, in
   __syncwarp();
 }
 
-// counts[e] and offsets[e] of the dispatch from the sorted ids, by all
-// threads of the block (a binary search per expert).
-__device__ inline void front_counts(FrontDecision& d, int E, int R) {
-  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
-    int lo = 0, hi = R;                    // first position with sorted id >= e
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (d.sorted[mid] < e) lo = mid + 1;
-      else hi = mid;
-    }
-    int lo2 = lo, hi2 = R;                 // first position with sorted id > e
-    while (lo2 < hi2) {
-      const int mid = (lo2 + hi2) >> 1;
-      if (d.sorted[mid] <= e) lo2 = mid + 1;
-      else hi2 = mid;
-    }
-    d.offsets[e] = lo;
-    if (e < E) d.counts[e] = lo2 - lo;
+// First dispatch position of expert e (and one past its last) in the sorted ids.
+__device__ inline void dispatch_range(const int* sorted, int R, int e, int& lo_out, int& hi_out) {
+  int lo = 0, hi = R;                    // first position with sorted id >= e
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (sorted[mid] < e) lo = mid + 1;
+    else hi = mid;
   }
+  int lo2 = lo, hi2 = R;                 // first position with sorted id > e
+  while (lo2 < hi2) {
+    const int mid = (lo2 + hi2) >> 1;
+    if (sorted[mid] <= e) lo2 = mid + 1;
+    else hi2 = mid;
+  }
+  lo_out = lo;
+  hi_out = lo2;
 }
 
 // Applies a decision to the cache state (one warp, once per call, after every

@@ -164,51 +164,54 @@ __device__ inline float ord_val(uint32_t k) { return __uint_as_float((k & 0x8000
 // One warp selects the top-k of one token's logits (E <= 512; order: logit
 // descending, id ascending) and renormalises the softmax over the selection.
 // On return lane r < k holds the r-th selected id in ascending order and its
-// weight.  Lane l holds experts l + 32 j and its best untaken candidate; a
-// round is two warp reductions (largest key, then the lowest id among the
-// lanes holding it), and only the lane that owned the winner rescans.
-// L2_ONLY: read the row through L2 (rows written by other CTAs of the launch).
-template <bool L2_ONLY>
-__device__ inline void topk_core(const float* row, int E, int k, int& id_out, float& w_out) {
+// weight.  Lane l holds experts l + 32 j (j < PER) as 64-bit words
+// (key << 32 | ~id), sorted in registers in descending order by a bitonic
+// network, so its head is its best candidate (largest logit, then lowest id).
+// A round is two warp reductions (largest head key, then the lowest id among
+// the lanes whose head holds it), and the lane that owned the winner pops its
+// head with a branch-free shift.  L2_ONLY: read the row through L2 (rows
+// written by other CTAs of the launch).
+template <bool L2_ONLY, int PER>
+__device__ inline void topk_sorted(const float* row, int E, int k, int& id_out, float& w_out) {
   const int lane = threadIdx.x & 31;
-  constexpr int kPer = kMaxRouteE / 32;
-  uint32_t key[kPer];
+  unsigned long long c[PER];
 #pragma unroll
-  for (int j = 0; j < kPer; ++j) {
+  for (int j = 0; j < PER; ++j) {
     const int e = lane + 32 * j;
     float v = 0.0f;
     if (e < E) v = L2_ONLY ? __ldcg(row + e) : row[e];
-    key[j] = (e < E) ? ord_key(v) : 0u;   // 0: no expert (every logit maps above 0)
+    // no expert: 0 (key 0, id field ~0xffffffff = 0) sorts below every expert
+    c[j] = (e < E) ? (((unsigned long long)ord_key(v) << 32) | (unsigned long long)(~(uint32_t)e)) : 0ull;
   }
-  uint32_t taken = 0;
-  uint32_t bk = 0u;
-  int bj = -1;
-  auto rescan = [&]() {
-    bk = 0u;
-    bj = -1;
 #pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      if (lane + 32 * j < E && !((taken >> j) & 1u) && (bj < 0 || key[j] > bk)) {
-        bk = key[j];
-        bj = j;
+  for (int size = 2; size <= PER; size <<= 1)
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1)
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        const int j = i ^ stride;
+        if (j > i) {
+          const bool desc = (i & size) == 0;   // the last merge (size == PER) is descending throughout
+          const unsigned long long a = c[i], b = c[j];
+          const bool sw = desc ? (a < b) : (a > b);
+          c[i] = sw ? b : a;
+          c[j] = sw ? a : b;
+        }
       }
-    }
-  };
-  rescan();
   float sel_v = -INFINITY;
   int sel_id = 0x7fffffff;
   for (int r = 0; r < k; ++r) {
-    const uint32_t m = __reduce_max_sync(0xffffffffu, bj >= 0 ? bk : 0u);
-    const uint32_t cand = (bj >= 0 && bk == m) ? (uint32_t)(lane + 32 * bj) : 0xffffffffu;
-    const int id = (int)__reduce_min_sync(0xffffffffu, cand);
-    if ((id & 31) == lane) {
-      taken |= 1u << (id >> 5);
-      rescan();
-    }
+    const uint32_t hk = (uint32_t)(c[0] >> 32);
+    const uint32_t m = __reduce_max_sync(0xffffffffu, hk);
+    const uint32_t id = __reduce_min_sync(0xffffffffu, hk == m ? ~(uint32_t)c[0] : 0xffffffffu);
     if (lane == r) {
       sel_v = ord_val(m);
-      sel_id = id;
+      sel_id = (int)id;
     }
+    const bool pop = (int)(id & 31u) == lane;
+#pragma unroll
+    for (int j = 0; j + 1 < PER; ++j) c[j] = pop ? c[j + 1] : c[j];
+    c[PER - 1] = pop ? 0ull : c[PER - 1];
   }
   const float vmax = __shfl_sync(0xffffffffu, sel_v, 0);
   const float ex = (lane < k) ? expf(sel_v - vmax) : 0.0f;
@@ -229,6 +232,14 @@ __device__ inline void topk_core(const float* row, int E, int k, int& id_out, fl
   }
   id_out = out_id;
   w_out = out_w;
+}
+
+// topk_sorted with as few candidates per lane as E allows.
+template <bool L2_ONLY>
+__device__ inline void topk_core(const float* row, int E, int k, int& id_out, float& w_out) {
+  if (E <= 128) topk_sorted<L2_ONLY, 4>(row, E, k, id_out, w_out);
+  else if (E <= 256) topk_sorted<L2_ONLY, 8>(row, E, k, id_out, w_out);
+  else topk_sorted<L2_ONLY, kMaxRouteE / 32>(row, E, k, id_out, w_out);
 }
 
 // topk_core writing the selection: ids_out[0..k) ascending, w_out[0..k).

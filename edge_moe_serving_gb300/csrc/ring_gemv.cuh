@@ -68,6 +68,56 @@ __device__ inline int find_expert(const int* s_pref, int E, int j) {
   return lo;
 }
 
+// Where instance j of a fused launch reads and writes: its expert, the
+// slot-table entry its weights stream from, its fill destination (a cache
+// slot, or -1), its first dispatch position and its number of token rows.
+struct InstInfo {
+  int e, entry, fill, pos0, ntok;
+};
+
+// Instances from the per-expert prefix: expert e with c rows has ceil(c / NT)
+// instances of up to NT rows each (the general fused expert-FFN launch).
+template <int NT>
+struct PrefixInsts {
+  const int* pref;
+  const int* off;
+  const int* ent;
+  const int* fill;
+  const int32_t* counts;
+  int E;
+  __device__ int count() const { return pref[E]; }
+  __device__ InstInfo get(int j) const {
+    const int e = find_expert(pref, E, j);
+    const int c = j - pref[e];
+    return {e, ent[e], fill[e], off[e] + c * NT, min(NT, counts[e] - c * NT)};
+  }
+  // what the weight stream needs: the expert, its entry and fill destination
+  __device__ void source(int j, int& e, int& entry, int& fill_dst) const {
+    e = find_expert(pref, E, j);
+    entry = ent[e];
+    fill_dst = fill[e];
+  }
+};
+
+// Instances listed one per entry (the one-launch decode layer: one instance per
+// routed expert, every expert's rows fit one instance).  `src` already names
+// the pool the weights stream from (a hit's cache slot, else the staging
+// slot), so the stream can start before `fill` is decided.
+struct DecInst {
+  int e, src, fill, pos0, ntok;
+};
+struct TableInsts {
+  const DecInst* t;
+  int n;
+  __device__ int count() const { return n; }
+  __device__ InstInfo get(int j) const { return {t[j].e, t[j].src, t[j].fill, t[j].pos0, t[j].ntok}; }
+  __device__ void source(int j, int& e, int& entry, int& fill_dst) const {
+    e = t[j].e;
+    entry = t[j].src;
+    fill_dst = -1;
+  }
+};
+
 // ---------------------------------------------------------------- TMA-ring variant
 // Used when the weight row length K is a multiple of 256 (every lane then owns
 // K/256 16-byte vectors of each row).  One producer thread streams "units" of
@@ -214,8 +264,8 @@ struct UnitWorker {
 
   // New instance j.  Down rows wait (bounded) until p.inst_done[j] >= need:
   // h of the instance is then complete.  Returns false on abort.
-  __device__ inline bool begin(const GemvParams& p, int j, const int* s_pref, const int* s_off, const int* s_ent,
-                               const int* s_fill, unsigned need, volatile int* abort_flag) {
+  template <class Insts>
+  __device__ inline bool begin(const GemvParams& p, const Insts& v, int j, unsigned need, volatile int* abort_flag) {
     const int lane = threadIdx.x & 31;
     cur_j = j;
     if (!GATEUP && p.inst_done != nullptr) {
@@ -232,12 +282,11 @@ struct UnitWorker {
       __syncwarp();
       if (*abort_flag) return false;
     }
-    const int e = find_expert(s_pref, p.E, j);
+    const InstInfo in = v.get(j);
     // any warp that meets an unbound expert reports it (units are spread over warps)
-    rs = ring_source(p, e, s_ent[e], s_fill[e], (lane == 0) ? p.status : nullptr);
-    const int c = j - s_pref[e];
-    pos0 = s_off[e] + c * NT;
-    ntok = min(NT, p.counts[e] - c * NT);
+    rs = ring_source(p, in.e, in.entry, in.fill, (lane == 0) ? p.status : nullptr);
+    pos0 = in.pos0;
+    ntok = in.ntok;
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       const int pos = pos0 + (t < ntok ? t : 0);
@@ -342,9 +391,8 @@ struct UnitWorker {
 // writes h; phase B streams down rows and writes y.  Units are grid-strided:
 // CTA b takes units b, b + G, b + 2G, ...  VC > 0: the single token's
 // activation row (K = 256*VC) is held in registers.
-template <int NT, bool GATEUP, int VC>
-__device__ inline void ring_phase(const GemvParams& p, const int* s_pref, const int* s_off, const int* s_ent,
-                                  const int* s_fill, int* s_cnt, uint8_t* ring, uint64_t* full_bar,
+template <int NT, bool GATEUP, int VC, class Insts>
+__device__ inline void ring_phase(const GemvParams& p, const Insts& v, int* s_cnt, uint8_t* ring, uint64_t* full_bar,
                                   uint64_t* empty_bar, volatile int* abort_flag, RingState& st, bool producer) {
   constexpr int NB = GATEUP ? 2 : 1;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -354,7 +402,7 @@ __device__ inline void ring_phase(const GemvParams& p, const int* s_pref, const 
   const int U = ring_rows(K, GATEUP);
   const int upi = (NTASK + U - 1) / U;
   const int bank_stride = kUnitBytes / NB;
-  const int total = s_pref[p.E] * upi;
+  const int total = v.count() * upi;
   const int G = gridDim.x;
   const int n_local = local_units(total);
   const int base = st.base;
@@ -370,8 +418,9 @@ __device__ inline void ring_phase(const GemvParams& p, const int* s_pref, const 
       const int n0 = (u - j * upi) * U;
       if (j != cur_j) {
         cur_j = j;
-        const int e = find_expert(s_pref, p.E, j);
-        rs = ring_source(p, e, s_ent[e], s_fill[e], nullptr);
+        int e, entry, fill_dst;
+        v.source(j, e, entry, fill_dst);
+        rs = ring_source(p, e, entry, fill_dst, nullptr);
       }
       const int ri = base + i;
       const int stage = ri % kRingStages;
@@ -409,7 +458,7 @@ __device__ inline void ring_phase(const GemvParams& p, const int* s_pref, const 
     const int u = blockIdx.x + i * G;
     const int j = u / upi;
     const int n0 = (u - j * upi) * U;
-    if (j != wk.cur_j && !wk.begin(p, j, s_pref, s_off, s_ent, s_fill, need, abort_flag)) break;
+    if (j != wk.cur_j && !wk.begin(p, v, j, need, abort_flag)) break;
     const int ri = base + i;
     const int stage = ri % kRingStages;
     const uint32_t use = (uint32_t)(ri / kRingStages);
@@ -437,7 +486,14 @@ __device__ inline void ring_phase(const GemvParams& p, const int* s_pref, const 
   }
 }
 
-// Shared memory of a fused-GEMV CTA besides the ring itself.
+// The ring's barriers and the CTA's abort flag.
+struct RingShared {
+  uint64_t full_bar[kRingStages];
+  uint64_t empty_bar[kRingStages];
+  int abort;
+};
+
+// Shared memory of a general fused-GEMV CTA besides the ring itself.
 struct FusedShared {
   int pref[kMaxE + 1];
   int warp[32];               // per-warp scan partials of build_prefix: any block of up to 1024 threads
@@ -445,46 +501,41 @@ struct FusedShared {
   int ent[kMaxE];
   int fill[kMaxE];
   int cnt[kMaxFusedInst];     // per-instance count of this CTA's finished gate/up units
-  uint64_t full_bar[kRingStages];
-  uint64_t empty_bar[kRingStages];
-  int abort;
+  RingShared r;
 };
 
 constexpr int kRingSmem = kRingStages * kUnitBytes + 128;
 
-__device__ inline void ring_init(FusedShared& fs) {
+__device__ inline void ring_init(RingShared& rs) {
   for (int s = 0; s < kRingStages; ++s) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&fs.full_bar[s])));
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&fs.empty_bar[s])));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&rs.full_bar[s])));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&rs.empty_bar[s])));
   }
-  fs.abort = 0;
+  rs.abort = 0;
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
-// Everything after the prologue of a fused launch: fs.off / fs.ent / fs.fill
-// hold each expert's first dispatch position, slot-table entry and fill
-// destination (-1: none), and p.counts / p.perm / p.combine_w may point to
-// shared memory.  Phase A (gate/up -> h) and phase B (down -> y) share one
-// weight ring, so the producer keeps streaming down rows while the consumers
-// wait for h: per instance (p.inst_done, a bounded wait on the counter of the
-// instance about to be read) or at a bounded grid-wide barrier; with
-// p.combine_out set, a second barrier and the gate-weighted combine follow.
-// grid_count[0..1] and the p.inst_done words must be zero at launch.
-template <int NT, int VA, int VB>
-__device__ void fused_ffn_body(const GemvParams& p, unsigned int* grid_count, FusedShared& fs, uint8_t* ring) {
+// The two streaming phases of a fused launch and what follows them, for
+// instances described by `v`, run by every thread of the CTA: warp
+// kConsumerWarps is the producer (its lane 0 streams; the other lanes return at
+// once), the others consume.  Phase A (gate/up -> h) and phase B (down -> y)
+// share one weight ring, so the producer keeps streaming down rows while the
+// consumers wait for h: per instance (p.inst_done, a bounded wait on the
+// counter of the instance about to be read; cnt[j] counts this CTA's finished
+// gate/up units of instance j and must be zero) or at a bounded grid-wide
+// barrier; with p.combine_out set, a second barrier and the gate-weighted
+// combine follow.  grid_count[0..1] and the p.inst_done words must be zero at
+// launch.
+template <int NT, int VA, int VB, class Insts>
+__device__ void fused_phases(const GemvParams& p, const Insts& v, unsigned int* grid_count, RingShared& rsh, int* cnt,
+                             uint8_t* ring) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  volatile int* abort_flag = &fs.abort;
-  build_prefix<NT>(p, fs.pref, fs.warp);   // ends with __syncthreads
-  if (p.inst_done != nullptr) {
-    for (int i = tid; i < fs.pref[p.E] && i < kMaxFusedInst; i += blockDim.x) fs.cnt[i] = 0;
-    __syncthreads();
-  }
+  volatile int* abort_flag = &rsh.abort;
   const bool producer = warp == kConsumerWarps;
   RingState st = {0, -1, -1, false};
 
   if (!producer || lane == 0) {
-    ring_phase<NT, true, VA>(p, fs.pref, fs.off, fs.ent, fs.fill, fs.cnt, ring, fs.full_bar, fs.empty_bar, abort_flag, st,
-                             producer);
+    ring_phase<NT, true, VA>(p, v, cnt, ring, rsh.full_bar, rsh.empty_bar, abort_flag, st, producer);
     if (!producer && p.inst_done == nullptr) {
       // grid-wide barrier: every h row of phase A is written before any is read
       __threadfence();
@@ -505,15 +556,14 @@ __device__ void fused_ffn_body(const GemvParams& p, unsigned int* grid_count, Fu
       asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
     }
     if (!*abort_flag)
-      ring_phase<NT, false, VB>(p, fs.pref, fs.off, fs.ent, fs.fill, fs.cnt, ring, fs.full_bar, fs.empty_bar, abort_flag,
-                                st, producer);
+      ring_phase<NT, false, VB>(p, v, cnt, ring, rsh.full_bar, rsh.empty_bar, abort_flag, st, producer);
     if (producer) {
       // drain: the copies of the last ring round land before the CTA exits (the last
       // kRingStages slots issued: each stage's latest use, whatever it carried)
       volatile int no_abort = 0;
       if (st.armed_last >= 0)
         for (int q = st.last_issued; q >= 0 && q > st.last_issued - kRingStages; --q)
-          ring_wait(&fs.full_bar[q % kRingStages], (uint32_t)(q / kRingStages) & 1u, &no_abort);
+          ring_wait(&rsh.full_bar[q % kRingStages], (uint32_t)(q / kRingStages) & 1u, &no_abort);
     } else {
       if (st.stored && lane == 0) bulk_wait_all();   // fused-fill writes complete before exit
       if (p.combine_out != nullptr) {
@@ -560,6 +610,22 @@ __device__ void fused_ffn_body(const GemvParams& p, unsigned int* grid_count, Fu
       }
     }
   }
+}
+
+// The general fused launch after its prologue: fs.off / fs.ent / fs.fill hold
+// each expert's first dispatch position, slot-table entry and fill
+// destination (-1: none); p.counts / p.perm / p.combine_w may point to shared
+// memory.  Builds the per-expert instance prefix, then fused_phases.
+template <int NT, int VA, int VB>
+__device__ void fused_ffn_body(const GemvParams& p, unsigned int* grid_count, FusedShared& fs, uint8_t* ring) {
+  const int tid = threadIdx.x;
+  build_prefix<NT>(p, fs.pref, fs.warp);   // ends with __syncthreads
+  if (p.inst_done != nullptr) {
+    for (int i = tid; i < fs.pref[p.E] && i < kMaxFusedInst; i += blockDim.x) fs.cnt[i] = 0;
+    __syncthreads();
+  }
+  const PrefixInsts<NT> v = {fs.pref, fs.off, fs.ent, fs.fill, p.counts, p.E};
+  fused_phases<NT, VA, VB>(p, v, grid_count, fs.r, fs.cnt, ring);
 }
 
 }  // namespace
