@@ -20,12 +20,14 @@
 //             decision to the cache state at once: every CTA read the
 //             pre-call state before the barrier
 //   FFN       the fused weight-streaming gate/up + down phases, admitted
-//             experts copied into their cache slots while they stream, then
-//             the gate-weighted combine (fused_phases)
+//             experts copied into their cache slots while they stream; each
+//             CTA computes whole output row blocks in the down phase and
+//             applies the gate-weighted combine to them (fused_phases)
 //
 // It computes exactly what the router, bind, dispatch, FFN and combine
 // launches compute for such calls; it replaces their four kernel boundaries
-// by two grid barriers.
+// by one grid barrier (after the router) and per-instance completion counters
+// (gate/up -> down).
 #include <algorithm>
 
 #include "front_warp.cuh"

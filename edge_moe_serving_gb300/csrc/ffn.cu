@@ -40,7 +40,7 @@ cudaError_t launch_ffn(const moe_cache& c, int layer, const int32_t* counts, con
   if ((fused_fills != nullptr || combine_out != nullptr) && gemv_max != INT_MAX) return cudaErrorNotSupported;
   if (combine_out != nullptr && !gemv_fused_ok(c.H, c.I)) return cudaErrorNotSupported;
   if (gemv_max > 0) {
-    GemvParams p;
+    GemvParams p = {};
     p.c = c;
     p.layer = layer;
     p.E = c.E;

@@ -391,9 +391,13 @@ struct UnitWorker {
 // writes h; phase B streams down rows and writes y.  Units are grid-strided:
 // CTA b takes units b, b + G, b + 2G, ...  VC > 0: the single token's
 // activation row (K = 256*VC) is held in registers.
+// owned (phase B only): instead of the stride, CTA b takes the row blocks
+// rb = b, b + G, b + 2G, ... of every instance, instance by instance, so that
+// it holds every expert output of those rows and can combine them itself.
 template <int NT, bool GATEUP, int VC, class Insts>
 __device__ inline void ring_phase(const GemvParams& p, const Insts& v, int* s_cnt, uint8_t* ring, uint64_t* full_bar,
-                                  uint64_t* empty_bar, volatile int* abort_flag, RingState& st, bool producer) {
+                                  uint64_t* empty_bar, volatile int* abort_flag, RingState& st, bool producer,
+                                  bool owned = false) {
   constexpr int NB = GATEUP ? 2 : 1;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int K = GATEUP ? p.H : p.I;
@@ -404,18 +408,30 @@ __device__ inline void ring_phase(const GemvParams& p, const Insts& v, int* s_cn
   const int bank_stride = kUnitBytes / NB;
   const int total = v.count() * upi;
   const int G = gridDim.x;
-  const int n_local = local_units(total);
+  owned = owned && !GATEUP;
+  const int M = local_units(upi);   // row blocks this CTA owns
+  const int n_local = owned ? v.count() * M : local_units(total);
   const int base = st.base;
   st.base += n_local;
+  // this CTA's i-th unit: instance j, first row n0
+  auto unit_of = [&](int i, int& j, int& n0) {
+    if (owned) {
+      j = i / M;
+      n0 = ((int)blockIdx.x + (i - j * M) * G) * U;
+    } else {
+      const int u = (int)blockIdx.x + i * G;
+      j = u / upi;
+      n0 = (u - j * upi) * U;
+    }
+  };
 
   if (producer) {
     int cur_j = -1;
     RingSrc rs;
     rs.ok = false;
     for (int i = 0; i < n_local && !*abort_flag; ++i) {
-      const int u = blockIdx.x + i * G;
-      const int j = u / upi;
-      const int n0 = (u - j * upi) * U;
+      int j, n0;
+      unit_of(i, j, n0);
       if (j != cur_j) {
         cur_j = j;
         int e, entry, fill_dst;
@@ -455,9 +471,8 @@ __device__ inline void ring_phase(const GemvParams& p, const Insts& v, int* s_cn
   // this warp's units: ring index ri = base + i with ri % C == warp
   const int i0 = ((warp - base) % kConsumerWarps + kConsumerWarps) % kConsumerWarps;
   for (int i = i0; i < n_local; i += kConsumerWarps) {
-    const int u = blockIdx.x + i * G;
-    const int j = u / upi;
-    const int n0 = (u - j * upi) * U;
+    int j, n0;
+    unit_of(i, j, n0);
     if (j != wk.cur_j && !wk.begin(p, v, j, need, abort_flag)) break;
     const int ri = base + i;
     const int stage = ri % kRingStages;
@@ -523,9 +538,10 @@ __device__ inline void ring_init(RingShared& rs) {
 // consumers wait for h: per instance (p.inst_done, a bounded wait on the
 // counter of the instance about to be read; cnt[j] counts this CTA's finished
 // gate/up units of instance j and must be zero) or at a bounded grid-wide
-// barrier; with p.combine_out set, a second barrier and the gate-weighted
-// combine follow.  grid_count[0..1] and the p.inst_done words must be zero at
-// launch.
+// barrier.  With p.combine_out set, phase B gives each CTA whole output row
+// blocks (every instance's rows rb = b, b + G, ...) and the CTA applies the
+// gate-weighted combine to its own rows when its units are done.
+// grid_count[0] and the p.inst_done words must be zero at launch.
 template <int NT, int VA, int VB, class Insts>
 __device__ void fused_phases(const GemvParams& p, const Insts& v, unsigned int* grid_count, RingShared& rsh, int* cnt,
                              uint8_t* ring) {
@@ -556,7 +572,8 @@ __device__ void fused_phases(const GemvParams& p, const Insts& v, unsigned int* 
       asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
     }
     if (!*abort_flag)
-      ring_phase<NT, false, VB>(p, v, cnt, ring, rsh.full_bar, rsh.empty_bar, abort_flag, st, producer);
+      ring_phase<NT, false, VB>(p, v, cnt, ring, rsh.full_bar, rsh.empty_bar, abort_flag, st, producer,
+                                p.combine_out != nullptr);
     if (producer) {
       // drain: the copies of the last ring round land before the CTA exits (the last
       // kRingStages slots issued: each stage's latest use, whatever it carried)
@@ -567,44 +584,26 @@ __device__ void fused_phases(const GemvParams& p, const Insts& v, unsigned int* 
     } else {
       if (st.stored && lane == 0) bulk_wait_all();   // fused-fill writes complete before exit
       if (p.combine_out != nullptr) {
-        // second grid-wide barrier: every y row is written; then the gate-weighted
-        // combine in fixed expert order, spread over all CTAs
-        __threadfence();
-        asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
-        if (tid == 0) {
-          __threadfence();
-          atomicAdd(grid_count + 1, 1u);
-          const unsigned long long t0 = gtimer();
-          while (*reinterpret_cast<volatile unsigned int*>(grid_count + 1) < gridDim.x) {
-            if (*abort_flag) break;
-            if (gtimer() - t0 > kGridWaitNs) {
-              *abort_flag = 1;
-              break;
-            }
-          }
-          __threadfence();
-        }
+        // Phase B ran with owned row blocks: every expert row of this CTA's
+        // output rows was written by its own warps, so once they are all done
+        // (a CTA barrier) it combines those rows itself, in fixed expert order,
+        // with no grid-wide barrier.
         asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
         if (!*abort_flag) {
-          const int H4 = p.H >> 2;
-          const int items = p.T * H4;
-          for (int it = blockIdx.x * (kConsumerWarps * 32) + tid; it < items; it += gridDim.x * (kConsumerWarps * 32)) {
-            const int t = it / H4, c4 = it - t * H4;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int jj = 0; jj < p.k; ++jj) {
-              const float w = p.combine_w[t * p.k + jj];
-              const float4 y = __ldcg(reinterpret_cast<const float4*>(p.y + (size_t)(t * p.k + jj) * p.H) + c4);
-              acc.x = fmaf(w, y.x, acc.x);
-              acc.y = fmaf(w, y.y, acc.y);
-              acc.z = fmaf(w, y.z, acc.z);
-              acc.w = fmaf(w, y.w, acc.w);
+          const int U = ring_rows(p.I, false);
+          const int M = local_units((p.H + U - 1) / U);
+          const int per_t = M * U;
+          const int items = p.T * per_t;
+          for (int it = tid; it < items; it += kConsumerWarps * 32) {
+            const int t = it / per_t, rest = it - t * per_t;
+            const int m = rest / U;
+            const int row = ((int)blockIdx.x + m * (int)gridDim.x) * U + (rest - m * U);
+            if (row < p.H) {
+              float acc = 0.0f;
+              for (int jj = 0; jj < p.k; ++jj)
+                acc = fmaf(p.combine_w[t * p.k + jj], __ldcg(p.y + (size_t)(t * p.k + jj) * p.H + row), acc);
+              p.combine_out[(size_t)t * p.H + row] = __float2bfloat16_rn(acc);
             }
-            __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-            __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-            uint2 packed;
-            packed.x = *reinterpret_cast<uint32_t*>(&lo);
-            packed.y = *reinterpret_cast<uint32_t*>(&hi);
-            reinterpret_cast<uint2*>(p.combine_out + (size_t)t * p.H)[c4] = packed;
           }
         }
       }
