@@ -100,6 +100,58 @@ __device__ inline bool grid_barrier(unsigned int* count, volatile int* abort_fla
 constexpr int kBarConsumers = 1;
 constexpr int kBarStream = 2;      // warp 0 -> producer warp: the weight sources are known
 
+// Logits of this CTA's R router rows (rows b, b + G, ...) for the T <= TT
+// token rows: every thread takes the float4 columns tid, tid + blockDim, ...
+// of all R x T dot products, then warp sums and a sum over the warps.  R and
+// TT are compile-time so the loop body carries no per-row or per-token branch.
+template <int R, int TT>
+__device__ inline void router_rows(const DecodeParams& d, const float* wrow, const __nv_bfloat16* xs, DecodeShared& sh,
+                                   int b, int G) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int H = d.g.H, T = d.g.T, E = d.g.E;
+  float acc[R][TT];
+#pragma unroll
+  for (int i = 0; i < R; ++i)
+#pragma unroll
+    for (int t = 0; t < TT; ++t) acc[i][t] = 0.0f;
+  const int H4 = H >> 2;
+  for (int q = tid; q < H4; q += blockDim.x) {
+    float4 xv[TT];
+#pragma unroll
+    for (int t = 0; t < TT; ++t) {
+      const uint2 u = (TT == 1 || t < T) ? reinterpret_cast<const uint2*>(xs + (size_t)t * H)[q] : make_uint2(0u, 0u);
+      xv[t] = make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
+    }
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      const float4 w = reinterpret_cast<const float4*>(wrow + (size_t)i * H)[q];
+#pragma unroll
+      for (int t = 0; t < TT; ++t) {
+        float a = acc[i][t];
+        a = fmaf(w.x, xv[t].x, a);
+        a = fmaf(w.y, xv[t].y, a);
+        a = fmaf(w.z, xv[t].z, a);
+        a = fmaf(w.w, xv[t].w, a);
+        acc[i][t] = a;
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < R; ++i)
+#pragma unroll
+    for (int t = 0; t < TT; ++t) {
+      const float s = warp_sum(acc[i][t]);
+      if (lane == 0) sh.red[warp][i][t] = s;
+    }
+  __syncthreads();
+  if (tid < R * T) {
+    const int i = tid / T, t = tid - (tid / T) * T;
+    float s = 0.0f;
+    for (int w = 0; w < kRingThreads / 32; ++w) s += sh.red[w][i][t];
+    d.logits[(size_t)t * E + b + i * G] = s + sh.bias[i];
+  }
+}
+
 template <int NT, int VA, int VB>
 __global__ void __launch_bounds__(kRingThreads, 1)
 decode_layer_kernel(DecodeParams d, unsigned int* grid_count) {
@@ -159,54 +211,11 @@ decode_layer_kernel(DecodeParams d, unsigned int* grid_count) {
   if (!bounded_wait(&sh.rbar, 0u, &sh.r.abort)) sh.r.abort = 1;
   __syncthreads();
   if (n_my > 0 && !sh.r.abort) {
-    float acc[kDecMaxRows][kDecMaxT];
-#pragma unroll
-    for (int i = 0; i < kDecMaxRows; ++i)
-#pragma unroll
-      for (int t = 0; t < kDecMaxT; ++t) acc[i][t] = 0.0f;
-    const int H4 = H >> 2;
-    for (int q = tid; q < H4; q += blockDim.x) {
-      float4 xv[kDecMaxT];
-#pragma unroll
-      for (int t = 0; t < kDecMaxT; ++t) {
-        if (t < T) {
-          const uint2 u = reinterpret_cast<const uint2*>(xs + (size_t)t * H)[q];
-          xv[t] = make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < kDecMaxRows; ++i) {
-        if (i < n_my) {
-          const float4 w = reinterpret_cast<const float4*>(wrow + (size_t)i * H)[q];
-#pragma unroll
-          for (int t = 0; t < kDecMaxT; ++t) {
-            if (t < T) {
-              float a = acc[i][t];
-              a = fmaf(w.x, xv[t].x, a);
-              a = fmaf(w.y, xv[t].y, a);
-              a = fmaf(w.z, xv[t].z, a);
-              a = fmaf(w.w, xv[t].w, a);
-              acc[i][t] = a;
-            }
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < kDecMaxRows; ++i)
-#pragma unroll
-      for (int t = 0; t < kDecMaxT; ++t) {
-        if (i < n_my && t < T) {
-          const float s = warp_sum(acc[i][t]);
-          if (lane == 0) sh.red[warp][i][t] = s;
-        }
-      }
-    __syncthreads();
-    if (tid < n_my * T) {
-      const int i = tid / T, t = tid - (tid / T) * T;
-      float s = 0.0f;
-      for (int w = 0; w < kRingThreads / 32; ++w) s += sh.red[w][i][t];
-      d.logits[(size_t)t * E + b + i * G] = s + sh.bias[i];
+    switch (n_my) {
+      case 1: router_rows<1, NT>(d, wrow, xs, sh, b, G); break;
+      case 2: router_rows<2, NT>(d, wrow, xs, sh, b, G); break;
+      case 3: router_rows<3, NT>(d, wrow, xs, sh, b, G); break;
+      default: router_rows<4, NT>(d, wrow, xs, sh, b, G); break;
     }
   }
   // ---------------------------------------------------------------- route, residency
