@@ -76,20 +76,26 @@ struct __align__(16) DecodeShared {
   int n_inst;
 };
 
+// Bounded grid-wide barrier: the CTA barrier orders every thread's stores
+// before thread 0's release arrival (release is cumulative), and thread 0's
+// acquire poll orders the other CTAs' stores before the closing CTA barrier.
 __device__ inline bool grid_barrier(unsigned int* count, volatile int* abort_flag) {
-  __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
-    atomicAdd(count, 1u);
-    const unsigned long long t0 = gtimer();
-    while (*reinterpret_cast<volatile unsigned int*>(count) < gridDim.x) {
-      if (*abort_flag) break;
-      if (gtimer() - t0 > kGridWaitNs) {
-        *abort_flag = 1;
-        break;
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(count) : "memory");
+    unsigned long long t0 = 0;
+    for (uint32_t it = 0; ld_acquire_u32(count) < gridDim.x; ++it) {
+      if ((it & 15) == 15) {
+        if (*abort_flag) break;
+        const unsigned long long now = gtimer();
+        if (t0 == 0) {
+          t0 = now;
+        } else if (now - t0 > kGridWaitNs) {
+          *abort_flag = 1;
+          break;
+        }
       }
     }
-    __threadfence();
   }
   __syncthreads();
   return !*abort_flag;

@@ -100,9 +100,10 @@ __device__ inline FrontLane front_route(const float* logits, int T, int k, int E
   const bool row = lane < R;
   d.ids[lane] = row ? my_id : -1;
   d.w[lane] = row ? my_w : 0.0f;
-  // 2. dispatch: bitonic sort of (expert, row) keys across the warp
+  // 2. dispatch: bitonic sort of (expert, row) keys across the warp (one
+  // token's ids already come in ascending order, distinct: nothing to sort)
   int key = row ? (my_id << 5) | lane : 0x7fffffff;
-  for (int size = 2; size <= 32; size <<= 1) {
+  for (int size = 2; T > 1 && size <= 32; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
       const int other = __shfl_xor_sync(0xffffffffu, key, stride);
       const bool up = (lane & size) == 0;
