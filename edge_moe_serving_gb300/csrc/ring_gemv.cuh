@@ -270,12 +270,17 @@ struct UnitWorker {
     cur_j = j;
     if (!GATEUP && p.inst_done != nullptr) {
       if (lane == 0) {
-        const unsigned long long t0 = gtimer();
-        while (ld_acquire_u32(p.inst_done + j) < need) {
-          if (*abort_flag) break;
-          if (gtimer() - t0 > kGridWaitNs) {
-            *abort_flag = 1;
-            break;
+        unsigned long long t0 = 0;
+        for (uint32_t it = 0; ld_acquire_u32(p.inst_done + j) < need; ++it) {
+          if ((it & 15) == 15) {
+            if (*abort_flag) break;
+            const unsigned long long now = gtimer();
+            if (t0 == 0) {
+              t0 = now;
+            } else if (now - t0 > kGridWaitNs) {
+              *abort_flag = 1;
+              break;
+            }
           }
         }
       }
@@ -483,17 +488,16 @@ __device__ inline void ring_phase(const GemvParams& p, const Insts& v, int* s_cn
       // Publish the instance once this CTA's units of it are all done: each
       // warp counts its unit with a CTA-scope acquire-release add (ordering
       // its lanes' h stores, which __syncwarp made visible to lane 0); the
-      // warp that completes the count fences at GPU scope, which carries every
-      // counted warp's stores, and raises the instance's counter.
+      // warp that completes the count raises the instance's counter with a
+      // GPU-scope release add, which (release being cumulative) carries every
+      // counted warp's stores.
       __syncwarp();
       if (lane == 0) {
         const int lo = j * upi, hi = lo + upi;
         const int first = lo + (((int)blockIdx.x - lo) % G + G) % G;   // first u >= lo with u % G == block
         const int mine = first < hi ? (hi - 1 - first) / G + 1 : 0;
-        if (atom_add_acq_rel_cta(&s_cnt[j], 1) + 1 == mine) {
-          __threadfence();
-          atomicAdd(p.inst_done + j, 1u);
-        }
+        if (atom_add_acq_rel_cta(&s_cnt[j], 1) + 1 == mine)
+          asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p.inst_done + j) : "memory");
       }
     }
     __syncwarp();

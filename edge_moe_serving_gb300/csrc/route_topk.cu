@@ -4,8 +4,10 @@
 // Two kernels, chosen by T:
 //  * T <= 32 (decode): one CTA per expert streams that expert's fp32 router
 //    row once and dots it with every token (the router weights are the only
-//    bytes of the step besides the experts).  The last CTA to finish (ticket
-//    counter) runs the top-k for all tokens.
+//    bytes of the step besides the experts).  Up to 4 tokens the last CTA to
+//    finish (ticket counter) runs the top-k for all tokens; 5..32 tokens take
+//    one pass with a per-token partial sum in every thread, then one warp per
+//    token selects.
 //  * T > 32 (prefill): the tensor-core router of route_tc.cu when H is a
 //    multiple of 64; otherwise a register-blocked fp32 SIMT GEMM where a CTA
 //    owns 32 tokens x all E experts, so the top-k runs in its epilogue from
@@ -90,6 +92,61 @@ route_small_kernel(const __nv_bfloat16* __restrict__ x, int T, int H,
     __syncwarp();
   }
   if (tid == 0) *ticket = 0u;  // ready for the next call
+}
+
+// 4 < T <= 32 tokens, logits only: one CTA per expert streams its fp32 router
+// row once, and every thread keeps one partial sum per token.  A butterfly
+// across the warp transposes and reduces the 32 partial sums in 31 shuffles
+// (lane t ends with token t's warp sum); the warps' sums add up in shared
+// memory.  One pass over the row for all tokens.
+__global__ void __launch_bounds__(kSmallThreads)
+route_wide_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, const float* __restrict__ w_router,
+                  const float* __restrict__ bias, int E, float* __restrict__ logits) {
+  __shared__ float red[kSmallThreads / 32][32];
+  pdl_wait();
+  pdl_trigger();
+  const int e = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float4* wrow = reinterpret_cast<const float4*>(w_router + (size_t)e * H);
+  const int H4 = H >> 2;
+  float acc[32];
+#pragma unroll
+  for (int t = 0; t < 32; ++t) acc[t] = 0.0f;
+  for (int h4 = tid; h4 < H4; h4 += kSmallThreads) {
+    const float4 w = __ldg(wrow + h4);
+#pragma unroll
+    for (int t = 0; t < 32; ++t) {
+      if (t < T) {
+        const uint2 xv = __ldg(reinterpret_cast<const uint2*>(x + (size_t)t * H) + h4);
+        float a = acc[t];
+        a = fmaf(w.x, bf16_lo(xv.x), a);
+        a = fmaf(w.y, bf16_hi(xv.x), a);
+        a = fmaf(w.z, bf16_lo(xv.y), a);
+        a = fmaf(w.w, bf16_hi(xv.y), a);
+        acc[t] = a;
+      }
+    }
+  }
+  // at offset o the lanes whose bit o is set keep the upper half of the 2o live sums
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < o; ++i) {
+      const float send = upper ? acc[i] : acc[i + o];
+      const float keep = upper ? acc[i + o] : acc[i];
+      acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  red[warp][lane] = acc[0];
+  __syncthreads();
+  if (tid < T) {
+    float s = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kSmallThreads / 32; ++w) s += red[w][tid];
+    if (bias) s += bias[e];
+    logits[(size_t)tid * E + e] = s;
+  }
 }
 
 // ---------------------------------------------------------------- prefill path
@@ -218,8 +275,7 @@ cudaError_t launch_route_topk(const __nv_bfloat16* x, int T, int H, const float*
       return launch_k(route_small_kernel<4, true>, E, kSmallThreads, 0, s, x, T, H, w_router, bias, E, k, logits,
                       ticket, topk_ids, topk_w);
     // more tokens: logits only, then one warp per token selects
-    err = launch_k(route_small_kernel<8, false>, E, kSmallThreads, 0, s, x, T, H, w_router, bias, E, k, logits,
-                   (unsigned int*)nullptr, (int32_t*)nullptr, (float*)nullptr);
+    err = launch_k(route_wide_kernel, E, kSmallThreads, 0, s, x, T, H, w_router, bias, E, logits);
     if (err != cudaSuccess) return err;
     return launch_topk(logits, nullptr, T, E, k, false, topk_ids, topk_w, s);
   }
@@ -247,8 +303,7 @@ cudaError_t launch_route_logits(const __nv_bfloat16* x, int T, int H, const floa
   if (T <= 4)
     return launch_k(route_small_kernel<4, false>, E, kSmallThreads, 0, s, x, T, H, w_router, bias, E, 1, logits,
                     (unsigned int*)nullptr, (int32_t*)nullptr, (float*)nullptr);
-  return launch_k(route_small_kernel<8, false>, E, kSmallThreads, 0, s, x, T, H, w_router, bias, E, 1, logits,
-                  (unsigned int*)nullptr, (int32_t*)nullptr, (float*)nullptr);
+  return launch_k(route_wide_kernel, E, kSmallThreads, 0, s, x, T, H, w_router, bias, E, logits);
 }
 
 }  // namespace moe

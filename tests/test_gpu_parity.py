@@ -87,7 +87,7 @@ def test_route_topk_small_shapes_and_ties():
         assert np.array_equal(ids.cpu().numpy()[ok], ref_ids[ok]), (T, H, E)
         assert np.abs(w.cpu().numpy()[ok] - ref_w[ok]).max() < 1e-5, (T, H, E)
     # ties: zero router weights -> every logit equal -> ids 0..k-1, weights 1/k
-    for T, H in ((1, 16), (40, 16), (40, 64), (257, 128)):
+    for T, H in ((1, 16), (3, 16), (20, 16), (32, 32), (40, 16), (40, 64), (257, 128)):
         x = to_dev_bf16(np.zeros((T, H), np.uint16), DEV)
         wr = torch.zeros((10, H), dtype=torch.float32, device=DEV)
         ids = torch.empty((T, 3), dtype=torch.int32, device=DEV)
