@@ -299,7 +299,7 @@ cudaError_t launch_one(const DecodeParams& d, unsigned int* grid_count, int grid
   cfg.dynamicSmemBytes = kRingSmem;
   cfg.stream = s;
   cudaLaunchAttribute attrs[1];
-  attrs[0].id = cudaLaunchAttributeCooperative;   // all CTAs resident: the grid barriers can complete
+  attrs[0].id = cudaLaunchAttributeCooperative;   // all CTAs resident: the grid barrier and the cross-CTA waits can complete
   attrs[0].val.cooperative = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
