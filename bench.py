@@ -481,6 +481,27 @@ def run_reference(args, rank, world):
             "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_bw_profile(args):
+    """moe_bench_bandwidth on one expert of the workload's shape (3*H*I bf16
+    bytes) in pinned host memory: B_P = copy engine into HBM, B_H = the SMs
+    reading it in place over NVLink-C2C, both alone and contended, and the
+    derived phi (the phi_q16 argument of the split)."""
+    import torch
+    import edge_moe_serving_gb300 as moe
+    cfg = CONFIGS[args.workload]
+    nbytes = 3 * cfg.H * cfg.I * 2
+    host = torch.empty(nbytes // 4, dtype=torch.int32).pin_memory()
+    host.random_(-2 ** 31, 2 ** 31 - 1)
+    dev = torch.empty(nbytes // 4, dtype=torch.int32, device="cuda")
+    iters = max(args.steps, 3)
+    prof = moe.moe_bench_bandwidth(host, dev, nbytes, iters, torch.cuda.Stream(), torch.cuda.Stream())
+    out = {f: getattr(prof, f) for f, _ in moe.moe_bw_profile._fields_ if f != "read_checksum"}
+    out = {k: (round(v, 4) if isinstance(v, float) else v) for k, v in out.items()}
+    return {"metric": "bandwidth profile of the q* split", "workload": cfg.name, "bytes_per_copy": nbytes,
+            "iters": iters, "unit": "GB/s", **out,
+            "note": "B_P: cudaMemcpyAsync pinned host -> HBM; B_H: SMs reading the pinned host buffer in place"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -493,9 +514,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ffn-mode", default="auto", choices=sorted(FFN_MODES),
                     help="expert-FFN kernel choice passed to moe_layer_forward (default: auto)")
+    ap.add_argument("--bw-profile", action="store_true",
+                    help="print the bandwidth profile of the q* split (B_P, B_H, contended pair, phi) instead")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.bw_profile:
+        print(json.dumps(run_bw_profile(args)))
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":

@@ -10,7 +10,7 @@ package fails loudly when the library is missing.
 import ctypes
 import os
 
-from ctypes import c_int, c_int32, c_uint32, c_uint64, c_ulonglong, c_size_t, c_void_p, c_char_p, POINTER
+from ctypes import c_double, c_int, c_int32, c_uint32, c_uint64, c_ulonglong, c_size_t, c_void_p, c_char_p, POINTER
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe.so")
@@ -48,6 +48,13 @@ class moe_layer_buffers(ctypes.Structure):
                 ("perm", c_void_p), ("inv_perm", c_void_p), ("y_rows", c_void_p)]
 
 
+class moe_bw_profile(ctypes.Structure):
+    _fields_ = [("b_p_gbs", c_double), ("b_h_gbs", c_double), ("b_p_contended_gbs", c_double),
+                ("b_h_contended_gbs", c_double), ("phi", c_double), ("phi_contended", c_double),
+                ("phi_q16", c_uint32), ("phi_contended_q16", c_uint32), ("hybrid_ok", c_int32),
+                ("read_checksum", c_uint32)]
+
+
 BIND_STATS_FIELDS = [f for f, _ in moe_bind_stats._fields_]
 
 
@@ -68,6 +75,9 @@ def _load():
         "moe_status_string": (c_char_p, [c_int]),
         "moe_check_bounded_wait": (c_int, [P, P]),
         "moe_kernel_launch_count": (c_ulonglong, []),
+        "moe_phi_to_q16": (c_uint32, [c_double]),
+        "moe_bw_derive": (c_int, [POINTER(moe_bw_profile)]),
+        "moe_bench_bandwidth": (c_int, [P, P, c_size_t, c_int, POINTER(moe_bw_profile), P, P]),
         "moe_route_topk_workspace_size": (c_size_t, [c_int, c_int, c_int]),
         "moe_route_topk": (c_int, [P, c_int, c_int, P, P, c_int, c_int, P, P, P, P, c_size_t, P, P]),
         "moe_dispatch_workspace_size": (c_size_t, [c_int, c_int, c_int]),
@@ -94,7 +104,8 @@ def _load():
 
 
 _lib = _load()
-EXPORTED = ["moe_version", "moe_status_string", "moe_check_bounded_wait", "moe_kernel_launch_count", "moe_route_topk_workspace_size",
+EXPORTED = ["moe_version", "moe_status_string", "moe_check_bounded_wait", "moe_kernel_launch_count",
+            "moe_phi_to_q16", "moe_bw_derive", "moe_bench_bandwidth", "moe_route_topk_workspace_size",
             "moe_route_topk",
             "moe_dispatch_workspace_size", "moe_dispatch", "moe_cache_bind_workspace_size",
             "moe_cache_bind_slots", "moe_expert_ffn_workspace_size", "moe_expert_ffn_grouped",
@@ -143,6 +154,25 @@ def moe_check_bounded_wait(dev_status, stream=None):
 
 def moe_kernel_launch_count():
     return int(_lib.moe_kernel_launch_count())
+
+
+def moe_phi_to_q16(phi):
+    return int(_lib.moe_phi_to_q16(float(phi)))
+
+
+def moe_bw_derive(b_p_gbs, b_h_gbs, b_p_contended_gbs=0.0, b_h_contended_gbs=0.0):
+    """moe_bw_derive on a profile holding the four rates; returns the profile."""
+    prof = moe_bw_profile(b_p_gbs, b_h_gbs, b_p_contended_gbs, b_h_contended_gbs)
+    _check("moe_bw_derive", _lib.moe_bw_derive(ctypes.byref(prof)))
+    return prof
+
+
+def moe_bench_bandwidth(host_src, dev_dst, nbytes, iters, copy_stream, read_stream):
+    """host_src: pinned host tensor (or address); returns the measured profile."""
+    prof = moe_bw_profile()
+    _check("moe_bench_bandwidth", _lib.moe_bench_bandwidth(
+        _p(host_src), _p(dev_dst), nbytes, iters, ctypes.byref(prof), _s(copy_stream), _s(read_stream)))
+    return prof
 
 
 def moe_route_topk_workspace_size(T, H, E):

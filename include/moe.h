@@ -158,6 +158,61 @@ int moe_check_bounded_wait(uint32_t* dev_status, moe_stream_t stream);
  * a graph capture is the number of kernels one replay runs. */
 unsigned long long moe_kernel_launch_count(void);
 
+/* ---------------------------------------------------------------- bandwidth profile
+ * The two measured bandwidths the q* split is made from ([P] section 3.2,
+ * Eq. 3-4: q* = m * B_P / B_H; [P] Table 1 measures them per machine on the
+ * deployed tensor shapes, because the ratio cannot be read from
+ * specification sheets), the contended pair (the write-up "FreeToken:
+ * bandwidth-adaptive edge MoE serving", section "The split, and what it is
+ * actually optimising": the preferred fetch fraction comes from measuring
+ * both sides while they contend) and the hybrid gate B_H > 2 B_P (same
+ * write-up, section "When to use it (and when not)").
+ *
+ * On GB300 the source-of-truth expert pool would sit in Grace memory behind
+ * NVLink-C2C, and the C branch runs on the GPU rather than on host cores:
+ * B_P is the copy engine moving expert bytes from pinned host memory into
+ * HBM (the fill path F), B_H the SMs reading that host memory in place (the
+ * in-place path C).  Rates are in GB/s (1e9 bytes per second). */
+typedef struct moe_bw_profile {
+  double b_p_gbs;            /* copy engine, pinned host -> device, running alone */
+  double b_h_gbs;            /* SMs reading the pinned host buffer in place, running alone */
+  double b_p_contended_gbs;  /* the copy while the in-place read runs */
+  double b_h_contended_gbs;  /* the in-place read while the copy runs */
+  double phi;                /* B_P / B_H (Eq. 4); 1 when B_H is 0 and B_P > 0 (no in-place path: every miss
+                                fills), 0 when both are 0 */
+  double phi_contended;      /* B_Pc / (B_Pc + B_Hc): the copy's share of the contended total, which is
+                                B_P / B_H when the two share the host bandwidth fully (B_Hc = B_H - B_P) */
+  uint32_t phi_q16;          /* moe_phi_to_q16(phi): the phi_q16 argument of the bind and layer calls */
+  uint32_t phi_contended_q16;
+  int32_t hybrid_ok;         /* 1 when B_H > 2 B_P (the split is worth running), else 0 */
+  uint32_t read_checksum;    /* moe_bench_bandwidth: XOR of every 32-bit word the in-place read saw */
+} moe_bw_profile;
+
+/* phi as the split's Q16 argument: round-half-even(phi * 65536), clamped to
+ * [0, 65536]; 0 for NaN or phi <= 0.  Host arithmetic, no GPU needed. */
+uint32_t moe_phi_to_q16(double phi);
+
+/* Fills phi, phi_contended, both Q16 forms and hybrid_ok of *prof from its
+ * four rates (host arithmetic, no GPU needed).  MOE_ERR_INVALID_ARG when prof
+ * is NULL or a rate is negative or not finite. */
+int moe_bw_derive(moe_bw_profile* prof);
+
+/* Measures the four rates, then moe_bw_derive.  host_src: `bytes` of pinned
+ * (page-locked) host memory that the device can address (cudaHostAlloc or
+ * cudaHostRegister; an expert-sized buffer is the deployed shape), owned by
+ * the caller; dev_dst: `bytes` of device memory, overwritten.  Each rate
+ * moves `iters` x `bytes` after one untimed pass; the contended pair runs the
+ * copies on copy_stream and the in-place reads on read_stream at once, with
+ * the read count scaled so that both take about as long.  bytes a positive
+ * multiple of 16 and both pointers 16-byte aligned, iters >= 1, the two
+ * streams distinct; else MOE_ERR_INVALID_ARG (also when the device cannot
+ * address host_src).  A profiling call, not for stream capture: it
+ * synchronises both streams and keeps its checksum word in a static device
+ * variable, so concurrent calls race.  MOE_ERR_CUDA on a launch or copy
+ * error. */
+int moe_bench_bandwidth(const void* host_src, void* dev_dst, size_t bytes, int iters, moe_bw_profile* out,
+                        moe_stream_t copy_stream, moe_stream_t read_stream);
+
 /* ---------------------------------------------------------------- router
  * Router scoring and top-k with renormalisation ([P] section 3.2: at each
  * MoE layer the router runs on the GPU and selects the active experts).

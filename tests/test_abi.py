@@ -33,6 +33,7 @@ def test_struct_layouts_match_header():
     assert ctypes.sizeof(moe.moe_layer) == 40
     assert ctypes.sizeof(moe.moe_layer_buffers) == 56
     assert ctypes.sizeof(moe.moe_cache) == 2 * 32 + 4 * 8 + 16
+    assert ctypes.sizeof(moe.moe_bw_profile) == 6 * 8 + 4 * 4
 
 
 def test_status_strings_and_version():
