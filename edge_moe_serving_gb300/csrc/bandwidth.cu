@@ -31,6 +31,7 @@ __device__ inline uint32_t xor4(const uint4& v) { return v.x ^ v.y ^ v.z ^ v.w; 
 // thread reaches the warp reduction (the loops are per thread).
 __global__ void __launch_bounds__(kReadThreads) host_read_kernel(const uint4* __restrict__ src, size_t n16,
                                                                  uint32_t* sink) {
+  pdl_wait();
   const size_t stride = (size_t)gridDim.x * blockDim.x;
   size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   uint32_t acc = 0;
