@@ -67,6 +67,7 @@ def test_route_topk_small_shapes_and_ties():
     # (T > 32, H % 64 == 0) runs on the tensor cores: ragged expert tiles
     # (E = 100, 130), ragged token tiles (T = 200, 129, 300), E = 512, tiny E.
     for T, H, E, k in ((1, 8, 3, 1), (5, 24, 33, 4), (33, 64, 100, 7), (70, 40, 512, 16), (31, 16, 64, 16),
+                       (32, 128, 512, 16), (17, 64, 256, 8),
                        (200, 128, 130, 6), (129, 192, 512, 16), (300, 64, 8, 2)):
         xb = gen.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
         wr = (rng.standard_normal((E, H)) * 0.1).astype(np.float32)
@@ -452,6 +453,42 @@ def test_layer_one_launch_multi_token(base, T, mode):
             assert got["stats"][kk] == v, (step, kk)
         assert_close(bf16_to_f64(got["out"]), ref["out"], what=f"{cfg.name} step {step}")
         assert_close(got["y_rows"].cpu().numpy(), token_major(ref), what=f"{cfg.name} step {step} y_rows")
+
+
+def test_layer_one_launch_max_shape():
+    """The one-launch decode layer at its limits: 512 experts (four router rows
+    per CTA), top-8 of 4 tokens (32 routed rows, instances of 4 rows), 1024
+    cache slots shared by 3 layers (the largest state copy, a full 32-word
+    hitmap, victims scanned 32 slots per lane), pure fill: ids, residency
+    state and stats bit-exact over a trace with fills, outputs within
+    tolerance."""
+    from moe_inputs.configs import LayerConfig, Q16
+    cfg = LayerConfig("decode_max", T=4, H=256, E=512, k=8, I=512, seed=41, n_layers=3, steps=6,
+                      cache_slots=1024, phi_q16=Q16, bias="zipf")
+    dc = DeviceCache(cfg, DEV)
+    dl = DeviceLayer(cfg, 0, DEV)
+    wc = ExpertCache(cfg, cap=64)
+    ref_state = gen.initial_cache(cfg)
+    fills = 0
+    for step in range(cfg.steps):
+        dl.set_bias(step)
+        seed = 700 + step
+        xb = _gap_safe_x_bits(cfg, step)
+        got = run_layer(dc, dl, to_dev_bf16(xb, DEV), cfg.T, cfg.phi_q16, cfg.min_fill, cfg.fill_policy, seed,
+                        ffn_mode=moe.MOE_FFN_GEMV)   # GEMV mode: no gathered rows, the one-launch path
+        assert got["status"] == 0
+        ref = oracle_layer(cfg, 0, step, wc, x_bits=xb)
+        assert np.array_equal(got["topk_ids"].cpu().numpy().reshape(cfg.T, cfg.k), ref["ids"]), step
+        assert np.array_equal(got["perm"].cpu().numpy(), ref["perm"]), step
+        ref_state, res = O.bind(ref_state, 0, ref["ids"], cfg.E, cfg.phi_q16, cfg.min_fill, cfg.fill_policy, seed)
+        st = dc.state()
+        for key in ("table", "owner", "stamp"):
+            assert np.array_equal(st[key], np.asarray(ref_state[key])), (step, key)
+        for kk, v in res["stats"].items():
+            assert got["stats"][kk] == v, (step, kk)
+        fills += res["stats"]["n_fill"]
+        assert_close(bf16_to_f64(got["out"]), ref["out"], what=f"{cfg.name} step {step}")
+    assert fills > 0
 
 
 def test_layer_decode_trace():
