@@ -48,7 +48,7 @@ __device__ inline int block_exclusive_scan(int v, int* warp_tot, int* total) {
 // position of expert e; wcnt is a zeroed [32][E] table (left zeroed on exit).
 __device__ inline void scatter_tile(const int32_t* __restrict__ ids, int R, int E, int base, int* cursor,
                              int* wcnt, int32_t* __restrict__ perm, int32_t* __restrict__ inv_perm) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int i = base + tid;
   const int e = (i < R) ? ids[i] : -1;
   const bool valid = (e >= 0 && e < E);
