@@ -331,7 +331,17 @@ int moe_combine(const float* y_rows, const float* topk_w, int T, int k, int H, v
  * moe_expert_ffn_grouped -> moe_combine on one stream ([P] section 3.2 decode
  * order: cache update, batch copy of F, grouped evaluation, merge).
  * out bf16 [T, H].  bufs_opt may name caller buffers for intermediates.
- * stats_dev: moe_bind_stats or NULL. */
+ * stats_dev: moe_bind_stats or NULL.
+ * How it runs (the results are those of the five calls in every case):
+ * decode-sized calls (T <= 8, T*k <= 32, E <= 512, at most 1024 cache slots,
+ * the fused GEMV's shapes, ffn_mode GEMV or AUTO with T <= 2) run as ONE
+ * cooperative launch (router, selection, residency decision and commit,
+ * fused FFN with the fills streamed into their slots, combine); other calls
+ * of at most 32 routed rows use a one-warp front end and one fused FFN launch;
+ * larger calls run the per-step launches, the FFN on the tensor-core GEMM
+ * under AUTO when T > 2.  The fused launches are cooperative (one CTA per
+ * SM, all resident together), so they start only once every SM can take one
+ * of their CTAs. */
 size_t moe_layer_workspace_size(const moe_layer* layer, const moe_cache* cache, int T,
                                 int ffn_mode);
 int moe_layer_forward(const moe_layer* layer, const moe_cache* cache, const void* x, int T,
