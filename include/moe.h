@@ -23,7 +23,8 @@
  *             multiples of 8.
  * Async.      Every call only enqueues work on `stream` (a cudaStream_t) and
  *             returns; no call synchronises with the host, so a sequence of
- *             calls may be captured into a CUDA graph.
+ *             calls may be captured into a CUDA graph.  The one exception is
+ *             the profiling call moe_bench_bandwidth.
  * Errors.     The return value is a host status (MOE_OK or MOE_ERR_*), from
  *             argument checks before any launch or from the launch itself.
  *             Errors found on the device (bad expert id, unbound slot, a
