@@ -491,6 +491,41 @@ def test_layer_one_launch_max_shape():
     assert fills > 0
 
 
+@pytest.mark.parametrize("T,n_layers,slots,mode", [(16, 1, None, moe.MOE_FFN_GEMV), (1, 256, 1536, moe.MOE_FFN_AUTO),
+                                                   (3, 256, 1536, moe.MOE_FFN_GEMV)])
+def test_layer_front_small_fused_combine(T, n_layers, slots, mode):
+    """Calls the one-launch kernel does not take (16 tokens; or a pool of more
+    than 1024 slots) but with at most 32 routed rows: the one-warp front end,
+    then the fused GEMV launch whose CTAs combine their own output rows.  ids,
+    residency state and stats bit-exact over a trace, outputs within
+    tolerance."""
+    from moe_inputs.configs import Q16
+    cfg = dataclasses.replace(CONFIGS["tiny"], name=f"front_t{T}_s{slots}", T=T, n_layers=n_layers, steps=4,
+                              cache_slots=slots, phi_q16=Q16 if slots else 0, bias="zipf")
+    assert cfg.T * cfg.k <= 32
+    dc = DeviceCache(cfg, DEV)
+    dl = DeviceLayer(cfg, 0, DEV)
+    wc = ExpertCache(cfg, cap=16)
+    ref_state = gen.initial_cache(cfg)
+    for step in range(cfg.steps):
+        dl.set_bias(step)
+        seed = 900 + step
+        xb = _gap_safe_x_bits(cfg, step)
+        got = run_layer(dc, dl, to_dev_bf16(xb, DEV), cfg.T, cfg.phi_q16, cfg.min_fill, cfg.fill_policy, seed,
+                        ffn_mode=mode)
+        assert got["status"] == 0
+        ref = oracle_layer(cfg, 0, step, wc, x_bits=xb)
+        assert np.array_equal(got["topk_ids"].cpu().numpy().reshape(cfg.T, cfg.k), ref["ids"]), step
+        assert np.array_equal(got["perm"].cpu().numpy(), ref["perm"]), step
+        ref_state, res = O.bind(ref_state, 0, ref["ids"], cfg.E, cfg.phi_q16, cfg.min_fill, cfg.fill_policy, seed)
+        st = dc.state()
+        for key in ("table", "owner", "stamp"):
+            assert np.array_equal(st[key], np.asarray(ref_state[key])), (step, key)
+        for kk, v in res["stats"].items():
+            assert got["stats"][kk] == v, (step, kk)
+        assert_close(bf16_to_f64(got["out"]), ref["out"], what=f"{cfg.name} step {step}")
+
+
 def test_layer_decode_trace():
     _decode_trace("decode", set(range(32)))
 
