@@ -100,7 +100,9 @@ extern "C" int moe_bw_derive(moe_bw_profile* prof) {
 extern "C" int moe_bench_bandwidth(const void* host_src, void* dev_dst, size_t bytes, int iters, moe_bw_profile* out,
                                    moe_stream_t copy_stream, moe_stream_t read_stream) {
   using namespace moe;
-  if (!host_src || !dev_dst || !out || iters < 1 || bytes == 0 || (bytes & 15) != 0 || copy_stream == read_stream)
+  // two distinct created streams: the legacy default stream (NULL) would serialise the contended pair
+  if (!host_src || !dev_dst || !out || iters < 1 || bytes == 0 || (bytes & 15) != 0 || copy_stream == read_stream ||
+      !copy_stream || !read_stream)
     return MOE_ERR_INVALID_ARG;
   if (((reinterpret_cast<uintptr_t>(host_src) | reinterpret_cast<uintptr_t>(dev_dst)) & 15) != 0)
     return MOE_ERR_INVALID_ARG;

@@ -206,8 +206,9 @@ int moe_bw_derive(moe_bw_profile* prof);
  * copies on copy_stream and the in-place reads on read_stream at once, with
  * the read count scaled so that both take about as long.  bytes a positive
  * multiple of 16 and both pointers 16-byte aligned, iters >= 1, the two
- * streams distinct; else MOE_ERR_INVALID_ARG (also when the device cannot
- * address host_src).  A profiling call, not for stream capture: it
+ * streams distinct and both created streams (not the legacy default stream,
+ * which would serialise the contended pair); else MOE_ERR_INVALID_ARG (also
+ * when the device cannot address host_src).  A profiling call, not for stream capture: it
  * synchronises both streams and keeps its checksum word in a static device
  * variable, so concurrent calls race.  MOE_ERR_CUDA on a launch or copy
  * error. */

@@ -82,7 +82,8 @@ def test_bench_bandwidth_rejects_bad_arguments_before_any_cuda_call():
            (4096, 4096, 0, 2, 1, 2),             # empty
            (4096, 4096, 1 << 20, 0, 1, 2),       # no repetition
            (4096, 4096, 1 << 20, 2, 3, 3),       # one stream for both sides
-           (4104, 4096, 1 << 20, 2, 1, 2)]       # host buffer not 16-byte aligned
+           (4104, 4096, 1 << 20, 2, 1, 2),      # host buffer not 16-byte aligned
+           (4096, 4096, 1 << 20, 2, 0, 2)]       # the legacy default stream
     for args in bad:
         with pytest.raises(moe.MoeError) as e:
             moe.moe_bench_bandwidth(*args)
