@@ -215,6 +215,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_b64, const __grid_constant__
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
+      // Thin calls (every group in one chunk of <= 32 rows) read each weight tile
+      // once: load it evict-first so it does not push out the reused token
+      // tiles or force write-backs of other lines.  Larger groups span several
+      // chunks whose CTAs share the weight tiles through L2 (measured: the
+      // hint slows prefill down), so they load with the default policy.
+      const uint64_t wpol = l2_evict_first();
       bool armed[kStages] = {};
       uint32_t armed_parity[kStages] = {};
       for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
@@ -235,8 +241,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_b64, const __grid_constant__
           mbar_expect_tx(&full_bar[stage], bytes);
           armed[stage] = true;
           armed_parity[stage] = phase;
-          tma_load_2d(sA, mw0, &full_bar[stage], k0, wrow0);
-          tma_load_2d(sA + kATile, mw1, &full_bar[stage], k0, wrow1);
+          if (CHUNK <= 32) {
+            tma_load_2d_hint(sA, mw0, &full_bar[stage], k0, wrow0, wpol);
+            tma_load_2d_hint(sA + kATile, mw1, &full_bar[stage], k0, wrow1, wpol);
+          } else {
+            tma_load_2d(sA, mw0, &full_bar[stage], k0, wrow0);
+            tma_load_2d(sA + kATile, mw1, &full_bar[stage], k0, wrow1);
+          }
           for (int i = 0; i < n64; ++i) tma_load_2d(sB + i * 64 * (kBK * 2), &map_b64, &full_bar[stage], k0, tl.r0 + 64 * i);
           for (int i = 0; i < n16; ++i) {
             const int r = 64 * n64 + 16 * i;

@@ -77,6 +77,15 @@ __device__ inline unsigned long long globaltimer_ns() {
   return t;
 }
 
+// L2 policy for bytes read once per call (expert weights): evict first, so
+// that a weight stream replaces its own lines rather than reusable ones
+// (token rows, h, expert rows) or lines that would need a write-back.
+__device__ inline uint64_t l2_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 __device__ inline bool mbar_try_wait_parity(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   const uint32_t addr = static_cast<uint32_t>(__cvta_generic_to_shared(bar));

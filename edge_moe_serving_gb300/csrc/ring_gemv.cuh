@@ -157,6 +157,13 @@ __device__ inline void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint
                : "memory");
 }
 
+// bulk_g2s with an L2 cache policy (weights: evict first).
+__device__ inline void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t policy) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+               ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+               : "memory");
+}
+
 __device__ inline void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
                ::"l"(dst), "r"(smem_addr(src)), "r"(bytes)
@@ -434,6 +441,7 @@ __device__ inline void ring_phase(const GemvParams& p, const Insts& v, int* s_cn
     int cur_j = -1;
     RingSrc rs;
     rs.ok = false;
+    const uint64_t wpol = l2_evict_first();   // weights are read once per call
     for (int i = 0; i < n_local && !*abort_flag; ++i) {
       int j, n0;
       unit_of(i, j, n0);
@@ -460,10 +468,10 @@ __device__ inline void ring_phase(const GemvParams& p, const Insts& v, int* s_cn
                    "r"(bytes * NB)
                    : "memory");
       if (GATEUP) {
-        bulk_g2s(dst, rs.src.gate + (size_t)n0 * K, bytes, &full_bar[stage]);
-        bulk_g2s(dst + bank_stride, rs.src.up + (size_t)n0 * K, bytes, &full_bar[stage]);
+        bulk_g2s_hint(dst, rs.src.gate + (size_t)n0 * K, bytes, &full_bar[stage], wpol);
+        bulk_g2s_hint(dst + bank_stride, rs.src.up + (size_t)n0 * K, bytes, &full_bar[stage], wpol);
       } else {
-        bulk_g2s(dst, rs.src.down + (size_t)n0 * K, bytes, &full_bar[stage]);
+        bulk_g2s_hint(dst, rs.src.down + (size_t)n0 * K, bytes, &full_bar[stage], wpol);
       }
       st.armed_last = ri;
     }
