@@ -108,10 +108,10 @@ def router_flops(cfg):
 #    experts x ~192 rows; profiles/gemm_prefill_profile.md) scaled by the
 #    units processed (4x the experts, 4x the rows): traffic there is each
 #    weight byte once plus the activations, both proportional.
-FFN_TRAFFIC = {"decode": 302663680 + 8519936 + 224 * 16384,
+FFN_TRAFFIC = {"decode": 302662912 + 32312064 + 224 * 16384,
                "prefill": 4 * (2253835008 + 48209408 + 1126691328 + 92532992)}
-TRAFFIC_NOTE = {"decode": ("ncu capture of decode_layer_kernel on decode_profile (1 fill) + 224 router rows; the "
-                           "fill's 50 MB are still dirty in L2 when the kernel ends (written back after it)"),
+TRAFFIC_NOTE = {"decode": ("ncu capture of decode_layer_kernel on decode_profile (1 fill) + 224 router rows; "
+                           "the rest of the fill's 50 MB is still in L2 when the kernel ends"),
                 "prefill": ("ncu capture of the layer call's two gemm_kernel launches on prefill_profile (bf16 expert "
                             "rows), x4 (units processed); the timed public call writes fp32 rows: +T*k*H*2 B")}
 

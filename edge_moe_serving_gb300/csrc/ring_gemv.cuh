@@ -164,9 +164,13 @@ __device__ inline void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes,
                : "memory");
 }
 
+// Shared -> global bulk store, evict-first in L2: a fused cache fill is not
+// read again in this call, so its lines are the first to go back to DRAM
+// (during the call) rather than lingering dirty behind the weight stream.
 __device__ inline void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
-               ::"l"(dst), "r"(smem_addr(src)), "r"(bytes)
+  const uint64_t pol = l2_evict_first();
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;"
+               ::"l"(dst), "r"(smem_addr(src)), "r"(bytes), "l"(pol)
                : "memory");
 }
 __device__ inline unsigned ld_acquire_u32(const unsigned* ptr) {
