@@ -271,6 +271,9 @@ fill_copy_kernel(moe_pool src, moe_pool dst, size_t bank_bytes, const int32_t* _
   pdl_wait();
   pdl_trigger();
   const int n_fill = *n_fill_p;
+  // the staging copy is read once (evict first); the cache slot keeps the
+  // default policy, since the expert FFN reads it right after this launch
+  const uint64_t pol = l2_evict_first();
   const size_t chunks = (bank_bytes + kCopyChunk - 1) / kCopyChunk;
   const size_t items = (size_t)n_fill * 3 * chunks;
   for (size_t item = blockIdx.x; item < items; item += gridDim.x) {
@@ -292,16 +295,16 @@ fill_copy_kernel(moe_pool src, moe_pool dst, size_t bank_bytes, const int32_t* _
     const size_t nv = len / 16;
     size_t v = threadIdx.x;
     for (; v + 3 * kCopyThreads < nv; v += 4 * kCopyThreads) {
-      const uint4 a = ldg_stream(s4 + v);
-      const uint4 b = ldg_stream(s4 + v + kCopyThreads);
-      const uint4 cc = ldg_stream(s4 + v + 2 * kCopyThreads);
-      const uint4 d = ldg_stream(s4 + v + 3 * kCopyThreads);
+      const uint4 a = ldg_stream_hint(s4 + v, pol);
+      const uint4 b = ldg_stream_hint(s4 + v + kCopyThreads, pol);
+      const uint4 cc = ldg_stream_hint(s4 + v + 2 * kCopyThreads, pol);
+      const uint4 d = ldg_stream_hint(s4 + v + 3 * kCopyThreads, pol);
       d4[v] = a;
       d4[v + kCopyThreads] = b;
       d4[v + 2 * kCopyThreads] = cc;
       d4[v + 3 * kCopyThreads] = d;
     }
-    for (; v < nv; v += kCopyThreads) d4[v] = ldg_stream(s4 + v);
+    for (; v < nv; v += kCopyThreads) d4[v] = ldg_stream_hint(s4 + v, pol);
   }
 }
 

@@ -132,6 +132,15 @@ __device__ inline uint4 ldg_stream(const void* p) {
   return r;
 }
 
+// ldg_stream with an L2 cache policy (bytes read once: evict first).
+__device__ inline uint4 ldg_stream_hint(const void* p, uint64_t policy) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p), "l"(policy));
+  return r;
+}
+
 __device__ inline uint4 ldg_cached(const void* p) {
   return __ldg(reinterpret_cast<const uint4*>(p));
 }
