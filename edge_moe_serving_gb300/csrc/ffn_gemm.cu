@@ -48,7 +48,6 @@ constexpr int kATile = kBM * kBK * 2;               // 16 KB
 // stages, twice the bytes in flight.
 template <int CHUNK>
 struct Shape {
-  static constexpr int kChunk = CHUNK;                            // token rows of one tile at most
   static constexpr int kStages = CHUNK <= 32 ? 6 : 3;
   static constexpr int kBTileMax = CHUNK * kBK * 2;
   static constexpr int kStageBytes = 2 * kATile + kBTileMax;
