@@ -337,12 +337,11 @@ cudaError_t launch_bind(const moe_cache& c, int layer, const int32_t* ids, int R
   const bool fused = counts != nullptr;
   size_t smem = bind_smem_bytes(c.cache.n_slots, c.E);
   if (fused) smem = std::max(smem, (size_t)c.E * 33 * sizeof(int));
-  static size_t attr_bytes[2] = {0, 0};
-  if (smem > attr_bytes[fused]) {
-    cudaError_t err = fused ? cudaFuncSetAttribute(bind_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
-                            : cudaFuncSetAttribute(bind_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static std::atomic<int> attr_fused[kMaxDevices], attr_plain[kMaxDevices];
+  {
+    cudaError_t err = fused ? ensure_smem(bind_kernel<true>, (int)smem, attr_fused)
+                            : ensure_smem(bind_kernel<false>, (int)smem, attr_plain);
     if (err != cudaSuccess) return err;
-    attr_bytes[fused] = smem;
   }
   int32_t* n_fill = reinterpret_cast<int32_t*>(ws);
   int32_t* fills = n_fill + 4;

@@ -283,13 +283,12 @@ decode_layer_kernel(DecodeParams d, unsigned int* grid_count) {
 
 template <int NT, int VA, int VB>
 cudaError_t launch_one(const DecodeParams& d, unsigned int* grid_count, int grid, cudaStream_t s) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(decode_layer_kernel<NT, VA, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kRingSmem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<unsigned char> attr[kMaxDevices];
+  cudaError_t e = once_per_device(attr, [] {
+    return cudaFuncSetAttribute(decode_layer_kernel<NT, VA, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kRingSmem);
+  });
+  if (e != cudaSuccess) return e;
   const size_t words = 4 + (size_t)d.g.T * d.g.k;   // barrier words, then one counter per instance
   cudaError_t err = cudaMemsetAsync(grid_count, 0, words * sizeof(unsigned int), s);
   if (err != cudaSuccess) return err;

@@ -132,18 +132,15 @@ cudaError_t launch_dispatch(const int32_t* ids, int R, int k, int E, int32_t* co
                             int32_t* offsets, int32_t* perm, int32_t* inv_perm,
                             const __nv_bfloat16* x, int H, __nv_bfloat16* x_perm, void* ws,
                             uint32_t* status, cudaStream_t s) {
-  static int attr_bytes = 0;
   const int need = (int)(sizeof(int) * 33 * (size_t)E);
-  if (need > attr_bytes) {
-    cudaError_t err = cudaFuncSetAttribute(dispatch_single_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)(sizeof(int) * 33 * kMaxE));
-    if (err != cudaSuccess) return err;
-    err = cudaFuncSetAttribute(tile_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)(sizeof(int) * 33 * kMaxE));
-    if (err != cudaSuccess) return err;
-    attr_bytes = (int)(sizeof(int) * 33 * kMaxE);
-  }
-  cudaError_t err;
+  static std::atomic<unsigned char> attr[kMaxDevices];
+  cudaError_t err = once_per_device(attr, [] {
+    const int max_bytes = (int)(sizeof(int) * 33 * kMaxE);
+    cudaError_t e = cudaFuncSetAttribute(dispatch_single_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_bytes);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(tile_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_bytes);
+  });
+  if (err != cudaSuccess) return err;
   if (R <= kSingleMaxR) {
     err = launch_k(dispatch_single_kernel, 1, kTile, need, s, ids, R, E, counts, offsets, perm, inv_perm, status);
   } else {

@@ -383,13 +383,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_b64, const __grid_constant__
 template <bool GATEUP, int CHUNK>
 cudaError_t launch_one(int grid, cudaStream_t s, const CUtensorMap& b64, const CUtensorMap& b16, const CUtensorMap& w0c,
                        const CUtensorMap& w1c, const CUtensorMap& w0s, const CUtensorMap& w1s, const GemmParams& p) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<GATEUP, CHUNK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Shape<CHUNK>::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<unsigned char> attr[kMaxDevices];
+  cudaError_t e = once_per_device(attr, [] {
+    return cudaFuncSetAttribute(gemm_kernel<GATEUP, CHUNK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Shape<CHUNK>::kSmemBytes);
+  });
+  if (e != cudaSuccess) return e;
   return launch_k(gemm_kernel<GATEUP, CHUNK>, grid, kThreads, Shape<CHUNK>::kSmemBytes, s, b64, b16, w0c, w1c, w0s,
                   w1s, p);
 }

@@ -196,13 +196,12 @@ gemv_fused_kernel(GemvParams p, unsigned int* grid_count) {
 
 template <int NT, int VA, int VB>
 cudaError_t launch_fused_one(const GemvParams& p, unsigned int* grid_count, cudaStream_t s) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_fused_kernel<NT, VA, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kRingSmem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<unsigned char> attr[kMaxDevices];
+  cudaError_t e = once_per_device(attr, [] {
+    return cudaFuncSetAttribute(gemv_fused_kernel<NT, VA, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kRingSmem);
+  });
+  if (e != cudaSuccess) return e;
   const size_t words = p.inst_done != nullptr ? 4 + (size_t)p.T * p.k : 2;
   cudaError_t err = cudaMemsetAsync(grid_count, 0, words * sizeof(unsigned int), s);
   if (err != cudaSuccess) return err;
@@ -246,13 +245,22 @@ cudaError_t launch_gemv_nt(const GemvParams& p, cudaStream_t s) {
   constexpr int NG_UP = 4, NG_DOWN = 8;
   const int thr_up = std::min(kMaxThreads, (int)align_up((size_t)(p.H / 8), 32));
   const int thr_dn = std::min(kMaxThreads, (int)align_up((size_t)(p.I / 8), 32));
-  static int grid_up[kMaxThreads / 32 + 1] = {0};
-  static int grid_dn[kMaxThreads / 32 + 1] = {0};
-  if (!grid_up[thr_up / 32]) grid_up[thr_up / 32] = grid_for(gemv_kernel<NT, NG_UP, true>, thr_up);
-  if (!grid_dn[thr_dn / 32]) grid_dn[thr_dn / 32] = grid_for(gemv_kernel<NT, NG_DOWN, false>, thr_dn);
-  cudaError_t err = launch_k(gemv_kernel<NT, NG_UP, true>, grid_up[thr_up / 32], thr_up, 0, s, p);
+  // grid per (device, block size); 0 = not computed yet
+  static std::atomic<int> grid_up[kMaxDevices][kMaxThreads / 32 + 1], grid_dn[kMaxDevices][kMaxThreads / 32 + 1];
+  const int dev = device_index();
+  int gu = dev >= 0 ? grid_up[dev][thr_up / 32].load(std::memory_order_relaxed) : 0;
+  int gd = dev >= 0 ? grid_dn[dev][thr_dn / 32].load(std::memory_order_relaxed) : 0;
+  if (!gu) {
+    gu = grid_for(gemv_kernel<NT, NG_UP, true>, thr_up);
+    if (dev >= 0) grid_up[dev][thr_up / 32].store(gu, std::memory_order_relaxed);
+  }
+  if (!gd) {
+    gd = grid_for(gemv_kernel<NT, NG_DOWN, false>, thr_dn);
+    if (dev >= 0) grid_dn[dev][thr_dn / 32].store(gd, std::memory_order_relaxed);
+  }
+  cudaError_t err = launch_k(gemv_kernel<NT, NG_UP, true>, gu, thr_up, 0, s, p);
   if (err != cudaSuccess) return err;
-  return launch_k(gemv_kernel<NT, NG_DOWN, false>, grid_dn[thr_dn / 32], thr_dn, 0, s, p);
+  return launch_k(gemv_kernel<NT, NG_DOWN, false>, gd, thr_dn, 0, s, p);
 }
 
 }  // namespace

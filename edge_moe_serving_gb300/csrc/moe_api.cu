@@ -9,13 +9,22 @@
 
 namespace moe {
 
+std::mutex& smem_attr_mutex() {
+  static std::mutex m;
+  return m;
+}
+
 int num_sms() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-      n = kNumSMs;
+  static std::atomic<int> cached[kMaxDevices];   // per device, 0 = not read yet
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return kNumSMs;
+  if (dev >= 0 && dev < kMaxDevices) {
+    const int c = cached[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
   }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = kNumSMs;
+  if (dev >= 0 && dev < kMaxDevices) cached[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <atomic>
+#include <mutex>
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -300,7 +301,48 @@ __device__ inline bool resolve_slot(const moe_cache& c, int32_t entry, int H, in
 }
 
 // ---------------------------------------------------------------- internal launchers
-int num_sms();
+int num_sms();   // SMs of the current device
+
+// Host-side setup that must be done once per device (kernel attributes are
+// per device): `done` is a zero-initialised static table, one flag per
+// device.  fn() runs until it succeeds on the current device; concurrent
+// first calls may both run it, so it must be idempotent (setting an
+// attribute to the same value is).
+constexpr int kMaxDevices = 64;
+
+// Current device, or -1 when it cannot be read or is beyond kMaxDevices.
+inline int device_index() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  return dev >= 0 && dev < kMaxDevices ? dev : -1;
+}
+
+// Raises `kern`'s dynamic shared memory limit on the current device to at
+// least `bytes`.  `cur` holds the limit set so far per device; the attribute
+// is only ever raised, under one lock, so a launch that saw cur >= its size
+// never meets a lower limit set by another thread.
+std::mutex& smem_attr_mutex();
+template <class K>
+inline cudaError_t ensure_smem(K* kern, int bytes, std::atomic<int> (&cur)[kMaxDevices]) {
+  const int dev = device_index();
+  if (dev >= 0 && cur[dev].load(std::memory_order_acquire) >= bytes) return cudaSuccess;
+  std::lock_guard<std::mutex> lock(smem_attr_mutex());
+  if (dev >= 0 && cur[dev].load(std::memory_order_relaxed) >= bytes) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && dev >= 0) cur[dev].store(bytes, std::memory_order_release);
+  return e;
+}
+
+template <class Fn>
+inline cudaError_t once_per_device(std::atomic<unsigned char> (&done)[kMaxDevices], Fn&& fn) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < kMaxDevices && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  e = fn();
+  if (e == cudaSuccess && dev >= 0 && dev < kMaxDevices) done[dev].store(1, std::memory_order_release);
+  return e;
+}
 
 cudaError_t launch_route_topk(const __nv_bfloat16* x, int T, int H, const float* w_router,
                               const float* bias, int E, int k, int32_t* topk_ids, float* topk_w,

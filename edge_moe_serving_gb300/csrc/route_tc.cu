@@ -261,11 +261,11 @@ size_t route_tc_ws_bytes(int T, int H, int E) {
 cudaError_t launch_route_tc(const __nv_bfloat16* x, int T, int H, const float* w_router, const float* bias, int E,
                             int k, int32_t* topk_ids, float* topk_w, float* logits_opt, void* ws, uint32_t* status,
                             cudaStream_t s) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRSmem);
+  static std::atomic<unsigned char> attr[kMaxDevices];
+  {
+    cudaError_t e = once_per_device(
+        attr, [] { return cudaFuncSetAttribute(logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRSmem); });
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   __nv_bfloat16* w3 = reinterpret_cast<__nv_bfloat16*>(ws);
   float* logits = logits_opt ? logits_opt

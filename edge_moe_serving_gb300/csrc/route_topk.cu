@@ -282,12 +282,13 @@ cudaError_t launch_route_topk(const __nv_bfloat16* x, int T, int H, const float*
   if (route_tc_ok(T, H, E))
     return launch_route_tc(x, T, H, w_router, bias, E, k, topk_ids, topk_w, logits_opt, ws, status, s);
   const size_t smem = large_smem(E);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t err = cudaFuncSetAttribute(route_large_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)large_smem(kMaxRouteE));
+  static std::atomic<unsigned char> attr[kMaxDevices];
+  {
+    cudaError_t err = once_per_device(attr, [] {
+      return cudaFuncSetAttribute(route_large_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)large_smem(kMaxRouteE));
+    });
     if (err != cudaSuccess) return err;
-    attr_set = true;
   }
   const int grid = (T + kLT - 1) / kLT;
   return launch_k(route_large_kernel, grid, kLThreads, smem, s, x, T, H, w_router, bias, E, k, logits_opt, topk_ids,
