@@ -14,11 +14,12 @@ from .configs import LayerConfig
 
 
 def to_dev_bf16(bits: np.ndarray, device) -> torch.Tensor:
-    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
+    # writable and C-contiguous (copied only when needed): torch.from_numpy warns on read-only arrays
+    return torch.from_numpy(np.require(bits, requirements=["C", "W"]).view(np.int16)).to(device).view(torch.bfloat16)
 
 
 def to_dev(a: np.ndarray, device) -> torch.Tensor:
-    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    return torch.from_numpy(np.require(a, requirements=["C", "W"])).to(device)
 
 
 class DeviceCache:
