@@ -132,6 +132,12 @@ LayerWs layer_ws(void* ws, const moe_layer_buffers* b, int T, int k, int E, int 
   return L;
 }
 
+// k in [1, min(E, kMaxK)], T * k representable with room for the row offsets
+bool layer_shape_ok(const moe_layer* layer, int T) {
+  return layer->k >= 1 && layer->k <= layer->E && layer->k <= kMaxK && T >= 0 &&
+         (long long)T * layer->k <= INT_MAX / 2;
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -251,7 +257,7 @@ int moe_combine(const float* y_rows, const float* topk_w, int T, int k, int H, v
 }
 
 size_t moe_layer_workspace_size(const moe_layer* layer, const moe_cache* cache, int T, int ffn_mode) {
-  if (!layer || !cache || T < 0 || layer->k < 1) return 0;
+  if (!layer || !cache || !layer_shape_ok(layer, T)) return 0;
   return layer_ws(nullptr, nullptr, T, layer->k, layer->E, layer->H, layer->I, ffn_mode).bytes;
 }
 
@@ -263,7 +269,8 @@ int moe_layer_forward(const moe_layer* layer, const moe_cache* cache, const void
   int st = check_cache(cache);
   if (st != MOE_OK) return st;
   if (layer->E != cache->E || layer->H != cache->H || layer->I != cache->I) return MOE_ERR_INVALID_ARG;
-  if (T < 0) return MOE_ERR_INVALID_ARG;
+  if (T < 0 || layer->k < 1 || layer->k > layer->E || layer->k > kMaxK) return MOE_ERR_INVALID_ARG;
+  if ((long long)T * layer->k > INT_MAX / 2) return MOE_ERR_UNSUPPORTED;
   const int k = layer->k, E = layer->E, H = layer->H, I = layer->I;
   if (T == 0) return MOE_OK;
   if (!x || !out) return MOE_ERR_INVALID_ARG;

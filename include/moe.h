@@ -343,7 +343,11 @@ int moe_combine(const float* y_rows, const float* topk_w, int T, int k, int H, v
  * larger calls run the per-step launches, the FFN on the tensor-core GEMM
  * under AUTO when T > 2.  The fused launches are cooperative (one CTA per
  * SM, all resident together), so they start only once every SM can take one
- * of their CTAs. */
+ * of their CTAs.
+ * Errors: MOE_ERR_INVALID_ARG when layer->k is outside [1, min(E, 16)], the
+ * layer's E, H, I differ from the cache's, or a required pointer is NULL;
+ * MOE_ERR_UNSUPPORTED when T * k exceeds INT_MAX / 2; the sub-calls' errors
+ * otherwise.  moe_layer_workspace_size returns 0 for such arguments. */
 size_t moe_layer_workspace_size(const moe_layer* layer, const moe_cache* cache, int T,
                                 int ffn_mode);
 int moe_layer_forward(const moe_layer* layer, const moe_cache* cache, const void* x, int T,

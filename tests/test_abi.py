@@ -77,3 +77,31 @@ def test_invalid_arguments_rejected_before_launch():
     assert L.moe_cache_bind_slots(ctypes.byref(c), 0, None, 0, 1, 0, 1, 7, 0, None, None, None, 0, None, None) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_cache_bind_slots(ctypes.byref(c), 0, None, 0, 1, 70000, 1, 0, 0, None, None, None, 0, None, None) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_cache_bind_slots(ctypes.byref(c), 1, None, 0, 1, 0, 1, 0, 0, None, None, None, 0, None, None) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_layer_calls_reject_bad_k_and_oversized_calls():
+    L = moe.lib()
+    c = moe.moe_cache()
+    c.cache = moe.moe_pool(16, 16, 16, 4)
+    c.slot_table, c.owner, c.stamp, c.clock = 16, 16, 16, 16
+    c.n_layers, c.E, c.H, c.I = 1, 8, 16, 16
+    lay = moe.moe_layer(16, None, 0, 8, 2, 16, 16)
+    assert L.moe_layer_workspace_size(ctypes.byref(lay), ctypes.byref(c), 4, moe.MOE_FFN_AUTO) > 0
+    # k outside [1, min(E, 16)]: no workspace size, rejected before any launch
+    for k in (0, -3, 9):
+        lay.k = k
+        assert L.moe_layer_workspace_size(ctypes.byref(lay), ctypes.byref(c), 4, moe.MOE_FFN_AUTO) == 0
+        assert L.moe_layer_forward(ctypes.byref(lay), ctypes.byref(c), None, 4, None, 0, 1, 0, 0, moe.MOE_FFN_AUTO,
+                                   None, None, 0, None, None, None) == moe.MOE_ERR_INVALID_ARG
+    c.E, lay.E, lay.k = 32, 32, 17
+    assert L.moe_layer_forward(ctypes.byref(lay), ctypes.byref(c), None, 4, None, 0, 1, 0, 0, moe.MOE_FFN_AUTO,
+                               None, None, 0, None, None, None) == moe.MOE_ERR_INVALID_ARG
+    # T * k beyond INT_MAX / 2 routed rows
+    lay.k = 2
+    assert L.moe_layer_workspace_size(ctypes.byref(lay), ctypes.byref(c), 1 << 30, moe.MOE_FFN_AUTO) == 0
+    assert L.moe_layer_forward(ctypes.byref(lay), ctypes.byref(c), None, 1 << 30, None, 0, 1, 0, 0,
+                               moe.MOE_FFN_AUTO, None, None, 0, None, None, None) == moe.MOE_ERR_UNSUPPORTED
+    # the layer's shape must be the cache's
+    lay.H = 24
+    assert L.moe_layer_forward(ctypes.byref(lay), ctypes.byref(c), None, 4, None, 0, 1, 0, 0, moe.MOE_FFN_AUTO,
+                               None, None, 0, None, None, None) == moe.MOE_ERR_INVALID_ARG
