@@ -78,6 +78,28 @@ def test_qrule_endpoints_and_floor():
     assert O.fill_count(0, fq, 1) == 0
 
 
+def test_phi_to_q16_is_the_nearest_q16_integer():
+    """phi in Q16 is the integer nearest to 65536 phi (exact rational
+    arithmetic on the double's value), ties to even, clamped to [0, 65536]."""
+    from fractions import Fraction
+
+    def nearest(phi):
+        v = Fraction(phi) * O.Q16
+        lo = v.numerator // v.denominator
+        rem = v - lo
+        if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and lo % 2 == 1):
+            lo += 1
+        return min(O.Q16, max(0, lo))
+
+    rng = np.random.default_rng(9)
+    grid = [2 / 3, 1 / 3, 0.415, 25.1 / 63.2, 11.8 / 47.5, 1.5 / O.Q16, 2.5 / O.Q16, 0.5 / O.Q16,
+            65535.5 / O.Q16, 1.0, 1.2, 0.0, -0.25] + rng.random(500).tolist()
+    for phi in grid:
+        assert O.phi_to_q16(phi) == nearest(phi), phi
+    assert O.phi_to_q16(2 / 3) == 43691                # 43690.67 rounds up
+    assert O.phi_to_q16(1.5 / O.Q16) == 2 and O.phi_to_q16(2.5 / O.Q16) == 2   # ties to even
+
+
 def test_qrule_balance_equation():
     """Eq. 4: q/(m-q) ~ B_P/(B_H-B_P); the continuous optimum q* = m B_P/B_H
     equalises T_fill = qS/B_P and T_cpu = (m-q)S/(B_H-B_P)."""
