@@ -31,6 +31,14 @@ Readings where the pages are silent (each one is also listed in the design doc):
     (policy 1, SplitMix64 keys); misses left in C, including overflow when
     fewer victims than q exist, are bound to the staging pool.
 
+Block-scaled FP4 experts ([P] section 5.1 "Models": the routed experts of
+DeepSeek-V4-Flash are natively MXFP4; section 4.1: expert kernels dequantise
+in-kernel).  The element and scale encodings follow the OCP Microscaling
+Formats (MX) v1.0 specification: FP4 E2M1 elements, one E8M0 scale per block
+of 32 consecutive elements along the input dimension.  Readings: two codes per
+byte, the even element in the low nibble; a weight row of K inputs is K/2 code
+bytes and K/32 scale bytes.
+
 Everything is fp64 except where the inputs are stored (bf16 / fp32 values are
 widened exactly).  Library primitives used as steps: numpy matmul, exp,
 bincount, cumsum, sort.
@@ -329,3 +337,50 @@ def bind(state, layer, topk_ids, E, phi_q16, min_fill=1, policy=FILL_LOWEST_ID, 
               "stats": {"n_unique": len(U), "n_hit": len(hits), "n_miss": m, "q": q,
                         "n_fill": len(fills), "n_overflow": q - len(fills), "n_staged": len(C)}}
     return st, result
+
+
+# ------------------------------------------------------------------ MXFP4 experts
+MX_BLOCK = 32
+
+
+def e2m1_value(code):
+    """FP4 E2M1 element (OCP MX v1.0): 1 sign bit, 2 exponent bits (bias 1),
+    1 mantissa bit; exponent field 0 is subnormal (0.5 * mantissa)."""
+    code = int(code) & 0xF
+    sign = -1.0 if code & 0x8 else 1.0
+    exp = (code >> 1) & 0x3
+    man = code & 0x1
+    if exp == 0:
+        return sign * 0.5 * man
+    return sign * 2.0 ** (exp - 1) * (1.0 + 0.5 * man)
+
+
+def e8m0_value(s):
+    """E8M0 block scale (OCP MX v1.0): 2^(s - 127); s = 255 is NaN."""
+    s = int(s) & 0xFF
+    return float("nan") if s == 0xFF else 2.0 ** (s - 127)
+
+
+def mx_dequant(codes, scales):
+    """Dequantise MXFP4 weight rows to fp64.
+
+    codes uint8 [rows, K/2] (element 2c in the low nibble of byte c, 2c+1 in
+    the high nibble); scales uint8 [rows, K/32]; returns [rows, K] with
+    W[r, i] = e2m1(code of i) * e8m0(scales[r, i // 32])."""
+    codes = np.asarray(codes, np.uint8)
+    scales = np.asarray(scales, np.uint8)
+    rows, half = codes.shape
+    K = 2 * half
+    assert K % MX_BLOCK == 0 and scales.shape == (rows, K // MX_BLOCK)
+    elem = np.array([e2m1_value(c) for c in range(16)])
+    scale = np.array([e8m0_value(v) for v in range(256)])
+    nib = np.empty((rows, K), np.int64)
+    nib[:, 0::2] = codes & 0xF
+    nib[:, 1::2] = codes >> 4
+    return elem[nib] * np.repeat(scale[scales], MX_BLOCK, axis=1)
+
+
+def mx_expert_weights(gate_q, gate_s, up_q, up_s, down_q, down_s):
+    """(W_gate, W_up, W_down) in fp64 of one MXFP4 expert (out x in rows)."""
+    return mx_dequant(gate_q, gate_s), mx_dequant(up_q, up_s), mx_dequant(down_q, down_s)
+

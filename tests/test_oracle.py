@@ -441,3 +441,84 @@ def test_bf16_rounding():
     assert back[2] == np.float32(1.015625)            # halfway rounds to even (up)
     assert back[3] == -2.5
     assert abs(back[4] - 3.0e-3) <= 3.0e-3 * 2 ** -8
+
+
+# ------------------------------------------------------------------ MXFP4 experts
+def _e2m1_table():
+    return {int(c, 16): float(v) for c, _bits, v in _rows("e2m1_ocp_mx.txt")}
+
+
+def test_e2m1_matches_the_mx_spec_table():
+    table = _e2m1_table()
+    assert sorted(table) == list(range(16))
+    for code, v in table.items():
+        got = O.e2m1_value(code)
+        assert got == v and np.signbit(got) == np.signbit(v), code
+    mags = [O.e2m1_value(c) for c in range(8)]
+    assert mags == sorted(mags) and max(mags) == 6.0
+
+
+def test_e8m0_is_a_power_of_two_with_bias_127():
+    for s in (0, 1, 100, 126, 127, 128, 200, 254):
+        assert O.e8m0_value(s) == np.ldexp(1.0, s - 127), s
+    assert np.isnan(O.e8m0_value(255))
+
+
+def _mx_encode_exact(dense):
+    """Brute-force MX encoder for weights that are exactly representable:
+    per block, the scale exponent is found by search and each element's code
+    by search over the spec table (values from the golden file)."""
+    table = _e2m1_table()
+    rows, K = dense.shape
+    codes = np.zeros((rows, K // 2), np.uint8)
+    scales = np.zeros((rows, K // 32), np.uint8)
+    for r in range(rows):
+        for b in range(K // 32):
+            blk = dense[r, 32 * b:32 * b + 32]
+            for s in range(255):
+                sc = np.ldexp(1.0, s - 127)
+                found = []
+                for v in blk:
+                    hit = [c for c, tv in table.items() if tv * sc == v and np.signbit(tv) == np.signbit(v)]
+                    if not hit:
+                        break
+                    found.append(hit[0])
+                if len(found) == 32:
+                    scales[r, b] = s
+                    for i, c in enumerate(found):
+                        col = 32 * b + i
+                        codes[r, col // 2] |= np.uint8(c << (4 * (col % 2)))
+                    break
+            else:
+                raise AssertionError("not representable")
+    return codes, scales
+
+
+def test_mx_dequant_round_trips_exactly_representable_weights():
+    """Rows of per-block scaled E2M1 values survive encode -> dequantise
+    exactly; each block has its own scale (a block holds the value 6, so its
+    scale is unique), so a wrong nibble order, block index or scale mapping
+    moves a value."""
+    rng = np.random.default_rng(17)
+    mags = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    rows, K = 5, 96
+    dense = np.zeros((rows, K))
+    for r in range(rows):
+        for b in range(K // 32):
+            v = rng.choice(mags, 32) * rng.choice([-1.0, 1.0], 32)
+            v[rng.integers(32)] = 6.0
+            dense[r, 32 * b:32 * b + 32] = v * np.ldexp(1.0, int(rng.integers(-12, 3)))
+    codes, scales = _mx_encode_exact(dense)
+    assert np.array_equal(O.mx_dequant(codes, scales), dense)
+
+
+def test_mx_dequant_layout_by_hand():
+    """One row, K = 64: byte 0 = 0x71 holds element 0 (code 1 = 0.5) low and
+    element 1 (code 7 = 6.0) high; the second block's scale 2^1 doubles it."""
+    codes = np.zeros((1, 32), np.uint8)
+    codes[0, 0] = 0x71
+    codes[0, 16] = 0xA3          # element 32: code 3 = 1.5, element 33: code A = -1.0
+    scales = np.array([[127, 128]], np.uint8)
+    W = O.mx_dequant(codes, scales)
+    assert W[0, 0] == 0.5 and W[0, 1] == 6.0 and W[0, 32] == 3.0 and W[0, 33] == -2.0
+    assert np.count_nonzero(W) == 4

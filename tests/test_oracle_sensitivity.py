@@ -115,6 +115,17 @@ MUTANTS = [
      [("now = st[\"clock\"] + 1", "now = st[\"clock\"]")]),
     ("fills not stamped", "bind",
      [("        stamp[v] = now\n", "\n")]),
+    ("E2M1 exponent bias 0", "e2m1_value",
+     [("2.0 ** (exp - 1)", "2.0 ** exp")]),
+    ("E2M1 subnormal read as 1.0", "e2m1_value",
+     [("return sign * 0.5 * man", "return sign * 1.0 * man")]),
+    ("E8M0 bias 128", "e8m0_value",
+     [("2.0 ** (s - 127)", "2.0 ** (s - 128)")]),
+    ("MX nibbles swapped", "mx_dequant",
+     [("nib[:, 0::2] = codes & 0xF", "nib[:, 0::2] = codes >> 4"),
+      ("nib[:, 1::2] = codes >> 4", "nib[:, 1::2] = codes & 0xF")]),
+    ("MX scale per element index mod 32", "mx_dequant",
+     [("np.repeat(scale[scales], MX_BLOCK, axis=1)", "np.tile(scale[scales], (1, MX_BLOCK))")]),
 ]
 
 
