@@ -48,6 +48,11 @@ class moe_layer_buffers(ctypes.Structure):
                 ("perm", c_void_p), ("inv_perm", c_void_p), ("y_rows", c_void_p)]
 
 
+class moe_pool_mxfp4(ctypes.Structure):
+    _fields_ = [("gate_q", c_void_p), ("gate_s", c_void_p), ("up_q", c_void_p), ("up_s", c_void_p),
+                ("down_q", c_void_p), ("down_s", c_void_p), ("n_slots", c_int32), ("reserved", c_int32)]
+
+
 class moe_bw_profile(ctypes.Structure):
     _fields_ = [("b_p_gbs", c_double), ("b_h_gbs", c_double), ("b_p_contended_gbs", c_double),
                 ("b_h_contended_gbs", c_double), ("phi", c_double), ("phi_contended", c_double),
@@ -90,6 +95,9 @@ def _load():
                                            P, P, c_size_t, P, P]),
         "moe_expert_ffn_grouped_noalloc": (c_int, [POINTER(moe_cache), c_int, P, P, P, P, P, c_int, c_int, P,
                                                    c_int, P, P, P]),
+        "moe_expert_ffn_mxfp4_workspace_size": (c_size_t, [c_int, c_int, c_int]),
+        "moe_expert_ffn_mxfp4": (c_int, [POINTER(moe_pool_mxfp4), POINTER(moe_pool_mxfp4), P, c_int, c_int,
+                                         c_int, c_int, c_int, P, P, P, P, c_int, c_int, P, P, c_size_t, P, P]),
         "moe_combine": (c_int, [P, P, c_int, c_int, c_int, P, P, P, P]),
         "moe_layer_workspace_size": (c_size_t, [POINTER(moe_layer), POINTER(moe_cache), c_int, c_int]),
         "moe_layer_forward": (c_int, [POINTER(moe_layer), POINTER(moe_cache), P, c_int, P, c_uint32, c_int,
@@ -109,7 +117,8 @@ EXPORTED = ["moe_version", "moe_status_string", "moe_check_bounded_wait", "moe_k
             "moe_route_topk",
             "moe_dispatch_workspace_size", "moe_dispatch", "moe_cache_bind_workspace_size",
             "moe_cache_bind_slots", "moe_expert_ffn_workspace_size", "moe_expert_ffn_grouped",
-            "moe_expert_ffn_grouped_noalloc", "moe_combine",
+            "moe_expert_ffn_grouped_noalloc", "moe_expert_ffn_mxfp4_workspace_size", "moe_expert_ffn_mxfp4",
+            "moe_combine",
             "moe_layer_workspace_size", "moe_layer_forward"]
 
 
@@ -229,6 +238,19 @@ def moe_expert_ffn_grouped_noalloc(cache, layer, counts, offsets, perm, x, x_per
     return _check("moe_expert_ffn_grouped_noalloc", _lib.moe_expert_ffn_grouped_noalloc(
         ctypes.byref(cache), layer, _p(counts), _p(offsets), _p(perm), _p(x), _p(x_perm_opt), T, k,
         _p(expert_mask_opt), ffn_mode, _p(y_rows), _p(dev_status), _s(stream)))
+
+
+def moe_expert_ffn_mxfp4_workspace_size(T, k, I):
+    return _lib.moe_expert_ffn_mxfp4_workspace_size(T, k, I)
+
+
+def moe_expert_ffn_mxfp4(cache_pool, staging_opt, slot_table, n_layers, layer, E, H, I, counts, offsets, perm, x,
+                         T, k, y_rows, ws, ws_bytes, dev_status, stream=None):
+    """cache_pool / staging_opt: moe_pool_mxfp4 structs (staging_opt may be None)."""
+    return _check("moe_expert_ffn_mxfp4", _lib.moe_expert_ffn_mxfp4(
+        ctypes.byref(cache_pool), ctypes.byref(staging_opt) if staging_opt is not None else None,
+        _p(slot_table), n_layers, layer, E, H, I, _p(counts), _p(offsets), _p(perm), _p(x), T, k, _p(y_rows),
+        _p(ws), ws_bytes, _p(dev_status), _s(stream)))
 
 
 def moe_combine(y_rows, topk_w, T, k, H, out, out_f32_opt, dev_status, stream=None):

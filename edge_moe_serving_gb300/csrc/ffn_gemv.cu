@@ -25,23 +25,6 @@ namespace {
 
 constexpr int kMaxThreads = 256;
 
-// Warp reduce-scatter of N (power of two >= 32) values: afterwards lane l
-// holds the warp totals of values [l*N/32, (l+1)*N/32) in v[0 .. N/32).
-template <int N>
-__device__ inline void warp_reduce_scatter(float (&v)[N]) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int o = 16, n = N; o > 0; o >>= 1, n >>= 1) {
-    const bool upper = (lane & o) != 0;
-#pragma unroll
-    for (int j = 0; j < n / 2; ++j) {
-      const float keep = upper ? v[j + n / 2] : v[j];
-      const float send = upper ? v[j] : v[j + n / 2];
-      v[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-    }
-  }
-}
-
 template <int NT, int NG, bool GATEUP>
 __global__ void __launch_bounds__(kMaxThreads)
 gemv_kernel(GemvParams p) {

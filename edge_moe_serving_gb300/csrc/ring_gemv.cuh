@@ -9,20 +9,23 @@
 namespace moe {
 namespace {
 
-// Instances per expert (prefix over experts of ceil(rows / NT), eligible only).
+// Instances per expert (prefix over experts of ceil(rows / NT), eligible
+// only: 0 < counts[e] <= max_rows and mask[e] != 0 when a mask is given).
+// Needs blockDim.x >= 32 and E <= kMaxE.
 template <int NT>
-__device__ void build_prefix(const GemvParams& p, int* s_pref, int* s_warp) {
+__device__ void build_prefix_counts(const int32_t* counts, int E, int max_rows, const uint8_t* mask, int* s_pref,
+                                    int* s_warp) {
   const int tid = threadIdx.x, nthreads = blockDim.x;
-  const int per_thread = (p.E + nthreads - 1) / nthreads;
+  const int per_thread = (E + nthreads - 1) / nthreads;
   const int e0 = tid * per_thread;
   int local[kMaxE / 32];
   int sum = 0;
   for (int u = 0; u < per_thread; ++u) {
     const int e = e0 + u;
     int n = 0;
-    if (e < p.E) {
-      const int cnt = p.counts[e];
-      const bool ok = cnt > 0 && cnt <= p.max_rows && (p.mask == nullptr || p.mask[e] != 0);
+    if (e < E) {
+      const int cnt = counts[e];
+      const bool ok = cnt > 0 && cnt <= max_rows && (mask == nullptr || mask[e] != 0);
       n = ok ? (cnt + NT - 1) / NT : 0;
     }
     local[u] = n;
@@ -45,16 +48,38 @@ __device__ void build_prefix(const GemvParams& p, int* s_pref, int* s_warp) {
       s_warp[w] = run;
       run += t;
     }
-    s_pref[p.E] = run;
+    s_pref[E] = run;
   }
   __syncthreads();
   int run = s_warp[warp] + inc - sum;
   for (int u = 0; u < per_thread; ++u) {
     const int e = e0 + u;
-    if (e < p.E) s_pref[e] = run;
+    if (e < E) s_pref[e] = run;
     run += local[u];
   }
   __syncthreads();
+}
+
+template <int NT>
+__device__ void build_prefix(const GemvParams& p, int* s_pref, int* s_warp) {
+  build_prefix_counts<NT>(p.counts, p.E, p.max_rows, p.mask, s_pref, s_warp);
+}
+
+// Warp reduce-scatter of N (power of two >= 32) values: afterwards lane l
+// holds the warp totals of values [l*N/32, (l+1)*N/32) in v[0 .. N/32).
+template <int N>
+__device__ inline void warp_reduce_scatter(float (&v)[N]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 16, n = N; o > 0; o >>= 1, n >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int j = 0; j < n / 2; ++j) {
+      const float keep = upper ? v[j + n / 2] : v[j];
+      const float send = upper ? v[j] : v[j + n / 2];
+      v[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
 }
 
 // largest e with s_pref[e] <= j < s_pref[e + 1]

@@ -317,6 +317,48 @@ int moe_expert_ffn_grouped_noalloc(const moe_cache* cache, int layer, const int3
                                    const uint8_t* expert_mask_opt, int ffn_mode, float* y_rows,
                                    uint32_t* dev_status, moe_stream_t stream);
 
+/* ---------------------------------------------------------------- MXFP4 experts
+ * Block-scaled FP4 expert banks ([P] section 5.1 "Models": the routed experts
+ * of DeepSeek-V4-Flash are natively MXFP4; section 4.1: expert kernels
+ * dequantise in-kernel).  Encoding of the OCP Microscaling Formats (MX) v1.0
+ * specification: FP4 E2M1 elements (values 0, 0.5, 1, 1.5, 2, 3, 4, 6 and
+ * their negatives) and one E8M0 scale 2^(s - 127) (s = 255: NaN) per block of
+ * 32 consecutive inputs of a weight row.  A row of K inputs is K/2 code bytes,
+ * input 2c in the low nibble of byte c and input 2c+1 in the high nibble, and
+ * K/32 scale bytes.  Banks are slot-major like the bf16 ones:
+ *   gate_q, up_q  [n_slots, I, H/2]   gate_s, up_s  [n_slots, I, H/32]
+ *   down_q        [n_slots, H, I/2]   down_s        [n_slots, H, I/32]
+ * Code banks 16-byte aligned; scale banks have no alignment requirement. */
+typedef struct moe_pool_mxfp4 {
+  const void* gate_q;
+  const void* gate_s;
+  const void* up_q;
+  const void* up_s;
+  const void* down_q;
+  const void* down_s;
+  int32_t n_slots;
+  int32_t reserved;   /* 0 */
+} moe_pool_mxfp4;
+
+/* moe_expert_ffn_grouped (GEMV mode) over MXFP4 banks: for each expert e with
+ * counts[e] > 0, rows pos in [offsets[e], offsets[e+1]), x row t = perm[pos]/k,
+ *   g = x_t W_gate^T, u = x_t W_up^T, h = bf16(silu(g) * u),
+ *   y_rows[perm[pos], :] = h W_down^T
+ * with W the dequantised weights of the slot that slot_table[layer*E + e]
+ * names (cache_pool, or staging_opt for MOE_STAGING_TAG entries; the same
+ * encoding as moe_cache).  Each block's 32 products are summed in fp32 and
+ * scaled by the block's power of two (exact), accumulation in fp32.
+ * slot_table: [n_layers*E] int32.  x bf16 [T, H]; y_rows fp32 [T*k, H],
+ * token-major.  H and I multiples of 32, E <= 1024.  An unbound or
+ * out-of-range entry sets MOE_DEV_ERR_UNBOUND / MOE_DEV_ERR_BAD_SLOT and
+ * leaves that expert's rows unwritten.  Workspace: the bf16 h rows. */
+size_t moe_expert_ffn_mxfp4_workspace_size(int T, int k, int I);
+int moe_expert_ffn_mxfp4(const moe_pool_mxfp4* cache_pool, const moe_pool_mxfp4* staging_opt,
+                         const int32_t* slot_table, int n_layers, int layer, int E, int H, int I,
+                         const int32_t* counts, const int32_t* offsets, const int32_t* perm,
+                         const void* x, int T, int k, float* y_rows, void* ws, size_t ws_bytes,
+                         uint32_t* dev_status, moe_stream_t stream);
+
 /* ---------------------------------------------------------------- combine
  * Gate-weighted merge of the expert outputs ([P] section 3.2: the partial
  * sums of the GPU set and the in-place set merge into the exact layer

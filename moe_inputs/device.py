@@ -112,3 +112,21 @@ class DeviceLayer:
 
 def x_dev(cfg: LayerConfig, layer: int, step: int, device="cuda") -> torch.Tensor:
     return to_dev_bf16(gen.x_bits(cfg, layer, step), device)
+
+
+class MxPool:
+    """One MXFP4 pool on the device: six slot-major uint8 banks (codes and
+    scales of gate, up, down) and the moe_pool_mxfp4 struct naming them.
+    ``experts`` maps slot -> (gate_q, gate_s, up_q, up_s, down_q, down_s)
+    arrays; slots not listed stay zero (never read)."""
+
+    def __init__(self, n_slots, H, I, experts, device="cuda"):
+        shapes = [(I, H // 2), (I, H // 32), (I, H // 2), (I, H // 32), (H, I // 2), (H, I // 32)]
+        self.banks = [torch.zeros((n_slots,) + s, dtype=torch.uint8, device=device) for s in shapes]
+        for slot, arrays in experts.items():
+            self.set(slot, arrays)
+        self.struct = moe.moe_pool_mxfp4(*[b.data_ptr() for b in self.banks], n_slots, 0)
+
+    def set(self, slot, arrays):
+        for bank, a in zip(self.banks, arrays):
+            bank[slot].copy_(torch.from_numpy(np.require(a, requirements=["C", "W"])))

@@ -24,6 +24,12 @@ key names the tensor, the layer and the step):
               starting at a seeded offset.  Every element is marginally
               N(0, 0.02); the windows keep generation of 50 GB of expert weights
               fast on any host while every expert still occupies its own bytes.
+* MXFP4       block-scaled FP4 expert banks (OCP MX encoding): code bytes
+              uniform over 0..255, so every E2M1 code of every element is
+              equally likely (RMS magnitude 2.93), and E8M0 block scales drawn
+              uniformly from 119..121 (2^-8 .. 2^-6), so that weights have a
+              spread near the bf16 experts' N(0, 0.02).  Key ``TAG_MX, seed,
+              layer, expert, bank``.
 * cache       the initial residency: a seeded random subset of the
               (layer, expert) pairs in cache slots 0..S-1, all stamps 0.
 """
@@ -35,7 +41,7 @@ import numpy as np
 
 from .configs import LayerConfig
 
-TAG_X, TAG_XREDRAW, TAG_WR, TAG_BIAS, TAG_HOT, TAG_POOL, TAG_OFF, TAG_CACHE = range(1, 9)
+TAG_X, TAG_XREDRAW, TAG_WR, TAG_BIAS, TAG_HOT, TAG_POOL, TAG_OFF, TAG_CACHE, TAG_MX = range(1, 10)
 BANKS = ("gate", "up", "down")
 STAGING_TAG = 1 << 30          # slot-table tag of the staging pool (pool B)
 REDRAW_DIR = os.path.join(os.path.dirname(os.path.abspath(__file__)), "redraws")
@@ -202,3 +208,26 @@ def initial_cache(cfg: LayerConfig):
         owner = pairs.copy()
     stamp = np.zeros(owner.size, np.uint32)
     return {"table": table, "owner": owner, "stamp": stamp, "clock": 0}
+
+
+# ---------------------------------------------------------------- MXFP4 experts
+MX_SCALE_EXPONENTS = (119, 121)   # inclusive range of the drawn E8M0 scale bytes
+
+
+def mx_bank(seed: int, layer: int, e: int, bank: int, rows: int, K: int):
+    """(codes uint8 [rows, K/2], scales uint8 [rows, K/32]) of one MXFP4 bank."""
+    g = _rng(TAG_MX, seed, layer, e, bank)
+    codes = np.frombuffer(g.bytes(rows * (K // 2)), dtype=np.uint8).reshape(rows, K // 2)
+    lo, hi = MX_SCALE_EXPONENTS
+    scales = g.integers(lo, hi + 1, size=(rows, K // 32), dtype=np.uint8)
+    return codes, scales
+
+
+def mx_expert(seed: int, layer: int, e: int, H: int, I: int):
+    """(gate_q, gate_s, up_q, up_s, down_q, down_s) of MXFP4 expert (layer, e):
+    gate and up rows [I] of H inputs, down rows [H] of I inputs."""
+    gq, gs = mx_bank(seed, layer, e, 0, I, H)
+    uq, us = mx_bank(seed, layer, e, 1, I, H)
+    dq, ds = mx_bank(seed, layer, e, 2, H, I)
+    return gq, gs, uq, us, dq, ds
+

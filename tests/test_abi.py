@@ -34,6 +34,7 @@ def test_struct_layouts_match_header():
     assert ctypes.sizeof(moe.moe_layer_buffers) == 56
     assert ctypes.sizeof(moe.moe_cache) == 2 * 32 + 4 * 8 + 16
     assert ctypes.sizeof(moe.moe_bw_profile) == 6 * 8 + 4 * 4
+    assert ctypes.sizeof(moe.moe_pool_mxfp4) == 6 * 8 + 2 * 4
 
 
 def test_status_strings_and_version():
@@ -105,3 +106,28 @@ def test_layer_calls_reject_bad_k_and_oversized_calls():
     lay.H = 24
     assert L.moe_layer_forward(ctypes.byref(lay), ctypes.byref(c), None, 4, None, 0, 1, 0, 0, moe.MOE_FFN_AUTO,
                                None, None, 0, None, None, None) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_mxfp4_ffn_argument_checks():
+    L = moe.lib()
+    call = L.moe_expert_ffn_mxfp4
+    pool = moe.moe_pool_mxfp4(16, 1, 16, 1, 16, 1, 4, 0)     # fake non-null pointers: never dereferenced
+    args = lambda pool, T=4, k=2, E=8, H=64, I=64, ws_bytes=1 << 20, x=16, layer=0: (
+        ctypes.byref(pool), None, 16, 1, layer, E, H, I, 16, 16, 16, x, T, k, 16, 16, ws_bytes, None, None)
+    assert moe.moe_expert_ffn_mxfp4_workspace_size(4, 2, 64) >= 4 * 2 * 64 * 2   # the bf16 h rows
+    assert moe.moe_expert_ffn_mxfp4_workspace_size(4, 2, 16) == 0
+    assert call(*args(pool, T=0)) == moe.MOE_OK
+    assert call(*args(pool, k=9)) == moe.MOE_ERR_INVALID_ARG          # k > E
+    assert call(*args(pool, layer=1)) == moe.MOE_ERR_INVALID_ARG      # layer out of range
+    assert call(*args(pool, H=48)) == moe.MOE_ERR_UNSUPPORTED         # not a multiple of 32
+    assert call(*args(pool, I=80)) == moe.MOE_ERR_UNSUPPORTED
+    assert call(*args(pool, E=2000)) == moe.MOE_ERR_UNSUPPORTED
+    assert call(*args(pool, x=24)) == moe.MOE_ERR_UNSUPPORTED         # x not 16-byte aligned
+    assert call(*args(pool, ws_bytes=64)) == moe.MOE_ERR_WORKSPACE
+    bad = moe.moe_pool_mxfp4(24, 1, 16, 1, 16, 1, 4, 0)              # misaligned code bank
+    assert call(*args(bad)) == moe.MOE_ERR_UNSUPPORTED
+    empty = moe.moe_pool_mxfp4(16, None, 16, 1, 16, 1, 4, 0)         # missing scale bank
+    assert call(*args(empty)) == moe.MOE_ERR_INVALID_ARG
+    assert call(None, None, 16, 1, 0, 8, 64, 64, 16, 16, 16, 16, 4, 2, 16, 16, 1 << 20, None,
+                None) == moe.MOE_ERR_INVALID_ARG
+

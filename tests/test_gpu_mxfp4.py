@@ -1,0 +1,139 @@
+"""GPU parity of the MXFP4 expert FFN (moe_expert_ffn_mxfp4) against the
+oracle: the same SwiGLU experts on the fp64 dequantised banks (FP4 E2M1
+elements, E8M0 scales per 32 inputs), through the slot table into both pools,
+on ragged groups, every row-chunk width, the decode and batched-decode shapes,
+and the unbound / out-of-range slot errors."""
+import numpy as np
+import pytest
+import torch
+
+import edge_moe_serving_gb300 as moe
+from moe_inputs import gen
+from moe_inputs.device import MxPool
+from oracle import moe_oracle as O
+from gpu_helpers import DEV, assert_close, status, status_bits, ws
+
+pytestmark = pytest.mark.gpu
+
+SEED = 41
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+
+
+def _route(rng, T, k, experts):
+    return np.stack([np.sort(rng.choice(experts, k, replace=False)) for _ in range(T)]).astype(np.int32)
+
+
+def _run(T, k, E, H, I, n_layers, layer, cached, staged, seed, unbound=(), bad=(), active=None):
+    """cached: experts placed in cache-pool slots (in a seeded order); staged:
+    experts bound to the staging pool; unbound: entry -1; bad: a cache slot
+    past the pool.  Returns (y from the GPU, oracle rows, status bits, ids)."""
+    rng = np.random.default_rng(seed)
+    ids = _route(rng, T, k, np.arange(E) if active is None else np.asarray(active))
+    x_bits = gen.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    n_cache = max(len(cached), 1)
+    slots = rng.permutation(n_cache)
+    table = np.full(n_layers * E, -1, np.int32)
+    base = layer * E
+    cache_experts, staging_experts = {}, {}
+    for s, e in zip(slots, cached):
+        table[base + e] = s
+        cache_experts[int(s)] = gen.mx_expert(SEED, layer, int(e), H, I)
+    for e in staged:
+        table[base + e] = gen.STAGING_TAG | (base + e)
+        staging_experts[base + int(e)] = gen.mx_expert(SEED, layer, int(e), H, I)
+    for e in unbound:
+        table[base + e] = -1
+    for e in bad:
+        table[base + e] = n_cache + 3
+    pool_a = MxPool(n_cache, H, I, cache_experts, DEV)
+    pool_b = MxPool(n_layers * E, H, I, staging_experts, DEV) if len(staged) else None
+
+    counts, offsets, perm, inv = O.dispatch(ids, E)
+    dev_i32 = lambda a: torch.from_numpy(np.asarray(a, np.int32)).to(DEV)
+    x = torch.from_numpy(x_bits.view(np.int16)).to(DEV).view(torch.bfloat16)
+    R = T * k
+    y = torch.full((R, H), 7.0, dtype=torch.float32, device=DEV)
+    nb = moe.moe_expert_ffn_mxfp4_workspace_size(T, k, I)
+    st = status()
+    moe.moe_expert_ffn_mxfp4(pool_a.struct, pool_b.struct if pool_b else None, dev_i32(table), n_layers, layer, E,
+                             H, I, dev_i32(counts), dev_i32(offsets), dev_i32(perm), x, T, k, y, ws(nb), nb, st)
+    torch.cuda.synchronize()
+
+    xf = gen.bf16_bits_to_f64(x_bits)
+    ref = np.full((R, H), np.nan)
+    weights = {}
+    for i, e in enumerate(ids.reshape(-1)):
+        e = int(e)
+        if e in unbound or e in bad:
+            continue
+        if e not in weights:
+            weights[e] = O.mx_expert_weights(*gen.mx_expert(SEED, layer, e, H, I))
+        ref[i] = O.swiglu_expert(xf[i // k][None, :], *weights[e])[0]
+    return y.cpu().numpy().astype(np.float64), ref, status_bits(st), ids
+
+
+def _check(y, ref, what):
+    ok = ~np.isnan(ref[:, 0])
+    assert ok.any()
+    assert_close(y[ok], ref[ok], what=what)
+
+
+@pytest.mark.parametrize("T,k,E,H,I", [(5, 3, 12, 256, 160), (2, 4, 16, 512, 256), (1, 2, 6, 64, 96),
+                                       (9, 5, 7, 128, 64)])
+def test_mxfp4_ffn_small_shapes_both_pools(T, k, E, H, I):
+    """Groups of 1..T rows (row chunks of 1, 2 and 4 plus ragged tails),
+    experts in the cache pool and in the staging pool, layer 1 of 2."""
+    experts = list(range(E))
+    cached, staged = experts[: E // 2 + 1], experts[E // 2 + 1:]
+    y, ref, st, _ = _run(T, k, E, H, I, 2, 1, cached, staged, seed=T * 100 + E)
+    assert st == 0
+    _check(y, ref, f"mxfp4 T={T} k={k} E={E} H={H} I={I}")
+
+
+def test_mxfp4_ffn_decode_shape():
+    """One token, 6 of 256 experts, hidden 4096, intermediate 2048."""
+    rng = np.random.default_rng(5)
+    active = np.sort(rng.choice(256, 6, replace=False))
+    y, ref, st, ids = _run(1, 6, 256, 4096, 2048, 1, 0, list(active[:5]), list(active[5:]), seed=6,
+                           active=active)
+    assert st == 0 and sorted(ids[0].tolist()) == active.tolist()
+    _check(y, ref, "mxfp4 decode shape")
+
+
+def test_mxfp4_ffn_batched_decode_shape():
+    """32 tokens, top-8 of 128 experts routed over 24 of them (groups of ~10
+    rows: several row chunks each), hidden 2048, intermediate 768."""
+    rng = np.random.default_rng(8)
+    active = np.sort(rng.choice(128, 24, replace=False))
+    y, ref, st, _ = _run(32, 8, 128, 2048, 768, 1, 0, list(active[:18]), list(active[18:]), seed=9,
+                         active=active)
+    assert st == 0
+    _check(y, ref, "mxfp4 batched decode shape")
+
+
+def test_mxfp4_ffn_unbound_and_bad_slot_rows_left_unwritten():
+    T, k, E, H, I = 4, 3, 8, 64, 64
+    y, ref, st, ids = _run(T, k, E, H, I, 1, 0, [0, 1, 2, 3, 4], [], seed=3, active=np.arange(8),
+                           unbound=(5,), bad=(6,))
+    flat = ids.reshape(-1)
+    skipped = np.isin(flat, [5, 6, 7])
+    if np.isin(flat, 5).any():
+        assert st & moe.MOE_DEV_ERR_UNBOUND
+    if np.isin(flat, 6).any():
+        assert st & moe.MOE_DEV_ERR_BAD_SLOT
+    assert np.all(y[skipped] == 7.0)            # sentinel kept: nothing written for those experts
+    keep = ~skipped
+    _check(y[keep], ref[keep], "mxfp4 rows of bound experts")
+
+
+def test_mxfp4_ffn_empty_call_launches_nothing():
+    pool = MxPool(1, 64, 64, {}, DEV)
+    before = moe.moe_kernel_launch_count()
+    moe.moe_expert_ffn_mxfp4(pool.struct, None, torch.zeros(8, dtype=torch.int32, device=DEV), 1, 0, 8, 64, 64,
+                             None, None, None, None, 0, 2, None, None, 0, None)
+    assert moe.moe_kernel_launch_count() == before
