@@ -27,8 +27,8 @@ key names the tensor, the layer and the step):
 * MXFP4       block-scaled FP4 expert banks (OCP MX encoding): code bytes
               uniform over 0..255, so every E2M1 code of every element is
               equally likely (RMS magnitude 2.93), and E8M0 block scales drawn
-              uniformly from 119..121 (2^-8 .. 2^-6), so that weights have a
-              spread near the bf16 experts' N(0, 0.02).  Key ``TAG_MX, seed,
+              uniformly from 119..120 (2^-8, 2^-7): weights with standard
+              deviation 0.018, near the bf16 experts' N(0, 0.02).  Key ``TAG_MX, seed,
               layer, expert, bank``.
 * cache       the initial residency: a seeded random subset of the
               (layer, expert) pairs in cache slots 0..S-1, all stamps 0.
@@ -211,7 +211,7 @@ def initial_cache(cfg: LayerConfig):
 
 
 # ---------------------------------------------------------------- MXFP4 experts
-MX_SCALE_EXPONENTS = (119, 121)   # inclusive range of the drawn E8M0 scale bytes
+MX_SCALE_EXPONENTS = (119, 120)   # inclusive range of the drawn E8M0 scale bytes
 
 
 def mx_bank(seed: int, layer: int, e: int, bank: int, rows: int, K: int):
