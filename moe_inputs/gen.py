@@ -30,6 +30,10 @@ key names the tensor, the layer and the step):
               uniformly from 119..120 (2^-8, 2^-7): weights with standard
               deviation 0.018, near the bf16 experts' N(0, 0.02).  Key ``TAG_MX, seed,
               layer, expert, bank``.
+* NVFP4       FP4 E2M1 code bytes uniform over 0..255, E4M3 block scales (one
+              per 16 inputs) uniform over the bytes 0x40..0x47 (2.0 .. 3.75)
+              and a tensor scale of 2^-9 per bank: weight standard deviation
+              about 0.017.  Key ``TAG_NV, seed, layer, expert, bank``.
 * cache       the initial residency: a seeded random subset of the
               (layer, expert) pairs in cache slots 0..S-1, all stamps 0.
 """
@@ -41,7 +45,7 @@ import numpy as np
 
 from .configs import LayerConfig
 
-TAG_X, TAG_XREDRAW, TAG_WR, TAG_BIAS, TAG_HOT, TAG_POOL, TAG_OFF, TAG_CACHE, TAG_MX = range(1, 10)
+TAG_X, TAG_XREDRAW, TAG_WR, TAG_BIAS, TAG_HOT, TAG_POOL, TAG_OFF, TAG_CACHE, TAG_MX, TAG_NV = range(1, 11)
 BANKS = ("gate", "up", "down")
 STAGING_TAG = 1 << 30          # slot-table tag of the staging pool (pool B)
 REDRAW_DIR = os.path.join(os.path.dirname(os.path.abspath(__file__)), "redraws")
@@ -230,4 +234,18 @@ def mx_expert(seed: int, layer: int, e: int, H: int, I: int):
     uq, us = mx_bank(seed, layer, e, 1, I, H)
     dq, ds = mx_bank(seed, layer, e, 2, H, I)
     return gq, gs, uq, us, dq, ds
+
+
+# ---------------------------------------------------------------- NVFP4 experts
+NV_SCALE_BYTES = (0x40, 0x47)     # inclusive range of the drawn E4M3 block-scale bytes
+NV_TENSOR_SCALE = 2.0 ** -9
+
+
+def nvfp4_bank(seed: int, layer: int, e: int, bank: int, rows: int, K: int):
+    """(codes uint8 [rows, K/2], E4M3 scales uint8 [rows, K/16], fp32 tensor scale)."""
+    g = _rng(TAG_NV, seed, layer, e, bank)
+    codes = np.frombuffer(g.bytes(rows * (K // 2)), dtype=np.uint8).reshape(rows, K // 2)
+    lo, hi = NV_SCALE_BYTES
+    scales = g.integers(lo, hi + 1, size=(rows, K // 16), dtype=np.uint8)
+    return codes, scales, np.float32(NV_TENSOR_SCALE)
 

@@ -39,6 +39,14 @@ of 32 consecutive elements along the input dimension.  Readings: two codes per
 byte, the even element in the low nibble; a weight row of K inputs is K/2 code
 bytes and K/32 scale bytes.
 
+NVFP4 experts ([P] section 5.1 "Models": GLM-5.2's routed experts and the
+laptop build of Qwen3.6-35B-A3B are NVFP4): FP4 E2M1 elements with one FP8
+E4M3 scale per block of 16 consecutive inputs and one fp32 scale per weight
+tensor, as NVIDIA describes the format; E4M3 as in the OCP 8-bit floating
+point specification (the variant without infinities).  Readings: the same
+nibble packing as MXFP4; the block scale is the raw E4M3 byte; one tensor
+scale per bank of an expert.
+
 Everything is fp64 except where the inputs are stored (bf16 / fp32 values are
 widened exactly).  Library primitives used as steps: numpy matmul, exp,
 bincount, cumsum, sort.
@@ -383,4 +391,42 @@ def mx_dequant(codes, scales):
 def mx_expert_weights(gate_q, gate_s, up_q, up_s, down_q, down_s):
     """(W_gate, W_up, W_down) in fp64 of one MXFP4 expert (out x in rows)."""
     return mx_dequant(gate_q, gate_s), mx_dequant(up_q, up_s), mx_dequant(down_q, down_s)
+
+
+# ------------------------------------------------------------------ NVFP4 experts
+NV_BLOCK = 16
+
+
+def e4m3_value(b):
+    """FP8 E4M3 (OCP 8-bit floating point, no infinities): 1 sign bit, 4
+    exponent bits (bias 7), 3 mantissa bits; exponent field 0 is subnormal
+    (2^-6 * mantissa / 8); exponent and mantissa all ones is NaN."""
+    b = int(b) & 0xFF
+    sign = -1.0 if b & 0x80 else 1.0
+    exp = (b >> 3) & 0xF
+    man = b & 0x7
+    if exp == 0xF and man == 0x7:
+        return float("nan")
+    if exp == 0:
+        return sign * 2.0 ** -6 * (man / 8.0)
+    return sign * 2.0 ** (exp - 7) * (1.0 + man / 8.0)
+
+
+def nvfp4_dequant(codes, scales, tensor_scale):
+    """Dequantise NVFP4 weight rows to fp64.
+
+    codes uint8 [rows, K/2] (element 2c in the low nibble of byte c); scales
+    uint8 [rows, K/16] (E4M3 bytes); tensor_scale: the fp32 scale of the
+    whole matrix.  W[r, i] = e2m1(code of i) * e4m3(scales[r, i // 16]) * tensor_scale."""
+    codes = np.asarray(codes, np.uint8)
+    scales = np.asarray(scales, np.uint8)
+    rows, half = codes.shape
+    K = 2 * half
+    assert K % NV_BLOCK == 0 and scales.shape == (rows, K // NV_BLOCK)
+    elem = np.array([e2m1_value(c) for c in range(16)])
+    scale = np.array([e4m3_value(v) for v in range(256)])
+    nib = np.empty((rows, K), np.int64)
+    nib[:, 0::2] = codes & 0xF
+    nib[:, 1::2] = codes >> 4
+    return elem[nib] * np.repeat(scale[scales], NV_BLOCK, axis=1) * float(np.float32(tensor_scale))
 

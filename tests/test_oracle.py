@@ -522,3 +522,69 @@ def test_mx_dequant_layout_by_hand():
     W = O.mx_dequant(codes, scales)
     assert W[0, 0] == 0.5 and W[0, 1] == 6.0 and W[0, 32] == 3.0 and W[0, 33] == -2.0
     assert np.count_nonzero(W) == 4
+
+
+def test_e8m0_equals_the_library_decoder_for_every_byte():
+    import torch
+    lib = torch.arange(256, dtype=torch.uint8).view(torch.float8_e8m0fnu).double().numpy()
+    ours = np.array([O.e8m0_value(s) for s in range(256)])
+    assert np.array_equal(np.isnan(lib), np.isnan(ours))
+    assert np.array_equal(lib[~np.isnan(lib)], ours[~np.isnan(ours)])
+
+
+# ------------------------------------------------------------------ NVFP4 experts
+def test_e4m3_matches_the_ofp8_spec_values():
+    for b, _bits, v in _rows("e4m3_ocp_fp8.txt"):
+        got = O.e4m3_value(int(b, 16))
+        if v == "nan":
+            assert np.isnan(got), b
+        else:
+            assert got == float(v), b
+
+
+def test_e4m3_equals_the_library_decoder_for_every_byte():
+    import torch
+    lib = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    ours = np.array([O.e4m3_value(b) for b in range(256)])
+    assert np.array_equal(np.isnan(lib), np.isnan(ours))
+    ok = ~np.isnan(lib)
+    assert np.array_equal(lib[ok], ours[ok]) and np.array_equal(np.signbit(lib[ok]), np.signbit(ours[ok]))
+
+
+def test_nvfp4_dequant_layout_by_hand():
+    """K = 32: two blocks of 16.  Byte 0 = 0x71: element 0 = 0.5, element 1 =
+    6.0 under scale 0x38 (1.0); byte 8 = 0xA3: element 16 = 1.5, element 17 =
+    -1.0 under scale 0x40 (2.0); tensor scale 0.25."""
+    codes = np.zeros((1, 16), np.uint8)
+    codes[0, 0] = 0x71
+    codes[0, 8] = 0xA3
+    scales = np.array([[0x38, 0x40]], np.uint8)
+    W = O.nvfp4_dequant(codes, scales, 0.25)
+    assert W[0, 0] == 0.125 and W[0, 1] == 1.5 and W[0, 16] == 0.75 and W[0, 17] == -0.5
+    assert np.count_nonzero(W) == 4
+
+
+def test_nvfp4_dequant_round_trips_exactly_representable_weights():
+    """Per 16-input block: E2M1 values times one E4M3 scale (drawn from exact
+    E4M3 values), times one tensor scale; a brute-force encoder over the spec
+    tables recovers bytes that dequantise back exactly."""
+    import torch
+    e2m1 = _e2m1_table()
+    e4m3 = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    rng = np.random.default_rng(23)
+    rows, K, ts = 4, 64, np.float32(0.0078125 * 3)
+    mags = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    scale_bytes = rng.integers(0x30, 0x50, size=(rows, K // 16))
+    dense = np.zeros((rows, K))
+    for r in range(rows):
+        for b in range(K // 16):
+            v = rng.choice(mags, 16) * rng.choice([-1.0, 1.0], 16)
+            v[rng.integers(16)] = 6.0
+            dense[r, 16 * b:16 * b + 16] = v * e4m3[scale_bytes[r, b]] * float(ts)
+    codes = np.zeros((rows, K // 2), np.uint8)
+    for r in range(rows):
+        for i in range(K):
+            sc = e4m3[scale_bytes[r, i // 16]] * float(ts)
+            hit = [c for c, tv in e2m1.items() if tv * sc == dense[r, i] and np.signbit(tv) == np.signbit(dense[r, i])]
+            codes[r, i // 2] |= np.uint8(hit[0] << (4 * (i % 2)))
+    assert np.array_equal(O.nvfp4_dequant(codes, scale_bytes.astype(np.uint8), ts), dense)
