@@ -131,3 +131,36 @@ def test_mxfp4_ffn_argument_checks():
     assert call(None, None, 16, 1, 0, 8, 64, 64, 16, 16, 16, 16, 4, 2, 16, 16, 1 << 20, None,
                 None) == moe.MOE_ERR_INVALID_ARG
 
+
+
+STRUCTS = ["moe_pool", "moe_cache", "moe_bind_stats", "moe_layer", "moe_layer_buffers", "moe_bw_profile",
+           "moe_pool_mxfp4"]
+
+
+def test_header_is_plain_c_and_matches_the_binding_layouts(tmp_path):
+    """include/moe.h compiles as C99 with warnings as errors; every struct's
+    size and every field's offset, as the C compiler lays them out, equal the
+    ctypes binding's."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    lines = ["#include <stddef.h>", "#include <stdio.h>", '#include "moe.h"', "int main(void) {"]
+    for name in STRUCTS:
+        lines.append(f'  printf("{name} %zu\\n", sizeof({name}));')
+        for field, _ in getattr(moe, name)._fields_:
+            lines.append(f'  printf("{name}.{field} %zu\\n", offsetof({name}, {field}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+                    str(src), "-o", str(exe)], check=True, capture_output=True)
+    out = dict(line.rsplit(" ", 1) for line in subprocess.run([str(exe)], check=True, capture_output=True,
+                                                               text=True).stdout.splitlines())
+    for name in STRUCTS:
+        ct = getattr(moe, name)
+        assert int(out[name]) == ctypes.sizeof(ct), name
+        for field, _ in ct._fields_:
+            assert int(out[f"{name}.{field}"]) == getattr(ct, field).offset, (name, field)
