@@ -1,0 +1,52 @@
+"""bench.py's reference arm (the CPU fp64 oracle) keeps the output contract
+on the host: one JSON line on rank 0 with the required keys, nothing on the
+other ranks, exit status 0."""
+import json
+import os
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+REQUIRED = {"metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+            "vs_baseline", "dtype", "data", "config", "impl", "cpu_baseline", "e2e"}
+
+
+def _run(env_extra, *args):
+    env = dict(os.environ, **env_extra)
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", *args],
+                          capture_output=True, text=True, env=env, timeout=300, cwd=ROOT)
+
+
+def test_reference_arm_prints_one_contract_line():
+    r = _run({"RANK": "0", "WORLD_SIZE": "1"}, "--workload", "tiny", "--steps", "2", "--warmup", "3",
+             "--reference-budget-s", "4")
+    assert r.returncode == 0, r.stderr
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert REQUIRED <= set(d)
+    assert d["impl"] == "reference" and d["steps"] == 2 and d["warmup"] == 3 and d["higher_is_better"] is True
+    assert d["value"] > 0 and d["unit"] == "tokens/s" and d["config"]["workload"] == "tiny"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_other_ranks_print_nothing():
+    r = _run({"RANK": "1", "WORLD_SIZE": "2"}, "--workload", "tiny", "--steps", "1", "--warmup", "3")
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == ""
+
+
+def test_warmup_below_three_is_raised_to_three():
+    r = _run({"RANK": "0", "WORLD_SIZE": "1"}, "--workload", "tiny", "--steps", "1", "--warmup", "1",
+             "--reference-budget-s", "2")
+    assert r.returncode == 0, r.stderr
+    assert json.loads(r.stdout.strip().splitlines()[-1])["warmup"] == 3
+
+
+def test_mxfp4_expert_bytes():
+    sys.path.insert(0, ROOT)
+    import bench
+    # three banks of H*I four-bit codes plus one E8M0 byte per 32 inputs
+    assert bench.mx_expert_bytes(4096, 2048) == 3 * (4096 * 2048 // 2 + 4096 * 2048 // 32) == 13369344
