@@ -349,9 +349,16 @@ typedef struct moe_pool_mxfp4 {
  * encoding as moe_cache).  Each block's 32 products are summed in fp32 and
  * scaled by the block's power of two (exact), accumulation in fp32.
  * slot_table: [n_layers*E] int32.  x bf16 [T, H]; y_rows fp32 [T*k, H],
- * token-major.  H and I multiples of 32, E <= 1024.  An unbound or
- * out-of-range entry sets MOE_DEV_ERR_UNBOUND / MOE_DEV_ERR_BAD_SLOT and
- * leaves that expert's rows unwritten.  Workspace: the bf16 h rows. */
+ * token-major.  counts / offsets / perm as moe_dispatch writes them.
+ * Errors: MOE_ERR_INVALID_ARG for a NULL pool, table or (T > 0) array, a
+ * pool missing a bank or with n_slots < 1, layer outside [0, n_layers), k
+ * outside [1, min(E, 16)], H or I below 32; MOE_ERR_UNSUPPORTED for H or I
+ * not a multiple of 32, E > 1024, T*k > INT_MAX/2, a code bank, x or y_rows
+ * not 16-byte aligned; MOE_ERR_WORKSPACE for ws_bytes below
+ * moe_expert_ffn_mxfp4_workspace_size(T, k, I) (the bf16 h rows, 0 for
+ * invalid arguments).  T = 0 returns MOE_OK and launches nothing.  On the
+ * device, an unbound or out-of-range entry sets MOE_DEV_ERR_UNBOUND /
+ * MOE_DEV_ERR_BAD_SLOT and leaves that expert's rows unwritten. */
 size_t moe_expert_ffn_mxfp4_workspace_size(int T, int k, int I);
 int moe_expert_ffn_mxfp4(const moe_pool_mxfp4* cache_pool, const moe_pool_mxfp4* staging_opt,
                          const int32_t* slot_table, int n_layers, int layer, int E, int H, int I,
