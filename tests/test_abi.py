@@ -164,3 +164,53 @@ def test_header_is_plain_c_and_matches_the_binding_layouts(tmp_path):
         assert int(out[name]) == ctypes.sizeof(ct), name
         for field, _ in ct._fields_:
             assert int(out[f"{name}.{field}"]) == getattr(ct, field).offset, (name, field)
+
+
+def test_library_is_usable_from_plain_c(tmp_path):
+    """A C99 program linked against libmoe.so (no Python) calls the host-side
+    entry points: version, status strings, phi in Q16, the bandwidth
+    derivation, workspace sizes and argument rejection before any launch."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include <string.h>
+#include "moe.h"
+#define CHECK(c) do { if (!(c)) { printf("FAIL %s:%d %s\n", __FILE__, __LINE__, #c); return 1; } } while (0)
+int main(void) {
+  moe_bw_profile p;
+  moe_pool_mxfp4 mx;
+  moe_layer lay;
+  moe_cache c;
+  CHECK(moe_version() >= 100);
+  CHECK(strcmp(moe_status_string(MOE_OK), "ok") == 0);
+  CHECK(moe_phi_to_q16(0.5) == 32768u && moe_phi_to_q16(2.0) == 65536u && moe_phi_to_q16(-1.0) == 0u);
+  memset(&p, 0, sizeof p);
+  p.b_p_gbs = 25.1; p.b_h_gbs = 63.2;
+  CHECK(moe_bw_derive(&p) == MOE_OK && p.phi_q16 == moe_phi_to_q16(25.1 / 63.2) && p.hybrid_ok == 1);
+  CHECK(moe_bw_derive(NULL) == MOE_ERR_INVALID_ARG);
+  CHECK(moe_dispatch_workspace_size(1, 6, 256) == 0);
+  CHECK(moe_expert_ffn_mxfp4_workspace_size(1, 6, 2048) >= 6u * 2048u * 2u);
+  CHECK(moe_route_topk(NULL, 4, 64, NULL, NULL, 4, 5, NULL, NULL, NULL, NULL, 0, NULL, NULL) == MOE_ERR_INVALID_ARG);
+  CHECK(moe_combine(NULL, NULL, 0, 2, 64, NULL, NULL, NULL, NULL) == MOE_OK);
+  memset(&mx, 0, sizeof mx);
+  CHECK(moe_expert_ffn_mxfp4(&mx, NULL, NULL, 1, 0, 8, 64, 64, NULL, NULL, NULL, NULL, 1, 2, NULL, NULL, 0, NULL,
+                             NULL) == MOE_ERR_INVALID_ARG);
+  memset(&lay, 0, sizeof lay);
+  memset(&c, 0, sizeof c);
+  CHECK(moe_layer_forward(&lay, &c, NULL, 1, NULL, 0, 1, 0, 0, MOE_FFN_AUTO, NULL, NULL, 0, NULL, NULL, NULL) ==
+        MOE_ERR_INVALID_ARG);
+  printf("ok\n");
+  return 0;
+}
+''')
+    exe = tmp_path / "use"
+    libdir = os.path.dirname(moe.LIB_PATH)
+    subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(src), "-o",
+                    str(exe), "-L", libdir, "-lmoe", f"-Wl,-rpath,{libdir}"], check=True, capture_output=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
