@@ -102,12 +102,12 @@ def router_flops(cfg):
 # captures summarised under profiles/ (a workload without an entry, or whose
 # kernels changed since their capture, reports null).
 #  decode: decode_layer_kernel captured on decode_profile (same six 50.3 MB
-#    experts per step, one cache fill; profiles/decode_layer_kernel_profile.md)
-#    plus the 224 extra 16 KB router rows of the 256-expert layer.
+#    experts per step, one cache fill) plus the 224 extra 16 KB router rows
+#    of the 256-expert layer.
 #  prefill: the two gemm_kernel launches captured on prefill_profile (64
-#    experts x ~192 rows; profiles/gemm_prefill_profile.md) scaled by the
-#    units processed (4x the experts, 4x the rows): traffic there is each
-#    weight byte once plus the activations, both proportional.
+#    experts x ~192 rows) scaled by the units processed (4x the experts, 4x
+#    the rows): traffic there is each weight byte once plus the activations,
+#    both proportional.
 FFN_TRAFFIC = {"decode": 302662912 + 32312064 + 224 * 16384,
                "prefill": 4 * (2253835008 + 48209408 + 1126691328 + 92532992)}
 TRAFFIC_NOTE = {"decode": ("ncu capture of decode_layer_kernel on decode_profile (1 fill) + 224 router rows; "

@@ -17,7 +17,7 @@ Source pages
      (the Q16 integer rounding of q*), section "Decode residency: one LRU
      across all layers" (overflow misses).
 
-Readings where the pages are silent (each one is also listed in the design doc):
+Readings where the pages are silent:
   * router scores: softmax over the router logits, top-k, renormalised over
     the k selected experts (the tiny workload's "top-2 softmax-renormalised");
   * top-k ties go to the lower expert id; selected ids are listed ascending;
