@@ -699,7 +699,9 @@ def main():
         print(json.dumps(run_bw_profile(args)))
         return
     if args.mxfp4:
-        print(json.dumps(run_mx(args)))
+        # one GPU's measurement: under torchrun, rank 0 alone runs and prints it
+        if int(os.environ.get("RANK", "0")) == 0:
+            print(json.dumps(run_mx(args)))
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

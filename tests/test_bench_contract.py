@@ -50,3 +50,11 @@ def test_mxfp4_expert_bytes():
     import bench
     # three banks of H*I four-bit codes plus one E8M0 byte per 32 inputs
     assert bench.mx_expert_bytes(4096, 2048) == 3 * (4096 * 2048 // 2 + 4096 * 2048 // 32) == 13369344
+
+
+def test_mxfp4_mode_other_ranks_exit_without_work():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--mxfp4", "--steps", "1"],
+                       capture_output=True, text=True, env=env, timeout=120, cwd=ROOT)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == ""
