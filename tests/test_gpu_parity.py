@@ -566,53 +566,6 @@ def test_layer_deterministic():
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
 
 
-def _prefill_sampled(name, layer, n_experts=4, n_tokens=8, ffn_mode=moe.MOE_FFN_AUTO):
-    cfg = CONFIGS[name]
-    dc = DeviceCache(cfg, DEV)
-    dl = DeviceLayer(cfg, layer, DEV)
-    got = run_layer(dc, dl, x_dev(cfg, layer, 0), cfg.T, cfg.phi_q16, cfg.min_fill, cfg.fill_policy, 0,
-                    ffn_mode=ffn_mode)
-    assert got["status"] == 0
-    x = gen.bf16_bits_to_f64(gen.x_bits(cfg, layer, 0))
-    ids_ref, w_ref = O.select_topk(O.router_logits(x, gen.w_router(cfg, layer), gen.bias(cfg, layer, 0)), cfg.k)
-    ids = got["topk_ids"].cpu().numpy().reshape(cfg.T, cfg.k)
-    assert np.array_equal(ids, ids_ref)
-    counts, offsets, perm, inv = O.dispatch(ids_ref, cfg.E)
-    assert np.array_equal(got["counts"].cpu().numpy(), counts)
-    assert np.array_equal(got["offsets"].cpu().numpy(), offsets)
-    assert np.array_equal(got["perm"].cpu().numpy(), perm)
-    assert np.array_equal(got["inv_perm"].cpu().numpy(), inv)
-    rng = np.random.default_rng(layer)
-    y = got["y_rows"].cpu().numpy()
-    wc = ExpertCache(cfg, cap=4)
-    # every row of a few experts (the largest group, the smallest, random ones)
-    active = np.nonzero(counts)[0]
-    pick = {int(active[np.argmax(counts[active])]), int(active[np.argmin(counts[active])])}
-    pick |= set(int(e) for e in rng.choice(active, n_experts, replace=False))
-    for e in sorted(pick):
-        rows = O.expert_rows(x, ids_ref, offsets, perm, lambda ee: wc(layer, ee), [e], cfg.k)[e]
-        got_rows = y[perm[offsets[e]:offsets[e + 1]]]        # token-major rows of the expert's dispatch rows
-        assert_close(got_rows, rows, what=f"{name} layer {layer} expert {e}")
-    # layer output of sampled tokens, one by one
-    toks = rng.choice(cfg.T, n_tokens, replace=False)
-    out = bf16_to_f64(got["out"])
-    for t in toks:
-        ref_t = np.zeros(cfg.H)
-        for j, e in enumerate(ids_ref[t]):
-            wg, wu, wd = wc(layer, int(e))
-            ref_t += w_ref[t, j] * O.swiglu_expert(x[t:t + 1], wg, wu, wd)[0]
-        assert_close(out[t], ref_t, what=f"{name} token {t}")
-
-
-def test_layer_prefill_sampled():
-    _prefill_sampled("prefill", 0)
-
-
-def test_layer_long_prefill_sampled():
-    _prefill_sampled("long_prefill", 0)
-    _prefill_sampled("long_prefill", 3)
-
-
 def test_empty_calls():
     cfg = CONFIGS["tiny"]
     dc = DeviceCache(cfg, DEV)
