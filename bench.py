@@ -8,10 +8,12 @@ workload: one decode token for the default 'decode' workload (hidden 4096,
 256 experts, top-6, intermediate 2048, 37% of experts resident, LRU, Zipf(1.1)
 routing), the whole 8192-token block for 'prefill', four stacked layers for
 'long_prefill'.  Inputs are synthetic (seeded; see moe_inputs) and resident
-in HBM before the timed region; each step is a CUDA-graph replay of one
-moe_layer_forward call, timed with CUDA events on its stream, and L2 is
-flushed (256 MB write) between steps outside the events.  Prints one JSON
-line on rank 0.  --impl reference times the CPU fp64 oracle instead.
+in HBM before the timed region; each step is one moe_layer_forward call per
+layer, timed with CUDA events on its stream, and L2 is flushed (256 MB write)
+between steps outside the events.  Prints one JSON line on rank 0: the decode
+workload's figures at the top level and, as sub-records of the same line,
+the 'prefill' and 'long_prefill' workloads (at least 20 timed steps each;
+--extra selects them).  --impl reference times the CPU fp64 oracle instead.
 """
 import argparse
 import json
@@ -120,19 +122,21 @@ FFN_MODES = {"auto": lambda m: m.MOE_FFN_AUTO, "gemv": lambda m: m.MOE_FFN_GEMV,
 
 
 # ------------------------------------------------------------------ our arm
-def run_ours(args, rank, world):
-    import torch
-    import edge_moe_serving_gb300 as moe
+EXTRA_DEFAULT = "prefill,long_prefill"   # sub-records of the default (decode) line
+
+
+def run_workload(cfg, args, world, dev, stream, peaks, moe, torch):
+    """Measure one workload: ``args.warmup`` untimed steps, then ``args.steps``
+    timed steps.  A step is one moe_layer_forward call per layer of the
+    workload, launched directly on ``stream`` (the decode layer is one kernel,
+    so a graph would only add its replay); CUDA events bracket each step and
+    L2 is flushed (256 MB write) between steps, outside the events.  Returns
+    the measurement record (tokens/s, step times, the dominant kernel's
+    roofline, clocks, end to end, launch counts)."""
     from moe_inputs.device import DeviceCache, DeviceLayer, to_dev_bf16
 
-    cfg = CONFIGS[args.workload]
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
-    torch.cuda.set_device(dev)
-    peaks = load_peaks()
     decode_like = cfg.steps > 1
     n_steps = args.warmup + args.steps
-    stream = torch.cuda.Stream(device=dev)
-
     dc = DeviceCache(cfg, dev)
     layers = [DeviceLayer(cfg, l, dev) for l in range(cfg.n_layers)]
     # per-step inputs (decode: a stream of tokens; prefill: one block per layer, reused every step)
@@ -147,74 +151,57 @@ def run_ours(args, rank, world):
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stats = torch.zeros(8, dtype=torch.int32, device=dev)
-    x_in = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
-    def layer_call(l, x, s):
-        moe.moe_layer_forward(layers[l].struct, dc.struct, x, T, out, cfg.phi_q16, cfg.min_fill, cfg.fill_policy,
-                              1000 + l, mode, None, ws, ws_bytes, status, stats, s)
+    def step_body(i):
+        # decode: step i's token row; prefill: every layer's resident block
+        for l in range(cfg.n_layers):
+            moe.moe_layer_forward(layers[l].struct, dc.struct, xs[i] if decode_like else xs[l], T, out, cfg.phi_q16,
+                                  cfg.min_fill, cfg.fill_policy, 1000 + l, mode, None, ws, ws_bytes, status, stats,
+                                  stream)
 
-    def step_body(s):
-        # decode: the step's token was staged into x_in; prefill: every layer's block is resident
-        if decode_like:
-            layer_call(0, x_in, s)
-        else:
-            for l in range(cfg.n_layers):
-                layer_call(l, xs[l], s)
-
-    # one eager call sets kernel attributes and occupancy caches before capture
+    # one call sets kernel attributes and occupancy caches; then the trace starts from the initial state
     with torch.cuda.stream(stream):
-        x_in.copy_(xs[0])
-        step_body(stream)
+        step_body(0)
     torch.cuda.synchronize()
     dc.reset()
     torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    n0 = moe.moe_kernel_launch_count()
-    with torch.cuda.graph(graph, stream=stream):
-        step_body(stream)
-    torch.cuda.synchronize()
-    kernels_per_step = moe.moe_kernel_launch_count() - n0
 
     def barrier():
         if world > 1:
             import torch.distributed as dist
             dist.barrier()
 
-    # warm-up steps (untimed), then K timed steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     stats_host = torch.zeros((args.steps, 8), dtype=torch.int32).pin_memory()
     with torch.cuda.stream(stream):
         for s in range(args.warmup):
-            if decode_like:
-                x_in.copy_(xs[s])
-            graph.replay()
+            step_body(s)
             flush.zero_()
     torch.cuda.synchronize()
     barrier()
     torch.cuda.synchronize()
     clocks = ClockSampler(dev.index)
     clocks.start()
+    n0 = moe.moe_kernel_launch_count()
     t0 = time.perf_counter()
     with torch.cuda.stream(stream):
         for i in range(args.steps):
-            s = args.warmup + i
-            if decode_like:
-                x_in.copy_(xs[s])
             ev[i][0].record(stream)
-            graph.replay()
+            step_body(args.warmup + i)
             ev[i][1].record(stream)
             stats_host[i].copy_(stats, non_blocking=True)   # residency counts of the step, outside the events
             flush.zero_()
     torch.cuda.synchronize()
     barrier()
     bracket_s = time.perf_counter() - t0
+    launches = moe.moe_kernel_launch_count() - n0
     clk = clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in ev]
     total_s = sum(step_ms) / 1e3
     dev_status = int(status.cpu().numpy().view(np.uint32)[0])
-
     total_s, value = aggregate_replicas(total_s, args.steps, T, world, dev)
+    kernels_per_step = launches / args.steps
 
     # ---- dominant kernel: decode-sized calls run the whole layer as one kernel (the timed
     # step itself); otherwise the expert-FFN call, timed alone
@@ -222,25 +209,44 @@ def run_ours(args, rank, world):
         roof = decode_step_roofline(cfg, step_ms, stats_host.numpy(), peaks)
     else:
         roof = measure_ffn_roofline(cfg, dc, layers, xs, decode_like, stream, peaks, args, moe, torch)
-
-    # ---- end to end through the public call with host buffers
     e2e = measure_e2e(cfg, dc, layers, decode_like, stream, args, moe, torch, ws, ws_bytes, status, stats)
+    rec = {"value": round(value, 3), "unit": UNIT, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(total_s * 1e3 / args.steps, 5),
+           "step_ms_p10_p50_p90": [round(float(np.percentile(step_ms, q)), 5) for q in (10, 50, 90)],
+           "bracket_ms_per_step": round(bracket_s * 1e3 / args.steps, 5),
+           "config": workload_config(cfg, world), "device_status": dev_status, "roofline": roof,
+           "clocks": clk, "e2e": e2e, "gpu_launches": int(launches), "gpu_launches_per_step": kernels_per_step}
+    if not decode_like:
+        # the whole step against the bf16 tensor peak (expert FFN + router FLOPs of every layer)
+        fl = cfg.n_layers * (expert_ffn_flops(cfg) + router_flops(cfg))
+        tf = fl * args.steps / total_s / 1e12
+        rec["step_roofline"] = {"bound": "tensor", "achieved": round(tf, 2), "peak": peaks["bf16_tflops"],
+                                "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4),
+                                "flops_per_step": fl, "peak_source": peaks["source"] + " (burst cuBLAS bf16)",
+                                "note": "whole step (every launch of every layer) over the CUDA-event step time"}
+    return rec
 
-    result = {
-        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(total_s * 1e3 / args.steps, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": workload_config(cfg, world),
-        "impl": "ours",
-        "step_ms_p10_p50_p90": [round(float(np.percentile(step_ms, q)), 5) for q in (10, 50, 90)],
-        "bracket_ms_per_step": round(bracket_s * 1e3 / args.steps, 5),
-        "device_status": dev_status,
-        "roofline": roof,
-        "clocks": clk,
-        "e2e": e2e,
-        "gpu_launches": kernels_per_step * args.steps,
-        "gpu_launches_per_step": kernels_per_step,
-    }
+
+def run_ours(args, rank, world):
+    import torch
+    import edge_moe_serving_gb300 as moe
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    stream = torch.cuda.Stream(device=dev)
+    rec = run_workload(CONFIGS[args.workload], args, world, dev, stream, peaks, moe, torch)
+    result = {"metric": METRIC, "value": rec["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+              "warmup": args.warmup, "ms_per_step": rec["ms_per_step"], "higher_is_better": True,
+              "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+              "config": rec["config"], "impl": "ours"}
+    result.update({k: v for k, v in rec.items() if k not in result})
+    extras = [] if args.extra in ("", "none") else [w for w in args.extra.split(",") if w != args.workload]
+    for name in extras:
+        torch.cuda.empty_cache()
+        sub = argparse.Namespace(**vars(args))
+        sub.steps = max(args.steps, 20)
+        result[name] = run_workload(CONFIGS[name], sub, world, dev, stream, peaks, moe, torch)
     return result
 
 
@@ -264,7 +270,7 @@ def workload_config(cfg, world):
             "cache_slots": cfg.cache_slots if cfg.cache_slots is not None else cfg.n_layers * cfg.E,
             "phi_q16": cfg.phi_q16, "fill_policy": "random" if cfg.fill_policy else "lowest_id",
             "routing_bias": cfg.bias, "l2": "flushed between steps (256 MB write)",
-            "parallelism": f"replicas x{world}", "graph": "one CUDA graph replay per step"}
+            "parallelism": f"replicas x{world}", "launch": "moe_layer_forward per layer, direct launches"}
 
 
 def decode_step_roofline(cfg, step_ms, stats, peaks):
@@ -273,7 +279,7 @@ def decode_step_roofline(cfg, step_ms, stats, peaks):
     bytes per step: every distinct routed expert's weights once, one more
     expert write per cache fill, the router weights, and the activations
     (token row, h, y rows, output).  Duration: the CUDA events around the
-    step's graph replay (the kernel and its 4 + T*k word counter reset)."""
+    step (the kernel and its 4 + T*k word counter reset)."""
     T, k, E, H, I = cfg.T, cfg.k, cfg.E, cfg.H, cfg.I
     R = T * k
     n_unique, n_fill = stats[:, 0].astype(np.float64), stats[:, 4].astype(np.float64)
@@ -292,10 +298,21 @@ def decode_step_roofline(cfg, step_ms, stats, peaks):
 
 
 def ffn_bytes(cfg, active):
-    """Algorithmic HBM bytes of one expert-FFN call: each active expert's
-    weights once, the gathered token rows, h written and read, y rows written."""
+    """Algorithmic HBM bytes of one expert-FFN call, as the method counts them:
+    each active expert's weights once, the layer's token rows in and its
+    output rows out (bf16).  The intermediates are implementation traffic,
+    reported by ffn_impl_bytes and not credited."""
+    return active * cfg.expert_bytes + cfg.T * cfg.H * 2 + cfg.T * cfg.H * 2
+
+
+def ffn_impl_bytes(cfg):
+    """Intermediate bytes of the timed public FFN call (not credited): the
+    gathered token rows written and read (GEMM path), h written and read,
+    and the fp32 expert rows written (the call's output) and read back by
+    the combine."""
     R = cfg.T * cfg.k
-    return active * cfg.expert_bytes + R * cfg.H * 2 + R * cfg.I * 2 * 2 + R * cfg.H * 4
+    gather = 2 * R * cfg.H * 2 if cfg.T > 2 else 0
+    return gather + 2 * R * cfg.I * 2 + 2 * R * cfg.H * 4
 
 
 def measure_ffn_roofline(cfg, dc, layers, xs, decode_like, stream, peaks, args, moe, torch):
@@ -368,7 +385,7 @@ def measure_ffn_roofline(cfg, dc, layers, xs, decode_like, stream, peaks, args, 
             flops.append(expert_ffn_flops(cfg))
             # per-expert roofline: each group takes the longer of its bytes at the HBM peak and its
             # FLOPs at the tensor peak (weights once + its rows' activations; 2*3*H*I FLOP per row)
-            g_bytes = (cnt > 0) * cfg.expert_bytes + cnt * (cfg.H * 2 + cfg.I * 2 * 2 + cfg.H * 4)
+            g_bytes = (cnt > 0) * cfg.expert_bytes + cnt * (cfg.H * 2 + cfg.H * 2) / cfg.k
             g_flops = cnt * 2.0 * 3 * cfg.H * cfg.I
             t_mixed.append(float(np.sum(np.maximum(g_bytes / (peaks["hbm_gbs"] * 1e9),
                                                    g_flops / (peaks["bf16_tflops"] * 1e12)))))
@@ -381,7 +398,10 @@ def measure_ffn_roofline(cfg, dc, layers, xs, decode_like, stream, peaks, args, 
     t_tc = float(np.mean(flops)) / (peaks["bf16_tflops"] * 1e12)
     hbm_part = {"bound": "hbm", "achieved": round(hbm, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(hbm / peaks["hbm_gbs"], 4), "peak_source": peaks["source"] + " (burst copy bandwidth)",
-                "algorithmic_bytes_per_call": int(np.mean(byts))}
+                "algorithmic_bytes_per_call": int(np.mean(byts)),
+                "implementation_bytes_per_call": int(ffn_impl_bytes(cfg)),
+                "bytes_note": "weights of the active experts once + token rows in + output rows out; "
+                              "implementation bytes (gathered rows, h, fp32 expert rows) reported, not credited"}
     tc_part = {"bound": "tensor", "achieved": round(tc, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                "frac": round(tc / peaks["bf16_tflops"], 4), "peak_source": peaks["source"] + " (burst cuBLAS bf16)",
                "flops_per_call": float(np.mean(flops))}
@@ -392,20 +412,27 @@ def measure_ffn_roofline(cfg, dc, layers, xs, decode_like, stream, peaks, args, 
            "call_us": round(t * 1e6, 3),
            "mixed_roofline": {"min_us": round(float(np.mean(t_mixed)) * 1e6, 3),
                               "frac": round(float(np.mean(t_mixed)) / t, 4),
-                              "note": "sum over experts of max(bytes / HBM peak, FLOP / bf16 peak)"},
+                              "note": "sum over experts of max(bytes / HBM peak, FLOP / bf16 peak), "
+                                      "bytes = weights once + the group's share of token rows in and out"},
            "timing": "graph replay of the FFN call, L2 flushed before each",
            "other_roofline": other}
     return out
 
 
 def measure_e2e(cfg, dc, layers, decode_like, stream, args, moe, torch, ws, ws_bytes, status, stats):
-    """The public call with host buffers: pinned H2D of the step's tokens,
-    moe_layer_forward, D2H of the output, host waits for it; wall clock."""
+    """The public call with host buffers: pinned H2D of each layer's input
+    block (decode: the step's token), moe_layer_forward, D2H of the output,
+    and the host waits for the step's outputs; wall clock."""
     dev = ws.device
     T, H = cfg.T, cfg.H
     n = args.steps
-    host_x = [torch.from_numpy(gen.x_bits(cfg, 0, (s if decode_like else 0)).view(np.int16)).view(torch.bfloat16)
-              .pin_memory() for s in range(n if decode_like else 1)]
+    pin = lambda bits: torch.from_numpy(np.require(bits, requirements=["C", "W"]).view(np.int16)) \
+        .view(torch.bfloat16).pin_memory()
+    if decode_like:
+        host_x = [[pin(gen.x_bits(cfg, 0, s))] for s in range(n)]
+    else:
+        blocks = [pin(gen.x_bits(cfg, l, 0)) for l in range(cfg.n_layers)]
+        host_x = [blocks] * n
     host_out = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
     x_dev = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
@@ -415,17 +442,16 @@ def measure_e2e(cfg, dc, layers, decode_like, stream, args, moe, torch, ws, ws_b
     with torch.cuda.stream(stream):
         for i in range(n):
             for l in range(cfg.n_layers):
-                hx = host_x[i] if decode_like else host_x[0]
-                x_dev.copy_(hx, non_blocking=True)
+                x_dev.copy_(host_x[i][l], non_blocking=True)
                 moe.moe_layer_forward(layers[l].struct, dc.struct, x_dev, T, out, cfg.phi_q16, cfg.min_fill,
-                                      cfg.fill_policy, 1000 + l, FFN_MODES[args.ffn_mode](moe), None, ws, ws_bytes, status, stats,
-                                      stream)
+                                      cfg.fill_policy, 1000 + l, FFN_MODES[args.ffn_mode](moe), None, ws, ws_bytes,
+                                      status, stats, stream)
                 host_out.copy_(out, non_blocking=True)
             stream.synchronize()
     el = time.perf_counter() - t0
     return {"value": round(n * T / el, 3), "unit": UNIT,
             "h2d_bytes_per_step": T * H * 2 * cfg.n_layers, "d2h_bytes_per_step": T * H * 2 * cfg.n_layers,
-            "note": "moe_layer_forward per layer, not graph-captured; host waits for each step's output"}
+            "note": "moe_layer_forward per layer; host waits for each step's output"}
 
 
 # ------------------------------------------------------------------ oracle arm
@@ -449,7 +475,7 @@ def run_oracle_bounded(cfg, budget_s, max_steps=None):
     """Time the oracle on a bounded sample of the workload (whole steps)."""
     from oracle import moe_oracle as O
     n_tokens = None
-    note = "whole decode steps"
+    note = "whole steps"
     if cfg.T > 64:
         # a prefill block takes many minutes in fp64: time its first 16 tokens (same layer shape)
         n_tokens = 16
@@ -465,7 +491,30 @@ def run_oracle_bounded(cfg, budget_s, max_steps=None):
             break
     tokens = steps * (n_tokens or cfg.T)
     return {"value": round(tokens / el, 5), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{steps} step(s) of '{cfg.name}' ({note}) in {el:.1f} s, fp64 numpy, BLAS on all cores"}
+            "sample": f"{steps} step(s) of '{cfg.name}' ({note}) in {el:.1f} s, fp64 numpy, " +
+                      ("BLAS on one thread" if os.environ.get("OPENBLAS_NUM_THREADS") == "1" else "BLAS on all cores")}
+
+
+SINGLE_THREAD_WORKLOADS = ("tiny", "decode", "batched_decode")
+ONE_THREAD_ENV = {"OPENBLAS_NUM_THREADS": "1", "OMP_NUM_THREADS": "1", "MKL_NUM_THREADS": "1"}
+
+
+def run_oracle_single_thread(budget_s):
+    """The oracle on one host thread (BLAS pinned to one thread in a child
+    process) on the three small workloads: {workload: cpu_baseline record}."""
+    out = {}
+    for name in SINGLE_THREAD_WORKLOADS:
+        env = dict(os.environ, **ONE_THREAD_ENV)
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-only", "--workload", name,
+                            "--cpu-baseline-s", str(budget_s)], capture_output=True, text=True, env=env,
+                           cwd=ROOT, timeout=budget_s * 10 + 120)
+        try:
+            rec = json.loads(r.stdout.strip().splitlines()[-1])
+            rec["cores"] = 1
+            out[name] = rec
+        except (ValueError, IndexError):
+            out[name] = {"error": (r.stderr or "no output").strip().splitlines()[-1:]}
+    return out
 
 
 def run_reference(args, rank, world):
@@ -692,7 +741,17 @@ def main():
                     help="decode step with MXFP4 expert banks (route, dispatch, MXFP4 FFN, combine) instead")
     ap.add_argument("--bw-profile", action="store_true",
                     help="print the bandwidth profile of the q* split (B_P, B_H, contended pair, phi) instead")
+    ap.add_argument("--extra", default=None,
+                    help="comma-separated workloads measured as sub-records of the line "
+                         f"(default for the decode workload: {EXTRA_DEFAULT}; 'none' for none)")
+    ap.add_argument("--oracle-only", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.extra is None:
+        args.extra = EXTRA_DEFAULT if args.workload == "decode" else "none"
+    if args.oracle_only:
+        # child process of run_oracle_single_thread: the oracle alone, as its environment sets the threads
+        print(json.dumps(run_oracle_bounded(CONFIGS[args.workload], args.cpu_baseline_s)))
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.bw_profile:
@@ -719,6 +778,7 @@ def main():
     if rank == 0:
         if not args.no_cpu_baseline:
             res["cpu_baseline"] = run_oracle_bounded(CONFIGS[args.workload], args.cpu_baseline_s)
+            res["cpu_baseline"]["single_thread"] = run_oracle_single_thread(min(args.cpu_baseline_s, 5.0))
         print(json.dumps(res))
     if world > 1:
         import torch.distributed as dist

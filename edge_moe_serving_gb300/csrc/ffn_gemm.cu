@@ -30,8 +30,10 @@
 // one second of %globaltimer); on expiry the CTA sets MOE_DEV_ERR_TIMEOUT,
 // drains its in-flight copies and MMAs, frees TMEM and returns.
 #include <algorithm>
+#include <climits>
 
 #include "ffn_params.cuh"
+#include "group_prefix.cuh"
 #include "tc_common.cuh"
 
 namespace moe {
@@ -77,63 +79,6 @@ struct GemmParams {
 };
 
 // ---------------------------------------------------------------- tile list
-// s_pref[e] = first chunk index of expert e; s_pref[E] = number of chunks.
-template <int kChunk>
-__device__ void build_chunk_prefix(const GemmParams& p, int* s_pref, int* s_warp) {
-  const int tid = threadIdx.x, nthreads = blockDim.x;
-  const int per_thread = (p.E + nthreads - 1) / nthreads;
-  const int e0 = tid * per_thread;
-  int local[(kMaxE + kThreads - 1) / kThreads];
-  int sum = 0;
-  for (int u = 0; u < per_thread; ++u) {
-    const int e = e0 + u;
-    int n = 0;
-    if (e < p.E) {
-      const int cnt = p.counts[e];
-      const bool ok = cnt > p.min_rows && (p.mask == nullptr || p.mask[e] != 0);
-      n = ok ? (cnt + kChunk - 1) / kChunk : 0;
-    }
-    local[u] = n;
-    sum += n;
-  }
-  const int lane = tid & 31, warp = tid >> 5;
-  int inc = sum;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += v;
-  }
-  if (lane == 31) s_warp[warp] = inc;
-  __syncthreads();
-  if (tid == 0) {
-    int run = 0;
-    for (int w = 0; w < nthreads / 32; ++w) {
-      const int t = s_warp[w];
-      s_warp[w] = run;
-      run += t;
-    }
-    s_pref[p.E] = run;
-  }
-  __syncthreads();
-  int run = s_warp[warp] + inc - sum;
-  for (int u = 0; u < per_thread; ++u) {
-    const int e = e0 + u;
-    if (e < p.E) s_pref[e] = run;
-    run += local[u];
-  }
-  __syncthreads();
-}
-
-__device__ inline int find_owner(const int* s_pref, int E, int j) {
-  int lo = 0, hi = E - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (s_pref[mid] <= j) lo = mid;
-    else hi = mid - 1;
-  }
-  return lo;
-}
-
 struct Tile {
   int e, r0, rows, N, fb, pool, slot;
   int32_t entry;
@@ -145,7 +90,7 @@ __device__ inline Tile decode_tile(const GemmParams& p, const int* s_pref, int t
   Tile tl;
   const int ci = t / p.n_fb;
   tl.fb = t - ci * p.n_fb;
-  tl.e = find_owner(s_pref, p.E, ci);
+  tl.e = find_group(s_pref, p.E, ci);
   const int j = ci - s_pref[tl.e];
   const int cnt = p.counts[tl.e];
   tl.r0 = p.offsets[tl.e] + j * kChunk;
@@ -199,7 +144,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_b64, const __grid_constant__
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   pdl_wait();
-  build_chunk_prefix<CHUNK>(p, s_pref, s_warp);   // contains __syncthreads
+  // chunks of CHUNK rows per expert with more than min_rows rows (contains __syncthreads)
+  build_group_prefix<CHUNK, (kMaxE + kThreads - 1) / kThreads>(p.counts, p.E, p.min_rows, INT_MAX, p.mask, s_pref,
+                                                               s_warp);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

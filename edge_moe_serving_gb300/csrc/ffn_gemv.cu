@@ -58,7 +58,7 @@ gemv_kernel(GemvParams p) {
     int gsize = NTASK - n0;
     if (gsize > NG) gsize = NG;
     if (end - tau < gsize) gsize = (int)(end - tau);
-    const int e = find_expert(s_pref, p.E, j);
+    const int e = find_group(s_pref, p.E, j);
     const int c = j - s_pref[e];
     const int cnt = p.counts[e];
     const int pos0 = p.offsets[e] + c * NT;

@@ -146,7 +146,7 @@ mx_gemv_kernel(MxParams p) {
   }
   pdl_wait();
   pdl_trigger();
-  build_prefix_counts<NT>(p.counts, p.E, 0x7FFFFFFF, nullptr, s_pref, s_warp);   // ends with __syncthreads
+  build_group_prefix<NT, kMaxE / 32>(p.counts, p.E, 0, INT_MAX, nullptr, s_pref, s_warp);   // ends with __syncthreads
   const long long total = (long long)s_pref[p.E] * NTASK;
   const long long per = (total + gridDim.x - 1) / gridDim.x;
   const long long begin = (long long)blockIdx.x * per;
@@ -159,7 +159,7 @@ mx_gemv_kernel(MxParams p) {
     int gsize = NTASK - n0;
     if (gsize > NG) gsize = NG;
     if (end - tau < gsize) gsize = (int)(end - tau);
-    const int e = find_expert(s_pref, p.E, j);
+    const int e = find_group(s_pref, p.E, j);
     const int c = j - s_pref[e];
     const int cnt = p.counts[e];
     const int pos0 = p.offsets[e] + c * NT;
@@ -315,6 +315,7 @@ extern "C" int moe_expert_ffn_mxfp4(const moe_pool_mxfp4* cache_pool, const moe_
   if (!counts || !offsets || !perm || !x || !y_rows) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(y_rows)) return MOE_ERR_UNSUPPORTED;
   if (!ws || ws_bytes < mx_ws_bytes(T, k, I)) return MOE_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_UNSUPPORTED;   // h rows are read as 16-byte vectors
   MxParams p = {};
   p.a = *cache_pool;
   if (staging_opt) p.b = *staging_opt;   // else n_slots 0: staging entries read as out of range

@@ -33,6 +33,8 @@ namespace {
 constexpr int kVersion = 100;   // 1.0.0
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// workspaces are carved into 256-byte aligned regions read with vector loads
+inline bool ws_aligned(const void* ws) { return (reinterpret_cast<uintptr_t>(ws) & 255u) == 0; }
 
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
@@ -139,6 +141,24 @@ bool layer_shape_ok(const moe_layer* layer, int T) {
 }
 
 }  // namespace
+
+// Argument checks of moe_expert_ffn_grouped that precede the workspace
+// check, in the order the header lists its errors (shared with the
+// allocation-free variant, which checks its built-in scratch after them).
+int ffn_check_args(const moe_cache* cache, int layer, const int32_t* counts, const int32_t* offsets,
+                   const int32_t* perm, const void* x, const void* x_perm_opt, int T, int k, int ffn_mode,
+                   const float* y_rows) {
+  int st = check_cache(cache);
+  if (st != MOE_OK) return st;
+  if (layer < 0 || layer >= cache->n_layers || T < 0 || k < 1 || k > cache->E) return MOE_ERR_INVALID_ARG;
+  if (ffn_mode != MOE_FFN_AUTO && ffn_mode != MOE_FFN_GEMV && ffn_mode != MOE_FFN_GEMM) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!counts || !offsets || !perm || !x || !y_rows) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y_rows) || (x_perm_opt && !aligned16(x_perm_opt))) return MOE_ERR_UNSUPPORTED;
+  if (ffn_mode == MOE_FFN_GEMM && !x_perm_opt) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -174,6 +194,7 @@ int moe_route_topk(const void* x, int T, int H, const float* w_router, const flo
   if (E > kMaxRouteE || (H % 8) || !aligned16(x) || !aligned16(w_router)) return MOE_ERR_UNSUPPORTED;
   const size_t need = route_ws_bytes(T, H, E);
   if (need && (!ws || ws_bytes < need)) return MOE_ERR_WORKSPACE;
+  if (need && !ws_aligned(ws)) return MOE_ERR_UNSUPPORTED;
   return cuda_status(launch_route_topk(reinterpret_cast<const __nv_bfloat16*>(x), T, H, w_router, bias, E, k,
                                        topk_ids, topk_w, logits_opt, ws, dev_status,
                                        reinterpret_cast<cudaStream_t>(stream)));
@@ -195,6 +216,7 @@ int moe_dispatch(const int32_t* topk_ids, int T, int k, int E, int32_t* counts, 
     return MOE_ERR_UNSUPPORTED;
   const size_t need = dispatch_ws_bytes(T, k, E);
   if (need && (!ws || ws_bytes < need)) return MOE_ERR_WORKSPACE;
+  if (need && !ws_aligned(ws)) return MOE_ERR_UNSUPPORTED;
   return cuda_status(launch_dispatch(topk_ids, T * k, k, E, counts, offsets, perm, inv_perm,
                                      reinterpret_cast<const __nv_bfloat16*>(x_opt), H,
                                      reinterpret_cast<__nv_bfloat16*>(x_perm_opt), ws, dev_status,
@@ -215,6 +237,7 @@ int moe_cache_bind_slots(const moe_cache* cache, int layer, const int32_t* topk_
   if (T > 0 && !topk_ids) return MOE_ERR_INVALID_ARG;
   const size_t need = bind_ws_bytes(T, k, cache->E);
   if (!ws || ws_bytes < need) return MOE_ERR_WORKSPACE;
+  if (!ws_aligned(ws)) return MOE_ERR_UNSUPPORTED;
   return cuda_status(launch_bind(*cache, layer, topk_ids, T * k, phi_q16, min_fill, fill_policy, seed,
                                  stats_dev, fills_opt, ws, dev_status, reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -228,16 +251,11 @@ int moe_expert_ffn_grouped(const moe_cache* cache, int layer, const int32_t* cou
                            const int32_t* perm, const void* x, const void* x_perm_opt, int T, int k,
                            const uint8_t* expert_mask_opt, int ffn_mode, float* y_rows, void* ws,
                            size_t ws_bytes, uint32_t* dev_status, moe_stream_t stream) {
-  int st = check_cache(cache);
-  if (st != MOE_OK) return st;
-  if (layer < 0 || layer >= cache->n_layers || T < 0 || k < 1 || k > cache->E) return MOE_ERR_INVALID_ARG;
-  if (ffn_mode != MOE_FFN_AUTO && ffn_mode != MOE_FFN_GEMV && ffn_mode != MOE_FFN_GEMM) return MOE_ERR_INVALID_ARG;
-  if (T == 0) return MOE_OK;
-  if (!counts || !offsets || !perm || !x || !y_rows) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(y_rows) || (x_perm_opt && !aligned16(x_perm_opt))) return MOE_ERR_UNSUPPORTED;
-  if (ffn_mode == MOE_FFN_GEMM && !x_perm_opt) return MOE_ERR_INVALID_ARG;
+  const int st = ffn_check_args(cache, layer, counts, offsets, perm, x, x_perm_opt, T, k, ffn_mode, y_rows);
+  if (st != MOE_OK || T == 0) return st;
   const size_t need = ffn_ws_bytes(T, k, cache->E, cache->H, cache->I, ffn_mode);
   if (!ws || ws_bytes < need) return MOE_ERR_WORKSPACE;
+  if (!ws_aligned(ws)) return MOE_ERR_UNSUPPORTED;
   cudaError_t err = launch_ffn(*cache, layer, counts, offsets, perm, reinterpret_cast<const __nv_bfloat16*>(x),
                                reinterpret_cast<const __nv_bfloat16*>(x_perm_opt), T, k, expert_mask_opt,
                                ffn_mode, y_rows, ws, dev_status, reinterpret_cast<cudaStream_t>(stream));
@@ -276,6 +294,7 @@ int moe_layer_forward(const moe_layer* layer, const moe_cache* cache, const void
   if (!x || !out) return MOE_ERR_INVALID_ARG;
   const LayerWs need = layer_ws(nullptr, nullptr, T, k, E, H, I, ffn_mode);
   if (!ws || ws_bytes < need.bytes) return MOE_ERR_WORKSPACE;
+  if (!ws_aligned(ws)) return MOE_ERR_UNSUPPORTED;
   const LayerWs L = layer_ws(ws, bufs_opt, T, k, E, H, I, ffn_mode);
   const size_t scratch_bytes = ws_bytes - (size_t)(reinterpret_cast<char*>(L.scratch) - reinterpret_cast<char*>(ws));
   const bool fuse_fill = ffn_mode != MOE_FFN_GEMM && !L.x_perm && gemv_fused_ok(H, I);

@@ -393,6 +393,9 @@ cudaError_t launch_bind(const moe_cache& c, int layer, const int32_t* ids, int R
                         int32_t* offsets = nullptr, int32_t* perm = nullptr, int32_t* inv_perm = nullptr);
 
 size_t ffn_ws_bytes(int T, int k, int E, int H, int I, int mode);
+int ffn_check_args(const moe_cache* cache, int layer, const int32_t* counts, const int32_t* offsets,
+                   const int32_t* perm, const void* x, const void* x_perm_opt, int T, int k, int ffn_mode,
+                   const float* y_rows);
 bool gemm_shape_ok(int H, int I);
 cudaError_t launch_ffn(const moe_cache& c, int layer, const int32_t* counts, const int32_t* offsets,
                        const int32_t* perm, const __nv_bfloat16* x, const __nv_bfloat16* x_perm,

@@ -5,6 +5,7 @@
 #pragma once
 
 #include "ffn_params.cuh"
+#include "group_prefix.cuh"
 
 namespace moe {
 namespace {
@@ -13,56 +14,8 @@ namespace {
 // only: 0 < counts[e] <= max_rows and mask[e] != 0 when a mask is given).
 // Needs blockDim.x >= 32 and E <= kMaxE.
 template <int NT>
-__device__ void build_prefix_counts(const int32_t* counts, int E, int max_rows, const uint8_t* mask, int* s_pref,
-                                    int* s_warp) {
-  const int tid = threadIdx.x, nthreads = blockDim.x;
-  const int per_thread = (E + nthreads - 1) / nthreads;
-  const int e0 = tid * per_thread;
-  int local[kMaxE / 32];
-  int sum = 0;
-  for (int u = 0; u < per_thread; ++u) {
-    const int e = e0 + u;
-    int n = 0;
-    if (e < E) {
-      const int cnt = counts[e];
-      const bool ok = cnt > 0 && cnt <= max_rows && (mask == nullptr || mask[e] != 0);
-      n = ok ? (cnt + NT - 1) / NT : 0;
-    }
-    local[u] = n;
-    sum += n;
-  }
-  // exclusive scan of per-thread sums
-  const int lane = tid & 31, warp = tid >> 5;
-  int inc = sum;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int n = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += n;
-  }
-  if (lane == 31) s_warp[warp] = inc;
-  __syncthreads();
-  if (tid == 0) {
-    int run = 0;
-    for (int w = 0; w < nthreads / 32; ++w) {
-      const int t = s_warp[w];
-      s_warp[w] = run;
-      run += t;
-    }
-    s_pref[E] = run;
-  }
-  __syncthreads();
-  int run = s_warp[warp] + inc - sum;
-  for (int u = 0; u < per_thread; ++u) {
-    const int e = e0 + u;
-    if (e < E) s_pref[e] = run;
-    run += local[u];
-  }
-  __syncthreads();
-}
-
-template <int NT>
 __device__ void build_prefix(const GemvParams& p, int* s_pref, int* s_warp) {
-  build_prefix_counts<NT>(p.counts, p.E, p.max_rows, p.mask, s_pref, s_warp);
+  build_group_prefix<NT, kMaxE / 32>(p.counts, p.E, 0, p.max_rows, p.mask, s_pref, s_warp);
 }
 
 // Warp reduce-scatter of N (power of two >= 32) values: afterwards lane l
@@ -80,17 +33,6 @@ __device__ inline void warp_reduce_scatter(float (&v)[N]) {
       v[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
     }
   }
-}
-
-// largest e with s_pref[e] <= j < s_pref[e + 1]
-__device__ inline int find_expert(const int* s_pref, int E, int j) {
-  int lo = 0, hi = E - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (s_pref[mid] <= j) lo = mid;
-    else hi = mid - 1;
-  }
-  return lo;
 }
 
 // Where instance j of a fused launch reads and writes: its expert, the
@@ -112,13 +54,13 @@ struct PrefixInsts {
   int E;
   __device__ int count() const { return pref[E]; }
   __device__ InstInfo get(int j) const {
-    const int e = find_expert(pref, E, j);
+    const int e = find_group(pref, E, j);
     const int c = j - pref[e];
     return {e, ent[e], fill[e], off[e] + c * NT, min(NT, counts[e] - c * NT)};
   }
   // what the weight stream needs: the expert, its entry and fill destination
   __device__ void source(int j, int& e, int& entry, int& fill_dst) const {
-    e = find_expert(pref, E, j);
+    e = find_group(pref, E, j);
     entry = ent[e];
     fill_dst = fill[e];
   }

@@ -34,7 +34,8 @@
  * Workspace.  Calls that need scratch take (ws, ws_bytes): a device buffer of
  *             at least the size the matching *_workspace_size() reports,
  *             256-byte aligned, with no content requirement.  A call that
- *             gets a smaller ws returns MOE_ERR_WORKSPACE without launching.
+ *             gets a smaller ws returns MOE_ERR_WORKSPACE, and one whose ws
+ *             is not 256-byte aligned MOE_ERR_UNSUPPORTED, without launching.
  *             Calls sharing one ws must not overlap on the GPU.
  */
 #ifndef MOE_H_
@@ -302,15 +303,17 @@ int moe_expert_ffn_grouped(const moe_cache* cache, int layer, const int32_t* cou
  * offers no allocator, a service running on a memory budget fixed at load
  * time, or a serving loop that must not call cudaMalloc/cudaFree because they
  * can synchronise the device.  The paper has no counterpart to this call.
- * Same arguments, results and errors as moe_expert_ffn_grouped; the scratch
- * is a static array of MOE_NOALLOC_FFN_SCRATCH_BYTES inside the library, held
- * by every device that loads it until the process exits.  Returns
+ * Same arguments, results and errors as moe_expert_ffn_grouped, checked in
+ * the same order; the scratch is a static array of
+ * MOE_NOALLOC_FFN_SCRATCH_BYTES inside the library, held by every device that
+ * loads it until the process exits.  After the argument checks, returns
  * MOE_ERR_WORKSPACE when the call would need more than that
  * (moe_expert_ffn_workspace_size(T, k, E, H, I, ffn_mode) bytes).  The first
- * call on a device looks up the array's device address with that device
- * current; make that first call before any stream capture.  All calls on a
- * device share the array, so calls that overlap on the GPU race; the array
- * needs no clearing between calls.  Allocates nothing. */
+ * call in a CUDA context (on each device, and again after a device reset)
+ * looks up the array's device address with that device current; make that
+ * first call before any stream capture.  All calls on a device share the
+ * array, so calls that overlap on the GPU race; the array needs no clearing
+ * between calls.  Allocates nothing. */
 int moe_expert_ffn_grouped_noalloc(const moe_cache* cache, int layer, const int32_t* counts,
                                    const int32_t* offsets, const int32_t* perm, const void* x,
                                    const void* x_perm_opt, int T, int k,

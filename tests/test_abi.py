@@ -124,6 +124,7 @@ def test_mxfp4_ffn_argument_checks():
     assert call(*args(pool, E=2000)) == moe.MOE_ERR_UNSUPPORTED
     assert call(*args(pool, x=24)) == moe.MOE_ERR_UNSUPPORTED         # x not 16-byte aligned
     assert call(*args(pool, ws_bytes=64)) == moe.MOE_ERR_WORKSPACE
+    assert call(*args(pool)) == moe.MOE_ERR_UNSUPPORTED               # ws (16) not 256-byte aligned
     bad = moe.moe_pool_mxfp4(24, 1, 16, 1, 16, 1, 4, 0)              # misaligned code bank
     assert call(*args(bad)) == moe.MOE_ERR_UNSUPPORTED
     empty = moe.moe_pool_mxfp4(16, None, 16, 1, 16, 1, 4, 0)         # missing scale bank
@@ -131,6 +132,40 @@ def test_mxfp4_ffn_argument_checks():
     assert call(None, None, 16, 1, 0, 8, 64, 64, 16, 16, 16, 16, 4, 2, 16, 16, 1 << 20, None,
                 None) == moe.MOE_ERR_INVALID_ARG
 
+
+def test_ffn_argument_checks_and_the_allocation_free_variant():
+    """The bf16 expert FFN's host checks, and the allocation-free variant's:
+    the same argument checks in the same order, then its scratch limit."""
+    L = moe.lib()
+    c = moe.moe_cache()
+    c.cache = moe.moe_pool(256, 256, 256, 4)                          # fake non-null pointers: never dereferenced
+    c.slot_table, c.owner, c.stamp, c.clock = 256, 256, 256, 256
+    c.n_layers, c.E, c.H, c.I = 1, 8, 64, 64
+    ffn = lambda c, T=4, k=2, mode=moe.MOE_FFN_AUTO, ws=256, ws_bytes=1 << 30, x=256, y=256, layer=0: \
+        L.moe_expert_ffn_grouped(ctypes.byref(c), layer, 256, 256, 256, x, None, T, k, None, mode, y, ws, ws_bytes,
+                                 None, None)
+    na = lambda c, T=4, k=2, mode=moe.MOE_FFN_AUTO, x=256, y=256, layer=0, counts=256: \
+        L.moe_expert_ffn_grouped_noalloc(ctypes.byref(c), layer, counts, 256, 256, x, None, T, k, None, mode, y, None,
+                                         None)
+    for call in (ffn, na):
+        assert call(c, T=0) == moe.MOE_OK
+        assert call(c, k=9) == moe.MOE_ERR_INVALID_ARG                 # k > E
+        assert call(c, layer=1) == moe.MOE_ERR_INVALID_ARG             # layer out of range
+        assert call(c, mode=7) == moe.MOE_ERR_INVALID_ARG              # unknown kernel choice
+        assert call(c, x=None) == moe.MOE_ERR_INVALID_ARG
+        assert call(c, y=264) == moe.MOE_ERR_UNSUPPORTED               # y rows not 16-byte aligned
+        assert call(c, mode=moe.MOE_FFN_GEMM) == moe.MOE_ERR_INVALID_ARG   # the GEMM needs the gathered rows
+    assert ffn(c, ws_bytes=64) == moe.MOE_ERR_WORKSPACE
+    assert ffn(c, ws=272) == moe.MOE_ERR_UNSUPPORTED                  # ws not 256-byte aligned
+    # beyond the built-in scratch: the workspace error comes after the argument checks
+    big = 1 << 16
+    assert moe.moe_expert_ffn_workspace_size(big, 2, 8, 64, 64, moe.MOE_FFN_AUTO) > moe.MOE_NOALLOC_FFN_SCRATCH_BYTES
+    assert na(c, T=big) == moe.MOE_ERR_WORKSPACE
+    assert na(c, T=big, counts=None) == moe.MOE_ERR_INVALID_ARG
+    assert na(c, T=big, k=9) == moe.MOE_ERR_INVALID_ARG
+    nopool = moe.moe_cache()
+    nopool.n_layers, nopool.E, nopool.H, nopool.I = 1, 8, 64, 64
+    assert na(nopool, T=big) == moe.MOE_ERR_INVALID_ARG
 
 
 STRUCTS = ["moe_pool", "moe_cache", "moe_bind_stats", "moe_layer", "moe_layer_buffers", "moe_bw_profile",

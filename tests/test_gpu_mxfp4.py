@@ -137,3 +137,55 @@ def test_mxfp4_ffn_empty_call_launches_nothing():
     moe.moe_expert_ffn_mxfp4(pool.struct, None, torch.zeros(8, dtype=torch.int32, device=DEV), 1, 0, 8, 64, 64,
                              None, None, None, None, 0, 2, None, None, 0, None)
     assert moe.moe_kernel_launch_count() == before
+
+
+def test_mxfp4_ffn_special_block_scales():
+    """E8M0 scales 0 (2^-127), 254 (2^127) and 255 (NaN) of the OCP MX
+    encoding.  Inputs 0..31 of the token rows are about 2^120 and inputs
+    32..63 about 2^-132, and every gate and up row scales those blocks by
+    2^-127 and 2^127, so both contribute order-one terms; the other blocks
+    are ordinary.  One gate row of expert 0 has a NaN block scale, which makes
+    every output of its token NaN; one down row of expert 1 has a NaN scale,
+    which makes one output element of the other token NaN.  Everything else
+    matches the oracle's fp64 dequantisation."""
+    T, k, E, H, I = 2, 1, 2, 128, 64
+    rng = np.random.default_rng(77)
+    experts = {}
+    for e in range(E):
+        gq, gs, uq, us, dq, ds = (np.array(a) for a in gen.mx_expert(SEED, 0, e, H, I))
+        for s in (gs, us):
+            s[:, 0] = 0          # 2^-127 on inputs 0..31
+            s[:, 1] = 254        # 2^127 on inputs 32..63
+        if e == 0:
+            gs[3, 2] = 255       # NaN: gate row 3 of expert 0
+        else:
+            ds[5, 0] = 255       # NaN: down row 5 of expert 1
+        experts[e] = (gq, gs, uq, us, dq, ds)
+    xf = rng.standard_normal((T, H)).astype(np.float32)
+    xf[:, :32] *= np.float32(2.0 ** 120)
+    xf[:, 32:64] *= np.float32(2.0 ** -132)
+    x_bits = gen.f32_to_bf16_bits(xf)
+    ids = np.array([[0], [1]], np.int32)
+    counts, offsets, perm, _ = O.dispatch(ids, E)
+    pool = MxPool(E, H, I, experts, DEV)
+    dev_i32 = lambda a: torch.from_numpy(np.asarray(a, np.int32)).to(DEV)
+    x = torch.from_numpy(x_bits.view(np.int16)).to(DEV).view(torch.bfloat16)
+    y = torch.zeros((T * k, H), dtype=torch.float32, device=DEV)
+    nb = moe.moe_expert_ffn_mxfp4_workspace_size(T, k, I)
+    st = status()
+    moe.moe_expert_ffn_mxfp4(pool.struct, None, dev_i32(np.arange(E)), 1, 0, E, H, I, dev_i32(counts),
+                             dev_i32(offsets), dev_i32(perm), x, T, k, y, ws(nb), nb, st)
+    torch.cuda.synchronize()
+    assert status_bits(st) == 0
+    got = y.cpu().numpy().astype(np.float64)
+    xd = gen.bf16_bits_to_f64(x_bits)
+    ref = np.stack([O.swiglu_expert(xd[t][None, :], *O.mx_expert_weights(*experts[int(ids[t, 0])]))[0]
+                    for t in range(T)])
+    assert np.isnan(ref[0]).all() and np.isnan(got[0]).all()
+    nan1 = np.isnan(ref[1])
+    assert nan1.tolist() == [c == 5 for c in range(H)]
+    assert np.array_equal(np.isnan(got[1]), nan1)
+    # the rescaled blocks carry real terms: dropping the 2^-127 block moves the reference by 16% (relative
+    # Frobenius), the 2^127 block by 98%, both far beyond the tolerance
+    assert np.abs(ref[1][~nan1]).max() > 0.05
+    assert_close(got[1][~nan1], ref[1][~nan1], what="mxfp4 rows with block scales 0 and 254")

@@ -68,11 +68,18 @@ def test_noalloc_matches_workspace_entry_point_twice():
 
 def test_noalloc_rejects_calls_beyond_its_scratch():
     cfg = CONFIGS["batched_decode"]
+    dc = DeviceCache(cfg, DEV)
     T = 4096                                  # h would need 4096*8*768*2 bytes > 4 MiB
     assert moe.moe_expert_ffn_workspace_size(T, cfg.k, cfg.E, cfg.H, cfg.I, moe.MOE_FFN_AUTO) > \
         moe.MOE_NOALLOC_FFN_SCRATCH_BYTES
-    c = moe.moe_cache()
-    c.E, c.H, c.I, c.n_layers = cfg.E, cfg.H, cfg.I, 1
-    rc = moe.lib().moe_expert_ffn_grouped_noalloc(c, 0, None, None, None, None, None, T, cfg.k, None,
-                                                  moe.MOE_FFN_AUTO, None, None, None)
+    R = T * cfg.k
+    i32 = torch.zeros(R + cfg.E + 1, dtype=torch.int32, device=DEV)
+    x = torch.zeros((T, cfg.H), dtype=torch.bfloat16, device=DEV)
+    y = torch.zeros((R, cfg.H), dtype=torch.float32, device=DEV)
+    st = status()
+    rc = moe.lib().moe_expert_ffn_grouped_noalloc(dc.struct, 0, i32.data_ptr(), i32.data_ptr(), i32.data_ptr(),
+                                                  x.data_ptr(), None, T, cfg.k, None, moe.MOE_FFN_AUTO,
+                                                  y.data_ptr(), st.data_ptr(), None)
     assert rc == moe.MOE_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert status_bits(st) == 0 and not y.any()   # nothing was launched
