@@ -12,8 +12,8 @@ in HBM before the timed region; each step is one moe_layer_forward call per
 layer, timed with CUDA events on its stream, and L2 is flushed (256 MB write)
 between steps outside the events.  Prints one JSON line on rank 0: the decode
 workload's figures at the top level and, as sub-records of the same line,
-the 'prefill' and 'long_prefill' workloads (at least 20 timed steps each;
---extra selects them).  --impl reference times the CPU fp64 oracle instead.
+the 'prefill' and 'long_prefill' workloads and the decode step with MXFP4
+experts 'decode_mxfp4' (at least 20 timed steps each; --extra selects them).  --impl reference times the CPU fp64 oracle instead.
 """
 import argparse
 import json
@@ -122,7 +122,7 @@ FFN_MODES = {"auto": lambda m: m.MOE_FFN_AUTO, "gemv": lambda m: m.MOE_FFN_GEMV,
 
 
 # ------------------------------------------------------------------ our arm
-EXTRA_DEFAULT = "prefill,long_prefill"   # sub-records of the default (decode) line
+EXTRA_DEFAULT = "prefill,long_prefill,decode_mxfp4"   # sub-records of the default (decode) line
 
 
 def run_workload(cfg, args, world, dev, stream, peaks, moe, torch):
@@ -246,7 +246,14 @@ def run_ours(args, rank, world):
         torch.cuda.empty_cache()
         sub = argparse.Namespace(**vars(args))
         sub.steps = max(args.steps, 20)
-        result[name] = run_workload(CONFIGS[name], sub, world, dev, stream, peaks, moe, torch)
+        if name == "decode_mxfp4":
+            sub.no_cpu_baseline = True
+            rec = run_mx(sub)
+            result[name] = {k: v for k, v in rec.items()
+                            if k not in ("metric", "n_gpus", "higher_is_better", "scaling", "vs_baseline", "data",
+                                         "impl")}
+        else:
+            result[name] = run_workload(CONFIGS[name], sub, world, dev, stream, peaks, moe, torch)
     return result
 
 
@@ -700,12 +707,14 @@ def run_mx(args):
         "step_ms_p10_p50_p90": [round(float(np.percentile(step_ms, q)), 5) for q in (10, 50, 90)],
         "bracket_ms_per_step": round(bracket_s * 1e3 / args.steps, 5),
         "device_status": dev_status,
-        "roofline": {"kernel": "mx_gemv_kernel gate/up + down (the expert FFN call)", "bound": "hbm",
+        "roofline": {"kernel": "mx_ring_kernel (the expert FFN call: gate/up and down in one weight-streaming launch)",
+                     "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 3), "traffic": None,
                      "peak_source": f"{peaks['source']} (burst copy bandwidth)",
                      "algorithmic_bytes_per_call": alg, "ffn_us": round(ffn_avg_s * 1e6, 3),
-                     "timing": "CUDA events around the FFN graph (two kernels), L2 flushed before each call"},
+                     "timing": "CUDA events around the FFN graph (counter reset + one kernel), L2 flushed before "
+                               "each call"},
         "clocks": clk,
         "e2e": {"value": round(args.steps * T / e2e_s, 3), "unit": UNIT, "h2d_bytes_per_step": T * H * 2,
                 "d2h_bytes_per_step": T * H * 2,

@@ -161,9 +161,11 @@ __device__ inline void router_rows(const DecodeParams& d, const float* wrow, con
 template <int NT, int VA, int VB>
 __global__ void __launch_bounds__(kRingThreads, 1)
 decode_layer_kernel(DecodeParams d, unsigned int* grid_count) {
-  extern __shared__ uint8_t ring_raw[];
+  extern __shared__ __align__(128) uint8_t ring_raw[];
   __shared__ DecodeShared sh;
-  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ring_raw) + 127) & ~uintptr_t(127));
+  // the ring is the dynamic shared array itself: pointers derived from it keep the shared
+  // address space, so stage reads compile to shared-memory loads
+  uint8_t* ring = ring_raw;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   GemvParams p = d.g;
   const int E = p.E, H = p.H, T = p.T, G = gridDim.x, b = blockIdx.x;

@@ -151,9 +151,11 @@ gemv_kernel(GemvParams p) {
 template <int NT, int VA, int VB>
 __global__ void __launch_bounds__(kRingThreads, 1)
 gemv_fused_kernel(GemvParams p, unsigned int* grid_count) {
-  extern __shared__ uint8_t ring_raw[];
+  extern __shared__ __align__(128) uint8_t ring_raw[];
   __shared__ __align__(16) FusedShared fs;
-  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ring_raw) + 127) & ~uintptr_t(127));
+  // the ring is the dynamic shared array itself: pointers derived from it keep the shared
+  // address space, so stage reads compile to shared-memory loads
+  uint8_t* ring = ring_raw;
   const int tid = threadIdx.x, lane = tid & 31;
   if (tid == 0) ring_init(fs.r);
   pdl_wait();

@@ -1,5 +1,7 @@
-// Grouped expert FFN over block-scaled FP4 (MXFP4) expert banks, for
-// decode-sized groups (FreeToken paper, section 5.1 "Models": the routed
+// Grouped expert FFN over block-scaled FP4 (MXFP4) expert banks: the entry
+// point, and the table-decode kernel for calls of more than one token (one-
+// token calls of qualifying shapes run on the ring kernel, ffn_mxfp4_ring.cu),
+// for decode-sized groups (FreeToken paper, section 5.1 "Models": the routed
 // experts of DeepSeek-V4-Flash are natively MXFP4; section 4.1: the expert
 // kernels dequantise in-kernel; section 3.2: grouped evaluation through the
 // (layer, expert) slot).  Encoding (OCP Microscaling Formats v1.0): FP4 E2M1
@@ -18,27 +20,15 @@
 // 32 products are summed in fp32 and then scaled by the block's power of two
 // (exact), so the result is the dot product with the dequantised row up to
 // fp32 summation order.
+#include <climits>
+
+#include "mxfp4.cuh"
 #include "ring_gemv.cuh"
 
 namespace moe {
 namespace {
 
 constexpr int kMxThreadsMax = 256;
-constexpr int kMxBlock = 32;   // inputs per E8M0 scale = one 16-byte code vector
-
-struct MxParams {
-  moe_pool_mxfp4 a;   // cache pool
-  moe_pool_mxfp4 b;   // staging pool (n_slots 0 when absent)
-  const int32_t* slot_table;
-  int layer, E, H, I, k;
-  const int32_t* counts;
-  const int32_t* offsets;
-  const int32_t* perm;
-  const __nv_bfloat16* x;
-  __nv_bfloat16* h;   // [R, I] by dispatch position
-  float* y;           // [R, H] token-major
-  uint32_t* status;
-};
 
 // FP4 E2M1 magnitudes by the low three code bits (the element table of the
 // OCP MX specification); bit 3 is the sign.
@@ -52,49 +42,6 @@ __device__ inline float e2m1(uint32_t c) {
   if (m == 6u) v = 4.0f;
   if (m == 7u) v = 6.0f;
   return (c & 8u) ? -v : v;
-}
-
-// E8M0 scale 2^(s - 127) as fp32 bits: s = 0 is the subnormal 2^-127, s = 255 NaN.
-__device__ inline float e8m0(uint32_t s) {
-  return __uint_as_float(s == 0u ? 0x00400000u : (s == 255u ? 0x7FC00000u : s << 23));
-}
-
-struct MxRows {
-  const uint8_t* q0;
-  const uint8_t* s0;
-  const uint8_t* q1;
-  const uint8_t* s1;
-};
-
-// Slot-table entry -> the slot's code and scale rows of one projection
-// (gate and up, or down twice).
-template <bool GATEUP>
-__device__ inline bool mx_resolve(const MxParams& p, int32_t entry, MxRows* out, uint32_t* status) {
-  if (entry < 0) {
-    set_status(status, MOE_DEV_ERR_UNBOUND);
-    return false;
-  }
-  const moe_pool_mxfp4& pool = (entry & MOE_STAGING_TAG) ? p.b : p.a;
-  const int32_t slot = entry & MOE_SLOT_MASK;
-  if ((entry & ~(MOE_STAGING_TAG | MOE_SLOT_MASK)) != 0 || slot >= pool.n_slots) {
-    set_status(status, MOE_DEV_ERR_BAD_SLOT);
-    return false;
-  }
-  const size_t rows = GATEUP ? (size_t)p.I : (size_t)p.H;   // output rows per slot
-  const size_t K = GATEUP ? (size_t)p.H : (size_t)p.I;       // inputs per row
-  const size_t qper = rows * (K / 2), sper = rows * (K / kMxBlock);
-  if (GATEUP) {
-    out->q0 = reinterpret_cast<const uint8_t*>(pool.gate_q) + (size_t)slot * qper;
-    out->s0 = reinterpret_cast<const uint8_t*>(pool.gate_s) + (size_t)slot * sper;
-    out->q1 = reinterpret_cast<const uint8_t*>(pool.up_q) + (size_t)slot * qper;
-    out->s1 = reinterpret_cast<const uint8_t*>(pool.up_s) + (size_t)slot * sper;
-  } else {
-    out->q0 = reinterpret_cast<const uint8_t*>(pool.down_q) + (size_t)slot * qper;
-    out->s0 = reinterpret_cast<const uint8_t*>(pool.down_s) + (size_t)slot * sper;
-    out->q1 = out->q0;
-    out->s1 = out->s0;
-  }
-  return true;
 }
 
 // Four code bytes (one 32-bit word: 8 inputs) -> 8 bf16 weights through the
@@ -283,7 +230,10 @@ int check_mx_pool(const moe_pool_mxfp4* pool) {
   return MOE_OK;
 }
 
-size_t mx_ws_bytes(int T, int k, int I) { return align_up((size_t)T * k * I * sizeof(__nv_bfloat16), 256); }
+// h rows (bf16 [T*k, I]), then the ring kernel's per-instance counters
+size_t mx_ws_bytes(int T, int k, int I) {
+  return align_up((size_t)T * k * I * sizeof(__nv_bfloat16), 256) + align_up((size_t)T * k * sizeof(unsigned int), 256);
+}
 
 }  // namespace
 }  // namespace moe
@@ -330,11 +280,14 @@ extern "C" int moe_expert_ffn_mxfp4(const moe_pool_mxfp4* cache_pool, const moe_
   p.perm = perm;
   p.x = reinterpret_cast<const __nv_bfloat16*>(x);
   p.h = reinterpret_cast<__nv_bfloat16*>(ws);
+  p.inst_done = reinterpret_cast<unsigned int*>(reinterpret_cast<char*>(ws) +
+                                                align_up((size_t)T * k * I * sizeof(__nv_bfloat16), 256));
   p.y = y_rows;
   p.status = dev_status;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t err;
-  if (T <= 1) err = launch_mx_nt<1>(p, s);
+  if (mx_ring_ok(p, T)) err = launch_mx_ring(p, T, s);
+  else if (T <= 1) err = launch_mx_nt<1>(p, s);
   else if (T <= 2) err = launch_mx_nt<2>(p, s);
   else err = launch_mx_nt<4>(p, s);
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;

@@ -1,0 +1,421 @@
+// MXFP4 expert FFN for one-token calls: a weight-streaming ring kernel
+// (FreeToken paper, section 3.2: grouped evaluation of the GPU execution set
+// through the (layer, expert) slot; section 4.1: expert kernels dequantise
+// in-kernel; section 5.1: DeepSeek-V4-Flash's routed experts are MXFP4).
+//
+// One launch, one CTA per SM.  A producer thread streams "units" (a few
+// consecutive weight rows: their FP4 code bytes and E8M0 scale bytes) into a
+// ring of shared-memory stages with cp.async.bulk (L2 evict-first: weights
+// are read once per call); six consumer warps each reduce every sixth unit.  Phase A streams gate and up rows and writes h = bf16(silu(g) * u);
+// phase B streams down rows and writes y.  Per-instance counters let a
+// consumer start the down rows of an expert as soon as every CTA finished its
+// gate/up rows of that expert, while the producer keeps streaming.
+//
+// Arithmetic of one 32-input block (16 code bytes, one scale s):
+//   * the token's activations of the block are rescaled once per call by a
+//     power of two g (largest magnitude into [2^7, 2^8)) and rounded to f16,
+//     exact for every element within 2^22 of the block's largest;
+//   * the hardware converts each code byte to two f16 E2M1 values (exact);
+//   * f16 x f16 products are exact in fp32 and are accumulated in fp32;
+//   * the block's sum is multiplied by 2^(s - 127) / g (exact: a power of
+//     two) and added to the row's fp32 accumulator.
+// So the result is the dot product with the dequantised row up to fp32
+// summation order, for any E8M0 scale including 2^-127, 2^127 and NaN.
+#include <climits>
+
+#include "mxfp4.cuh"
+#include "ring_gemv.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kMxStages = 6;   // ~100 KB in flight per SM: the first stage lands sooner than with 12 (measured)
+constexpr int kMxCodeBytes = 16384;     // code bytes per stage (both banks of a gate/up unit)
+constexpr int kMxScaleOff = 16384;      // scale bytes follow the codes
+constexpr int kMxStageBytes = 17408;    // 16 KB of codes + 1 KB of scales
+constexpr int kMxCW = 6;                // consumer warps (one stage each)
+constexpr int kMxThreads = (kMxCW + 1) * 32;
+constexpr int kMxSmem = kMxStages * kMxStageBytes + 128;
+static_assert(kMxStages % kMxCW == 0, "each ring stage must have one consumer warp");
+static_assert(kMxStageBytes % 128 == 0, "stages stay 128-byte aligned");
+
+// Rows per unit: gate/up units hold U rows of each bank (U * K/2 code bytes
+// per bank), down units U rows; at most 16.
+__host__ __device__ inline int mx_rows_gateup(int H) { return min(16, kMxCodeBytes / H); }
+__host__ __device__ inline int mx_rows_down(int I) { return min(16, 2 * kMxCodeBytes / I); }
+
+// The token's activations of the V blocks a lane owns (blocks lane + 32c,
+// inputs 32v .. 32v+31), rescaled by a power of two per block and rounded to
+// f16: a[c][i] holds inputs 32v + 2i (low half) and 32v + 2i + 1 (high
+// half); inv[c] is the block's back-scale 1/g.
+template <int V>
+struct ActRegs {
+  uint32_t a[V][16];
+  float inv[V];
+};
+
+__device__ inline uint32_t bf16_exp(uint32_t packed_half) { return (packed_half >> 7) & 0xFFu; }
+
+// Loads and rescales one block of 32 bf16 activations (64 bytes at `src`,
+// read through L2: h was written by other CTAs of this launch).
+__device__ inline void stage_block(const __nv_bfloat16* src, uint32_t (&a)[16], float& inv) {
+  uint4 raw[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) raw[i] = __ldcg(reinterpret_cast<const uint4*>(src) + i);
+  uint32_t w[16];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    w[4 * i + 0] = raw[i].x;
+    w[4 * i + 1] = raw[i].y;
+    w[4 * i + 2] = raw[i].z;
+    w[4 * i + 3] = raw[i].w;
+  }
+  uint32_t emax = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) emax = max(emax, max(bf16_exp(w[i] & 0xFFFFu), bf16_exp(w[i] >> 16)));
+  // g = 2^n with n = 134 - emax, so the largest magnitude lands in [2^7, 2^8);
+  // n is kept within the normal exponents (blocks of zeros or subnormals get
+  // 2^127, a block holding an inf or NaN 2^-121: its sum is inf or NaN anyway)
+  const int n = min(127, max(-126, 134 - (int)emax));
+  const float g = __uint_as_float((uint32_t)(n + 127) << 23);
+  inv = (n == 127) ? __uint_as_float(0x00400000u) : __uint_as_float((uint32_t)(127 - n) << 23);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const __half lo = __float2half_rn(bf16_lo(w[i]) * g);
+    const __half hi = __float2half_rn(bf16_hi(w[i]) * g);
+    a[i] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+  }
+}
+
+template <int V>
+__device__ inline void stage_row(const __nv_bfloat16* row, ActRegs<V>& r) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int c = 0; c < V; ++c) stage_block(row + (size_t)(lane + 32 * c) * kMxBlock, r.a[c], r.inv[c]);
+}
+
+// Four code bytes -> four f16 pairs (E2M1 values, exact): pair b holds the
+// elements of byte b, low nibble in the low half.
+__device__ inline void e2m1x8(uint32_t w, uint32_t (&h)[4]) {
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}\n"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
+}
+
+// s0 += w.lo * a.lo, s1 += w.hi * a.hi: f16 products (exact in fp32) added in fp32.
+__device__ inline void fma_f16_pair(uint32_t w, uint32_t a, float& s0, float& s1) {
+  asm("{\n .reg .b16 wl, wh, al, ah;\n mov.b32 {wl, wh}, %2;\n mov.b32 {al, ah}, %3;\n"
+      " fma.rn.f32.f16 %0, wl, al, %0;\n fma.rn.f32.f16 %1, wh, ah, %1;\n}\n"
+      : "+f"(s0), "+f"(s1)
+      : "r"(w), "r"(a));
+}
+
+// Sum of the 32 products of one code vector (one block) with its staged activations.
+__device__ inline float block_dot(const uint4& q, const uint32_t (&a)[16]) {
+  float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+  uint32_t h[4];
+  e2m1x8(q.x, h);
+  fma_f16_pair(h[0], a[0], s0, s1);
+  fma_f16_pair(h[1], a[1], s2, s3);
+  fma_f16_pair(h[2], a[2], s0, s1);
+  fma_f16_pair(h[3], a[3], s2, s3);
+  e2m1x8(q.y, h);
+  fma_f16_pair(h[0], a[4], s0, s1);
+  fma_f16_pair(h[1], a[5], s2, s3);
+  fma_f16_pair(h[2], a[6], s0, s1);
+  fma_f16_pair(h[3], a[7], s2, s3);
+  e2m1x8(q.z, h);
+  fma_f16_pair(h[0], a[8], s0, s1);
+  fma_f16_pair(h[1], a[9], s2, s3);
+  fma_f16_pair(h[2], a[10], s0, s1);
+  fma_f16_pair(h[3], a[11], s2, s3);
+  e2m1x8(q.w, h);
+  fma_f16_pair(h[0], a[12], s0, s1);
+  fma_f16_pair(h[1], a[13], s2, s3);
+  fma_f16_pair(h[2], a[14], s0, s1);
+  fma_f16_pair(h[3], a[15], s2, s3);
+  return (s0 + s1) + (s2 + s3);
+}
+
+
+// The ring's barriers, the CTA's abort flag and its bookkeeping.
+struct MxRing {
+  uint64_t full_bar[kMxStages];
+  uint64_t empty_bar[kMxStages];
+  int abort;
+};
+
+struct MxRingState {
+  int base;          // ring index of the current phase's first unit
+  int armed_last;    // producer: last ring index with copies in flight
+  int last_issued;   // producer: last ring index it completed or armed
+};
+
+// The call's instances (one per routed row of the one token, at most kMaxK),
+// looked up once by the whole CTA so that the producer and the consumers read
+// their sources from shared memory: expert, dispatch position, token-major
+// expert row and slot-table entry.
+struct MxInsts {
+  int e[kMaxK], pos[kMaxK], yrow[kMaxK], entry[kMaxK];
+  int n;
+};
+
+// One phase over the call's instances: units of U consecutive rows,
+// grid-strided over the CTAs (CTA b takes units b, b + G, ...).
+template <bool GATEUP, int V>
+__device__ void mx_phase(const MxParams& p, const MxInsts& in, int* s_cnt, uint8_t* ring, MxRing& rg,
+                         MxRingState& st, bool producer) {
+  constexpr int NB = GATEUP ? 2 : 1;
+  constexpr int KC = 1024 * V;                                   // inputs per weight row
+  constexpr int KBC = KC / kMxBlock;                             // blocks (scale bytes) per row
+  constexpr int UC = GATEUP ? 16 / V : (32 / V < 16 ? 32 / V : 16);   // rows per unit
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int K = GATEUP ? p.H : p.I;          // inputs per weight row
+  const int NTASK = GATEUP ? p.I : p.H;      // rows per expert
+  const int KB = K / kMxBlock;               // scale bytes (blocks) per row
+  const int U = GATEUP ? mx_rows_gateup(p.H) : mx_rows_down(p.I);
+  const int upi = (NTASK + U - 1) / U;
+  const int G = gridDim.x;
+  const int n_local = local_units(in.n * upi);
+  const int base = st.base;
+  volatile int* abort_flag = &rg.abort;
+  st.base += n_local;
+  const int bank_codes = kMxCodeBytes / NB;  // offset of the second bank's codes in a stage
+  const int bank_scales = (kMxStageBytes - kMxScaleOff) / NB;   // offset of the second bank's scales
+
+  if (producer) {
+    int cur_j = -1;
+    bool ok = false;
+    MxRows rw;
+    const uint64_t pol = l2_evict_first();
+    for (int i = 0; i < n_local && !*abort_flag; ++i) {
+      const int u = (int)blockIdx.x + i * G;
+      const int j = u / upi, n0 = (u - j * upi) * U;
+      if (j != cur_j) {
+        cur_j = j;
+        ok = mx_resolve<GATEUP>(p, in.entry[j], &rw, nullptr);
+      }
+      const int ri = base + i;
+      const int stage = ri % kMxStages;
+      const uint32_t use = (uint32_t)(ri / kMxStages);
+      if (!ring_wait(&rg.empty_bar[stage], (use & 1u) ^ 1u, abort_flag)) break;
+      st.last_issued = ri;
+      if (!ok) {
+        // unbound or bad slot: complete the stage's phase without data
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&rg.full_bar[stage])) : "memory");
+        continue;
+      }
+      const int rows = min(U, NTASK - n0);
+      const uint32_t cb = (uint32_t)rows * (uint32_t)(K / 2), sb = (uint32_t)rows * (uint32_t)KB;
+      uint8_t* dst = ring + (size_t)stage * kMxStageBytes;
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(&rg.full_bar[stage])),
+                   "r"(NB * (cb + sb))
+                   : "memory");
+      bulk_g2s_hint(dst, rw.q0 + (size_t)n0 * (K / 2), cb, &rg.full_bar[stage], pol);
+      bulk_g2s_hint(dst + kMxScaleOff, rw.s0 + (size_t)n0 * KB, sb, &rg.full_bar[stage], pol);
+      if (GATEUP) {
+        bulk_g2s_hint(dst + bank_codes, rw.q1 + (size_t)n0 * (K / 2), cb, &rg.full_bar[stage], pol);
+        bulk_g2s_hint(dst + kMxScaleOff + bank_scales, rw.s1 + (size_t)n0 * KB, sb, &rg.full_bar[stage], pol);
+      }
+      st.armed_last = ri;
+    }
+    return;
+  }
+
+  // consumers: this warp's units are the ring indices ri = base + i with ri % kMxCW == warp
+  const int ua = mx_rows_gateup(p.H);
+  const unsigned need = (unsigned)min(G, (p.I + ua - 1) / ua);   // CTAs holding gate/up units of an instance
+  ActRegs<V> act;
+  int cur_j = -1, pos = 0, yrow = 0, staged_tok = -1;
+  bool ok = false;
+  MxRows rw;   // only the validity matters here: the rows sit in the stage
+  const int i0 = ((warp - base) % kMxCW + kMxCW) % kMxCW;
+  for (int i = i0; i < n_local; i += kMxCW) {
+    const int u = (int)blockIdx.x + i * G;
+    const int j = u / upi, n0 = (u - j * upi) * U;
+    if (j != cur_j) {
+      cur_j = j;
+      pos = in.pos[j];
+      yrow = in.yrow[j];
+      if (!GATEUP) {
+        // h of instance j is complete once every CTA holding its gate/up units has published them
+        if (lane == 0) {
+          unsigned long long t0 = 0;
+          for (uint32_t it = 0; ld_acquire_u32(p.inst_done + j) < need; ++it) {
+            if ((it & 15) == 15) {
+              if (*abort_flag) break;
+              const unsigned long long now = gtimer();
+              if (t0 == 0) {
+                t0 = now;
+              } else if (now - t0 > kGridWaitNs) {
+                *abort_flag = 1;
+                break;
+              }
+            }
+          }
+        }
+        __syncwarp();
+        if (*abort_flag) break;
+      }
+      // any warp meeting an unbound expert reports it (its units are spread over warps)
+      ok = mx_resolve<GATEUP>(p, in.entry[j], &rw, lane == 0 ? p.status : nullptr);
+      if (ok) {
+        if (!GATEUP) {
+          stage_row<V>(p.h + (size_t)pos * p.I, act);
+        } else if (yrow / p.k != staged_tok) {
+          // every gate/up instance of the token reads the same activations: staged once
+          staged_tok = yrow / p.k;
+          stage_row<V>(p.x + (size_t)staged_tok * p.H, act);
+        }
+      }
+    }
+    const int ri = base + i;
+    const int stage = ri % kMxStages;
+    const uint32_t use = (uint32_t)(ri / kMxStages);
+    if (!ring_wait(&rg.full_bar[stage], use & 1u, abort_flag)) break;
+    if (ok) {
+      const uint8_t* sw = ring + (size_t)stage * kMxStageBytes;
+      const int rows = min(UC, NTASK - n0);
+      for (int r = 0; r < rows; ++r) {
+        const uint8_t* qrow = sw + (size_t)r * (KC / 2);
+        const uint8_t* srow = sw + kMxScaleOff + r * KBC;
+        float acc0 = 0.0f, acc1 = 0.0f;
+#pragma unroll
+        for (int c = 0; c < V; ++c) {
+          const int v = lane + 32 * c;
+          const uint4 q0 = *reinterpret_cast<const uint4*>(qrow + v * 16);
+          acc0 = fmaf(block_dot(q0, act.a[c]), e8m0(srow[v]) * act.inv[c], acc0);
+          if (GATEUP) {
+            const uint4 q1 = *reinterpret_cast<const uint4*>(qrow + bank_codes + v * 16);
+            acc1 = fmaf(block_dot(q1, act.a[c]), e8m0(srow[bank_scales + v]) * act.inv[c], acc1);
+          }
+        }
+        acc0 = warp_sum(acc0);
+        if (GATEUP) {
+          acc1 = warp_sum(acc1);
+          if (lane == 0) p.h[(size_t)pos * p.I + n0 + r] = __float2bfloat16_rn(silu(acc0) * acc1);
+        } else if (lane == 0) {
+          p.y[(size_t)yrow * p.H + n0 + r] = acc0;
+        }
+      }
+    }
+    if (GATEUP) {
+      // publish instance j once this CTA's gate/up units of it are all done (as in the bf16 ring kernel:
+      // a CTA-scope acquire-release count, then one GPU-scope release add by the completing warp)
+      __syncwarp();
+      if (lane == 0) {
+        const int lo = j * upi, hi = lo + upi;
+        const int first = lo + (((int)blockIdx.x - lo) % G + G) % G;
+        const int mine = first < hi ? (hi - 1 - first) / G + 1 : 0;
+        if (atom_add_acq_rel_cta(&s_cnt[j], 1) + 1 == mine)
+          asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p.inst_done + j) : "memory");
+      }
+    }
+    __syncwarp();
+    if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&rg.empty_bar[stage])) : "memory");
+  }
+}
+
+template <int VA, int VB>
+__global__ void __launch_bounds__(kMxThreads, 1) mx_ring_kernel(MxParams p) {
+  extern __shared__ __align__(128) uint8_t ring_raw[];
+  __shared__ MxRing rg;
+  __shared__ int s_pref[kMaxE + 1];
+  __shared__ int s_warp[kMxThreads / 32];
+  __shared__ int s_cnt[kMaxK];
+  __shared__ MxInsts in;
+  // the ring is the dynamic shared array itself: pointers derived from it keep the shared
+  // address space, so stage reads compile to shared-memory loads
+  uint8_t* ring = ring_raw;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int s = 0; s < kMxStages; ++s) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&rg.full_bar[s])));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&rg.empty_bar[s])));
+    }
+    rg.abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (tid < kMaxK) s_cnt[tid] = 0;
+  pdl_wait();
+  build_group_prefix<1, kMaxE / 32>(p.counts, p.E, 0, INT_MAX, nullptr, s_pref, s_warp);   // ends with __syncthreads
+  if (tid < kMaxK) {
+    // instance tid: the tid-th routed row in dispatch order (expert ids ascending)
+    const int n = min(s_pref[p.E], kMaxK);
+    if (tid == 0) in.n = n;
+    if (tid < n) {
+      const int e = find_group(s_pref, p.E, tid);
+      const int pos = p.offsets[e] + (tid - s_pref[e]);
+      in.e[tid] = e;
+      in.pos[tid] = pos;
+      in.yrow[tid] = p.perm[pos];   // token-major expert row: token yrow / k, its (yrow % k)-th expert
+      in.entry[tid] = p.slot_table[p.layer * p.E + e];
+    }
+  }
+  __syncthreads();
+  const bool producer = warp == kMxCW;
+  MxRingState st = {0, -1, -1};
+  if (!producer || lane == 0) {
+    mx_phase<true, VA>(p, in, s_cnt, ring, rg, st, producer);
+    if (!rg.abort) mx_phase<false, VB>(p, in, s_cnt, ring, rg, st, producer);
+    if (producer && st.armed_last >= 0) {
+      // drain: the copies of the last ring round land before the CTA exits
+      volatile int no_abort = 0;
+      for (int q = st.last_issued; q >= 0 && q > st.last_issued - kMxStages; --q)
+        ring_wait(&rg.full_bar[q % kMxStages], (uint32_t)(q / kMxStages) & 1u, &no_abort);
+    }
+  }
+  pdl_trigger();
+  __syncthreads();
+  if (rg.abort && tid == 0) set_status(p.status, MOE_DEV_ERR_TIMEOUT);
+}
+
+template <int VA, int VB>
+cudaError_t launch_vv(const MxParams& p, cudaStream_t s) {
+  static std::atomic<int> smem_set[kMaxDevices];
+  cudaError_t e = ensure_smem(mx_ring_kernel<VA, VB>, kMxSmem, smem_set);
+  if (e != cudaSuccess) return e;
+  return launch_k(mx_ring_kernel<VA, VB>, num_sms(), kMxThreads, kMxSmem, s, p);
+}
+
+template <int VA>
+cudaError_t launch_va(const MxParams& p, cudaStream_t s) {
+  switch (p.I / 1024) {
+    case 1: return launch_vv<VA, 1>(p, s);
+    case 2: return launch_vv<VA, 2>(p, s);
+    default: return launch_vv<VA, 4>(p, s);
+  }
+}
+
+// rows of 1024, 2048 or 4096 inputs: 1, 2 or 4 blocks per lane, whose staged activations stay in registers
+inline bool v_ok(int K) { return K == 1024 || K == 2048 || K == 4096; }
+inline bool al16(const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; }
+inline bool pool_ok(const moe_pool_mxfp4& b) {
+  return b.n_slots == 0 || (al16(b.gate_q) && al16(b.up_q) && al16(b.down_q) && al16(b.gate_s) && al16(b.up_s) &&
+                            al16(b.down_s));
+}
+
+}  // namespace
+
+// One token (so every instance is one routed row and the token's activations
+// stay in registers), rows of 1024, 2048 or 4096 inputs (each lane owns whole
+// 32-input blocks), 16-byte aligned banks (bulk copies of code and scale rows).
+bool mx_ring_ok(const MxParams& p, int T) {
+  return T == 1 && p.k <= kMaxK && v_ok(p.H) && v_ok(p.I) && pool_ok(p.a) && pool_ok(p.b) &&
+         p.inst_done != nullptr;
+}
+
+cudaError_t launch_mx_ring(const MxParams& p, int T, cudaStream_t s) {
+  const size_t R = (size_t)T * p.k;
+  cudaError_t err = cudaMemsetAsync(p.inst_done, 0, R * sizeof(unsigned int), s);
+  if (err != cudaSuccess) return err;
+  switch (p.H / 1024) {
+    case 1: return launch_va<1>(p, s);
+    case 2: return launch_va<2>(p, s);
+    default: return launch_va<4>(p, s);
+  }
+}
+
+}  // namespace moe

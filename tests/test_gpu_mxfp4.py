@@ -139,16 +139,43 @@ def test_mxfp4_ffn_empty_call_launches_nothing():
     assert moe.moe_kernel_launch_count() == before
 
 
-def test_mxfp4_ffn_special_block_scales():
+@pytest.mark.parametrize("H,I,k", [(1024, 1024, 4), (2048, 4096, 6), (4096, 1024, 5)])
+def test_mxfp4_ffn_one_token_ring_kernel(H, I, k):
+    """One-token calls run on the weight-streaming ring kernel (one launch):
+    experts in both pools, layer 1 of 2, every row width it takes."""
+    E = 16
+    experts = list(range(E))
+    before = moe.moe_kernel_launch_count()
+    y, ref, st, _ = _run(1, k, E, H, I, 2, 1, experts[:9], experts[9:], seed=H + I + k)
+    assert moe.moe_kernel_launch_count() - before == 1
+    assert st == 0
+    _check(y, ref, f"mxfp4 ring kernel H={H} I={I} k={k}")
+
+
+def test_mxfp4_ffn_one_token_unbound_and_bad_slot():
+    T, k, E, H, I = 1, 4, 8, 1024, 2048
+    y, ref, st, ids = _run(T, k, E, H, I, 1, 0, [0, 1, 3, 4], [], seed=12, active=np.array([0, 2, 3, 5]),
+                           unbound=(2,), bad=(5,))
+    assert sorted(ids[0].tolist()) == [0, 2, 3, 5]
+    assert st & moe.MOE_DEV_ERR_UNBOUND and st & moe.MOE_DEV_ERR_BAD_SLOT
+    skipped = np.isin(ids.reshape(-1), [2, 5])
+    assert np.all(y[skipped] == 7.0)
+    _check(y[~skipped], ref[~skipped], "mxfp4 ring kernel rows of bound experts")
+
+
+@pytest.mark.parametrize("T,k,H,I", [(2, 1, 128, 64), (1, 2, 1024, 1024)])
+def test_mxfp4_ffn_special_block_scales(T, k, H, I):
     """E8M0 scales 0 (2^-127), 254 (2^127) and 255 (NaN) of the OCP MX
     encoding.  Inputs 0..31 of the token rows are about 2^120 and inputs
     32..63 about 2^-132, and every gate and up row scales those blocks by
     2^-127 and 2^127, so both contribute order-one terms; the other blocks
     are ordinary.  One gate row of expert 0 has a NaN block scale, which makes
-    every output of its token NaN; one down row of expert 1 has a NaN scale,
-    which makes one output element of the other token NaN.  Everything else
-    matches the oracle's fp64 dequantisation."""
-    T, k, E, H, I = 2, 1, 2, 128, 64
+    every output of its routed row NaN; one down row of expert 1 has a NaN
+    scale, which makes one output element of the other routed row NaN.
+    Everything else matches the oracle's fp64 dequantisation.  Two tokens of
+    one expert each run on the table kernel, one token routed to both experts
+    on the ring kernel."""
+    E = 2
     rng = np.random.default_rng(77)
     experts = {}
     for e in range(E):
@@ -165,7 +192,8 @@ def test_mxfp4_ffn_special_block_scales():
     xf[:, :32] *= np.float32(2.0 ** 120)
     xf[:, 32:64] *= np.float32(2.0 ** -132)
     x_bits = gen.f32_to_bf16_bits(xf)
-    ids = np.array([[0], [1]], np.int32)
+    # two tokens with one expert each (table kernel), or one token routed to both (ring kernel)
+    ids = np.array([[0], [1]] if T == 2 else [[0, 1]], np.int32)
     counts, offsets, perm, _ = O.dispatch(ids, E)
     pool = MxPool(E, H, I, experts, DEV)
     dev_i32 = lambda a: torch.from_numpy(np.asarray(a, np.int32)).to(DEV)
@@ -179,13 +207,13 @@ def test_mxfp4_ffn_special_block_scales():
     assert status_bits(st) == 0
     got = y.cpu().numpy().astype(np.float64)
     xd = gen.bf16_bits_to_f64(x_bits)
-    ref = np.stack([O.swiglu_expert(xd[t][None, :], *O.mx_expert_weights(*experts[int(ids[t, 0])]))[0]
-                    for t in range(T)])
+    ref = np.stack([O.swiglu_expert(xd[r // k][None, :], *O.mx_expert_weights(*experts[int(ids.reshape(-1)[r])]))[0]
+                    for r in range(T * k)])
     assert np.isnan(ref[0]).all() and np.isnan(got[0]).all()
     nan1 = np.isnan(ref[1])
     assert nan1.tolist() == [c == 5 for c in range(H)]
     assert np.array_equal(np.isnan(got[1]), nan1)
-    # the rescaled blocks carry real terms: dropping the 2^-127 block moves the reference by 16% (relative
-    # Frobenius), the 2^127 block by 98%, both far beyond the tolerance
+    # the rescaled blocks carry real terms: dropping the 2^-127 block moves the reference by 16% (26% at
+    # hidden 1024; relative Frobenius), the 2^127 block by 98% (83%), far beyond the tolerance
     assert np.abs(ref[1][~nan1]).max() > 0.05
     assert_close(got[1][~nan1], ref[1][~nan1], what="mxfp4 rows with block scales 0 and 254")
