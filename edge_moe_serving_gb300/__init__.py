@@ -53,6 +53,12 @@ class moe_pool_mxfp4(ctypes.Structure):
                 ("down_q", c_void_p), ("down_s", c_void_p), ("n_slots", c_int32), ("reserved", c_int32)]
 
 
+class moe_pool_nvfp4(ctypes.Structure):
+    _fields_ = [("gate_q", c_void_p), ("gate_s", c_void_p), ("up_q", c_void_p), ("up_s", c_void_p),
+                ("down_q", c_void_p), ("down_s", c_void_p), ("tensor_scale", c_void_p), ("n_slots", c_int32),
+                ("reserved", c_int32)]
+
+
 class moe_bw_profile(ctypes.Structure):
     _fields_ = [("b_p_gbs", c_double), ("b_h_gbs", c_double), ("b_p_contended_gbs", c_double),
                 ("b_h_contended_gbs", c_double), ("phi", c_double), ("phi_contended", c_double),
@@ -98,6 +104,9 @@ def _load():
         "moe_expert_ffn_mxfp4_workspace_size": (c_size_t, [c_int, c_int, c_int]),
         "moe_expert_ffn_mxfp4": (c_int, [POINTER(moe_pool_mxfp4), POINTER(moe_pool_mxfp4), P, c_int, c_int,
                                          c_int, c_int, c_int, P, P, P, P, c_int, c_int, P, P, c_size_t, P, P]),
+        "moe_expert_ffn_nvfp4_workspace_size": (c_size_t, [c_int, c_int, c_int]),
+        "moe_expert_ffn_nvfp4": (c_int, [POINTER(moe_pool_nvfp4), POINTER(moe_pool_nvfp4), P, c_int, c_int,
+                                         c_int, c_int, c_int, P, P, P, P, c_int, c_int, P, P, c_size_t, P, P]),
         "moe_combine": (c_int, [P, P, c_int, c_int, c_int, P, P, P, P]),
         "moe_layer_workspace_size": (c_size_t, [POINTER(moe_layer), POINTER(moe_cache), c_int, c_int]),
         "moe_layer_forward": (c_int, [POINTER(moe_layer), POINTER(moe_cache), P, c_int, P, c_uint32, c_int,
@@ -118,7 +127,7 @@ EXPORTED = ["moe_version", "moe_status_string", "moe_check_bounded_wait", "moe_k
             "moe_dispatch_workspace_size", "moe_dispatch", "moe_cache_bind_workspace_size",
             "moe_cache_bind_slots", "moe_expert_ffn_workspace_size", "moe_expert_ffn_grouped",
             "moe_expert_ffn_grouped_noalloc", "moe_expert_ffn_mxfp4_workspace_size", "moe_expert_ffn_mxfp4",
-            "moe_combine",
+            "moe_expert_ffn_nvfp4_workspace_size", "moe_expert_ffn_nvfp4", "moe_combine",
             "moe_layer_workspace_size", "moe_layer_forward"]
 
 
@@ -248,6 +257,19 @@ def moe_expert_ffn_mxfp4(cache_pool, staging_opt, slot_table, n_layers, layer, E
                          T, k, y_rows, ws, ws_bytes, dev_status, stream=None):
     """cache_pool / staging_opt: moe_pool_mxfp4 structs (staging_opt may be None)."""
     return _check("moe_expert_ffn_mxfp4", _lib.moe_expert_ffn_mxfp4(
+        ctypes.byref(cache_pool), ctypes.byref(staging_opt) if staging_opt is not None else None,
+        _p(slot_table), n_layers, layer, E, H, I, _p(counts), _p(offsets), _p(perm), _p(x), T, k, _p(y_rows),
+        _p(ws), ws_bytes, _p(dev_status), _s(stream)))
+
+
+def moe_expert_ffn_nvfp4_workspace_size(T, k, I):
+    return _lib.moe_expert_ffn_nvfp4_workspace_size(T, k, I)
+
+
+def moe_expert_ffn_nvfp4(cache_pool, staging_opt, slot_table, n_layers, layer, E, H, I, counts, offsets, perm, x,
+                         T, k, y_rows, ws, ws_bytes, dev_status, stream=None):
+    """cache_pool / staging_opt: moe_pool_nvfp4 structs (staging_opt may be None)."""
+    return _check("moe_expert_ffn_nvfp4", _lib.moe_expert_ffn_nvfp4(
         ctypes.byref(cache_pool), ctypes.byref(staging_opt) if staging_opt is not None else None,
         _p(slot_table), n_layers, layer, E, H, I, _p(counts), _p(offsets), _p(perm), _p(x), T, k, _p(y_rows),
         _p(ws), ws_bytes, _p(dev_status), _s(stream)))

@@ -230,9 +230,71 @@ int check_mx_pool(const moe_pool_mxfp4* pool) {
   return MOE_OK;
 }
 
+// An NVFP4 pool in the MXFP4 pool's layout (the same six banks; only the
+// scale rows are twice as long) plus its tensor scales.
+moe_pool_mxfp4 as_mx_pool(const moe_pool_nvfp4& n) {
+  moe_pool_mxfp4 m = {};
+  m.gate_q = n.gate_q;
+  m.gate_s = n.gate_s;
+  m.up_q = n.up_q;
+  m.up_s = n.up_s;
+  m.down_q = n.down_q;
+  m.down_s = n.down_s;
+  m.n_slots = n.n_slots;
+  return m;
+}
+
+int check_nv_pool(const moe_pool_nvfp4* pool) {
+  const moe_pool_mxfp4 m = as_mx_pool(*pool);
+  const int st = check_mx_pool(&m);
+  if (st != MOE_OK) return st;
+  if (!pool->tensor_scale) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(pool->tensor_scale) & 3u) != 0) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
 // h rows (bf16 [T*k, I]), then the ring kernel's per-instance counters
 size_t mx_ws_bytes(int T, int k, int I) {
   return align_up((size_t)T * k * I * sizeof(__nv_bfloat16), 256) + align_up((size_t)T * k * sizeof(unsigned int), 256);
+}
+
+// Checks shared by the two FP4 entry points (the pools are checked by the
+// caller), then the parameter block.
+int fp4_common(const int32_t* slot_table, int n_layers, int layer, int E, int H, int I, const int32_t* counts,
+               const int32_t* offsets, const int32_t* perm, const void* x, int T, int k, float* y_rows, void* ws,
+               size_t ws_bytes, uint32_t* dev_status, MxParams* p) {
+  if (T == 0) return MOE_OK;
+  if (!counts || !offsets || !perm || !x || !y_rows) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y_rows)) return MOE_ERR_UNSUPPORTED;
+  if (!ws || ws_bytes < mx_ws_bytes(T, k, I)) return MOE_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_UNSUPPORTED;   // h rows are read as 16-byte vectors
+  p->slot_table = slot_table;
+  p->layer = layer;
+  p->E = E;
+  p->H = H;
+  p->I = I;
+  p->k = k;
+  p->counts = counts;
+  p->offsets = offsets;
+  p->perm = perm;
+  p->x = reinterpret_cast<const __nv_bfloat16*>(x);
+  p->h = reinterpret_cast<__nv_bfloat16*>(ws);
+  p->inst_done = reinterpret_cast<unsigned int*>(reinterpret_cast<char*>(ws) +
+                                                 align_up((size_t)T * k * I * sizeof(__nv_bfloat16), 256));
+  p->y = y_rows;
+  p->status = dev_status;
+  return MOE_OK;
+}
+
+int shape_check(const void* cache_pool, const int32_t* slot_table, int n_layers, int layer, int E, int H, int I, int T,
+                int k, int block) {
+  if (!cache_pool || !slot_table || n_layers < 1 || layer < 0 || layer >= n_layers || E < 1 || T < 0 || k < 1 ||
+      k > E || k > kMaxK || H < block || I < block)
+    return MOE_ERR_INVALID_ARG;
+  if (E > kMaxE || (H % block) || (I % block) || (long long)n_layers * E > MOE_SLOT_MASK ||
+      (long long)T * k > INT_MAX / 2)
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
 }
 
 }  // namespace
@@ -249,46 +311,59 @@ extern "C" int moe_expert_ffn_mxfp4(const moe_pool_mxfp4* cache_pool, const moe_
                                     const void* x, int T, int k, float* y_rows, void* ws, size_t ws_bytes,
                                     uint32_t* dev_status, moe_stream_t stream) {
   using namespace moe;
-  if (!cache_pool || !slot_table || n_layers < 1 || layer < 0 || layer >= n_layers || E < 1 || T < 0 || k < 1 ||
-      k > E || k > kMaxK || H < kMxBlock || I < kMxBlock)
-    return MOE_ERR_INVALID_ARG;
-  if (E > kMaxE || (H % kMxBlock) || (I % kMxBlock) || (long long)n_layers * E > MOE_SLOT_MASK ||
-      (long long)T * k > INT_MAX / 2)
-    return MOE_ERR_UNSUPPORTED;
-  int st = check_mx_pool(cache_pool);
+  int st = shape_check(cache_pool, slot_table, n_layers, layer, E, H, I, T, k, kMxBlock);
+  if (st != MOE_OK) return st;
+  st = check_mx_pool(cache_pool);
   if (st != MOE_OK) return st;
   if (staging_opt) {
     st = check_mx_pool(staging_opt);
     if (st != MOE_OK) return st;
   }
-  if (T == 0) return MOE_OK;
-  if (!counts || !offsets || !perm || !x || !y_rows) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(y_rows)) return MOE_ERR_UNSUPPORTED;
-  if (!ws || ws_bytes < mx_ws_bytes(T, k, I)) return MOE_ERR_WORKSPACE;
-  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_UNSUPPORTED;   // h rows are read as 16-byte vectors
   MxParams p = {};
   p.a = *cache_pool;
   if (staging_opt) p.b = *staging_opt;   // else n_slots 0: staging entries read as out of range
-  p.slot_table = slot_table;
-  p.layer = layer;
-  p.E = E;
-  p.H = H;
-  p.I = I;
-  p.k = k;
-  p.counts = counts;
-  p.offsets = offsets;
-  p.perm = perm;
-  p.x = reinterpret_cast<const __nv_bfloat16*>(x);
-  p.h = reinterpret_cast<__nv_bfloat16*>(ws);
-  p.inst_done = reinterpret_cast<unsigned int*>(reinterpret_cast<char*>(ws) +
-                                                align_up((size_t)T * k * I * sizeof(__nv_bfloat16), 256));
-  p.y = y_rows;
-  p.status = dev_status;
+  st = fp4_common(slot_table, n_layers, layer, E, H, I, counts, offsets, perm, x, T, k, y_rows, ws, ws_bytes,
+                  dev_status, &p);
+  if (st != MOE_OK || T == 0) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t err;
-  if (mx_ring_ok(p, T)) err = launch_mx_ring(p, T, s);
+  if (fp4_ring_ok(p, T, false)) err = launch_fp4_ring(p, T, false, s);
   else if (T <= 1) err = launch_mx_nt<1>(p, s);
   else if (T <= 2) err = launch_mx_nt<2>(p, s);
   else err = launch_mx_nt<4>(p, s);
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+extern "C" size_t moe_expert_ffn_nvfp4_workspace_size(int T, int k, int I) {
+  if (T < 0 || k < 1 || I < 16 || (long long)T * k > INT_MAX / 2) return 0;
+  return moe::mx_ws_bytes(T, k, I);
+}
+
+extern "C" int moe_expert_ffn_nvfp4(const moe_pool_nvfp4* cache_pool, const moe_pool_nvfp4* staging_opt,
+                                    const int32_t* slot_table, int n_layers, int layer, int E, int H, int I,
+                                    const int32_t* counts, const int32_t* offsets, const int32_t* perm,
+                                    const void* x, int T, int k, float* y_rows, void* ws, size_t ws_bytes,
+                                    uint32_t* dev_status, moe_stream_t stream) {
+  using namespace moe;
+  int st = shape_check(cache_pool, slot_table, n_layers, layer, E, H, I, T, k, 16);
+  if (st != MOE_OK) return st;
+  st = check_nv_pool(cache_pool);
+  if (st != MOE_OK) return st;
+  if (staging_opt) {
+    st = check_nv_pool(staging_opt);
+    if (st != MOE_OK) return st;
+  }
+  MxParams p = {};
+  p.a = as_mx_pool(*cache_pool);
+  p.ts_a = cache_pool->tensor_scale;
+  if (staging_opt) {
+    p.b = as_mx_pool(*staging_opt);
+    p.ts_b = staging_opt->tensor_scale;
+  }
+  st = fp4_common(slot_table, n_layers, layer, E, H, I, counts, offsets, perm, x, T, k, y_rows, ws, ws_bytes,
+                  dev_status, &p);
+  if (st != MOE_OK || T == 0) return st;
+  // decode-sized calls only: the ring kernel (rows of 1024, 2048 or 4096 inputs, at most 64 routed rows)
+  if (!fp4_ring_ok(p, T, true)) return MOE_ERR_UNSUPPORTED;
+  return launch_fp4_ring(p, T, true, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -1,7 +1,9 @@
-// MXFP4 expert FFN for one-token calls: a weight-streaming ring kernel
-// (FreeToken paper, section 3.2: grouped evaluation of the GPU execution set
-// through the (layer, expert) slot; section 4.1: expert kernels dequantise
-// in-kernel; section 5.1: DeepSeek-V4-Flash's routed experts are MXFP4).
+// Block-scaled FP4 expert FFN for decode-sized calls: a weight-streaming ring
+// kernel over MXFP4 or NVFP4 banks (FreeToken paper, section 3.2: grouped
+// evaluation of the GPU execution set through the (layer, expert) slot;
+// section 4.1: expert kernels dequantise in-kernel; section 5.1: the routed
+// experts of DeepSeek-V4-Flash are MXFP4, those of GLM-5.2 and of the laptop
+// Qwen3.6 build NVFP4).  Every routed row is its own instance.
 //
 // One launch, one CTA per SM.  A producer thread streams "units" (a few
 // consecutive weight rows: their FP4 code bytes and E8M0 scale bytes) into a
@@ -11,16 +13,20 @@
 // consumer start the down rows of an expert as soon as every CTA finished its
 // gate/up rows of that expert, while the producer keeps streaming.
 //
-// Arithmetic of one 32-input block (16 code bytes, one scale s):
+// Arithmetic of one 32-input code vector (16 code bytes):
 //   * the token's activations of the block are rescaled once per call by a
 //     power of two g (largest magnitude into [2^7, 2^8)) and rounded to f16,
 //     exact for every element within 2^22 of the block's largest;
 //   * the hardware converts each code byte to two f16 E2M1 values (exact);
 //   * f16 x f16 products are exact in fp32 and are accumulated in fp32;
-//   * the block's sum is multiplied by 2^(s - 127) / g (exact: a power of
-//     two) and added to the row's fp32 accumulator.
-// So the result is the dot product with the dequantised row up to fp32
-// summation order, for any E8M0 scale including 2^-127, 2^127 and NaN.
+//   * MXFP4 (one E8M0 scale s per 32 inputs): the vector's sum is multiplied
+//     by 2^(s - 127) / g (exact: a power of two) and added to the row's fp32
+//     accumulator, so the result is the dot product with the dequantised row
+//     up to fp32 summation order, for any E8M0 scale including 2^-127, 2^127
+//     and NaN;
+//   * NVFP4 (one E4M3 scale per 16 inputs, one fp32 scale per bank): each
+//     half's sum is multiplied by its E4M3 value (converted exactly by the
+//     hardware) times 1/g, and the row's sum by the bank's tensor scale.
 #include <climits>
 
 #include "mxfp4.cuh"
@@ -32,7 +38,7 @@ namespace {
 constexpr int kMxStages = 6;   // ~100 KB in flight per SM: the first stage lands sooner than with 12 (measured)
 constexpr int kMxCodeBytes = 16384;     // code bytes per stage (both banks of a gate/up unit)
 constexpr int kMxScaleOff = 16384;      // scale bytes follow the codes
-constexpr int kMxStageBytes = 17408;    // 16 KB of codes + 1 KB of scales
+constexpr int kMxStageBytes = 18432;    // 16 KB of codes + up to 2 KB of scales (NVFP4)
 constexpr int kMxCW = 6;                // consumer warps (one stage each)
 constexpr int kMxThreads = (kMxCW + 1) * 32;
 constexpr int kMxSmem = kMxStages * kMxStageBytes + 128;
@@ -112,31 +118,56 @@ __device__ inline void fma_f16_pair(uint32_t w, uint32_t a, float& s0, float& s1
       : "r"(w), "r"(a));
 }
 
-// Sum of the 32 products of one code vector (one block) with its staged activations.
-__device__ inline float block_dot(const uint4& q, const uint32_t (&a)[16]) {
+// Sums of the products of one code vector with its staged activations: lo
+// over inputs 0..15 (words x, y), hi over inputs 16..31 (words z, w).
+__device__ inline void block_dot(const uint4& q, const uint32_t (&a)[16], float& lo, float& hi) {
   float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
   uint32_t h[4];
   e2m1x8(q.x, h);
   fma_f16_pair(h[0], a[0], s0, s1);
-  fma_f16_pair(h[1], a[1], s2, s3);
+  fma_f16_pair(h[1], a[1], s0, s1);
   fma_f16_pair(h[2], a[2], s0, s1);
-  fma_f16_pair(h[3], a[3], s2, s3);
+  fma_f16_pair(h[3], a[3], s0, s1);
+  e2m1x8(q.z, h);
+  fma_f16_pair(h[0], a[8], s2, s3);
+  fma_f16_pair(h[1], a[9], s2, s3);
+  fma_f16_pair(h[2], a[10], s2, s3);
+  fma_f16_pair(h[3], a[11], s2, s3);
   e2m1x8(q.y, h);
   fma_f16_pair(h[0], a[4], s0, s1);
-  fma_f16_pair(h[1], a[5], s2, s3);
+  fma_f16_pair(h[1], a[5], s0, s1);
   fma_f16_pair(h[2], a[6], s0, s1);
-  fma_f16_pair(h[3], a[7], s2, s3);
-  e2m1x8(q.z, h);
-  fma_f16_pair(h[0], a[8], s0, s1);
-  fma_f16_pair(h[1], a[9], s2, s3);
-  fma_f16_pair(h[2], a[10], s0, s1);
-  fma_f16_pair(h[3], a[11], s2, s3);
+  fma_f16_pair(h[3], a[7], s0, s1);
   e2m1x8(q.w, h);
-  fma_f16_pair(h[0], a[12], s0, s1);
+  fma_f16_pair(h[0], a[12], s2, s3);
   fma_f16_pair(h[1], a[13], s2, s3);
-  fma_f16_pair(h[2], a[14], s0, s1);
+  fma_f16_pair(h[2], a[14], s2, s3);
   fma_f16_pair(h[3], a[15], s2, s3);
-  return (s0 + s1) + (s2 + s3);
+  lo = s0 + s1;
+  hi = s2 + s3;
+}
+
+// Two E4M3 scale bytes (the low byte scales inputs 0..15 of the vector) ->
+// their values, exactly (every E4M3 value is an f16 value; NaN stays NaN).
+__device__ inline float2 e4m3x2(uint16_t b) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(b));
+  return make_float2(__half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu))),
+                     __half2float(__ushort_as_half((unsigned short)(h >> 16))));
+}
+
+// The vector's contribution to a row: MXFP4 scales the whole vector by its
+// E8M0 power of two, NVFP4 each half by its E4M3 value; inv undoes the
+// activations' power-of-two rescaling.
+template <bool NV>
+__device__ inline float vector_term(const uint4& q, const uint32_t (&a)[16], const uint8_t* srow, int v, float inv) {
+  float lo, hi;
+  block_dot(q, a, lo, hi);
+  if (NV) {
+    const float2 sc = e4m3x2(*reinterpret_cast<const uint16_t*>(srow + 2 * v));
+    return fmaf(lo, sc.x * inv, hi * (sc.y * inv));
+  }
+  return (lo + hi) * (e8m0(srow[v]) * inv);
 }
 
 
@@ -153,28 +184,29 @@ struct MxRingState {
   int last_issued;   // producer: last ring index it completed or armed
 };
 
-// The call's instances (one per routed row of the one token, at most kMaxK),
+// The call's instances (one per routed row, at most kFp4RingMaxRows),
 // looked up once by the whole CTA so that the producer and the consumers read
 // their sources from shared memory: expert, dispatch position, token-major
 // expert row and slot-table entry.
 struct MxInsts {
-  int e[kMaxK], pos[kMaxK], yrow[kMaxK], entry[kMaxK];
+  int e[kFp4RingMaxRows], pos[kFp4RingMaxRows], yrow[kFp4RingMaxRows], entry[kFp4RingMaxRows];
   int n;
 };
 
 // One phase over the call's instances: units of U consecutive rows,
 // grid-strided over the CTAs (CTA b takes units b, b + G, ...).
-template <bool GATEUP, int V>
+template <bool GATEUP, int V, bool NV>
 __device__ void mx_phase(const MxParams& p, const MxInsts& in, int* s_cnt, uint8_t* ring, MxRing& rg,
                          MxRingState& st, bool producer) {
   constexpr int NB = GATEUP ? 2 : 1;
   constexpr int KC = 1024 * V;                                   // inputs per weight row
-  constexpr int KBC = KC / kMxBlock;                             // blocks (scale bytes) per row
+  constexpr int SB = NV ? 16 : kMxBlock;                        // inputs per scale byte
+  constexpr int KBC = KC / SB;                                   // scale bytes per row
   constexpr int UC = GATEUP ? 16 / V : (32 / V < 16 ? 32 / V : 16);   // rows per unit
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int K = GATEUP ? p.H : p.I;          // inputs per weight row
   const int NTASK = GATEUP ? p.I : p.H;      // rows per expert
-  const int KB = K / kMxBlock;               // scale bytes (blocks) per row
+  const int KB = K / SB;                     // scale bytes per row
   const int U = GATEUP ? mx_rows_gateup(p.H) : mx_rows_down(p.I);
   const int upi = (NTASK + U - 1) / U;
   const int G = gridDim.x;
@@ -183,7 +215,7 @@ __device__ void mx_phase(const MxParams& p, const MxInsts& in, int* s_cnt, uint8
   volatile int* abort_flag = &rg.abort;
   st.base += n_local;
   const int bank_codes = kMxCodeBytes / NB;  // offset of the second bank's codes in a stage
-  const int bank_scales = (kMxStageBytes - kMxScaleOff) / NB;   // offset of the second bank's scales
+  const int bank_scales = bank_codes * 2 / SB;                    // offset of the second bank's scales
 
   if (producer) {
     int cur_j = -1;
@@ -195,7 +227,7 @@ __device__ void mx_phase(const MxParams& p, const MxInsts& in, int* s_cnt, uint8
       const int j = u / upi, n0 = (u - j * upi) * U;
       if (j != cur_j) {
         cur_j = j;
-        ok = mx_resolve<GATEUP>(p, in.entry[j], &rw, nullptr);
+        ok = mx_resolve<GATEUP, SB>(p, in.entry[j], &rw, nullptr);
       }
       const int ri = base + i;
       const int stage = ri % kMxStages;
@@ -230,7 +262,7 @@ __device__ void mx_phase(const MxParams& p, const MxInsts& in, int* s_cnt, uint8
   ActRegs<V> act;
   int cur_j = -1, pos = 0, yrow = 0, staged_tok = -1;
   bool ok = false;
-  MxRows rw;   // only the validity matters here: the rows sit in the stage
+  MxRows rw;   // the rows sit in the stage; the tensor scales are read from here
   const int i0 = ((warp - base) % kMxCW + kMxCW) % kMxCW;
   for (int i = i0; i < n_local; i += kMxCW) {
     const int u = (int)blockIdx.x + i * G;
@@ -260,7 +292,7 @@ __device__ void mx_phase(const MxParams& p, const MxInsts& in, int* s_cnt, uint8
         if (*abort_flag) break;
       }
       // any warp meeting an unbound expert reports it (its units are spread over warps)
-      ok = mx_resolve<GATEUP>(p, in.entry[j], &rw, lane == 0 ? p.status : nullptr);
+      ok = mx_resolve<GATEUP, SB>(p, in.entry[j], &rw, lane == 0 ? p.status : nullptr);
       if (ok) {
         if (!GATEUP) {
           stage_row<V>(p.h + (size_t)pos * p.I, act);
@@ -285,16 +317,14 @@ __device__ void mx_phase(const MxParams& p, const MxInsts& in, int* s_cnt, uint8
 #pragma unroll
         for (int c = 0; c < V; ++c) {
           const int v = lane + 32 * c;
-          const uint4 q0 = *reinterpret_cast<const uint4*>(qrow + v * 16);
-          acc0 = fmaf(block_dot(q0, act.a[c]), e8m0(srow[v]) * act.inv[c], acc0);
-          if (GATEUP) {
-            const uint4 q1 = *reinterpret_cast<const uint4*>(qrow + bank_codes + v * 16);
-            acc1 = fmaf(block_dot(q1, act.a[c]), e8m0(srow[bank_scales + v]) * act.inv[c], acc1);
-          }
+          acc0 += vector_term<NV>(*reinterpret_cast<const uint4*>(qrow + v * 16), act.a[c], srow, v, act.inv[c]);
+          if (GATEUP)
+            acc1 += vector_term<NV>(*reinterpret_cast<const uint4*>(qrow + bank_codes + v * 16), act.a[c],
+                                    srow + bank_scales, v, act.inv[c]);
         }
-        acc0 = warp_sum(acc0);
+        acc0 = warp_sum(acc0) * rw.t0;
         if (GATEUP) {
-          acc1 = warp_sum(acc1);
+          acc1 = warp_sum(acc1) * rw.t1;
           if (lane == 0) p.h[(size_t)pos * p.I + n0 + r] = __float2bfloat16_rn(silu(acc0) * acc1);
         } else if (lane == 0) {
           p.y[(size_t)yrow * p.H + n0 + r] = acc0;
@@ -318,13 +348,13 @@ __device__ void mx_phase(const MxParams& p, const MxInsts& in, int* s_cnt, uint8
   }
 }
 
-template <int VA, int VB>
+template <int VA, int VB, bool NV>
 __global__ void __launch_bounds__(kMxThreads, 1) mx_ring_kernel(MxParams p) {
   extern __shared__ __align__(128) uint8_t ring_raw[];
   __shared__ MxRing rg;
   __shared__ int s_pref[kMaxE + 1];
   __shared__ int s_warp[kMxThreads / 32];
-  __shared__ int s_cnt[kMaxK];
+  __shared__ int s_cnt[kFp4RingMaxRows];
   __shared__ MxInsts in;
   // the ring is the dynamic shared array itself: pointers derived from it keep the shared
   // address space, so stage reads compile to shared-memory loads
@@ -338,12 +368,12 @@ __global__ void __launch_bounds__(kMxThreads, 1) mx_ring_kernel(MxParams p) {
     rg.abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (tid < kMaxK) s_cnt[tid] = 0;
+  if (tid < kFp4RingMaxRows) s_cnt[tid] = 0;
   pdl_wait();
   build_group_prefix<1, kMaxE / 32>(p.counts, p.E, 0, INT_MAX, nullptr, s_pref, s_warp);   // ends with __syncthreads
-  if (tid < kMaxK) {
+  if (tid < kFp4RingMaxRows) {
     // instance tid: the tid-th routed row in dispatch order (expert ids ascending)
-    const int n = min(s_pref[p.E], kMaxK);
+    const int n = min(s_pref[p.E], kFp4RingMaxRows);
     if (tid == 0) in.n = n;
     if (tid < n) {
       const int e = find_group(s_pref, p.E, tid);
@@ -358,8 +388,8 @@ __global__ void __launch_bounds__(kMxThreads, 1) mx_ring_kernel(MxParams p) {
   const bool producer = warp == kMxCW;
   MxRingState st = {0, -1, -1};
   if (!producer || lane == 0) {
-    mx_phase<true, VA>(p, in, s_cnt, ring, rg, st, producer);
-    if (!rg.abort) mx_phase<false, VB>(p, in, s_cnt, ring, rg, st, producer);
+    mx_phase<true, VA, NV>(p, in, s_cnt, ring, rg, st, producer);
+    if (!rg.abort) mx_phase<false, VB, NV>(p, in, s_cnt, ring, rg, st, producer);
     if (producer && st.armed_last >= 0) {
       // drain: the copies of the last ring round land before the CTA exits
       volatile int no_abort = 0;
@@ -372,20 +402,29 @@ __global__ void __launch_bounds__(kMxThreads, 1) mx_ring_kernel(MxParams p) {
   if (rg.abort && tid == 0) set_status(p.status, MOE_DEV_ERR_TIMEOUT);
 }
 
-template <int VA, int VB>
+template <int VA, int VB, bool NV>
 cudaError_t launch_vv(const MxParams& p, cudaStream_t s) {
   static std::atomic<int> smem_set[kMaxDevices];
-  cudaError_t e = ensure_smem(mx_ring_kernel<VA, VB>, kMxSmem, smem_set);
+  cudaError_t e = ensure_smem(mx_ring_kernel<VA, VB, NV>, kMxSmem, smem_set);
   if (e != cudaSuccess) return e;
-  return launch_k(mx_ring_kernel<VA, VB>, num_sms(), kMxThreads, kMxSmem, s, p);
+  return launch_k(mx_ring_kernel<VA, VB, NV>, num_sms(), kMxThreads, kMxSmem, s, p);
 }
 
-template <int VA>
+template <int VA, bool NV>
 cudaError_t launch_va(const MxParams& p, cudaStream_t s) {
   switch (p.I / 1024) {
-    case 1: return launch_vv<VA, 1>(p, s);
-    case 2: return launch_vv<VA, 2>(p, s);
-    default: return launch_vv<VA, 4>(p, s);
+    case 1: return launch_vv<VA, 1, NV>(p, s);
+    case 2: return launch_vv<VA, 2, NV>(p, s);
+    default: return launch_vv<VA, 4, NV>(p, s);
+  }
+}
+
+template <bool NV>
+cudaError_t launch_fmt(const MxParams& p, cudaStream_t s) {
+  switch (p.H / 1024) {
+    case 1: return launch_va<1, NV>(p, s);
+    case 2: return launch_va<2, NV>(p, s);
+    default: return launch_va<4, NV>(p, s);
   }
 }
 
@@ -399,23 +438,21 @@ inline bool pool_ok(const moe_pool_mxfp4& b) {
 
 }  // namespace
 
-// One token (so every instance is one routed row and the token's activations
-// stay in registers), rows of 1024, 2048 or 4096 inputs (each lane owns whole
-// 32-input blocks), 16-byte aligned banks (bulk copies of code and scale rows).
-bool mx_ring_ok(const MxParams& p, int T) {
-  return T == 1 && p.k <= kMaxK && v_ok(p.H) && v_ok(p.I) && pool_ok(p.a) && pool_ok(p.b) &&
-         p.inst_done != nullptr;
+// At most kFp4RingMaxRows routed rows (each its own instance; its token's
+// activations stay in registers), rows of 1024, 2048 or 4096 inputs (each
+// lane owns whole 32-input code vectors), 16-byte aligned banks (bulk copies
+// of code and scale rows).
+bool fp4_ring_ok(const MxParams& p, int T, bool nv) {
+  (void)nv;
+  return T >= 1 && (long long)T * p.k <= kFp4RingMaxRows && v_ok(p.H) && v_ok(p.I) && pool_ok(p.a) &&
+         pool_ok(p.b) && p.inst_done != nullptr;
 }
 
-cudaError_t launch_mx_ring(const MxParams& p, int T, cudaStream_t s) {
+cudaError_t launch_fp4_ring(const MxParams& p, int T, bool nv, cudaStream_t s) {
   const size_t R = (size_t)T * p.k;
   cudaError_t err = cudaMemsetAsync(p.inst_done, 0, R * sizeof(unsigned int), s);
   if (err != cudaSuccess) return err;
-  switch (p.H / 1024) {
-    case 1: return launch_va<1>(p, s);
-    case 2: return launch_va<2>(p, s);
-    default: return launch_va<4>(p, s);
-  }
+  return nv ? launch_fmt<true>(p, s) : launch_fmt<false>(p, s);
 }
 
 }  // namespace moe

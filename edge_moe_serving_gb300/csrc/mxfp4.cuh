@@ -25,6 +25,10 @@ struct MxParams {
   float* y;           // [R, H] token-major
   uint32_t* status;
   unsigned int* inst_done;   // ring kernel: per-instance gate/up completion counters (zero at launch)
+  // NVFP4 banks only: fp32 tensor scale of every (slot, bank) of each pool, [n_slots][3] (gate, up,
+  // down); null for MXFP4
+  const float* ts_a;
+  const float* ts_b;
 };
 
 struct MxRows {
@@ -32,6 +36,7 @@ struct MxRows {
   const uint8_t* s0;
   const uint8_t* q1;
   const uint8_t* s1;
+  float t0, t1;       // NVFP4 tensor scales of the two banks (1 for MXFP4)
 };
 
 namespace {
@@ -42,14 +47,16 @@ __device__ inline float e8m0(uint32_t s) {
 }
 
 // Slot-table entry -> the slot's code and scale rows of one projection
-// (gate and up, or down twice).
-template <bool GATEUP>
+// (gate and up, or down twice).  SB: inputs per scale byte (32 for MXFP4's
+// E8M0 scales, 16 for NVFP4's E4M3 scales).
+template <bool GATEUP, int SB = kMxBlock>
 __device__ inline bool mx_resolve(const MxParams& p, int32_t entry, MxRows* out, uint32_t* status) {
   if (entry < 0) {
     set_status(status, MOE_DEV_ERR_UNBOUND);
     return false;
   }
-  const moe_pool_mxfp4& pool = (entry & MOE_STAGING_TAG) ? p.b : p.a;
+  const bool staged = (entry & MOE_STAGING_TAG) != 0;
+  const moe_pool_mxfp4& pool = staged ? p.b : p.a;
   const int32_t slot = entry & MOE_SLOT_MASK;
   if ((entry & ~(MOE_STAGING_TAG | MOE_SLOT_MASK)) != 0 || slot >= pool.n_slots) {
     set_status(status, MOE_DEV_ERR_BAD_SLOT);
@@ -57,27 +64,33 @@ __device__ inline bool mx_resolve(const MxParams& p, int32_t entry, MxRows* out,
   }
   const size_t rows = GATEUP ? (size_t)p.I : (size_t)p.H;   // output rows per slot
   const size_t K = GATEUP ? (size_t)p.H : (size_t)p.I;       // inputs per row
-  const size_t qper = rows * (K / 2), sper = rows * (K / kMxBlock);
+  const size_t qper = rows * (K / 2), sper = rows * (K / SB);
+  const float* ts = staged ? p.ts_b : p.ts_a;
   if (GATEUP) {
     out->q0 = reinterpret_cast<const uint8_t*>(pool.gate_q) + (size_t)slot * qper;
     out->s0 = reinterpret_cast<const uint8_t*>(pool.gate_s) + (size_t)slot * sper;
     out->q1 = reinterpret_cast<const uint8_t*>(pool.up_q) + (size_t)slot * qper;
     out->s1 = reinterpret_cast<const uint8_t*>(pool.up_s) + (size_t)slot * sper;
+    out->t0 = ts ? ts[(size_t)slot * 3 + 0] : 1.0f;
+    out->t1 = ts ? ts[(size_t)slot * 3 + 1] : 1.0f;
   } else {
     out->q0 = reinterpret_cast<const uint8_t*>(pool.down_q) + (size_t)slot * qper;
     out->s0 = reinterpret_cast<const uint8_t*>(pool.down_s) + (size_t)slot * sper;
     out->q1 = out->q0;
     out->s1 = out->s0;
+    out->t0 = out->t1 = ts ? ts[(size_t)slot * 3 + 2] : 1.0f;
   }
   return true;
 }
 
 }  // namespace
 
-// One-token calls on the weight-streaming ring kernel (ffn_mxfp4_ring.cu):
-// whether the shape and banks qualify, and the launch (counters cleared on
-// the stream first).  inst_done: R + 4 words of workspace.
-bool mx_ring_ok(const MxParams& p, int T);
-cudaError_t launch_mx_ring(const MxParams& p, int T, cudaStream_t s);
+// The weight-streaming ring kernel (ffn_mxfp4_ring.cu) over MXFP4 or NVFP4
+// banks (nv): whether the shape and banks qualify (at most kFp4RingMaxRows
+// routed rows, each its own instance), and the launch (the inst_done
+// counters, one word per routed row, cleared on the stream first).
+constexpr int kFp4RingMaxRows = 64;
+bool fp4_ring_ok(const MxParams& p, int T, bool nv);
+cudaError_t launch_fp4_ring(const MxParams& p, int T, bool nv, cudaStream_t s);
 
 }  // namespace moe

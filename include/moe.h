@@ -350,7 +350,12 @@ typedef struct moe_pool_mxfp4 {
  * with W the dequantised weights of the slot that slot_table[layer*E + e]
  * names (cache_pool, or staging_opt for MOE_STAGING_TAG entries; the same
  * encoding as moe_cache).  Each block's 32 products are summed in fp32 and
- * scaled by the block's power of two (exact), accumulation in fp32.
+ * scaled by the block's power of two (exact), accumulation in fp32.  Calls
+ * of at most 64 routed rows with H and I in {1024, 2048, 4096} and 16-byte
+ * aligned scale banks run on one weight-streaming launch (the token's
+ * activations rescaled per 32-input block by a power of two into f16, exact
+ * f16 products of the E2M1 values); other calls on a two-launch table-decode
+ * kernel.
  * slot_table: [n_layers*E] int32.  x bf16 [T, H]; y_rows fp32 [T*k, H],
  * token-major.  counts / offsets / perm as moe_dispatch writes them.
  * Errors: MOE_ERR_INVALID_ARG for a NULL pool, table or (T > 0) array, a
@@ -358,12 +363,57 @@ typedef struct moe_pool_mxfp4 {
  * outside [1, min(E, 16)], H or I below 32; MOE_ERR_UNSUPPORTED for H or I
  * not a multiple of 32, E > 1024, T*k > INT_MAX/2, a code bank, x or y_rows
  * not 16-byte aligned; MOE_ERR_WORKSPACE for ws_bytes below
- * moe_expert_ffn_mxfp4_workspace_size(T, k, I) (the bf16 h rows, 0 for
- * invalid arguments).  T = 0 returns MOE_OK and launches nothing.  On the
+ * moe_expert_ffn_mxfp4_workspace_size(T, k, I) (the bf16 h rows and one
+ * counter per routed row, 0 for invalid arguments), MOE_ERR_UNSUPPORTED for
+ * a ws that is not 256-byte aligned.  T = 0 returns MOE_OK and launches nothing.  On the
  * device, an unbound or out-of-range entry sets MOE_DEV_ERR_UNBOUND /
  * MOE_DEV_ERR_BAD_SLOT and leaves that expert's rows unwritten. */
 size_t moe_expert_ffn_mxfp4_workspace_size(int T, int k, int I);
 int moe_expert_ffn_mxfp4(const moe_pool_mxfp4* cache_pool, const moe_pool_mxfp4* staging_opt,
+                         const int32_t* slot_table, int n_layers, int layer, int E, int H, int I,
+                         const int32_t* counts, const int32_t* offsets, const int32_t* perm,
+                         const void* x, int T, int k, float* y_rows, void* ws, size_t ws_bytes,
+                         uint32_t* dev_status, moe_stream_t stream);
+
+/* ---------------------------------------------------------------- NVFP4 experts
+ * Block-scaled FP4 banks in NVIDIA's NVFP4 format ([P] section 5.1 "Models":
+ * the routed experts of GLM-5.2 and of the laptop build of Qwen3.6-35B-A3B
+ * are NVFP4; section 4.1: expert kernels dequantise in-kernel): FP4 E2M1
+ * elements packed as in MXFP4, one FP8 E4M3 scale byte per block of 16
+ * consecutive inputs (the OCP 8-bit E4M3 without infinities: 0x7F and 0xFF
+ * are NaN), and one fp32 scale per bank of each expert:
+ *   W[r, i] = e2m1(code of i) * e4m3(scale of block i/16) * tensor_scale
+ * Banks are slot-major; a row of K inputs is K/2 code bytes and K/16 scale
+ * bytes:
+ *   gate_q, up_q  [n_slots, I, H/2]   gate_s, up_s  [n_slots, I, H/16]
+ *   down_q        [n_slots, H, I/2]   down_s        [n_slots, H, I/16]
+ *   tensor_scale  fp32 [n_slots, 3]   (gate, up, down of each slot)
+ * Code and scale banks 16-byte aligned, tensor_scale 4-byte aligned. */
+typedef struct moe_pool_nvfp4 {
+  const void* gate_q;
+  const void* gate_s;
+  const void* up_q;
+  const void* up_s;
+  const void* down_q;
+  const void* down_s;
+  const float* tensor_scale;
+  int32_t n_slots;
+  int32_t reserved;   /* 0 */
+} moe_pool_nvfp4;
+
+/* moe_expert_ffn_mxfp4 over NVFP4 banks, same arguments, layouts, results
+ * and device errors, for decode-sized calls: T*k at most 64 routed rows and
+ * H, I in {1024, 2048, 4096} (one weight-streaming launch; every routed row
+ * reads its expert's weights once).  Each 16-input half of a 32-input code
+ * vector sums its exact f16 products in fp32 and is scaled by its E4M3 value
+ * (exact in fp32) and the activations' power-of-two back-scale; the row's
+ * fp32 sum is scaled by the bank's tensor scale.  Errors: as
+ * moe_expert_ffn_mxfp4 with 16 in place of 32 for the H and I checks, plus
+ * MOE_ERR_INVALID_ARG for a NULL tensor_scale, MOE_ERR_UNSUPPORTED for a
+ * misaligned bank or tensor_scale and for calls outside the decode-sized
+ * shapes above.  moe_expert_ffn_nvfp4_workspace_size(T, k, I) bytes of ws. */
+size_t moe_expert_ffn_nvfp4_workspace_size(int T, int k, int I);
+int moe_expert_ffn_nvfp4(const moe_pool_nvfp4* cache_pool, const moe_pool_nvfp4* staging_opt,
                          const int32_t* slot_table, int n_layers, int layer, int E, int H, int I,
                          const int32_t* counts, const int32_t* offsets, const int32_t* perm,
                          const void* x, int T, int k, float* y_rows, void* ws, size_t ws_bytes,

@@ -130,3 +130,25 @@ class MxPool:
     def set(self, slot, arrays):
         for bank, a in zip(self.banks, arrays):
             bank[slot].copy_(torch.from_numpy(np.require(a, requirements=["C", "W"])))
+
+
+class NvPool:
+    """One NVFP4 pool on the device: six slot-major uint8 banks (codes and
+    E4M3 scales of gate, up, down), the fp32 tensor scales [n_slots, 3] and
+    the moe_pool_nvfp4 struct naming them.  ``experts`` maps slot ->
+    ((gate_q, gate_s, gate_ts), (up_q, up_s, up_ts), (down_q, down_s,
+    down_ts)); slots not listed stay zero (never read)."""
+
+    def __init__(self, n_slots, H, I, experts, device="cuda"):
+        shapes = [(I, H // 2), (I, H // 16), (I, H // 2), (I, H // 16), (H, I // 2), (H, I // 16)]
+        self.banks = [torch.zeros((n_slots,) + s, dtype=torch.uint8, device=device) for s in shapes]
+        self.tscale = torch.zeros((n_slots, 3), dtype=torch.float32, device=device)
+        for slot, banks in experts.items():
+            self.set(slot, banks)
+        self.struct = moe.moe_pool_nvfp4(*[b.data_ptr() for b in self.banks], self.tscale.data_ptr(), n_slots, 0)
+
+    def set(self, slot, banks):
+        for b, (codes, scales, ts) in enumerate(banks):
+            self.banks[2 * b][slot].copy_(torch.from_numpy(np.require(codes, requirements=["C", "W"])))
+            self.banks[2 * b + 1][slot].copy_(torch.from_numpy(np.require(scales, requirements=["C", "W"])))
+            self.tscale[slot, b] = float(ts)

@@ -249,3 +249,11 @@ def nvfp4_bank(seed: int, layer: int, e: int, bank: int, rows: int, K: int):
     scales = g.integers(lo, hi + 1, size=(rows, K // 16), dtype=np.uint8)
     return codes, scales, np.float32(NV_TENSOR_SCALE)
 
+
+
+def nvfp4_expert(seed: int, layer: int, e: int, H: int, I: int):
+    """((gate_q, gate_s, gate_ts), (up_q, up_s, up_ts), (down_q, down_s, down_ts))
+    of NVFP4 expert (layer, e): gate and up rows [I] of H inputs, down rows [H]
+    of I inputs."""
+    return (nvfp4_bank(seed, layer, e, 0, I, H), nvfp4_bank(seed, layer, e, 1, I, H),
+            nvfp4_bank(seed, layer, e, 2, H, I))

@@ -35,6 +35,7 @@ def test_struct_layouts_match_header():
     assert ctypes.sizeof(moe.moe_cache) == 2 * 32 + 4 * 8 + 16
     assert ctypes.sizeof(moe.moe_bw_profile) == 6 * 8 + 4 * 4
     assert ctypes.sizeof(moe.moe_pool_mxfp4) == 6 * 8 + 2 * 4
+    assert ctypes.sizeof(moe.moe_pool_nvfp4) == 7 * 8 + 2 * 4
 
 
 def test_status_strings_and_version():
@@ -133,6 +134,25 @@ def test_mxfp4_ffn_argument_checks():
                 None) == moe.MOE_ERR_INVALID_ARG
 
 
+def test_nvfp4_ffn_argument_checks():
+    L = moe.lib()
+    call = L.moe_expert_ffn_nvfp4
+    pool = moe.moe_pool_nvfp4(16, 16, 16, 16, 16, 16, 16, 4, 0)    # fake non-null pointers: never dereferenced
+    args = lambda pool, T=4, k=2, E=8, H=64, I=64, ws_bytes=1 << 20, x=16, ws=256: (
+        ctypes.byref(pool), None, 16, 1, 0, E, H, I, 16, 16, 16, x, T, k, 16, ws, ws_bytes, None, None)
+    assert moe.moe_expert_ffn_nvfp4_workspace_size(4, 2, 64) >= 4 * 2 * 64 * 2
+    assert call(*args(pool, T=0)) == moe.MOE_OK
+    assert call(*args(pool, k=9)) == moe.MOE_ERR_INVALID_ARG
+    assert call(*args(pool, H=40)) == moe.MOE_ERR_UNSUPPORTED          # not a multiple of 16
+    assert call(*args(pool, ws_bytes=64)) == moe.MOE_ERR_WORKSPACE
+    assert call(*args(pool, ws=272)) == moe.MOE_ERR_UNSUPPORTED        # ws not 256-byte aligned
+    assert call(*args(pool)) == moe.MOE_ERR_UNSUPPORTED                # rows of 64 inputs: not a decode-kernel shape
+    no_ts = moe.moe_pool_nvfp4(16, 16, 16, 16, 16, 16, None, 4, 0)
+    assert call(*args(no_ts)) == moe.MOE_ERR_INVALID_ARG
+    odd_ts = moe.moe_pool_nvfp4(16, 16, 16, 16, 16, 16, 18, 4, 0)
+    assert call(*args(odd_ts)) == moe.MOE_ERR_UNSUPPORTED
+
+
 def test_ffn_argument_checks_and_the_allocation_free_variant():
     """The bf16 expert FFN's host checks, and the allocation-free variant's:
     the same argument checks in the same order, then its scratch limit."""
@@ -169,7 +189,7 @@ def test_ffn_argument_checks_and_the_allocation_free_variant():
 
 
 STRUCTS = ["moe_pool", "moe_cache", "moe_bind_stats", "moe_layer", "moe_layer_buffers", "moe_bw_profile",
-           "moe_pool_mxfp4"]
+           "moe_pool_mxfp4", "moe_pool_nvfp4"]
 
 
 def test_header_is_plain_c_and_matches_the_binding_layouts(tmp_path):

@@ -139,17 +139,19 @@ def test_mxfp4_ffn_empty_call_launches_nothing():
     assert moe.moe_kernel_launch_count() == before
 
 
-@pytest.mark.parametrize("H,I,k", [(1024, 1024, 4), (2048, 4096, 6), (4096, 1024, 5)])
-def test_mxfp4_ffn_one_token_ring_kernel(H, I, k):
-    """One-token calls run on the weight-streaming ring kernel (one launch):
-    experts in both pools, layer 1 of 2, every row width it takes."""
+@pytest.mark.parametrize("T,H,I,k", [(1, 1024, 1024, 4), (1, 2048, 4096, 6), (1, 4096, 1024, 5), (3, 1024, 2048, 4),
+                                     (8, 1024, 1024, 8)])
+def test_mxfp4_ffn_ring_kernel(T, H, I, k):
+    """Calls of up to 64 routed rows run on the weight-streaming ring kernel
+    (one launch): experts in both pools, layer 1 of 2, every row width it
+    takes, one token and several."""
     E = 16
     experts = list(range(E))
     before = moe.moe_kernel_launch_count()
-    y, ref, st, _ = _run(1, k, E, H, I, 2, 1, experts[:9], experts[9:], seed=H + I + k)
+    y, ref, st, _ = _run(T, k, E, H, I, 2, 1, experts[:9], experts[9:], seed=T * 1000 + H + I + k)
     assert moe.moe_kernel_launch_count() - before == 1
     assert st == 0
-    _check(y, ref, f"mxfp4 ring kernel H={H} I={I} k={k}")
+    _check(y, ref, f"mxfp4 ring kernel T={T} H={H} I={I} k={k}")
 
 
 def test_mxfp4_ffn_one_token_unbound_and_bad_slot():
