@@ -24,7 +24,8 @@ MOE_SLOT_MASK = (1 << 30) - 1
 
 
 class moe_pool(ctypes.Structure):
-    _fields_ = [("w_gate", c_void_p), ("w_up", c_void_p), ("w_down", c_void_p), ("n_slots", c_int32)]
+    _fields_ = [("w_gate", c_void_p), ("w_up", c_void_p), ("w_down", c_void_p), ("n_slots", c_int32),
+                ("host", c_int32)]
 
 
 class moe_cache(ctypes.Structure):
@@ -108,6 +109,9 @@ def _load():
         "moe_expert_ffn_nvfp4": (c_int, [POINTER(moe_pool_nvfp4), POINTER(moe_pool_nvfp4), P, c_int, c_int,
                                          c_int, c_int, c_int, P, P, P, P, c_int, c_int, P, P, c_size_t, P, P]),
         "moe_combine": (c_int, [P, P, c_int, c_int, c_int, P, P, P, P]),
+        "moe_prefill_double_buffered": (c_int, [POINTER(moe_layer), c_int, POINTER(moe_pool), POINTER(moe_pool),
+                                                POINTER(moe_cache), POINTER(c_void_p), c_int, POINTER(c_void_p),
+                                                c_int, c_int, P, c_size_t, P, P, P]),
         "moe_layer_workspace_size": (c_size_t, [POINTER(moe_layer), POINTER(moe_cache), c_int, c_int]),
         "moe_layer_forward": (c_int, [POINTER(moe_layer), POINTER(moe_cache), P, c_int, P, c_uint32, c_int,
                                       c_int, c_uint64, c_int, POINTER(moe_layer_buffers), P, c_size_t, P, P,
@@ -128,7 +132,7 @@ EXPORTED = ["moe_version", "moe_status_string", "moe_check_bounded_wait", "moe_k
             "moe_cache_bind_slots", "moe_expert_ffn_workspace_size", "moe_expert_ffn_grouped",
             "moe_expert_ffn_grouped_noalloc", "moe_expert_ffn_mxfp4_workspace_size", "moe_expert_ffn_mxfp4",
             "moe_expert_ffn_nvfp4_workspace_size", "moe_expert_ffn_nvfp4", "moe_combine",
-            "moe_layer_workspace_size", "moe_layer_forward"]
+            "moe_layer_workspace_size", "moe_layer_forward", "moe_prefill_double_buffered"]
 
 
 def lib():
@@ -290,3 +294,18 @@ def moe_layer_forward(layer, cache, x, T, out, phi_q16, min_fill, fill_policy, s
         ctypes.byref(layer), ctypes.byref(cache), _p(x), T, _p(out), phi_q16, min_fill, fill_policy, seed,
         ffn_mode, ctypes.byref(bufs_opt) if bufs_opt is not None else None, _p(ws), ws_bytes, _p(dev_status),
         _p(stats_dev), _s(stream)))
+
+
+def moe_prefill_double_buffered(layers, source, layer_buf, state, x, T, out, ffn_mode, overlap, ws, ws_bytes,
+                                dev_status, stream, copy_stream):
+    """layers: list of moe_layer structs; source: moe_pool; layer_buf: two
+    moe_pool structs (the second may be an empty moe_pool()); state: moe_cache
+    (its residency arrays); x, out: lists of per-layer tensors or addresses."""
+    n = len(layers)
+    larr = (moe_layer * n)(*layers)
+    barr = (moe_pool * 2)(*layer_buf)
+    xs = (c_void_p * n)(*[_p(t) for t in x])
+    outs = (c_void_p * n)(*[_p(t) for t in out])
+    return _check("moe_prefill_double_buffered", _lib.moe_prefill_double_buffered(
+        larr, n, ctypes.byref(source), barr, ctypes.byref(state), xs, T, outs, ffn_mode, overlap, _p(ws), ws_bytes,
+        _p(dev_status), _s(stream), _s(copy_stream)))

@@ -294,6 +294,21 @@ fill_copy_kernel(moe_pool src, moe_pool dst, size_t bank_bytes, const int32_t* _
     uint4* d4 = reinterpret_cast<uint4*>(db + (size_t)d_slot * bank_bytes + lo);
     const size_t nv = len / 16;
     size_t v = threadIdx.x;
+    if (src.host) {
+      // a host-resident staging pool: plain streaming loads over the CPU-GPU link
+      for (; v + 3 * kCopyThreads < nv; v += 4 * kCopyThreads) {
+        const uint4 a = __ldcs(s4 + v);
+        const uint4 b = __ldcs(s4 + v + kCopyThreads);
+        const uint4 cc = __ldcs(s4 + v + 2 * kCopyThreads);
+        const uint4 d = __ldcs(s4 + v + 3 * kCopyThreads);
+        d4[v] = a;
+        d4[v + kCopyThreads] = b;
+        d4[v + 2 * kCopyThreads] = cc;
+        d4[v + 3 * kCopyThreads] = d;
+      }
+      for (; v < nv; v += kCopyThreads) d4[v] = __ldcs(s4 + v);
+      continue;
+    }
     for (; v + 3 * kCopyThreads < nv; v += 4 * kCopyThreads) {
       const uint4 a = ldg_stream_hint(s4 + v, pol);
       const uint4 b = ldg_stream_hint(s4 + v + kCopyThreads, pol);

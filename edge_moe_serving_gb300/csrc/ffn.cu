@@ -34,10 +34,14 @@ cudaError_t launch_ffn(const moe_cache& c, int layer, const int32_t* counts, con
     // the GEMM pads a group only to 16 token rows, so it takes small groups too
     gemv_max = 0;
   }
+  // A host-resident staging pool is read with plain loads only: the kernels
+  // below take the cache pool's experts, and a plain GEMV pass the staged ones.
+  const bool host_stage = c.staging.w_gate != nullptr && c.staging.host != 0;
   // bf16 expert rows are written by the GEMM only
-  if (y_rows_bf16 != nullptr && gemv_max != 0) return cudaErrorNotSupported;
-  // a fused fill or combine is only done by the fused GEMV kernel
-  if ((fused_fills != nullptr || combine_out != nullptr) && gemv_max != INT_MAX) return cudaErrorNotSupported;
+  if (y_rows_bf16 != nullptr && (gemv_max != 0 || host_stage)) return cudaErrorNotSupported;
+  // a fused fill or combine is only done by the fused GEMV kernel, over every expert
+  if ((fused_fills != nullptr || combine_out != nullptr) && (gemv_max != INT_MAX || host_stage))
+    return cudaErrorNotSupported;
   if (combine_out != nullptr && !gemv_fused_ok(c.H, c.I)) return cudaErrorNotSupported;
   if (gemv_max > 0) {
     GemvParams p = {};
@@ -65,12 +69,38 @@ cudaError_t launch_ffn(const moe_cache& c, int layer, const int32_t* counts, con
     p.grid_count = reinterpret_cast<unsigned int*>(reinterpret_cast<char*>(ws) +
                                                    align_up((size_t)R * c.I * sizeof(__nv_bfloat16), 256));
     p.inst_done = R <= kMaxFusedInst ? p.grid_count + 4 : nullptr;
+    p.pool_filter = host_stage ? kPoolDeviceOnly : kPoolAll;
     cudaError_t err = launch_gemv(p, s);
     if (err != cudaSuccess) return err;
   }
-  if (gemv_max != INT_MAX)
-    return launch_gemm(c, layer, counts, offsets, perm, mask, gemv_max, x_perm, T, R, h, y_rows, y_rows_bf16, status,
-                       s);
+  if (gemv_max != INT_MAX) {
+    cudaError_t err = launch_gemm(c, layer, counts, offsets, perm, mask, gemv_max, x_perm, T, R, h, y_rows,
+                                  y_rows_bf16, status, s);
+    if (err != cudaSuccess) return err;
+  }
+  if (host_stage) {
+    // the staged experts, every group size, on the plain-load GEMV (h and y rows disjoint from the pass above)
+    GemvParams q = {};
+    q.c = c;
+    q.layer = layer;
+    q.E = c.E;
+    q.H = c.H;
+    q.I = c.I;
+    q.k = k;
+    q.T = T;
+    q.counts = counts;
+    q.offsets = offsets;
+    q.perm = perm;
+    q.x = x;
+    q.x_perm = x_perm;
+    q.mask = mask;
+    q.max_rows = INT_MAX;
+    q.h = h;
+    q.y = y_rows;
+    q.status = status;
+    q.pool_filter = kPoolStagingOnly;
+    return launch_gemv_plain(q, s);
+  }
   return cudaSuccess;
 }
 

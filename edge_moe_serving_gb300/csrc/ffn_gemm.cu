@@ -70,6 +70,7 @@ struct GemmParams {
   int n_fb;                // feature blocks per chunk
   int K;                   // reduction length (H for gate/up, I for down)
   int has_staging;
+  int skip_staging;        // the staging pool is host-resident: its experts are left to the plain GEMV
   int32_t cache_slots, staging_slots;
   const int32_t* perm;     // dispatch position -> token-major row
   __nv_bfloat16* h;        // gate/up output [R, I] (dispatch order)
@@ -82,7 +83,7 @@ struct GemmParams {
 struct Tile {
   int e, r0, rows, N, fb, pool, slot;
   int32_t entry;
-  bool ok;
+  bool ok, skip;   // skip: a staged expert left to another launch (not an error)
 };
 
 template <int kChunk>
@@ -100,7 +101,8 @@ __device__ inline Tile decode_tile(const GemmParams& p, const int* s_pref, int t
   tl.entry = entry;
   tl.pool = (entry >= 0 && (entry & MOE_STAGING_TAG)) ? 1 : 0;
   tl.slot = entry & MOE_SLOT_MASK;
-  tl.ok = entry >= 0 && (entry & ~(MOE_STAGING_TAG | MOE_SLOT_MASK)) == 0 &&
+  tl.skip = p.skip_staging && entry >= 0 && tl.pool == 1;
+  tl.ok = !tl.skip && entry >= 0 && (entry & ~(MOE_STAGING_TAG | MOE_SLOT_MASK)) == 0 &&
           tl.slot < (tl.pool ? p.staging_slots : p.cache_slots) && (tl.pool == 0 || p.has_staging);
   return tl;
 }
@@ -266,7 +268,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_b64, const __grid_constant__
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const Tile tl = decode_tile<CHUNK>(p, s_pref, t);
       if (!tl.ok) {
-        if (tid == 64) set_status(p.status, tl.entry < 0 ? MOE_DEV_ERR_UNBOUND : MOE_DEV_ERR_BAD_SLOT);
+        if (tid == 64 && !tl.skip) set_status(p.status, tl.entry < 0 ? MOE_DEV_ERR_UNBOUND : MOE_DEV_ERR_BAD_SLOT);
         continue;
       }
       if (!mbar_wait(&tmem_full, tphase, abort_flag)) break;
@@ -350,7 +352,9 @@ cudaError_t launch_gemm(const moe_cache& c, int layer, const int32_t* counts, co
                         int T, int R, __nv_bfloat16* h, float* y, __nv_bfloat16* y16, uint32_t* status,
                         cudaStream_t s) {
   if (!gemm_shape_ok(c.H, c.I)) return cudaErrorNotSupported;
-  const bool has_stage = c.staging.w_gate != nullptr;
+  // a host-resident staging pool gets no tensor map: its experts run on the plain GEMV
+  const bool host_stage = c.staging.w_gate != nullptr && c.staging.host != 0;
+  const bool has_stage = c.staging.w_gate != nullptr && !host_stage;
   const uint64_t H = (uint64_t)c.H, I = (uint64_t)c.I;
   GemmParams p;
   p.counts = counts;
@@ -364,6 +368,7 @@ cudaError_t launch_gemm(const moe_cache& c, int layer, const int32_t* counts, co
   p.I = c.I;
   p.min_rows = min_rows;
   p.has_staging = has_stage ? 1 : 0;
+  p.skip_staging = host_stage ? 1 : 0;
   p.cache_slots = c.cache.n_slots;
   p.staging_slots = has_stage ? c.staging.n_slots : 0;
   p.h = h;

@@ -65,10 +65,11 @@ gemv_kernel(GemvParams p) {
     const int ntok = min(NT, cnt - c * NT);
     BankSet bs;
     const int32_t entry = p.c.slot_table[p.layer * p.E + e];
-    if (!resolve_slot(p.c, entry, p.H, p.I, &bs, tid == 0 ? p.status : nullptr)) {
+    if (!resolve_filtered(p.c, entry, p.pool_filter, p.H, p.I, &bs, tid == 0 ? p.status : nullptr)) {
       tau += gsize;
       continue;
     }
+    const bool host_src = p.c.staging.host != 0 && (entry & MOE_STAGING_TAG) != 0;
     const __nv_bfloat16* wrow0;
     const __nv_bfloat16* wrow1;
     if (GATEUP) {
@@ -98,7 +99,11 @@ gemv_kernel(GemvParams p) {
         uint4 w[NG][NR];
 #pragma unroll
         for (int g = 0; g < NG; ++g) {
-          if (g < gsize) {
+          if (g < gsize && host_src) {
+            // the host-resident staging pool: plain streaming loads over the CPU-GPU link
+            w[g][0] = __ldcs(reinterpret_cast<const uint4*>(wrow0 + (size_t)g * K + (size_t)v * 8));
+            if (NR == 2) w[g][NR - 1] = __ldcs(reinterpret_cast<const uint4*>(wrow1 + (size_t)g * K + (size_t)v * 8));
+          } else if (g < gsize) {
             w[g][0] = ldg_stream(wrow0 + (size_t)g * K + (size_t)v * 8);
             if (NR == 2) w[g][NR - 1] = ldg_stream(wrow1 + (size_t)g * K + (size_t)v * 8);
           } else {
@@ -250,6 +255,16 @@ cudaError_t launch_gemv_nt(const GemvParams& p, cudaStream_t s) {
 
 }  // namespace
 
+// The plain-load kernel for any row length, rows per pass bounded by the
+// tokens of the call.
+cudaError_t launch_gemv_plain(const GemvParams& p, cudaStream_t s) {
+  const int bound = std::min(p.T, p.max_rows);
+  if (bound <= 1) return launch_gemv_nt<1>(p, s);
+  if (bound <= 2) return launch_gemv_nt<2>(p, s);
+  if (bound <= 4) return launch_gemv_nt<4>(p, s);
+  return launch_gemv_nt<8>(p, s);
+}
+
 // Rows per pass: bounded by the tokens of the call (a group never exceeds T).
 // Row lengths that are multiples of 256 take the fused TMA-ring kernel.
 cudaError_t launch_gemv(const GemvParams& p, cudaStream_t s) {
@@ -261,10 +276,7 @@ cudaError_t launch_gemv(const GemvParams& p, cudaStream_t s) {
     if (bound <= 4) return launch_ring_nt<4>(p, grid_count, s);
     return launch_ring_nt<8>(p, grid_count, s);
   }
-  if (bound <= 1) return launch_gemv_nt<1>(p, s);
-  if (bound <= 2) return launch_gemv_nt<2>(p, s);
-  if (bound <= 4) return launch_gemv_nt<4>(p, s);
-  return launch_gemv_nt<8>(p, s);
+  return launch_gemv_plain(p, s);
 }
 
 }  // namespace moe

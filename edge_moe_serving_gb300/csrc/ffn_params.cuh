@@ -32,7 +32,11 @@ struct GemvParams {
   // Fused combine (optional): out[t] = sum_j combine_w[t*k+j] * y[t*k+j] after the FFN.
   const float* combine_w;
   __nv_bfloat16* combine_out;
+  int pool_filter;    // kPoolAll, or the pool whose experts this launch takes (host-resident staging pools)
 };
+
+// The plain-load GEMV (no bulk copies): the kernel that may read host memory.
+cudaError_t launch_gemv_plain(const GemvParams& p, cudaStream_t s);
 
 
 cudaError_t launch_gemv(const GemvParams& p, cudaStream_t s);

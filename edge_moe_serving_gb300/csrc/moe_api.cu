@@ -51,6 +51,7 @@ int check_cache(const moe_cache* c) {
   if ((long long)c->n_layers * c->E > MOE_SLOT_MASK) return MOE_ERR_UNSUPPORTED;
   int st = check_pool(c->cache, true);
   if (st != MOE_OK) return st;
+  if (c->cache.host != 0) return MOE_ERR_UNSUPPORTED;   // the cache pool is the GPU's own memory
   return check_pool(c->staging, false);
 }
 
@@ -297,7 +298,10 @@ int moe_layer_forward(const moe_layer* layer, const moe_cache* cache, const void
   if (!ws_aligned(ws)) return MOE_ERR_UNSUPPORTED;
   const LayerWs L = layer_ws(ws, bufs_opt, T, k, E, H, I, ffn_mode);
   const size_t scratch_bytes = ws_bytes - (size_t)(reinterpret_cast<char*>(L.scratch) - reinterpret_cast<char*>(ws));
-  const bool fuse_fill = ffn_mode != MOE_FFN_GEMM && !L.x_perm && gemv_fused_ok(H, I);
+  // A host-resident staging pool is read with plain loads only (the fill copy of the bind step
+  // and the plain GEMV pass of the FFN), so its calls take the per-step launches.
+  const bool host_stage = cache->staging.w_gate != nullptr && cache->staging.host != 0;
+  const bool fuse_fill = ffn_mode != MOE_FFN_GEMM && !L.x_perm && gemv_fused_ok(H, I) && !host_stage;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (fuse_fill && L.logits && decode_layer_ok(T, k, E, H, I, cache->cache.n_slots) && layer->w_router &&
       aligned16(x) && aligned16(layer->w_router)) {
@@ -367,7 +371,7 @@ int moe_layer_forward(const moe_layer* layer, const moe_cache* cache, const void
                                  reinterpret_cast<__nv_bfloat16*>(out));
     return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
   }
-  if (L.x_perm && gemm_shape_ok(H, I) && !(bufs_opt && bufs_opt->y_rows)) {
+  if (L.x_perm && gemm_shape_ok(H, I) && !(bufs_opt && bufs_opt->y_rows) && !host_stage) {
     // Every group runs on the GEMM and nobody reads the expert rows but the
     // combine: keep them in bf16 (half the bytes written and read back).
     __nv_bfloat16* y16 = reinterpret_cast<__nv_bfloat16*>(L.y_rows);

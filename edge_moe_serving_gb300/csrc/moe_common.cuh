@@ -300,6 +300,19 @@ __device__ inline bool resolve_slot(const moe_cache& c, int32_t entry, int H, in
   return true;
 }
 
+// resolve_slot for kernels that take part of the experts only: filter 1
+// skips (silently) experts bound to the staging pool, filter 2 those bound
+// to the cache pool; unbound and malformed entries are reported either way.
+constexpr int kPoolAll = 0, kPoolDeviceOnly = 1, kPoolStagingOnly = 2;
+__device__ inline bool resolve_filtered(const moe_cache& c, int32_t entry, int filter, int H, int I, BankSet* out,
+                                        uint32_t* status) {
+  if (entry >= 0) {
+    const bool staged = (entry & MOE_STAGING_TAG) != 0;
+    if ((filter == kPoolDeviceOnly && staged) || (filter == kPoolStagingOnly && !staged)) return false;
+  }
+  return resolve_slot(c, entry, H, I, out, status);
+}
+
 // ---------------------------------------------------------------- internal launchers
 int num_sms();   // SMs of the current device
 

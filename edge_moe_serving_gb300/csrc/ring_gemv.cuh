@@ -193,7 +193,7 @@ __device__ inline RingSrc ring_source(const GemvParams& p, int e, int entry, int
     r.dst_down = reinterpret_cast<__nv_bfloat16*>(p.c.cache.w_down) + (size_t)fill_dst * per;
     r.fill = r.ok;
   } else {
-    r.ok = resolve_slot(p.c, entry, p.H, p.I, &r.src, status);
+    r.ok = resolve_filtered(p.c, entry, p.pool_filter, p.H, p.I, &r.src, status);
   }
   return r;
 }

@@ -78,12 +78,19 @@ typedef struct CUstream_st* moe_stream_t; /* same type as cudaStream_t; NULL = l
 #define MOE_STAGING_TAG (1 << 30)
 #define MOE_SLOT_MASK ((1 << 30) - 1)
 
-/* One pool of expert banks (bf16, see Layout above). */
+/* One pool of expert banks (bf16, see Layout above).  host = 1: the banks
+ * live in host memory that the GPU reads in place (pinned memory of a Grace
+ * host over NVLink-C2C: the source-of-truth pool of [P] section 3); the
+ * kernels then read it only with plain loads (the fill copy, and a
+ * weight-streaming GEMV for the experts computed in place), never with the
+ * tensor-memory-accelerator copies of the ring and GEMM kernels.  Only the
+ * staging pool may be host-resident. */
 typedef struct moe_pool {
   void* w_gate;   /* [n_slots, I, H] */
   void* w_up;     /* [n_slots, I, H] */
   void* w_down;   /* [n_slots, H, I] */
   int32_t n_slots;
+  int32_t host;   /* 0: device memory; 1: host memory read in place */
 } moe_pool;
 
 /* The expert cache of [P] section 3: one elastic slot pool shared by every
@@ -456,6 +463,36 @@ int moe_layer_forward(const moe_layer* layer, const moe_cache* cache, const void
                       void* out, uint32_t phi_q16, int min_fill, int fill_policy, uint64_t seed,
                       int ffn_mode, const moe_layer_buffers* bufs_opt, void* ws, size_t ws_bytes,
                       uint32_t* dev_status, moe_bind_stats* stats_dev, moe_stream_t stream);
+
+/* Full-layer double-buffered prefill ([P] section 3.1 and Figure 2 (1),
+ * prefill codesign; [W] "Prefill: full-layer double buffering"; [P] section
+ * 5.3: disabled when the pool cannot spare two layers).  Runs n_layers
+ * stacked layers, each on its own input block x[l] (bf16 [T, H]) into out[l]
+ * (bf16 [T, H]), with every expert of every layer in `source`, a pool that
+ * may live in host memory (pinned, or any memory the copy engine and the GPU
+ * reach): layer l's experts are its slots l*E .. l*E+E-1.  layer_buf[0] and
+ * layer_buf[1] are HBM pools of at least E slots.  The copy engine moves
+ * layer l's three banks into layer_buf[l % 2] on copy_stream (one
+ * cudaMemcpyAsync per bank) while layer l-1 computes from the other buffer
+ * on `stream` (moe_layer_forward with phi = 0: every expert is resident in
+ * the buffer).  overlap = 0, or a layer_buf[1] with fewer than E slots or a
+ * NULL bank, loads on demand into layer_buf[0]: each layer's copy waits for
+ * the previous layer.  state: the residency arrays of a cache of n_layers
+ * layers and E slots (slot_table [n_layers*E] with entry l*E+e = e; owner,
+ * stamp [E]; clock), its pools ignored.  ws: moe_layer_workspace_size(layer,
+ * cache, T, ffn_mode) bytes, reused by every layer.  Every launch and copy
+ * only enqueues: the copies fork from `stream` at the call and join it
+ * before the layer that reads them.  The events the call creates are
+ * released once the work completes.  Errors: MOE_ERR_INVALID_ARG for
+ * layers whose shapes differ or whose layer index is not their position, a
+ * source of fewer than n_layers*E slots, a missing layer_buf[0], state
+ * arrays missing or of another shape, copy_stream NULL or equal to stream;
+ * any error of moe_layer_forward; MOE_ERR_CUDA for a failed copy or event
+ * call.  T = 0 returns MOE_OK and launches nothing. */
+int moe_prefill_double_buffered(const moe_layer* layers, int n_layers, const moe_pool* source,
+                                const moe_pool* layer_buf, const moe_cache* state, const void* const* x, int T,
+                                void* const* out, int ffn_mode, int overlap, void* ws, size_t ws_bytes,
+                                uint32_t* dev_status, moe_stream_t stream, moe_stream_t copy_stream);
 
 #ifdef __cplusplus
 }

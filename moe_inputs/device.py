@@ -25,17 +25,23 @@ def to_dev(a: np.ndarray, device) -> torch.Tensor:
 class DeviceCache:
     """Cache pool (A), staging pool (B) and residency state on one device."""
 
-    def __init__(self, cfg: LayerConfig, device="cuda", staging_layers=None):
+    def __init__(self, cfg: LayerConfig, device="cuda", staging_layers=None, staging_host=False):
+        """staging_host: the staging pool (every (layer, expert) pair) lives in
+        pinned host memory, which the GPU reads in place and copies from; the
+        cache pool stays in device memory."""
         self.cfg = cfg
         self.device = device
+        self.staging_host = staging_host
         L, E, H, I = cfg.n_layers, cfg.E, cfg.H, cfg.I
         LE = L * E
-        self.staging = [torch.empty((LE,) + gen.bank_shape(cfg, b), dtype=torch.bfloat16, device=device)
+        where = dict(device="cpu", pin_memory=True) if staging_host else dict(device=device)
+        self.staging = [torch.empty((LE,) + gen.bank_shape(cfg, b), dtype=torch.bfloat16, **where)
                         for b in range(3)]
         n = I * H
         for layer in range(L):
             for b in range(3):
-                pool = to_dev_bf16(gen.bank_pool(cfg, layer, b), device)
+                bits = gen.bank_pool(cfg, layer, b)
+                pool = to_dev_bf16(bits, "cpu" if staging_host else device)
                 offs = gen.bank_offsets(cfg, layer, b)
                 dst = self.staging[b]
                 for e in range(E):
@@ -44,17 +50,24 @@ class DeviceCache:
                 del pool
         st = gen.initial_cache(cfg)
         self.identity = cfg.cache_slots is None
-        if self.identity:
+        if self.identity and not staging_host:
             self.cache = self.staging
         else:
-            owner = torch.from_numpy(st["owner"].astype(np.int64)).to(device)
-            self.cache = [self.staging[b].index_select(0, owner) for b in range(3)]
+            self.cache = [self._gather(b, st["owner"]) for b in range(3)]
         self.table = to_dev(st["table"].astype(np.int32), device)
         self.owner = to_dev(st["owner"].astype(np.int32), device)
         self.stamp = to_dev(st["stamp"].astype(np.uint32).view(np.int32), device)
         self.clock = torch.zeros(1, dtype=torch.int32, device=device)
         self.initial = st
         self.struct = self._make_struct()
+
+    def _gather(self, b, owner):
+        """Cache-pool contents of bank b: the staging slots the owners name."""
+        idx = torch.from_numpy(np.asarray(owner, np.int64))
+        src = self.staging[b]
+        if self.staging_host:
+            return src.index_select(0, idx).to(self.device)
+        return src.index_select(0, idx.to(self.device))
 
     def n_cache_slots(self):
         return self.cache[0].shape[0]
@@ -64,7 +77,7 @@ class DeviceCache:
         c.cache = moe.moe_pool(self.cache[0].data_ptr(), self.cache[1].data_ptr(), self.cache[2].data_ptr(),
                                self.n_cache_slots())
         c.staging = moe.moe_pool(self.staging[0].data_ptr(), self.staging[1].data_ptr(),
-                                 self.staging[2].data_ptr(), self.staging[0].shape[0])
+                                 self.staging[2].data_ptr(), self.staging[0].shape[0], 1 if self.staging_host else 0)
         c.slot_table = self.table.data_ptr()
         c.owner = self.owner.data_ptr()
         c.stamp = self.stamp.data_ptr()
@@ -86,10 +99,9 @@ class DeviceCache:
         self.owner.copy_(to_dev(st["owner"].astype(np.int32), self.device))
         self.stamp.zero_()
         self.clock.zero_()
-        if not self.identity:
-            owner = torch.from_numpy(st["owner"].astype(np.int64)).to(self.device)
+        if self.cache is not self.staging:
             for b in range(3):
-                self.cache[b].copy_(self.staging[b].index_select(0, owner))
+                self.cache[b].copy_(self._gather(b, st["owner"]))
 
 
 class DeviceLayer:
