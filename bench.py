@@ -122,7 +122,7 @@ FFN_MODES = {"auto": lambda m: m.MOE_FFN_AUTO, "gemv": lambda m: m.MOE_FFN_GEMV,
 
 
 # ------------------------------------------------------------------ our arm
-EXTRA_DEFAULT = "prefill,long_prefill,decode_mxfp4"   # sub-records of the default (decode) line
+EXTRA_DEFAULT = "prefill,long_prefill,decode_mxfp4,decode_host_pool,long_prefill_streamed"   # sub-records of the default line
 
 
 def run_workload(cfg, args, world, dev, stream, peaks, moe, torch):
@@ -246,6 +246,12 @@ def run_ours(args, rank, world):
         torch.cuda.empty_cache()
         sub = argparse.Namespace(**vars(args))
         sub.steps = max(args.steps, 20)
+        if name == "decode_host_pool":
+            result[name] = run_host_pool_decode(sub, dev, stream, moe, torch)
+            continue
+        if name == "long_prefill_streamed":
+            result[name] = run_streamed_prefill(sub, dev, stream, moe, torch)
+            continue
         if name == "decode_mxfp4":
             sub.no_cpu_baseline = True
             rec = run_mx(sub)
@@ -459,6 +465,154 @@ def measure_e2e(cfg, dc, layers, decode_like, stream, args, moe, torch, ws, ws_b
     return {"value": round(n * T / el, 3), "unit": UNIT,
             "h2d_bytes_per_step": T * H * 2 * cfg.n_layers, "d2h_bytes_per_step": T * H * 2 * cfg.n_layers,
             "note": "moe_layer_forward per layer; host waits for each step's output"}
+
+
+# ------------------------------------------------------------------ host-resident source pool
+def c2c_rates(moe, torch, nbytes):
+    """B_P (copy engine) and B_H (SMs in place) of pinned host memory, GB/s."""
+    host = torch.empty(nbytes // 4, dtype=torch.int32).pin_memory()
+    dev = torch.empty(nbytes // 4, dtype=torch.int32, device="cuda")
+    prof = moe.moe_bench_bandwidth(host, dev, nbytes, 5, torch.cuda.Stream(), torch.cuda.Stream())
+    return prof.b_p_gbs, prof.b_h_gbs
+
+
+def run_host_pool_decode(args, dev, stream, moe, torch):
+    """The decode workload with its staging pool (every expert) in pinned host
+    memory read over NVLink-C2C: fills are copied into HBM cache slots and
+    in-place experts evaluated from host memory, with plain loads.  One
+    moe_layer_forward per step, events around it, L2 flushed between steps.
+    The bytes that cross the link per step (each fill's expert and each
+    in-place expert, once) over the step time, against the measured rate of
+    SM reads of pinned host memory."""
+    from moe_inputs.device import DeviceCache, DeviceLayer, to_dev_bf16
+    cfg = CONFIGS["decode"]
+    n_steps = args.warmup + args.steps
+    dc = DeviceCache(cfg, dev, staging_host=True)
+    dl = DeviceLayer(cfg, 0, dev)
+    xs = [to_dev_bf16(gen.x_bits(cfg, 0, s), dev) for s in range(n_steps)]
+    mode = FFN_MODES[args.ffn_mode](moe)
+    nb = moe.moe_layer_workspace_size(dl.struct, dc.struct, cfg.T, mode)
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+    out = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stats = torch.zeros(8, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    call = lambda i: moe.moe_layer_forward(dl.struct, dc.struct, xs[i], cfg.T, out, cfg.phi_q16, cfg.min_fill,
+                                           cfg.fill_policy, 1000, mode, None, ws, nb, status, stats, stream)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            call(i)
+            flush.zero_()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    st_host = torch.zeros((args.steps, 8), dtype=torch.int32).pin_memory()
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    n0 = moe.moe_kernel_launch_count()
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            call(args.warmup + i)
+            ev[i][1].record(stream)
+            st_host[i].copy_(stats, non_blocking=True)
+            flush.zero_()
+    torch.cuda.synchronize()
+    launches = moe.moe_kernel_launch_count() - n0
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    t = sum(step_ms) / 1e3
+    sh = st_host.numpy()
+    fields = moe.BIND_STATS_FIELDS
+    n_fill = sh[:, fields.index("n_fill")].astype(np.float64)
+    n_staged = sh[:, fields.index("n_staged")].astype(np.float64)
+    link_bytes = float(np.sum((n_fill + n_staged) * cfg.expert_bytes))
+    b_p, b_h = c2c_rates(moe, torch, cfg.expert_bytes)
+    achieved = link_bytes / t / 1e9
+    return {"value": round(args.steps * cfg.T / t, 3), "unit": UNIT, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(t * 1e3 / args.steps, 5),
+            "step_ms_p10_p50_p90": [round(float(np.percentile(step_ms, q)), 5) for q in (10, 50, 90)],
+            "config": dict(workload_config(cfg, 1), workload="decode_host_pool",
+                           staging_pool="pinned host memory, read over NVLink-C2C with plain loads"),
+            "device_status": int(status.cpu().numpy().view(np.uint32)[0]),
+            "roofline": {"kernel": "whole step (fills and in-place experts cross the CPU-GPU link)", "bound": "c2c",
+                         "achieved": round(achieved, 2), "peak": round(b_h, 2), "unit": "GB/s",
+                         "frac": round(achieved / b_h, 4) if b_h > 0 else None,
+                         "peak_source": "measured in this run: SMs reading pinned host memory in place "
+                                        f"(B_H; the copy engine's B_P = {b_p:.1f} GB/s)",
+                         "link_bytes_per_step": int(link_bytes / args.steps),
+                         "fills_per_step": round(float(np.mean(n_fill)), 3),
+                         "in_place_per_step": round(float(np.mean(n_staged)), 3)},
+            "clocks": clk, "gpu_launches": int(launches), "gpu_launches_per_step": launches / args.steps}
+
+
+def run_streamed_prefill(args, dev, stream, moe, torch):
+    """The long-prefill stack (4 layers x 16384 tokens) with every expert in
+    a pinned host pool: moe_prefill_double_buffered copies each layer's
+    experts into one of two HBM layer buffers with the copy engine, the next
+    layer's while this one computes (overlap), or layer by layer on demand.
+    Both timed; the copy rate (the layers' expert bytes over the stack time)
+    against the measured copy-engine rate B_P."""
+    from moe_inputs.device import DeviceCache, DeviceLayer, to_dev_bf16
+    cfg = CONFIGS["long_prefill"]
+    L, E, T, H = cfg.n_layers, cfg.E, cfg.T, cfg.H
+    src = DeviceCache(cfg, dev, staging_host=True)
+    bufs = [[torch.empty((E,) + gen.bank_shape(cfg, b), dtype=torch.bfloat16, device=dev) for b in range(3)]
+            for _ in range(2)]
+    source = moe.moe_pool(*[t.data_ptr() for t in src.staging], L * E, 1)
+    layer_buf = [moe.moe_pool(*[t.data_ptr() for t in bb], E) for bb in bufs]
+    state = moe.moe_cache()
+    table = torch.from_numpy(np.tile(np.arange(E, dtype=np.int32), L)).to(dev)
+    owner = torch.arange(E, dtype=torch.int32, device=dev)
+    stamp = torch.zeros(E, dtype=torch.int32, device=dev)
+    clock = torch.zeros(1, dtype=torch.int32, device=dev)
+    state.slot_table, state.owner, state.stamp, state.clock = (table.data_ptr(), owner.data_ptr(), stamp.data_ptr(),
+                                                               clock.data_ptr())
+    state.n_layers, state.E, state.H, state.I = L, E, H, cfg.I
+    layers = [DeviceLayer(cfg, l, dev) for l in range(L)]
+    xs = [to_dev_bf16(gen.x_bits(cfg, l, 0), dev) for l in range(L)]
+    outs = [torch.empty((T, H), dtype=torch.bfloat16, device=dev) for _ in range(L)]
+    mode = FFN_MODES[args.ffn_mode](moe)
+    nb = moe.moe_layer_workspace_size(layers[0].struct, src.struct, T, mode)
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    copy_stream = torch.cuda.Stream(device=dev)
+    steps = max(3, min(args.steps, 8))
+    res = {}
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    for overlap in (1, 0):
+        def step():
+            moe.moe_prefill_double_buffered([dl.struct for dl in layers], source, layer_buf, state, xs, T, outs, mode,
+                                            overlap, ws, nb, status, stream, copy_stream)
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                step()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        with torch.cuda.stream(stream):
+            for i in range(steps):
+                ev[i][0].record(stream)
+                step()
+                ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        res[overlap] = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    clk = clocks.stop()
+    copied = float(L * E * cfg.expert_bytes)
+    b_p, b_h = c2c_rates(moe, torch, cfg.expert_bytes)
+    achieved = copied / (res[1] / 1e3) / 1e9
+    return {"value": round(T / (res[1] / 1e3), 3), "unit": UNIT, "steps": steps, "warmup": 2,
+            "ms_per_step": round(res[1], 4), "ms_per_step_on_demand": round(res[0], 4),
+            "overlap_gain": round(res[0] / res[1], 4),
+            "config": dict(workload_config(cfg, 1), workload="long_prefill_streamed",
+                           source_pool="every expert of the 4 layers in pinned host memory",
+                           layer_buffers="2 x 256 experts in HBM"),
+            "device_status": int(status.cpu().numpy().view(np.uint32)[0]),
+            "roofline": {"kernel": "copy engine, host pool -> HBM layer buffers (overlapped with the layers)",
+                         "bound": "c2c", "achieved": round(achieved, 2), "peak": round(b_p, 2), "unit": "GB/s",
+                         "frac": round(achieved / b_p, 4) if b_p > 0 else None,
+                         "peak_source": "measured in this run: copy engine, pinned host -> HBM (B_P)",
+                         "copied_bytes_per_step": int(copied)},
+            "clocks": clk}
 
 
 # ------------------------------------------------------------------ oracle arm
