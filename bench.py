@@ -110,8 +110,9 @@ def router_flops(cfg):
 #    experts x ~192 rows) scaled by the units processed (4x the experts, 4x
 #    the rows): traffic there is each weight byte once plus the activations,
 #    both proportional.
-FFN_TRAFFIC = {"decode": 302662912 + 32312064 + 224 * 16384,
-               "prefill": 4 * (2253835008 + 48209408 + 1126691328 + 92532992)}
+FFN_TRAFFIC = {"decode": 302663424 + 30414336 + 224 * 16384,
+               "prefill": 4 * (2255529216 + 48149760 + 1126688000 + 89227008)}
+MX_TRAFFIC = 81629184   # mx_ring_kernel on the MXFP4 decode call: 1.8826 TB/s x 43.36 us (ncu)
 TRAFFIC_NOTE = {"decode": ("ncu capture of decode_layer_kernel on decode_profile (1 fill) + 224 router rows; "
                            "the rest of the fill's 50 MB is still in L2 when the kernel ends"),
                 "prefill": ("ncu capture of the layer call's two gemm_kernel launches on prefill_profile (bf16 expert "
@@ -864,7 +865,8 @@ def run_mx(args):
         "roofline": {"kernel": "mx_ring_kernel (the expert FFN call: gate/up and down in one weight-streaming launch)",
                      "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(achieved / peaks["hbm_gbs"], 3), "traffic": None,
+                     "frac": round(achieved / peaks["hbm_gbs"], 3), "traffic": MX_TRAFFIC,
+                     "traffic_note": "ncu capture of mx_ring_kernel on this call (dram bytes per second x duration)",
                      "peak_source": f"{peaks['source']} (burst copy bandwidth)",
                      "algorithmic_bytes_per_call": alg, "ffn_us": round(ffn_avg_s * 1e6, 3),
                      "timing": "CUDA events around the FFN graph (counter reset + one kernel), L2 flushed before "
