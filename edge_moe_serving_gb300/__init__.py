@@ -60,6 +60,15 @@ class moe_pool_nvfp4(ctypes.Structure):
                 ("reserved", c_int32)]
 
 
+MOE_FP4_MXFP4, MOE_FP4_NVFP4 = 0, 1
+
+
+class moe_cache_fp4(ctypes.Structure):
+    _fields_ = [("cache", moe_pool_nvfp4), ("staging", moe_pool_nvfp4), ("slot_table", c_void_p),
+                ("owner", c_void_p), ("stamp", c_void_p), ("clock", c_void_p), ("n_layers", c_int32),
+                ("E", c_int32), ("H", c_int32), ("I", c_int32), ("format", c_int32), ("reserved", c_int32)]
+
+
 class moe_bw_profile(ctypes.Structure):
     _fields_ = [("b_p_gbs", c_double), ("b_h_gbs", c_double), ("b_p_contended_gbs", c_double),
                 ("b_h_contended_gbs", c_double), ("phi", c_double), ("phi_contended", c_double),
@@ -108,6 +117,9 @@ def _load():
         "moe_expert_ffn_nvfp4_workspace_size": (c_size_t, [c_int, c_int, c_int]),
         "moe_expert_ffn_nvfp4": (c_int, [POINTER(moe_pool_nvfp4), POINTER(moe_pool_nvfp4), P, c_int, c_int,
                                          c_int, c_int, c_int, P, P, P, P, c_int, c_int, P, P, c_size_t, P, P]),
+        "moe_layer_fp4_workspace_size": (c_size_t, [POINTER(moe_layer), POINTER(moe_cache_fp4), c_int]),
+        "moe_layer_forward_fp4": (c_int, [POINTER(moe_layer), POINTER(moe_cache_fp4), P, c_int, P, c_uint32, c_int,
+                                          c_int, c_uint64, P, c_size_t, P, P, P]),
         "moe_combine": (c_int, [P, P, c_int, c_int, c_int, P, P, P, P]),
         "moe_prefill_double_buffered": (c_int, [POINTER(moe_layer), c_int, POINTER(moe_pool), POINTER(moe_pool),
                                                 POINTER(moe_cache), POINTER(c_void_p), c_int, POINTER(c_void_p),
@@ -131,7 +143,8 @@ EXPORTED = ["moe_version", "moe_status_string", "moe_check_bounded_wait", "moe_k
             "moe_dispatch_workspace_size", "moe_dispatch", "moe_cache_bind_workspace_size",
             "moe_cache_bind_slots", "moe_expert_ffn_workspace_size", "moe_expert_ffn_grouped",
             "moe_expert_ffn_grouped_noalloc", "moe_expert_ffn_mxfp4_workspace_size", "moe_expert_ffn_mxfp4",
-            "moe_expert_ffn_nvfp4_workspace_size", "moe_expert_ffn_nvfp4", "moe_combine",
+            "moe_expert_ffn_nvfp4_workspace_size", "moe_expert_ffn_nvfp4", "moe_layer_fp4_workspace_size",
+            "moe_layer_forward_fp4", "moe_combine",
             "moe_layer_workspace_size", "moe_layer_forward", "moe_prefill_double_buffered"]
 
 
@@ -277,6 +290,18 @@ def moe_expert_ffn_nvfp4(cache_pool, staging_opt, slot_table, n_layers, layer, E
         ctypes.byref(cache_pool), ctypes.byref(staging_opt) if staging_opt is not None else None,
         _p(slot_table), n_layers, layer, E, H, I, _p(counts), _p(offsets), _p(perm), _p(x), T, k, _p(y_rows),
         _p(ws), ws_bytes, _p(dev_status), _s(stream)))
+
+
+def moe_layer_fp4_workspace_size(layer, cache, T):
+    return _lib.moe_layer_fp4_workspace_size(ctypes.byref(layer), ctypes.byref(cache), T)
+
+
+def moe_layer_forward_fp4(layer, cache, x, T, out, phi_q16, min_fill, fill_policy, seed, ws, ws_bytes, dev_status,
+                          stats_dev, stream=None):
+    """cache: a moe_cache_fp4 struct (format MOE_FP4_MXFP4 or MOE_FP4_NVFP4)."""
+    return _check("moe_layer_forward_fp4", _lib.moe_layer_forward_fp4(
+        ctypes.byref(layer), ctypes.byref(cache), _p(x), T, _p(out), phi_q16, min_fill, fill_policy, seed, _p(ws),
+        ws_bytes, _p(dev_status), _p(stats_dev), _s(stream)))
 
 
 def moe_combine(y_rows, topk_w, T, k, H, out, out_f32_opt, dev_status, stream=None):

@@ -426,6 +426,43 @@ int moe_expert_ffn_nvfp4(const moe_pool_nvfp4* cache_pool, const moe_pool_nvfp4*
                          const void* x, int T, int k, float* y_rows, void* ws, size_t ws_bytes,
                          uint32_t* dev_status, moe_stream_t stream);
 
+/* ---------------------------------------------------------------- the layer over FP4 experts
+ * An expert cache whose pools hold block-scaled FP4 experts ([P] section 5.1:
+ * DeepSeek-V4-Flash serves MXFP4 experts, GLM-5.2 and the laptop Qwen3.6
+ * NVFP4 ones; [P] section 4.1: the fill copy moves every bank of an admitted
+ * expert under one list).  The residency arrays are moe_cache's; both pools
+ * have the moe_pool_nvfp4 layout (for MXFP4 the scale banks hold K/32 bytes
+ * per row and tensor_scale is NULL). */
+#define MOE_FP4_MXFP4 0
+#define MOE_FP4_NVFP4 1
+typedef struct moe_cache_fp4 {
+  moe_pool_nvfp4 cache;     /* pool A: the slots the LRU manages */
+  moe_pool_nvfp4 staging;   /* pool B: every (layer, expert) pair at slot layer*E + expert; optional */
+  int32_t* slot_table;      /* [n_layers * E], as moe_cache */
+  int32_t* owner;           /* [cache.n_slots] */
+  uint32_t* stamp;          /* [cache.n_slots] */
+  uint32_t* clock;          /* [1] */
+  int32_t n_layers, E, H, I;
+  int32_t format;           /* MOE_FP4_MXFP4 or MOE_FP4_NVFP4 */
+  int32_t reserved;         /* 0 */
+} moe_cache_fp4;
+
+/* moe_layer_forward over an FP4 expert cache, with per-step launches: router
+ * and top-k, the residency bind (the same decisions and state updates as
+ * moe_cache_bind_slots) with a fill copy of the admitted experts' six code
+ * and scale banks (and tensor scales) from the staging pool into their cache
+ * slots, dispatch, the FP4 expert FFN (moe_expert_ffn_mxfp4 /
+ * moe_expert_ffn_nvfp4) and the combine.  Arguments as moe_layer_forward
+ * (layer->E, H, I equal to the cache's); stats_dev optional.  Errors: those
+ * of the steps, plus MOE_ERR_INVALID_ARG for an unknown format or a shape
+ * mismatch and MOE_ERR_WORKSPACE below moe_layer_fp4_workspace_size.  NVFP4
+ * calls of more than 64 routed rows return MOE_ERR_UNSUPPORTED. */
+size_t moe_layer_fp4_workspace_size(const moe_layer* layer, const moe_cache_fp4* cache, int T);
+int moe_layer_forward_fp4(const moe_layer* layer, const moe_cache_fp4* cache, const void* x, int T, void* out,
+                          uint32_t phi_q16, int min_fill, int fill_policy, uint64_t seed, void* ws,
+                          size_t ws_bytes, uint32_t* dev_status, moe_bind_stats* stats_dev,
+                          moe_stream_t stream);
+
 /* ---------------------------------------------------------------- combine
  * Gate-weighted merge of the expert outputs ([P] section 3.2: the partial
  * sums of the GPU set and the in-place set merge into the exact layer

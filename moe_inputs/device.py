@@ -164,3 +164,65 @@ class NvPool:
             self.banks[2 * b][slot].copy_(torch.from_numpy(np.require(codes, requirements=["C", "W"])))
             self.banks[2 * b + 1][slot].copy_(torch.from_numpy(np.require(scales, requirements=["C", "W"])))
             self.tscale[slot, b] = float(ts)
+
+
+class Fp4Cache:
+    """An FP4 expert cache on one device: the staging pool (every (layer,
+    expert) pair of ``cfg`` at slot layer*E + expert), the cache pool holding
+    the initial owners of gen.initial_cache(cfg), the residency arrays and the
+    moe_cache_fp4 struct.  ``fmt``: moe.MOE_FP4_MXFP4 (banks from
+    gen.mx_expert) or moe.MOE_FP4_NVFP4 (gen.nvfp4_expert)."""
+
+    def __init__(self, cfg: LayerConfig, fmt, seed, device="cuda"):
+        self.cfg, self.fmt, self.seed, self.device = cfg, fmt, seed, device
+        nv = fmt == moe.MOE_FP4_NVFP4
+        sb = 16 if nv else 32
+        L, E, H, I = cfg.n_layers, cfg.E, cfg.H, cfg.I
+        LE = L * E
+        shapes = [(I, H // 2), (I, H // sb), (I, H // 2), (I, H // sb), (H, I // 2), (H, I // sb)]
+        host = [np.zeros((LE,) + s, np.uint8) for s in shapes]
+        tscale = np.zeros((LE, 3), np.float32)
+        for layer in range(L):
+            for e in range(E):
+                slot = layer * E + e
+                if nv:
+                    for b, (codes, scales, ts) in enumerate(gen.nvfp4_expert(seed, layer, e, H, I)):
+                        host[2 * b][slot], host[2 * b + 1][slot], tscale[slot, b] = codes, scales, ts
+                else:
+                    for b, a in enumerate(gen.mx_expert(seed, layer, e, H, I)):
+                        host[b][slot] = a
+        self.staging = [torch.from_numpy(a).to(device) for a in host]
+        self.staging_ts = torch.from_numpy(tscale).to(device) if nv else None
+        st = gen.initial_cache(cfg)
+        idx = torch.from_numpy(np.asarray(st["owner"], np.int64)).to(device)
+        self.cache = [b.index_select(0, idx) for b in self.staging]
+        self.cache_ts = self.staging_ts.index_select(0, idx) if nv else None
+        self.table = to_dev(st["table"].astype(np.int32), device)
+        self.owner = to_dev(st["owner"].astype(np.int32), device)
+        self.stamp = to_dev(st["stamp"].astype(np.uint32).view(np.int32), device)
+        self.clock = torch.zeros(1, dtype=torch.int32, device=device)
+        self.initial = st
+        c = moe.moe_cache_fp4()
+        ptr = lambda t: None if t is None else t.data_ptr()
+        c.cache = moe.moe_pool_nvfp4(*[b.data_ptr() for b in self.cache], ptr(self.cache_ts), len(st["owner"]), 0)
+        c.staging = moe.moe_pool_nvfp4(*[b.data_ptr() for b in self.staging], ptr(self.staging_ts), LE, 0)
+        c.slot_table, c.owner, c.stamp, c.clock = (self.table.data_ptr(), self.owner.data_ptr(),
+                                                   self.stamp.data_ptr(), self.clock.data_ptr())
+        c.n_layers, c.E, c.H, c.I, c.format = L, E, H, I, fmt
+        self.struct = c
+
+    def state(self):
+        """Residency state as numpy, in the oracle's format."""
+        return {"table": self.table.cpu().numpy().astype(np.int64),
+                "owner": self.owner.cpu().numpy().astype(np.int64),
+                "stamp": self.stamp.cpu().numpy().view(np.uint32).astype(np.int64),
+                "clock": int(self.clock.cpu().numpy().view(np.uint32)[0])}
+
+    def cache_matches_owners(self):
+        """Whether every cache slot's banks (and tensor scales) equal, byte for
+        byte, the staging slot of the (layer, expert) pair that owns it."""
+        idx = self.owner.to(torch.int64)
+        pairs = list(zip(self.cache, self.staging))
+        if self.cache_ts is not None:
+            pairs.append((self.cache_ts, self.staging_ts))
+        return all(torch.equal(c, s.index_select(0, idx)) for c, s in pairs)

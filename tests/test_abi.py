@@ -36,6 +36,7 @@ def test_struct_layouts_match_header():
     assert ctypes.sizeof(moe.moe_bw_profile) == 6 * 8 + 4 * 4
     assert ctypes.sizeof(moe.moe_pool_mxfp4) == 6 * 8 + 2 * 4
     assert ctypes.sizeof(moe.moe_pool_nvfp4) == 7 * 8 + 2 * 4
+    assert ctypes.sizeof(moe.moe_cache_fp4) == 2 * 64 + 4 * 8 + 6 * 4
 
 
 def test_status_strings_and_version():
@@ -188,8 +189,49 @@ def test_ffn_argument_checks_and_the_allocation_free_variant():
     assert na(nopool, T=big) == moe.MOE_ERR_INVALID_ARG
 
 
+def test_fp4_layer_argument_checks():
+    """Every check of the FP4 layer call comes before its first launch (the
+    bind would update the residency state): fake non-null pointers, never
+    dereferenced."""
+    L = moe.lib()
+
+    def cache(fmt=moe.MOE_FP4_MXFP4, H=1024, I=1024, ts=256, staging=False, scale=256):
+        c = moe.moe_cache_fp4()
+        c.cache = moe.moe_pool_nvfp4(256, scale, 256, 256, 256, 256, ts, 4, 0)
+        if staging:
+            c.staging = moe.moe_pool_nvfp4(256, 256, 256, 256, 256, 256, ts, 7, 0)
+        c.slot_table, c.owner, c.stamp, c.clock = 256, 256, 256, 256
+        c.n_layers, c.E, c.H, c.I, c.format = 1, 8, H, I, fmt
+        return c
+
+    def call(c, T=1, k=2, H=None, I=None, phi=0, policy=0, ws=256, ws_bytes=1 << 30, x=256):
+        lay = moe.moe_layer(256, None, 0, 8, k, H or c.H, I or c.I)
+        return L.moe_layer_forward_fp4(ctypes.byref(lay), ctypes.byref(c), x, T, 256, phi, 1, policy, 0, ws, ws_bytes,
+                                       None, None, None)
+
+    mx, nv = cache(), cache(moe.MOE_FP4_NVFP4)
+    lay = moe.moe_layer(256, None, 0, 8, 2, 1024, 1024)
+    assert moe.moe_layer_fp4_workspace_size(lay, mx, 4) >= 4 * 2 * 1024 * 4     # the fp32 expert rows
+    assert call(mx, T=0) == moe.MOE_OK
+    assert call(cache(fmt=2)) == moe.MOE_ERR_INVALID_ARG                         # unknown format
+    assert call(mx, H=2048) == moe.MOE_ERR_INVALID_ARG                           # layer and cache disagree
+    assert call(mx, k=9) == moe.MOE_ERR_INVALID_ARG                              # k > E
+    assert call(mx, policy=5) == moe.MOE_ERR_INVALID_ARG
+    assert call(mx, phi=16384) == moe.MOE_ERR_INVALID_ARG                        # fills need a staging pool
+    assert call(cache(staging=True), phi=16384) == moe.MOE_ERR_INVALID_ARG       # staging smaller than n_layers*E
+    assert call(cache(H=1040, I=1040)) == moe.MOE_ERR_UNSUPPORTED                # not a multiple of 32
+    assert call(cache(scale=264)) == moe.MOE_ERR_UNSUPPORTED                     # scale bank not 16-byte aligned
+    assert call(mx, ws_bytes=64) == moe.MOE_ERR_WORKSPACE
+    assert call(mx, ws=272) == moe.MOE_ERR_UNSUPPORTED                           # ws not 256-byte aligned
+    assert call(mx, x=264) == moe.MOE_ERR_UNSUPPORTED                            # x not 16-byte aligned
+    assert call(cache(moe.MOE_FP4_NVFP4, ts=None)) == moe.MOE_ERR_INVALID_ARG    # NVFP4 without tensor scales
+    assert call(cache(moe.MOE_FP4_NVFP4, ts=258)) == moe.MOE_ERR_UNSUPPORTED     # tensor scales not 4-byte aligned
+    assert call(nv, T=33) == moe.MOE_ERR_UNSUPPORTED                             # NVFP4: at most 64 routed rows
+    assert call(cache(moe.MOE_FP4_NVFP4, H=1536, I=1536)) == moe.MOE_ERR_UNSUPPORTED   # not a ring-kernel shape
+
+
 STRUCTS = ["moe_pool", "moe_cache", "moe_bind_stats", "moe_layer", "moe_layer_buffers", "moe_bw_profile",
-           "moe_pool_mxfp4", "moe_pool_nvfp4"]
+           "moe_pool_mxfp4", "moe_pool_nvfp4", "moe_cache_fp4"]
 
 
 def test_header_is_plain_c_and_matches_the_binding_layouts(tmp_path):
