@@ -126,20 +126,51 @@ FFN_MODES = {"auto": lambda m: m.MOE_FFN_AUTO, "gemv": lambda m: m.MOE_FFN_GEMV,
 EXTRA_DEFAULT = "prefill,long_prefill,decode_mxfp4,decode_host_pool,long_prefill_streamed"   # sub-records of the default line
 
 
+L2_BYTES = 129 << 20   # the GB300's L2
+
+
+def inputs_exceed_l2(cfg):
+    """Whether every step reads more than twice the L2 in expert weights alone
+    (at least k distinct experts per token, every layer), so that steps can
+    run back to back with no flush between them: a step cannot find the
+    previous step's weights in L2."""
+    return cfg.n_layers * cfg.k * cfg.expert_bytes > 2 * L2_BYTES
+
+
 def run_workload(cfg, args, world, dev, stream, peaks, moe, torch):
     """Measure one workload: ``args.warmup`` untimed steps, then ``args.steps``
     timed steps.  A step is one moe_layer_forward call per layer of the
     workload, launched directly on ``stream`` (the decode layer is one kernel,
-    so a graph would only add its replay); CUDA events bracket each step and
-    L2 is flushed (256 MB write) between steps, outside the events.  Returns
-    the measurement record (tokens/s, step times, the dominant kernel's
-    roofline, clocks, end to end, launch counts)."""
+    so a graph would only add its replay).  Timing: where every step reads
+    more than twice the L2 in expert weights (decode, prefill, long prefill),
+    the timed steps run back to back between one pair of CUDA events, as a
+    serving loop issues them; otherwise CUDA events bracket each step and L2
+    is flushed (256 MB write) between steps, outside the events.  Decode-like
+    workloads also get the isolated-step figures: the same trace again from
+    the initial state, each step between its own events after a flush.
+    Returns the measurement record (tokens/s, step times, the dominant
+    kernel's roofline, clocks, end to end, launch counts)."""
     from moe_inputs.device import DeviceCache, DeviceLayer, to_dev_bf16
 
     decode_like = cfg.steps > 1
+    back_to_back = inputs_exceed_l2(cfg)
     n_steps = args.warmup + args.steps
     dc = DeviceCache(cfg, dev)
     layers = [DeviceLayer(cfg, l, dev) for l in range(cfg.n_layers)]
+    # back to back, consecutive steps read their router weights from copies (equal values) that together
+    # exceed twice the L2, as the layers of a model would: no step finds its router rows in L2 (the expert
+    # weights stream evict-first, so a few router copies would stay resident)
+    router_sets = [[dl.struct for dl in layers]]
+    router_copies = []
+    if back_to_back:
+        per_set = cfg.n_layers * cfg.E * cfg.H * 4
+        for _ in range(-(-2 * L2_BYTES // per_set)):
+            row = []
+            for dl in layers:
+                w = dl.w_router.clone()
+                router_copies.append(w)
+                row.append(moe.moe_layer(w.data_ptr(), dl.struct.bias, dl.layer, cfg.E, cfg.k, cfg.H, cfg.I))
+            router_sets.append(row)
     # per-step inputs (decode: a stream of tokens; prefill: one block per layer, reused every step)
     if decode_like:
         xs = [to_dev_bf16(gen.x_bits(cfg, 0, s), dev) for s in range(n_steps)]
@@ -151,15 +182,16 @@ def run_workload(cfg, args, world, dev, stream, peaks, moe, torch):
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    stats = torch.zeros(8, dtype=torch.int32, device=dev)
+    stats = torch.zeros((n_steps, 8), dtype=torch.int32, device=dev)   # each step's residency counts
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     def step_body(i):
         # decode: step i's token row; prefill: every layer's resident block
+        lay = router_sets[i % len(router_sets)]
         for l in range(cfg.n_layers):
-            moe.moe_layer_forward(layers[l].struct, dc.struct, xs[i] if decode_like else xs[l], T, out, cfg.phi_q16,
-                                  cfg.min_fill, cfg.fill_policy, 1000 + l, mode, None, ws, ws_bytes, status, stats,
-                                  stream)
+            moe.moe_layer_forward(lay[l], dc.struct, xs[i] if decode_like else xs[l], T, out, cfg.phi_q16,
+                                  cfg.min_fill, cfg.fill_policy, 1000 + l, mode, None, ws, ws_bytes, status,
+                                  stats[i], stream)
 
     # one call sets kernel attributes and occupancy caches; then the trace starts from the initial state
     with torch.cuda.stream(stream):
@@ -173,12 +205,27 @@ def run_workload(cfg, args, world, dev, stream, peaks, moe, torch):
             import torch.distributed as dist
             dist.barrier()
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    stats_host = torch.zeros((args.steps, 8), dtype=torch.int32).pin_memory()
-    with torch.cuda.stream(stream):
-        for s in range(args.warmup):
-            step_body(s)
-            flush.zero_()
+    def isolated_steps():
+        """Each step of the trace between its own events, L2 flushed before it."""
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_steps)]
+        with torch.cuda.stream(stream):
+            for i in range(n_steps):
+                flush.zero_()
+                ev[i][0].record(stream)
+                step_body(i)
+                ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in ev[args.warmup:]]
+
+    if back_to_back:
+        with torch.cuda.stream(stream):
+            for s in range(args.warmup):
+                step_body(s)
+    else:
+        with torch.cuda.stream(stream):
+            for s in range(args.warmup):
+                step_body(s)
+                flush.zero_()
     torch.cuda.synchronize()
     barrier()
     torch.cuda.synchronize()
@@ -186,37 +233,69 @@ def run_workload(cfg, args, world, dev, stream, peaks, moe, torch):
     clocks.start()
     n0 = moe.moe_kernel_launch_count()
     t0 = time.perf_counter()
-    with torch.cuda.stream(stream):
-        for i in range(args.steps):
-            ev[i][0].record(stream)
-            step_body(args.warmup + i)
-            ev[i][1].record(stream)
-            stats_host[i].copy_(stats, non_blocking=True)   # residency counts of the step, outside the events
-            flush.zero_()
-    torch.cuda.synchronize()
+    if back_to_back:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for i in range(args.steps):
+                step_body(args.warmup + i)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        total_ms = e0.elapsed_time(e1)
+        step_ms = None
+    else:
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                ev[i][0].record(stream)
+                step_body(args.warmup + i)
+                ev[i][1].record(stream)
+                flush.zero_()
+        torch.cuda.synchronize()
+        step_ms = [a.elapsed_time(b) for a, b in ev]
+        total_ms = sum(step_ms)
     barrier()
     bracket_s = time.perf_counter() - t0
     launches = moe.moe_kernel_launch_count() - n0
     clk = clocks.stop()
-    step_ms = [a.elapsed_time(b) for a, b in ev]
-    total_s = sum(step_ms) / 1e3
+    total_s = total_ms / 1e3
     dev_status = int(status.cpu().numpy().view(np.uint32)[0])
+    step_stats = stats[args.warmup:].cpu().numpy()
     total_s, value = aggregate_replicas(total_s, args.steps, T, world, dev)
     kernels_per_step = launches / args.steps
+    isolated = None
+    if decode_like:
+        dc.reset()
+        torch.cuda.synchronize()
+        iso_ms = isolated_steps()
+        isolated = {"ms_per_step": round(float(np.mean(iso_ms)), 5),
+                    "step_ms_p10_p50_p90": [round(float(np.percentile(iso_ms, q)), 5) for q in (10, 50, 90)],
+                    "tokens_per_s": round(len(iso_ms) * T / (sum(iso_ms) / 1e3), 3),
+                    "note": "the same trace from the initial state, each step between its own CUDA events "
+                            "after a 256 MB L2-flush write: the latency of one call, launch included"}
 
     # ---- dominant kernel: decode-sized calls run the whole layer as one kernel (the timed
     # step itself); otherwise the expert-FFN call, timed alone
     if kernels_per_step == cfg.n_layers:
-        roof = decode_step_roofline(cfg, step_ms, stats_host.numpy(), peaks)
+        roof = decode_step_roofline(cfg, total_ms, args.steps, step_stats, peaks, back_to_back)
     else:
         roof = measure_ffn_roofline(cfg, dc, layers, xs, decode_like, stream, peaks, args, moe, torch)
-    e2e = measure_e2e(cfg, dc, layers, decode_like, stream, args, moe, torch, ws, ws_bytes, status, stats)
+    e2e = measure_e2e(cfg, dc, layers, decode_like, stream, args, moe, torch, ws, ws_bytes, status, stats[0])
     rec = {"value": round(value, 3), "unit": UNIT, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": round(total_s * 1e3 / args.steps, 5),
-           "step_ms_p10_p50_p90": [round(float(np.percentile(step_ms, q)), 5) for q in (10, 50, 90)],
+           "timing": ("back to back: one CUDA-event pair around the timed steps (every step reads more than "
+                      "twice the L2 in expert weights; consecutive steps read the router weights from %d "
+                      "copies in turn, %.0f MB in all)" % (len(router_sets), len(router_sets) * cfg.n_layers * cfg.E
+                                                            * cfg.H * 4 / 1e6)) if back_to_back else
+                     "CUDA events around each step, L2 flushed between steps",
            "bracket_ms_per_step": round(bracket_s * 1e3 / args.steps, 5),
-           "config": workload_config(cfg, world), "device_status": dev_status, "roofline": roof,
+           "config": workload_config(cfg, world, back_to_back), "device_status": dev_status, "roofline": roof,
            "clocks": clk, "e2e": e2e, "gpu_launches": int(launches), "gpu_launches_per_step": kernels_per_step}
+    if step_ms is not None:
+        rec["step_ms_p10_p50_p90"] = [round(float(np.percentile(step_ms, q)), 5) for q in (10, 50, 90)]
+    if isolated is not None:
+        rec["isolated_step"] = isolated
     if not decode_like:
         # the whole step against the bf16 tensor peak (expert FFN + router FLOPs of every layer)
         fl = cfg.n_layers * (expert_ffn_flops(cfg) + router_flops(cfg))
@@ -278,37 +357,45 @@ def aggregate_replicas(local_s, steps, tokens_per_step, world, device="cpu"):
     return job_s, world * steps * tokens_per_step / job_s
 
 
-def workload_config(cfg, world):
+def workload_config(cfg, world, back_to_back=False):
+    l2 = ("inputs larger than L2: at least %.0f MB of expert weights per step (L2 129 MB), steps back to back, "
+          "no flush" % (cfg.n_layers * cfg.k * cfg.expert_bytes / 1e6)) if back_to_back else \
+        "flushed between steps (256 MB write)"
     return {"workload": cfg.name, "tokens_per_layer_call": cfg.T, "hidden": cfg.H, "experts": cfg.E,
             "top_k": cfg.k, "intermediate": cfg.I, "layers_per_step": cfg.n_layers,
             "cache_slots": cfg.cache_slots if cfg.cache_slots is not None else cfg.n_layers * cfg.E,
             "phi_q16": cfg.phi_q16, "fill_policy": "random" if cfg.fill_policy else "lowest_id",
-            "routing_bias": cfg.bias, "l2": "flushed between steps (256 MB write)",
+            "routing_bias": cfg.bias, "l2": l2,
             "parallelism": f"replicas x{world}", "launch": "moe_layer_forward per layer, direct launches"}
 
 
-def decode_step_roofline(cfg, step_ms, stats, peaks):
+def decode_step_roofline(cfg, total_ms, steps, stats, peaks, back_to_back):
     """Decode-sized steps are one kernel (router, residency decision, fused
     gate/up + down weight streaming with cache fills, combine).  Algorithmic
-    bytes per step: every distinct routed expert's weights once, one more
-    expert write per cache fill, the router weights, and the activations
-    (token row, h, y rows, output).  Duration: the CUDA events around the
-    step (the kernel and its 4 + T*k word counter reset)."""
-    T, k, E, H, I = cfg.T, cfg.k, cfg.E, cfg.H, cfg.I
-    R = T * k
+    bytes per step, as the method counts them: every distinct routed expert's
+    weights once, the router weights, the token row in and the output row out;
+    each cache fill writes one more expert (the fill's read is the stream's
+    own), reported beside them and included in the credited bytes.  Duration:
+    the timed steps' CUDA-event time over the number of steps (the kernel and
+    its 4 + T*k word counter reset)."""
+    T, E, H = cfg.T, cfg.E, cfg.H
     n_unique, n_fill = stats[:, 0].astype(np.float64), stats[:, 4].astype(np.float64)
-    act = T * H * 2 + R * I * 2 * 2 + R * H * 4 * 2 + T * H * 2
-    byts = (n_unique + n_fill) * cfg.expert_bytes + E * H * 4 + act
-    t = float(np.sum(step_ms)) / 1e3
-    achieved = float(np.sum(byts)) / t / 1e9
+    method = n_unique * cfg.expert_bytes + E * H * 4 + 2 * T * H * 2
+    fills = n_fill * cfg.expert_bytes
+    t = total_ms / 1e3
+    achieved = float(np.sum(method + fills)) / t / 1e9
+    no_fill = float(np.sum(method)) / t / 1e9
     peak = peaks["hbm_gbs"]
     return {"kernel": "decode_layer_kernel (whole layer in one cooperative launch)", "bound": "hbm",
             "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
             "traffic": FFN_TRAFFIC.get(cfg.name), "traffic_note": TRAFFIC_NOTE.get(cfg.name),
             "peak_source": peaks["source"] + " (burst copy bandwidth)",
-            "algorithmic_bytes_per_step": int(np.mean(byts)), "step_us": round(t / len(step_ms) * 1e6, 3),
-            "fills_per_step": round(float(np.mean(n_fill)), 3),
-            "timing": "CUDA events around each timed step (the kernel is the whole step)"}
+            "algorithmic_bytes_per_step": int(np.mean(method + fills)),
+            "fill_bytes_per_step": int(np.mean(fills)), "fills_per_step": round(float(np.mean(n_fill)), 3),
+            "frac_without_fill_bytes": round(no_fill / peak, 4),
+            "step_us": round(t / steps * 1e6, 3),
+            "timing": ("one CUDA-event pair around the timed steps, back to back" if back_to_back else
+                       "CUDA events around each timed step") + " (the kernel is the whole step)"}
 
 
 def ffn_bytes(cfg, active):
@@ -688,8 +775,8 @@ def run_reference(args, rank, world):
     cb = run_oracle_bounded(cfg, per_step_budget * args.steps, max_steps=args.steps)
     return {"metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": workload_config(cfg, world),
-            "impl": "reference", "cpu_baseline": cb,
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(cfg, world, inputs_exceed_l2(cfg)), "impl": "reference", "cpu_baseline": cb,
             "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
