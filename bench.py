@@ -123,7 +123,7 @@ FFN_MODES = {"auto": lambda m: m.MOE_FFN_AUTO, "gemv": lambda m: m.MOE_FFN_GEMV,
 
 
 # ------------------------------------------------------------------ our arm
-EXTRA_DEFAULT = "prefill,long_prefill,decode_mxfp4,decode_host_pool,long_prefill_streamed"   # sub-records of the default line
+EXTRA_DEFAULT = "prefill,long_prefill,decode_mxfp4,prefill_mxfp4,decode_host_pool,long_prefill_streamed"   # sub-records of the default line
 
 
 L2_BYTES = 129 << 20   # the GB300's L2
@@ -331,6 +331,9 @@ def run_ours(args, rank, world):
             continue
         if name == "long_prefill_streamed":
             result[name] = run_streamed_prefill(sub, dev, stream, moe, torch)
+            continue
+        if name in ("prefill_mxfp4", "prefill_nvfp4"):
+            result[name] = run_fp4_prefill(sub, dev, stream, moe, torch, name.split("_")[1])
             continue
         if name == "decode_mxfp4":
             sub.no_cpu_baseline = True
@@ -811,6 +814,115 @@ def mx_expert_bytes(H, I):
     return 3 * (H * I // 2 + H * I // 32)
 
 
+def run_fp4_prefill(args, dev, stream, moe, torch, fmt_name="mxfp4"):
+    """The 8192-token prefill layer over FP4 experts: moe_layer_forward_fp4
+    (router + top-k, residency bind, dispatch, the FP4 expert FFN on the
+    tensor-core GEMM, combine) with all 256 experts resident, phi = 0.  Steps
+    back to back between one pair of CUDA events (each reads 3.4 GB of expert
+    codes and scales, over twice the L2).  The FFN call alone (gather +
+    gate/up + down GEMMs) is then timed after route and dispatch, with an L2
+    flush before it."""
+    from moe_inputs.device import DeviceLayer, Fp4Cache, to_dev_bf16
+    peaks = load_peaks()
+    cfg = CONFIGS["prefill"]
+    fmt = moe.MOE_FP4_MXFP4 if fmt_name == "mxfp4" else moe.MOE_FP4_NVFP4
+    T, H, E, k, I = cfg.T, cfg.H, cfg.E, cfg.k, cfg.I
+    fc = Fp4Cache(cfg, fmt, MX_SEED, dev)
+    dl = DeviceLayer(cfg, 0, dev)
+    x = to_dev_bf16(gen.x_bits(cfg, 0, 0), dev)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    nb = moe.moe_layer_fp4_workspace_size(dl.struct, fc.struct, T)
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+
+    def step():
+        moe.moe_layer_forward_fp4(dl.struct, fc.struct, x, T, out, 0, 1, 0, 0, ws, nb, status, None, stream)
+
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    n0 = moe.moe_kernel_launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    launches = moe.moe_kernel_launch_count() - n0
+    step_s = e0.elapsed_time(e1) / 1e3 / args.steps
+
+    # the FFN call alone, after route and dispatch, L2 flushed before it
+    R = T * k
+    i32 = lambda n: torch.empty(max(n, 1), dtype=torch.int32, device=dev)
+    ids, counts, offsets, perm, inv = i32(R), i32(E), i32(E + 1), i32(R), i32(R)
+    w = torch.empty(R, dtype=torch.float32, device=dev)
+    y = torch.empty((R, H), dtype=torch.float32, device=dev)
+    nr, nd = moe.moe_route_topk_workspace_size(T, H, E), moe.moe_dispatch_workspace_size(T, k, E)
+    nf = (moe.moe_expert_ffn_mxfp4_workspace_size if fmt == moe.MOE_FP4_MXFP4 else
+          moe.moe_expert_ffn_nvfp4_workspace_size)(T, k, H, I)
+    ws_r, ws_d, ws_f = (torch.empty(max(n, 256), dtype=torch.uint8, device=dev) for n in (nr, nd, nf))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    c = fc.struct.cache
+    if fmt == moe.MOE_FP4_MXFP4:
+        pool = moe.moe_pool_mxfp4(c.gate_q, c.gate_s, c.up_q, c.up_s, c.down_q, c.down_s, c.n_slots, 0)
+        ffn_call = moe.moe_expert_ffn_mxfp4
+    else:
+        pool = c
+        ffn_call = moe.moe_expert_ffn_nvfp4
+    with torch.cuda.stream(stream):
+        moe.moe_route_topk(x, T, H, dl.w_router, dl.bias, E, k, ids, w, None, ws_r, nr, status, stream)
+        moe.moe_dispatch(ids, T, k, E, counts, offsets, perm, inv, None, H, None, ws_d, nd, status, stream)
+    fev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup + args.steps):
+            flush.zero_()
+            if i >= args.warmup:
+                fev[i - args.warmup][0].record(stream)
+            ffn_call(pool, None, fc.table, 1, 0, E, H, I, counts, offsets, perm, x, T, k, y, ws_f, nf, status, stream)
+            if i >= args.warmup:
+                fev[i - args.warmup][1].record(stream)
+    torch.cuda.synchronize()
+    ffn_s = sum(a.elapsed_time(b) for a, b in fev) / 1e3 / args.steps
+    dev_status = int(status.cpu().numpy().view(np.uint32)[0])
+    fl = expert_ffn_flops(cfg)
+    tf = fl / ffn_s / 1e12
+    sb = 32 if fmt == moe.MOE_FP4_MXFP4 else 16
+    byts = 3 * E * (H * I // 2 + H * I // sb) + 2 * T * H * 2   # every expert's codes and scales, x in, out
+    step_fl = fl + router_flops(cfg)
+    return {"value": round(T / step_s, 3), "unit": UNIT, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(step_s * 1e3, 5),
+            "dtype": f"{fmt_name} weights expanded to bf16 in shared memory, bf16 activations, fp32 accumulation",
+            "config": {"workload": f"prefill_{fmt_name}", "tokens_per_layer_call": T, "hidden": H, "experts": E,
+                       "top_k": k, "intermediate": I, "residency": "all 256 experts resident, phi = 0",
+                       "l2": "inputs larger than L2 (%.1f GB of codes and scales per step), steps back to back"
+                             % (byts / 1e9),
+                       "launch": "moe_layer_forward_fp4, direct launches"},
+            "device_status": dev_status,
+            "roofline": {"kernel": "fp4_gemm_kernel (gate/up + down) with the token-row gather: the FFN call",
+                         "bound": "tensor", "achieved": round(tf, 2), "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4),
+                         "peak_source": peaks["source"] + " (burst cuBLAS bf16; the MMAs are bf16)",
+                         "flops_per_call": fl, "call_us": round(ffn_s * 1e6, 3), "traffic": None,
+                         "other_roofline": {"bound": "hbm", "achieved": round(byts / ffn_s / 1e9, 2),
+                                            "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                            "frac": round(byts / ffn_s / 1e9 / peaks["hbm_gbs"], 4),
+                                            "algorithmic_bytes_per_call": byts},
+                         "timing": "CUDA events around the FFN call, L2 flushed before each"},
+            "step_roofline": {"bound": "tensor", "achieved": round(step_fl / step_s / 1e12, 2),
+                              "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                              "frac": round(step_fl / step_s / 1e12 / peaks["bf16_tflops"], 4),
+                              "flops_per_step": step_fl},
+            "clocks": clk, "gpu_launches": int(launches), "gpu_launches_per_step": launches / args.steps}
+
+
 def oracle_mx_step(cfg, step, O):
     x = gen.bf16_bits_to_f64(gen.x_bits(cfg, 0, step))
     ids, w = O.select_topk(O.router_logits(x, gen.w_router(cfg), gen.bias(cfg)), cfg.k)
@@ -852,7 +964,7 @@ def run_mx(args):
     x_in = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     nr, nd, nm = (moe.moe_route_topk_workspace_size(T, H, E), moe.moe_dispatch_workspace_size(T, k, E),
-                  moe.moe_expert_ffn_mxfp4_workspace_size(T, k, I))
+                  moe.moe_expert_ffn_mxfp4_workspace_size(T, k, H, I))
     ws_r, ws_d, ws_m = (torch.empty(max(n, 256), dtype=torch.uint8, device=dev) for n in (nr, nd, nm))
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 

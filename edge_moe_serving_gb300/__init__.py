@@ -111,10 +111,10 @@ def _load():
                                            P, P, c_size_t, P, P]),
         "moe_expert_ffn_grouped_noalloc": (c_int, [POINTER(moe_cache), c_int, P, P, P, P, P, c_int, c_int, P,
                                                    c_int, P, P, P]),
-        "moe_expert_ffn_mxfp4_workspace_size": (c_size_t, [c_int, c_int, c_int]),
+        "moe_expert_ffn_mxfp4_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int]),
         "moe_expert_ffn_mxfp4": (c_int, [POINTER(moe_pool_mxfp4), POINTER(moe_pool_mxfp4), P, c_int, c_int,
                                          c_int, c_int, c_int, P, P, P, P, c_int, c_int, P, P, c_size_t, P, P]),
-        "moe_expert_ffn_nvfp4_workspace_size": (c_size_t, [c_int, c_int, c_int]),
+        "moe_expert_ffn_nvfp4_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int]),
         "moe_expert_ffn_nvfp4": (c_int, [POINTER(moe_pool_nvfp4), POINTER(moe_pool_nvfp4), P, c_int, c_int,
                                          c_int, c_int, c_int, P, P, P, P, c_int, c_int, P, P, c_size_t, P, P]),
         "moe_layer_fp4_workspace_size": (c_size_t, [POINTER(moe_layer), POINTER(moe_cache_fp4), c_int]),
@@ -266,8 +266,8 @@ def moe_expert_ffn_grouped_noalloc(cache, layer, counts, offsets, perm, x, x_per
         _p(expert_mask_opt), ffn_mode, _p(y_rows), _p(dev_status), _s(stream)))
 
 
-def moe_expert_ffn_mxfp4_workspace_size(T, k, I):
-    return _lib.moe_expert_ffn_mxfp4_workspace_size(T, k, I)
+def moe_expert_ffn_mxfp4_workspace_size(T, k, H, I):
+    return _lib.moe_expert_ffn_mxfp4_workspace_size(T, k, H, I)
 
 
 def moe_expert_ffn_mxfp4(cache_pool, staging_opt, slot_table, n_layers, layer, E, H, I, counts, offsets, perm, x,
@@ -279,8 +279,8 @@ def moe_expert_ffn_mxfp4(cache_pool, staging_opt, slot_table, n_layers, layer, E
         _p(ws), ws_bytes, _p(dev_status), _s(stream)))
 
 
-def moe_expert_ffn_nvfp4_workspace_size(T, k, I):
-    return _lib.moe_expert_ffn_nvfp4_workspace_size(T, k, I)
+def moe_expert_ffn_nvfp4_workspace_size(T, k, H, I):
+    return _lib.moe_expert_ffn_nvfp4_workspace_size(T, k, H, I)
 
 
 def moe_expert_ffn_nvfp4(cache_pool, staging_opt, slot_table, n_layers, layer, E, H, I, counts, offsets, perm, x,

@@ -16,7 +16,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libmoe.so")
 SOURCES = ["moe_api.cu", "route_topk.cu", "route_tc.cu", "dispatch.cu", "bind.cu", "ffn.cu", "ffn_gemv.cu",
            "ffn_gemm.cu", "combine.cu", "ffn_noalloc.cu",
-           "front_small.cu", "decode_layer.cu", "selftest.cu", "bandwidth.cu", "ffn_mxfp4.cu", "ffn_mxfp4_ring.cu", "prefill_stack.cu",
+           "front_small.cu", "decode_layer.cu", "selftest.cu", "bandwidth.cu", "ffn_mxfp4.cu", "ffn_mxfp4_ring.cu", "ffn_fp4_gemm.cu", "prefill_stack.cu",
            "fp4_layer.cu"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 

@@ -253,9 +253,12 @@ int check_nv_pool(const moe_pool_nvfp4* pool) {
   return MOE_OK;
 }
 
-// h rows (bf16 [T*k, I]), then the ring kernel's per-instance counters
-size_t mx_ws_bytes(int T, int k, int I) {
-  return align_up((size_t)T * k * I * sizeof(__nv_bfloat16), 256) + align_up((size_t)T * k * sizeof(unsigned int), 256);
+// h rows (bf16 [T*k, I]), the ring kernel's per-instance counters, then the
+// token rows in dispatch order (bf16 [T*k, H], the tensor-core GEMM's operand)
+size_t mx_ws_bytes(int T, int k, int H, int I) {
+  const size_t R = (size_t)T * k;
+  return align_up(R * I * sizeof(__nv_bfloat16), 256) + align_up(R * sizeof(unsigned int), 256) +
+         align_up(R * H * sizeof(__nv_bfloat16), 256);
 }
 
 // Checks shared by the two FP4 entry points (the pools are checked by the
@@ -266,7 +269,7 @@ int fp4_common(const int32_t* slot_table, int n_layers, int layer, int E, int H,
   if (T == 0) return MOE_OK;
   if (!counts || !offsets || !perm || !x || !y_rows) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(y_rows)) return MOE_ERR_UNSUPPORTED;
-  if (!ws || ws_bytes < mx_ws_bytes(T, k, I)) return MOE_ERR_WORKSPACE;
+  if (!ws || ws_bytes < mx_ws_bytes(T, k, H, I)) return MOE_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_UNSUPPORTED;   // h rows are read as 16-byte vectors
   p->slot_table = slot_table;
   p->layer = layer;
@@ -279,8 +282,10 @@ int fp4_common(const int32_t* slot_table, int n_layers, int layer, int E, int H,
   p->perm = perm;
   p->x = reinterpret_cast<const __nv_bfloat16*>(x);
   p->h = reinterpret_cast<__nv_bfloat16*>(ws);
-  p->inst_done = reinterpret_cast<unsigned int*>(reinterpret_cast<char*>(ws) +
-                                                 align_up((size_t)T * k * I * sizeof(__nv_bfloat16), 256));
+  const size_t h_bytes = align_up((size_t)T * k * I * sizeof(__nv_bfloat16), 256);
+  p->inst_done = reinterpret_cast<unsigned int*>(reinterpret_cast<char*>(ws) + h_bytes);
+  p->x_perm = reinterpret_cast<__nv_bfloat16*>(reinterpret_cast<char*>(ws) + h_bytes +
+                                               align_up((size_t)T * k * sizeof(unsigned int), 256));
   p->y = y_rows;
   p->status = dev_status;
   return MOE_OK;
@@ -297,12 +302,20 @@ int shape_check(const void* cache_pool, const int32_t* slot_table, int n_layers,
   return MOE_OK;
 }
 
+// The tensor-core GEMM: the token rows gathered in dispatch order, then the
+// gate/up and down launches.
+cudaError_t run_fp4_gemm(const MxParams& p, bool nv, int T, cudaStream_t s) {
+  const cudaError_t err = launch_gather(p.x, p.H, p.k, p.perm, p.offsets, p.E, T * p.k, p.x_perm, s);
+  if (err != cudaSuccess) return err;
+  return launch_fp4_gemm(p, nv, p.x_perm, T, s);
+}
+
 }  // namespace
 }  // namespace moe
 
-extern "C" size_t moe_expert_ffn_mxfp4_workspace_size(int T, int k, int I) {
-  if (T < 0 || k < 1 || I < moe::kMxBlock || (long long)T * k > INT_MAX / 2) return 0;
-  return moe::mx_ws_bytes(T, k, I);
+extern "C" size_t moe_expert_ffn_mxfp4_workspace_size(int T, int k, int H, int I) {
+  if (T < 0 || k < 1 || H < moe::kMxBlock || I < moe::kMxBlock || (long long)T * k > INT_MAX / 2) return 0;
+  return moe::mx_ws_bytes(T, k, H, I);
 }
 
 extern "C" int moe_expert_ffn_mxfp4(const moe_pool_mxfp4* cache_pool, const moe_pool_mxfp4* staging_opt,
@@ -328,15 +341,16 @@ extern "C" int moe_expert_ffn_mxfp4(const moe_pool_mxfp4* cache_pool, const moe_
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t err;
   if (fp4_ring_ok(p, T, false)) err = launch_fp4_ring(p, T, false, s);
+  else if (fp4_gemm_ok(p, false)) err = run_fp4_gemm(p, false, T, s);
   else if (T <= 1) err = launch_mx_nt<1>(p, s);
   else if (T <= 2) err = launch_mx_nt<2>(p, s);
   else err = launch_mx_nt<4>(p, s);
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-extern "C" size_t moe_expert_ffn_nvfp4_workspace_size(int T, int k, int I) {
-  if (T < 0 || k < 1 || I < 16 || (long long)T * k > INT_MAX / 2) return 0;
-  return moe::mx_ws_bytes(T, k, I);
+extern "C" size_t moe_expert_ffn_nvfp4_workspace_size(int T, int k, int H, int I) {
+  if (T < 0 || k < 1 || H < 16 || I < 16 || (long long)T * k > INT_MAX / 2) return 0;
+  return moe::mx_ws_bytes(T, k, H, I);
 }
 
 extern "C" int moe_expert_ffn_nvfp4(const moe_pool_nvfp4* cache_pool, const moe_pool_nvfp4* staging_opt,
@@ -363,7 +377,11 @@ extern "C" int moe_expert_ffn_nvfp4(const moe_pool_nvfp4* cache_pool, const moe_
   st = fp4_common(slot_table, n_layers, layer, E, H, I, counts, offsets, perm, x, T, k, y_rows, ws, ws_bytes,
                   dev_status, &p);
   if (st != MOE_OK || T == 0) return st;
-  // decode-sized calls only: the ring kernel (rows of 1024, 2048 or 4096 inputs, at most 64 routed rows)
-  if (!fp4_ring_ok(p, T, true)) return MOE_ERR_UNSUPPORTED;
-  return launch_fp4_ring(p, T, true, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  // the ring kernel for decode-sized calls, the tensor-core GEMM for the rest
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t err;
+  if (fp4_ring_ok(p, T, true)) err = launch_fp4_ring(p, T, true, s);
+  else if (fp4_gemm_ok(p, true)) err = run_fp4_gemm(p, true, T, s);
+  else return MOE_ERR_UNSUPPORTED;
+  return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

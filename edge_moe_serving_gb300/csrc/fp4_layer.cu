@@ -76,6 +76,11 @@ fp4_fill_kernel(FillBanks fb, const int32_t* __restrict__ fills, const int32_t* 
 
 inline bool a16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool ring_dim(int d) { return d == 1024 || d == 2048 || d == 4096; }   // the ring kernel's H and I
+// NVFP4 calls run on the ring kernel (at most 64 routed rows, rows of 1024, 2048 or 4096 inputs) or on
+// the tensor-core GEMM (I a multiple of 128, H of 256, every row's 16-input scales in 8-byte groups)
+inline bool nv_ffn_shape(long long R, int H, int I) {
+  return (R <= kFp4RingMaxRows && ring_dim(H) && ring_dim(I)) || (I % 128 == 0 && H % 256 == 0);
+}
 
 struct Fp4Ws {
   int32_t* ids;
@@ -109,8 +114,8 @@ Fp4Ws fp4_ws(void* ws, int T, int k, int E, int H, int I) {
   L.y_rows = static_cast<float*>(take(R * H * 4));
   L.bind_ws = take(bind_ws_bytes(T, k, E));
   L.scratch_bytes = std::max({route_ws_bytes(T, H, E), dispatch_ws_bytes(T, k, E),
-                              moe_expert_ffn_mxfp4_workspace_size(T, k, I),
-                              moe_expert_ffn_nvfp4_workspace_size(T, k, I), (size_t)256});
+                              moe_expert_ffn_mxfp4_workspace_size(T, k, H, I),
+                              moe_expert_ffn_nvfp4_workspace_size(T, k, H, I), (size_t)256});
   L.scratch = take(L.scratch_bytes);
   L.bytes = off;
   return L;
@@ -182,7 +187,7 @@ extern "C" int moe_layer_forward_fp4(const moe_layer* layer, const moe_cache_fp4
   if ((long long)T * k > INT_MAX / 2 || E > kMaxE || H % SB || I % SB ||
       (long long)cache->n_layers * E > MOE_SLOT_MASK || cache->cache.n_slots > kMaxCacheSlots)
     return MOE_ERR_UNSUPPORTED;
-  if (nv && ((long long)T * k > kFp4RingMaxRows || !ring_dim(H) || !ring_dim(I))) return MOE_ERR_UNSUPPORTED;
+  if (nv && !nv_ffn_shape((long long)T * k, H, I)) return MOE_ERR_UNSUPPORTED;
   int st = pool_check(cache->cache, nv, true);
   if (st != MOE_OK) return st;
   st = pool_check(cache->staging, nv, false);

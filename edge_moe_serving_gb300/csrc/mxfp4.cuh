@@ -22,6 +22,7 @@ struct MxParams {
   const int32_t* perm;
   const __nv_bfloat16* x;
   __nv_bfloat16* h;   // [R, I] by dispatch position
+  __nv_bfloat16* x_perm;   // [R, H] token rows in dispatch order (the tensor-core GEMM's operand)
   float* y;           // [R, H] token-major
   uint32_t* status;
   unsigned int* inst_done;   // ring kernel: per-instance gate/up completion counters (zero at launch)
@@ -92,5 +93,12 @@ __device__ inline bool mx_resolve(const MxParams& p, int32_t entry, MxRows* out,
 constexpr int kFp4RingMaxRows = 64;
 bool fp4_ring_ok(const MxParams& p, int T, bool nv);
 cudaError_t launch_fp4_ring(const MxParams& p, int T, bool nv, cudaStream_t s);
+
+// The tensor-core GEMM over FP4 banks (ffn_fp4_gemm.cu): whether the shape
+// qualifies (I a multiple of 128, H of 256, every row's scales a multiple of
+// 16 bytes), and the two launches (gate/up into p.h, down into p.y) over the
+// token rows gathered in dispatch order (x_perm, bf16 [T*k, H]).
+bool fp4_gemm_ok(const MxParams& p, bool nv);
+cudaError_t launch_fp4_gemm(const MxParams& p, bool nv, const __nv_bfloat16* x_perm, int T, cudaStream_t s);
 
 }  // namespace moe

@@ -356,13 +356,19 @@ typedef struct moe_pool_mxfp4 {
  *   y_rows[perm[pos], :] = h W_down^T
  * with W the dequantised weights of the slot that slot_table[layer*E + e]
  * names (cache_pool, or staging_opt for MOE_STAGING_TAG entries; the same
- * encoding as moe_cache).  Each block's 32 products are summed in fp32 and
- * scaled by the block's power of two (exact), accumulation in fp32.  Calls
- * of at most 64 routed rows with H and I in {1024, 2048, 4096} and 16-byte
- * aligned scale banks run on one weight-streaming launch (the token's
- * activations rescaled per 32-input block by a power of two into f16, exact
- * f16 products of the E2M1 values); other calls on a two-launch table-decode
- * kernel.
+ * encoding as moe_cache).  Three kernels, by the call's shape:
+ * - at most 64 routed rows, H and I in {1024, 2048, 4096}, 16-byte aligned
+ *   scale banks: one weight-streaming launch (the token's activations
+ *   rescaled per 32-input block by a power of two into f16, exact f16
+ *   products of the E2M1 values, each block's sum scaled by its power of two);
+ * - otherwise, with I a multiple of 128, H of 256, H/32 and I/32 multiples of
+ *   8 and 8-byte aligned scale banks: the tensor-core GEMM (the token rows
+ *   gathered in dispatch order; the weights expanded exactly into bf16 in
+ *   shared memory, E2M1 value times the block's power of two, then
+ *   tcgen05.mma against the bf16 token rows, fp32 accumulation).  The
+ *   expansion is exact for weights below 2^128 in magnitude: every code up to
+ *   the scale byte 252; larger weights become infinities;
+ * - otherwise: a two-launch table-decode kernel.
  * slot_table: [n_layers*E] int32.  x bf16 [T, H]; y_rows fp32 [T*k, H],
  * token-major.  counts / offsets / perm as moe_dispatch writes them.
  * Errors: MOE_ERR_INVALID_ARG for a NULL pool, table or (T > 0) array, a
@@ -370,12 +376,13 @@ typedef struct moe_pool_mxfp4 {
  * outside [1, min(E, 16)], H or I below 32; MOE_ERR_UNSUPPORTED for H or I
  * not a multiple of 32, E > 1024, T*k > INT_MAX/2, a code bank, x or y_rows
  * not 16-byte aligned; MOE_ERR_WORKSPACE for ws_bytes below
- * moe_expert_ffn_mxfp4_workspace_size(T, k, I) (the bf16 h rows and one
- * counter per routed row, 0 for invalid arguments), MOE_ERR_UNSUPPORTED for
+ * moe_expert_ffn_mxfp4_workspace_size(T, k, H, I) (the bf16 h rows, one
+ * counter per routed row and the gathered bf16 token rows; 0 for invalid
+ * arguments), MOE_ERR_UNSUPPORTED for
  * a ws that is not 256-byte aligned.  T = 0 returns MOE_OK and launches nothing.  On the
  * device, an unbound or out-of-range entry sets MOE_DEV_ERR_UNBOUND /
  * MOE_DEV_ERR_BAD_SLOT and leaves that expert's rows unwritten. */
-size_t moe_expert_ffn_mxfp4_workspace_size(int T, int k, int I);
+size_t moe_expert_ffn_mxfp4_workspace_size(int T, int k, int H, int I);
 int moe_expert_ffn_mxfp4(const moe_pool_mxfp4* cache_pool, const moe_pool_mxfp4* staging_opt,
                          const int32_t* slot_table, int n_layers, int layer, int E, int H, int I,
                          const int32_t* counts, const int32_t* offsets, const int32_t* perm,
@@ -409,17 +416,22 @@ typedef struct moe_pool_nvfp4 {
 } moe_pool_nvfp4;
 
 /* moe_expert_ffn_mxfp4 over NVFP4 banks, same arguments, layouts, results
- * and device errors, for decode-sized calls: T*k at most 64 routed rows and
- * H, I in {1024, 2048, 4096} (one weight-streaming launch; every routed row
- * reads its expert's weights once).  Each 16-input half of a 32-input code
- * vector sums its exact f16 products in fp32 and is scaled by its E4M3 value
- * (exact in fp32) and the activations' power-of-two back-scale; the row's
- * fp32 sum is scaled by the bank's tensor scale.  Errors: as
- * moe_expert_ffn_mxfp4 with 16 in place of 32 for the H and I checks, plus
- * MOE_ERR_INVALID_ARG for a NULL tensor_scale, MOE_ERR_UNSUPPORTED for a
- * misaligned bank or tensor_scale and for calls outside the decode-sized
- * shapes above.  moe_expert_ffn_nvfp4_workspace_size(T, k, I) bytes of ws. */
-size_t moe_expert_ffn_nvfp4_workspace_size(int T, int k, int I);
+ * and device errors.  Two kernels, by the call's shape:
+ * - T*k at most 64 routed rows and H, I in {1024, 2048, 4096}: one
+ *   weight-streaming launch (every routed row reads its expert's weights
+ *   once).  Each 16-input half of a 32-input code vector sums its exact f16
+ *   products in fp32 and is scaled by its E4M3 value (exact in fp32) and the
+ *   activations' power-of-two back-scale;
+ * - otherwise, with I a multiple of 128 and H of 256: the tensor-core GEMM,
+ *   the weights expanded exactly into bf16 (E2M1 value times E4M3 value) and
+ *   multiplied against the bf16 token rows with fp32 accumulation.
+ * Either way the row's fp32 sum is scaled by the bank's tensor scale.
+ * Errors: as moe_expert_ffn_mxfp4 with 16 in place of 32 for the H and I
+ * checks, plus MOE_ERR_INVALID_ARG for a NULL tensor_scale,
+ * MOE_ERR_UNSUPPORTED for a misaligned bank or tensor_scale and for calls
+ * that fit neither kernel.  moe_expert_ffn_nvfp4_workspace_size(T, k, H, I)
+ * bytes of ws. */
+size_t moe_expert_ffn_nvfp4_workspace_size(int T, int k, int H, int I);
 int moe_expert_ffn_nvfp4(const moe_pool_nvfp4* cache_pool, const moe_pool_nvfp4* staging_opt,
                          const int32_t* slot_table, int n_layers, int layer, int E, int H, int I,
                          const int32_t* counts, const int32_t* offsets, const int32_t* perm,
@@ -456,7 +468,8 @@ typedef struct moe_cache_fp4 {
  * (layer->E, H, I equal to the cache's); stats_dev optional.  Errors: those
  * of the steps, plus MOE_ERR_INVALID_ARG for an unknown format or a shape
  * mismatch and MOE_ERR_WORKSPACE below moe_layer_fp4_workspace_size.  NVFP4
- * calls of more than 64 routed rows return MOE_ERR_UNSUPPORTED. */
+ * calls that fit neither of moe_expert_ffn_nvfp4's kernels return
+ * MOE_ERR_UNSUPPORTED before any launch. */
 size_t moe_layer_fp4_workspace_size(const moe_layer* layer, const moe_cache_fp4* cache, int T);
 int moe_layer_forward_fp4(const moe_layer* layer, const moe_cache_fp4* cache, const void* x, int T, void* out,
                           uint32_t phi_q16, int min_fill, int fill_policy, uint64_t seed, void* ws,

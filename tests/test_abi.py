@@ -116,8 +116,8 @@ def test_mxfp4_ffn_argument_checks():
     pool = moe.moe_pool_mxfp4(16, 1, 16, 1, 16, 1, 4, 0)     # fake non-null pointers: never dereferenced
     args = lambda pool, T=4, k=2, E=8, H=64, I=64, ws_bytes=1 << 20, x=16, layer=0: (
         ctypes.byref(pool), None, 16, 1, layer, E, H, I, 16, 16, 16, x, T, k, 16, 16, ws_bytes, None, None)
-    assert moe.moe_expert_ffn_mxfp4_workspace_size(4, 2, 64) >= 4 * 2 * 64 * 2   # the bf16 h rows
-    assert moe.moe_expert_ffn_mxfp4_workspace_size(4, 2, 16) == 0
+    assert moe.moe_expert_ffn_mxfp4_workspace_size(4, 2, 64, 64) >= 2 * 4 * 2 * 64 * 2   # the bf16 h and token rows
+    assert moe.moe_expert_ffn_mxfp4_workspace_size(4, 2, 64, 16) == 0
     assert call(*args(pool, T=0)) == moe.MOE_OK
     assert call(*args(pool, k=9)) == moe.MOE_ERR_INVALID_ARG          # k > E
     assert call(*args(pool, layer=1)) == moe.MOE_ERR_INVALID_ARG      # layer out of range
@@ -141,7 +141,7 @@ def test_nvfp4_ffn_argument_checks():
     pool = moe.moe_pool_nvfp4(16, 16, 16, 16, 16, 16, 16, 4, 0)    # fake non-null pointers: never dereferenced
     args = lambda pool, T=4, k=2, E=8, H=64, I=64, ws_bytes=1 << 20, x=16, ws=256: (
         ctypes.byref(pool), None, 16, 1, 0, E, H, I, 16, 16, 16, x, T, k, 16, ws, ws_bytes, None, None)
-    assert moe.moe_expert_ffn_nvfp4_workspace_size(4, 2, 64) >= 4 * 2 * 64 * 2
+    assert moe.moe_expert_ffn_nvfp4_workspace_size(4, 2, 64, 64) >= 2 * 4 * 2 * 64 * 2
     assert call(*args(pool, T=0)) == moe.MOE_OK
     assert call(*args(pool, k=9)) == moe.MOE_ERR_INVALID_ARG
     assert call(*args(pool, H=40)) == moe.MOE_ERR_UNSUPPORTED          # not a multiple of 16
@@ -226,8 +226,10 @@ def test_fp4_layer_argument_checks():
     assert call(mx, x=264) == moe.MOE_ERR_UNSUPPORTED                            # x not 16-byte aligned
     assert call(cache(moe.MOE_FP4_NVFP4, ts=None)) == moe.MOE_ERR_INVALID_ARG    # NVFP4 without tensor scales
     assert call(cache(moe.MOE_FP4_NVFP4, ts=258)) == moe.MOE_ERR_UNSUPPORTED     # tensor scales not 4-byte aligned
-    assert call(nv, T=33) == moe.MOE_ERR_UNSUPPORTED                             # NVFP4: at most 64 routed rows
-    assert call(cache(moe.MOE_FP4_NVFP4, H=1536, I=1536)) == moe.MOE_ERR_UNSUPPORTED   # not a ring-kernel shape
+    # NVFP4 shapes that fit neither the ring kernel (<= 64 routed rows of 1024, 2048 or 4096 inputs) nor the
+    # tensor-core GEMM (I a multiple of 128, H of 256)
+    assert call(cache(moe.MOE_FP4_NVFP4, H=1040, I=1040), T=33) == moe.MOE_ERR_UNSUPPORTED
+    assert call(cache(moe.MOE_FP4_NVFP4, H=1040, I=1040)) == moe.MOE_ERR_UNSUPPORTED
 
 
 STRUCTS = ["moe_pool", "moe_cache", "moe_bind_stats", "moe_layer", "moe_layer_buffers", "moe_bw_profile",
@@ -291,7 +293,7 @@ int main(void) {
   CHECK(moe_bw_derive(&p) == MOE_OK && p.phi_q16 == moe_phi_to_q16(25.1 / 63.2) && p.hybrid_ok == 1);
   CHECK(moe_bw_derive(NULL) == MOE_ERR_INVALID_ARG);
   CHECK(moe_dispatch_workspace_size(1, 6, 256) == 0);
-  CHECK(moe_expert_ffn_mxfp4_workspace_size(1, 6, 2048) >= 6u * 2048u * 2u);
+  CHECK(moe_expert_ffn_mxfp4_workspace_size(1, 6, 4096, 2048) >= 6u * (4096u + 2048u) * 2u);
   CHECK(moe_route_topk(NULL, 4, 64, NULL, NULL, 4, 5, NULL, NULL, NULL, NULL, 0, NULL, NULL) == MOE_ERR_INVALID_ARG);
   CHECK(moe_combine(NULL, NULL, 0, 2, 64, NULL, NULL, NULL, NULL) == MOE_OK);
   memset(&mx, 0, sizeof mx);

@@ -11,8 +11,7 @@ bytes, scale bytes and tensor scales equal those of the pair that owns it
 fp64 layer on the dequantised experts within the output tolerance.  Phi = 1
 (every miss filled), 0.25 with the random fill policy (fills and staged
 experts in one call) and 0 (no fills); one-token calls and batched calls
-(the ring kernel up to 64 routed rows, the table-decode kernel above it for
-MXFP4)."""
+(the ring kernel up to 64 routed rows, the tensor-core GEMM above it)."""
 import dataclasses
 
 import numpy as np
@@ -114,28 +113,31 @@ def test_fp4_layer_no_fills_reads_staged_in_place():
     assert t["n_fill"] == 0 and t["n_staged"] > 0
 
 
-@pytest.mark.parametrize("fmt,T", [(moe.MOE_FP4_MXFP4, 8), (moe.MOE_FP4_NVFP4, 8), (moe.MOE_FP4_MXFP4, 16)])
+@pytest.mark.parametrize("fmt,T", [(moe.MOE_FP4_MXFP4, 8), (moe.MOE_FP4_NVFP4, 8), (moe.MOE_FP4_MXFP4, 16),
+                                   (moe.MOE_FP4_NVFP4, 16)])
 def test_fp4_layer_batched_calls(fmt, T):
-    """48 routed rows (one ring launch) and, for MXFP4, 96 routed rows (the
-    table-decode kernel)."""
+    """48 routed rows (one ring launch) and 96 routed rows (the tensor-core
+    GEMM)."""
     cfg = dataclasses.replace(FP4, T=T)
     t = _trace(cfg, fmt, T, Q16 // 4, FILL_RANDOM, 4, check_every=1)
     assert t["n_fill"] > 0
 
 
-def test_fp4_layer_nvfp4_rejects_calls_beyond_the_ring_before_the_bind():
-    """An NVFP4 call of more than 64 routed rows is refused before any launch:
-    the residency state is unchanged."""
-    cfg = dataclasses.replace(FP4, T=11)
+def test_fp4_layer_nvfp4_rejects_calls_that_fit_neither_kernel_before_the_bind():
+    """An NVFP4 call whose shape neither FFN kernel takes (rows of 1040
+    inputs) is refused before any launch: the residency state is unchanged."""
+    cfg = dataclasses.replace(FP4, H=1040, I=1040, E=8, cache_slots=4)
     fc = Fp4Cache(cfg, moe.MOE_FP4_NVFP4, SEED, DEV)
     dl = DeviceLayer(cfg, 0, DEV)
     before = fc.state()
-    x = x_dev(cfg, 0, 0)[:11].contiguous()
-    out = torch.empty((11, cfg.H), dtype=torch.bfloat16, device=DEV)
-    nb = moe.moe_layer_fp4_workspace_size(dl.struct, fc.struct, 11)
-    rc = moe.lib().moe_layer_forward_fp4(dl.struct, fc.struct, x.data_ptr(), 11, out.data_ptr(), Q16, 1, 0, 0,
+    x = x_dev(cfg, 0, 0)[:1].contiguous()
+    out = torch.empty((1, cfg.H), dtype=torch.bfloat16, device=DEV)
+    nb = moe.moe_layer_fp4_workspace_size(dl.struct, fc.struct, 1)
+    n0 = moe.moe_kernel_launch_count()
+    rc = moe.lib().moe_layer_forward_fp4(dl.struct, fc.struct, x.data_ptr(), 1, out.data_ptr(), Q16, 1, 0, 0,
                                          ws(nb).data_ptr(), nb, None, None, None)
     assert rc == moe.MOE_ERR_UNSUPPORTED
+    assert moe.moe_kernel_launch_count() == n0
     after = fc.state()
     for key in ("table", "owner", "stamp"):
         assert np.array_equal(before[key], after[key])

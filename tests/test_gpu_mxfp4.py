@@ -58,7 +58,7 @@ def _run(T, k, E, H, I, n_layers, layer, cached, staged, seed, unbound=(), bad=(
     x = torch.from_numpy(x_bits.view(np.int16)).to(DEV).view(torch.bfloat16)
     R = T * k
     y = torch.full((R, H), 7.0, dtype=torch.float32, device=DEV)
-    nb = moe.moe_expert_ffn_mxfp4_workspace_size(T, k, I)
+    nb = moe.moe_expert_ffn_mxfp4_workspace_size(T, k, H, I)
     st = status()
     moe.moe_expert_ffn_mxfp4(pool_a.struct, pool_b.struct if pool_b else None, dev_i32(table), n_layers, layer, E,
                              H, I, dev_i32(counts), dev_i32(offsets), dev_i32(perm), x, T, k, y, ws(nb), nb, st)
@@ -201,7 +201,7 @@ def test_mxfp4_ffn_special_block_scales(T, k, H, I):
     dev_i32 = lambda a: torch.from_numpy(np.asarray(a, np.int32)).to(DEV)
     x = torch.from_numpy(x_bits.view(np.int16)).to(DEV).view(torch.bfloat16)
     y = torch.zeros((T * k, H), dtype=torch.float32, device=DEV)
-    nb = moe.moe_expert_ffn_mxfp4_workspace_size(T, k, I)
+    nb = moe.moe_expert_ffn_mxfp4_workspace_size(T, k, H, I)
     st = status()
     moe.moe_expert_ffn_mxfp4(pool.struct, None, dev_i32(np.arange(E)), 1, 0, E, H, I, dev_i32(counts),
                              dev_i32(offsets), dev_i32(perm), x, T, k, y, ws(nb), nb, st)
@@ -219,3 +219,78 @@ def test_mxfp4_ffn_special_block_scales(T, k, H, I):
     # hidden 1024; relative Frobenius), the 2^127 block by 98% (83%), far beyond the tolerance
     assert np.abs(ref[1][~nan1]).max() > 0.05
     assert_close(got[1][~nan1], ref[1][~nan1], what="mxfp4 rows with block scales 0 and 254")
+
+
+@pytest.mark.parametrize("T,k,E,H,I", [(64, 4, 8, 1024, 512), (320, 4, 4, 512, 512), (24, 6, 12, 1024, 768),
+                                       (40, 3, 6, 2048, 256)])
+def test_mxfp4_ffn_tensor_core_gemm(T, k, E, H, I):
+    """Calls beyond the ring kernel whose shapes the tensor-core GEMM takes:
+    the token rows gathered in dispatch order, then the gate/up and down
+    launches (three launches in all).  Groups of a few rows to several
+    256-row chunks (320 tokens over 4 experts), the thin 32-row chunks of
+    calls of at most 32 tokens (24 tokens), scale rows of 24 bytes
+    (intermediate 768), experts in both pools, layer 1 of 2."""
+    experts = list(range(E))
+    before = moe.moe_kernel_launch_count()
+    y, ref, st, _ = _run(T, k, E, H, I, 2, 1, experts[: E // 2 + 1], experts[E // 2 + 1:], seed=T * 7 + E + H)
+    assert moe.moe_kernel_launch_count() - before == 3
+    assert st == 0
+    _check(y, ref, f"mxfp4 tensor-core GEMM T={T} k={k} E={E} H={H} I={I}")
+
+
+def test_mxfp4_ffn_tensor_core_gemm_special_block_scales():
+    """The tensor-core GEMM's exact expansion at the ends of its range: gate
+    and up rows scale inputs 0..31 by 2^-127 (E8M0 byte 0: bf16 subnormal
+    weights) and inputs 32..63 by 2^125 (byte 252, the largest scale every
+    code fits in bf16 with).  Each token has one nonzero input in each of
+    those blocks, about 2^125 at input 0 and in [2^-126, 2^-125) at input 32,
+    so that both blocks carry one order-one term and the outputs stay near
+    unit scale.  A NaN block scale (255) in gate row 3 of expert 0 makes every
+    output of its rows NaN; one in down row 5 of expert 1 makes element 5 of
+    its rows NaN."""
+    T, k, E, H, I = 40, 1, 2, 512, 256
+    rng = np.random.default_rng(78)
+    experts = {}
+    for e in range(E):
+        gq, gs, uq, us, dq, ds = (np.array(a) for a in gen.mx_expert(SEED, 0, e, H, I))
+        for s in (gs, us):
+            s[:, 0] = 0          # 2^-127 on inputs 0..31
+            s[:, 1] = 252        # 2^125 on inputs 32..63
+        if e == 0:
+            gs[3, 2] = 255
+        else:
+            ds[5, 0] = 255
+        experts[e] = (gq, gs, uq, us, dq, ds)
+    xf = rng.standard_normal((T, H)).astype(np.float32)
+    xf[:, 0] *= np.float32(2.0 ** 125)
+    mag = (1.0 + 0.9 * rng.random(T)) * 2.0 ** -126                  # normal bf16 values in [2^-126, 2^-125)
+    xf[:, 32] = (np.sign(xf[:, 32]) * mag).astype(np.float32)
+    xf[:, 1:32] = 0.0
+    xf[:, 33:64] = 0.0
+    x_bits = gen.f32_to_bf16_bits(xf)
+    ids = (np.arange(T) % 2).astype(np.int32)[:, None]
+    counts, offsets, perm, _ = O.dispatch(ids, E)
+    pool = MxPool(E, H, I, experts, DEV)
+    dev_i32 = lambda a: torch.from_numpy(np.asarray(a, np.int32)).to(DEV)
+    x = torch.from_numpy(x_bits.view(np.int16)).to(DEV).view(torch.bfloat16)
+    y = torch.zeros((T * k, H), dtype=torch.float32, device=DEV)
+    nb = moe.moe_expert_ffn_mxfp4_workspace_size(T, k, H, I)
+    st = status()
+    before = moe.moe_kernel_launch_count()
+    moe.moe_expert_ffn_mxfp4(pool.struct, None, dev_i32(np.arange(E)), 1, 0, E, H, I, dev_i32(counts),
+                             dev_i32(offsets), dev_i32(perm), x, T, k, y, ws(nb), nb, st)
+    torch.cuda.synchronize()
+    assert moe.moe_kernel_launch_count() - before == 3          # gather + the two GEMM launches
+    assert status_bits(st) == 0
+    got = y.cpu().numpy().astype(np.float64)
+    xd = gen.bf16_bits_to_f64(x_bits)
+    w = {e: O.mx_expert_weights(*experts[e]) for e in range(E)}
+    ref = np.stack([O.swiglu_expert(xd[t][None, :], *w[int(ids[t, 0])])[0] for t in range(T)])
+    rows0, rows1 = ids[:, 0] == 0, ids[:, 0] == 1
+    assert np.isnan(ref[rows0]).all() and np.isnan(got[rows0]).all()
+    nan1 = np.isnan(ref[rows1])
+    assert nan1[:, 5].all() and nan1.sum() == rows1.sum()
+    assert np.array_equal(np.isnan(got[rows1]), nan1)
+    keep = ~nan1
+    assert np.abs(ref[rows1][keep]).max() > 0.05
+    assert_close(got[rows1][keep], ref[rows1][keep], what="mxfp4 GEMM rows with block scales 0 and 252")

@@ -63,7 +63,7 @@ def _run(T, k, E, H, I, n_layers, layer, cached, staged, seed, unbound=(), bad=(
     x = torch.from_numpy(x_bits.view(np.int16)).to(DEV).view(torch.bfloat16)
     R = T * k
     y = torch.full((R, H), 7.0, dtype=torch.float32, device=DEV)
-    nb = moe.moe_expert_ffn_nvfp4_workspace_size(T, k, I)
+    nb = moe.moe_expert_ffn_nvfp4_workspace_size(T, k, H, I)
     st = status()
     before = moe.moe_kernel_launch_count()
     moe.moe_expert_ffn_nvfp4(pool_a.struct, pool_b.struct if pool_b else None, dev_i32(table), n_layers, layer, E,
@@ -141,18 +141,32 @@ def test_nvfp4_ffn_unbound_and_bad_slot_rows_left_unwritten():
     _check(y[~skipped], ref[~skipped], "nvfp4 rows of bound experts")
 
 
-def test_nvfp4_ffn_rejects_calls_beyond_the_decode_kernel():
-    """More than 64 routed rows, or rows of other widths: MOE_ERR_UNSUPPORTED
-    before any launch."""
+def test_nvfp4_ffn_rejects_calls_that_fit_neither_kernel():
+    """More than 64 routed rows with rows the tensor-core GEMM does not take,
+    or rows of other widths: MOE_ERR_UNSUPPORTED before any launch."""
     L = moe.lib()
     pool = NvPool(2, 1024, 1024, {}, DEV)
     i32 = torch.zeros(1024, dtype=torch.int32, device=DEV)
     x = torch.zeros((16, 1024), dtype=torch.bfloat16, device=DEV)
     y = torch.zeros((16 * 8, 1024), dtype=torch.float32, device=DEV)
-    w = ws(moe.moe_expert_ffn_nvfp4_workspace_size(16, 8, 1024))
+    w = ws(moe.moe_expert_ffn_nvfp4_workspace_size(16, 8, 1024, 1024))
     before = moe.moe_kernel_launch_count()
     args = lambda T, k, H, I: (pool.struct, None, i32.data_ptr(), 1, 0, 8, H, I, i32.data_ptr(), i32.data_ptr(),
                                i32.data_ptr(), x.data_ptr(), T, k, y.data_ptr(), w.data_ptr(), w.numel(), None, None)
-    assert L.moe_expert_ffn_nvfp4(*args(9, 8, 1024, 1024)) == moe.MOE_ERR_UNSUPPORTED    # 72 routed rows
-    assert L.moe_expert_ffn_nvfp4(*args(1, 2, 1024, 1536)) == moe.MOE_ERR_UNSUPPORTED    # I not 1024/2048/4096
+    assert L.moe_expert_ffn_nvfp4(*args(9, 8, 1040, 1040)) == moe.MOE_ERR_UNSUPPORTED    # 72 rows of 1040 inputs
+    assert L.moe_expert_ffn_nvfp4(*args(1, 2, 1024, 1040)) == moe.MOE_ERR_UNSUPPORTED    # I not 1024/2048/4096
     assert moe.moe_kernel_launch_count() == before
+
+
+@pytest.mark.parametrize("T,k,E,H,I", [(64, 4, 8, 1024, 512), (320, 4, 4, 512, 256), (24, 6, 12, 1024, 768)])
+def test_nvfp4_ffn_tensor_core_gemm(T, k, E, H, I):
+    """Calls beyond the ring kernel on the tensor-core GEMM (gather + gate/up
+    + down: three launches): groups of a few rows to several 256-row chunks,
+    the thin 32-row chunks of calls of at most 32 tokens, experts in both
+    pools, layer 1 of 2, a distinct tensor scale per bank."""
+    experts = list(range(E))
+    y, ref, st, _, launches = _run(T, k, E, H, I, 2, 1, experts[: E // 2 + 1], experts[E // 2 + 1:],
+                                   seed=T * 11 + E + H)
+    assert launches == 3
+    assert st == 0
+    _check(y, ref, f"nvfp4 tensor-core GEMM T={T} k={k} E={E} H={H} I={I}")
