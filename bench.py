@@ -335,12 +335,18 @@ def run_ours(args, rank, world):
         if name in ("prefill_mxfp4", "prefill_nvfp4"):
             result[name] = run_fp4_prefill(sub, dev, stream, moe, torch, name.split("_")[1])
             continue
-        if name == "decode_mxfp4":
-            sub.no_cpu_baseline = True
-            rec = run_mx(sub)
-            result[name] = {k: v for k, v in rec.items()
-                            if k not in ("metric", "n_gpus", "higher_is_better", "scaling", "vs_baseline", "data",
-                                         "impl")}
+        if name in ("decode_mxfp4", "decode_nvfp4"):
+            result[name] = run_fp4_decode(sub, dev, stream, moe, torch, name.split("_")[1])
+            if name == "decode_mxfp4":
+                # the expert FFN call alone (every expert resident), with its own roofline
+                sub.no_cpu_baseline = True
+                torch.cuda.empty_cache()
+                rec = run_mx(sub)
+                result[name]["ffn_call"] = {k: rec[k] for k in ("value", "ms_per_step", "roofline", "clocks")}
+                result[name]["ffn_call"]["note"] = ("router + top-k, dispatch, moe_expert_ffn_mxfp4 and the combine "
+                                                    "as four public calls in one graph, every expert resident; "
+                                                    "roofline: the FFN call alone")
+            continue
         else:
             result[name] = run_workload(CONFIGS[name], sub, world, dev, stream, peaks, moe, torch)
     return result
@@ -815,16 +821,16 @@ def mx_expert_bytes(H, I):
 
 
 def run_fp4_prefill(args, dev, stream, moe, torch, fmt_name="mxfp4"):
-    """The 8192-token prefill layer over FP4 experts: moe_layer_forward_fp4
+    """The 8192-token prefill layer (or --fp4-workload) over FP4 experts: moe_layer_forward_fp4
     (router + top-k, residency bind, dispatch, the FP4 expert FFN on the
-    tensor-core GEMM, combine) with all 256 experts resident, phi = 0.  Steps
-    back to back between one pair of CUDA events (each reads 3.4 GB of expert
-    codes and scales, over twice the L2).  The FFN call alone (gather +
+    tensor-core GEMM, combine) with all experts resident, phi = 0.  Steps
+    back to back between one pair of CUDA events (prefill: each reads 3.6 GB
+    of expert codes and scales, over twice the L2).  The FFN call alone (gather +
     gate/up + down GEMMs) is then timed after route and dispatch, with an L2
     flush before it."""
     from moe_inputs.device import DeviceLayer, Fp4Cache, to_dev_bf16
     peaks = load_peaks()
-    cfg = CONFIGS["prefill"]
+    cfg = CONFIGS[args.fp4_workload]
     fmt = moe.MOE_FP4_MXFP4 if fmt_name == "mxfp4" else moe.MOE_FP4_NVFP4
     T, H, E, k, I = cfg.T, cfg.H, cfg.E, cfg.k, cfg.I
     fc = Fp4Cache(cfg, fmt, MX_SEED, dev)
@@ -900,8 +906,8 @@ def run_fp4_prefill(args, dev, stream, moe, torch, fmt_name="mxfp4"):
     return {"value": round(T / step_s, 3), "unit": UNIT, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(step_s * 1e3, 5),
             "dtype": f"{fmt_name} weights expanded to bf16 in shared memory, bf16 activations, fp32 accumulation",
-            "config": {"workload": f"prefill_{fmt_name}", "tokens_per_layer_call": T, "hidden": H, "experts": E,
-                       "top_k": k, "intermediate": I, "residency": "all 256 experts resident, phi = 0",
+            "config": {"workload": f"{cfg.name}_{fmt_name}", "tokens_per_layer_call": T, "hidden": H, "experts": E,
+                       "top_k": k, "intermediate": I, "residency": f"all {E} experts resident, phi = 0",
                        "l2": "inputs larger than L2 (%.1f GB of codes and scales per step), steps back to back"
                              % (byts / 1e9),
                        "launch": "moe_layer_forward_fp4, direct launches"},
@@ -932,6 +938,110 @@ def oracle_mx_step(cfg, step, O):
             W = O.mx_expert_weights(*gen.mx_expert(MX_SEED, 0, int(e), cfg.H, cfg.I))
             out[t] += w[t, j] * O.swiglu_expert(x[t][None, :], *W)[0]
     return out
+
+
+def run_fp4_decode(args, dev, stream, moe, torch, fmt_name="mxfp4"):
+    """The decode workload (one token per step, 256 experts, top-6, a 95-slot
+    LRU cache pool, every miss filled) with FP4 expert banks: one
+    moe_layer_forward_fp4 call per step, which runs the whole layer as one
+    cooperative kernel.  A step reads about 80 MB of expert codes and scales
+    (under twice the L2), so each step is timed between its own CUDA events
+    after a 256 MB L2-flush write.  Roofline: the method's bytes of the step
+    (distinct routed experts' codes and scales, one more expert written per
+    fill, the router weights, the token row in and the output row out) over
+    the step time."""
+    from moe_inputs.device import DeviceLayer, Fp4Cache, to_dev_bf16
+    peaks = load_peaks()
+    cfg = CONFIGS["decode"]
+    fmt = moe.MOE_FP4_MXFP4 if fmt_name == "mxfp4" else moe.MOE_FP4_NVFP4
+    T, H, E, k, I = cfg.T, cfg.H, cfg.E, cfg.k, cfg.I
+    n_steps = args.warmup + args.steps
+    fc = Fp4Cache(cfg, fmt, MX_SEED, dev)
+    dl = DeviceLayer(cfg, 0, dev)
+    xs = [to_dev_bf16(gen.x_bits(cfg, 0, s), dev) for s in range(n_steps)]
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stats = torch.zeros((n_steps, 8), dtype=torch.int32, device=dev)
+    nb = moe.moe_layer_fp4_workspace_size(dl.struct, fc.struct, T)
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step(i, st=None):
+        moe.moe_layer_forward_fp4(dl.struct, fc.struct, xs[i], T, out, cfg.phi_q16, cfg.min_fill, cfg.fill_policy,
+                                  1000, ws, nb, status, stats[i] if st is None else st, stream)
+
+    with torch.cuda.stream(stream):
+        step(0)
+    torch.cuda.synchronize()
+    fc.reset()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+            flush.zero_()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    n0 = moe.moe_kernel_launch_count()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            step(args.warmup + i)
+            ev[i][1].record(stream)
+            flush.zero_()
+    torch.cuda.synchronize()
+    bracket_s = time.perf_counter() - t0
+    clk = clocks.stop()
+    launches = moe.moe_kernel_launch_count() - n0
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    dev_status = int(status.cpu().numpy().view(np.uint32)[0])
+    st = stats[args.warmup:].cpu().numpy().astype(np.float64)
+    sb = 32 if fmt == moe.MOE_FP4_MXFP4 else 16
+    xb = 3 * (H * I // 2 + H * I // sb) + (12 if fmt == moe.MOE_FP4_NVFP4 else 0)   # one FP4 expert's bytes
+    method = st[:, 0] * xb + E * H * 4 + 2 * T * H * 2
+    fills = st[:, 4] * xb
+    total_s = sum(step_ms) / 1e3
+    achieved = float(np.sum(method + fills)) / total_s / 1e9
+
+    # end to end: the public call with the token row from pinned host memory, the output read back
+    x_host = [x.cpu().pin_memory() for x in xs[:args.steps]]
+    out_host = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    x_in = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    fc.reset()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            x_in.copy_(x_host[i], non_blocking=True)
+            moe.moe_layer_forward_fp4(dl.struct, fc.struct, x_in, T, out, cfg.phi_q16, cfg.min_fill,
+                                      cfg.fill_policy, 1000, ws, nb, status, stats[0], stream)
+            out_host.copy_(out, non_blocking=True)
+            stream.synchronize()
+    e2e_s = time.perf_counter() - t0
+    return {"value": round(args.steps * T / total_s, 3), "unit": UNIT, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(total_s * 1e3 / args.steps, 5),
+            "step_ms_p10_p50_p90": [round(float(np.percentile(step_ms, q)), 5) for q in (10, 50, 90)],
+            "bracket_ms_per_step": round(bracket_s * 1e3 / args.steps, 5),
+            "dtype": f"{fmt_name} weights, bf16 activations",
+            "config": {"workload": f"decode_{fmt_name}", "tokens_per_layer_call": T, "hidden": H, "experts": E,
+                       "top_k": k, "intermediate": I, "cache_slots": cfg.cache_slots, "phi_q16": cfg.phi_q16,
+                       "fill_policy": "lowest_id", "routing_bias": cfg.bias,
+                       "l2": "flushed between steps (256 MB write)",
+                       "launch": "moe_layer_forward_fp4 per step (the whole layer in one cooperative kernel)"},
+            "device_status": dev_status,
+            "roofline": {"kernel": "decode_fp4_kernel (the whole step)", "bound": "hbm",
+                         "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                         "peak_source": peaks["source"] + " (burst copy bandwidth)",
+                         "algorithmic_bytes_per_step": int(np.mean(method + fills)),
+                         "fill_bytes_per_step": int(np.mean(fills)), "fills_per_step": round(float(np.mean(st[:, 4])), 3),
+                         "timing": "CUDA events around each step (the kernel and its barrier-word reset)"},
+            "clocks": clk,
+            "e2e": {"value": round(args.steps * T / e2e_s, 3), "unit": UNIT, "h2d_bytes_per_step": T * H * 2,
+                    "d2h_bytes_per_step": T * H * 2,
+                    "note": "moe_layer_forward_fp4 per step; host waits for each step's output"},
+            "gpu_launches": int(launches), "gpu_launches_per_step": launches / args.steps}
 
 
 def run_mx(args):
@@ -1109,6 +1219,9 @@ def main():
                     help="comma-separated workloads measured as sub-records of the line "
                          f"(default for the decode workload: {EXTRA_DEFAULT}; 'none' for none)")
     ap.add_argument("--oracle-only", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--fp4-workload", default="prefill", choices=sorted(CONFIGS),
+                    help="the layer shape of the prefill_mxfp4 / prefill_nvfp4 records (prefill_profile: a small "
+                         "case for profiling)")
     args = ap.parse_args()
     if args.extra is None:
         args.extra = EXTRA_DEFAULT if args.workload == "decode" else "none"

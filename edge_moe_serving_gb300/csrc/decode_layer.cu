@@ -30,15 +30,12 @@
 // (gate/up -> down).
 #include <algorithm>
 
+#include "decode_front.cuh"
 #include "front_warp.cuh"
 #include "ring_gemv.cuh"
 
 namespace moe {
 namespace {
-
-constexpr int kDecMaxT = 8;        // token rows converted to fp32 in shared memory
-constexpr int kDecMaxRows = 4;     // router rows per CTA
-constexpr int kDecMaxSlots = 1024; // cache-pool slots whose state the decision copies
 
 struct DecodeParams {
   GemvParams g;                    // perm / combine_w are pointed at shared memory in the kernel
@@ -76,87 +73,10 @@ struct __align__(16) DecodeShared {
   int n_inst;
 };
 
-// Bounded grid-wide barrier: the CTA barrier orders every thread's stores
-// before thread 0's release arrival (release is cumulative), and thread 0's
-// acquire poll orders the other CTAs' stores before the closing CTA barrier.
-__device__ inline bool grid_barrier(unsigned int* count, volatile int* abort_flag) {
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(count) : "memory");
-    unsigned long long t0 = 0;
-    for (uint32_t it = 0; ld_acquire_u32(count) < gridDim.x; ++it) {
-      if ((it & 15) == 15) {
-        if (*abort_flag) break;
-        const unsigned long long now = gtimer();
-        if (t0 == 0) {
-          t0 = now;
-        } else if (now - t0 > kGridWaitNs) {
-          *abort_flag = 1;
-          break;
-        }
-      }
-    }
-  }
-  __syncthreads();
-  return !*abort_flag;
-}
-
 // Named barriers besides __syncthreads (0) and the consumers' barrier inside
 // fused_phases (1, also used here once the decision is complete).
 constexpr int kBarConsumers = 1;
 constexpr int kBarStream = 2;      // warp 0 -> producer warp: the weight sources are known
-
-// Logits of this CTA's R router rows (rows b, b + G, ...) for the T <= TT
-// token rows: every thread takes the float4 columns tid, tid + blockDim, ...
-// of all R x T dot products, then warp sums and a sum over the warps.  R and
-// TT are compile-time so the loop body carries no per-row or per-token branch.
-template <int R, int TT>
-__device__ inline void router_rows(const DecodeParams& d, const float* wrow, const __nv_bfloat16* xs, DecodeShared& sh,
-                                   int b, int G) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int H = d.g.H, T = d.g.T, E = d.g.E;
-  float acc[R][TT];
-#pragma unroll
-  for (int i = 0; i < R; ++i)
-#pragma unroll
-    for (int t = 0; t < TT; ++t) acc[i][t] = 0.0f;
-  const int H4 = H >> 2;
-  for (int q = tid; q < H4; q += blockDim.x) {
-    float4 xv[TT];
-#pragma unroll
-    for (int t = 0; t < TT; ++t) {
-      const uint2 u = (TT == 1 || t < T) ? reinterpret_cast<const uint2*>(xs + (size_t)t * H)[q] : make_uint2(0u, 0u);
-      xv[t] = make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
-    }
-#pragma unroll
-    for (int i = 0; i < R; ++i) {
-      const float4 w = reinterpret_cast<const float4*>(wrow + (size_t)i * H)[q];
-#pragma unroll
-      for (int t = 0; t < TT; ++t) {
-        float a = acc[i][t];
-        a = fmaf(w.x, xv[t].x, a);
-        a = fmaf(w.y, xv[t].y, a);
-        a = fmaf(w.z, xv[t].z, a);
-        a = fmaf(w.w, xv[t].w, a);
-        acc[i][t] = a;
-      }
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < R; ++i)
-#pragma unroll
-    for (int t = 0; t < TT; ++t) {
-      const float s = warp_sum(acc[i][t]);
-      if (lane == 0) sh.red[warp][i][t] = s;
-    }
-  __syncthreads();
-  if (tid < R * T) {
-    const int i = tid / T, t = tid - (tid / T) * T;
-    float s = 0.0f;
-    for (int w = 0; w < kRingThreads / 32; ++w) s += sh.red[w][i][t];
-    d.logits[(size_t)t * E + b + i * G] = s + sh.bias[i];
-  }
-}
 
 template <int NT, int VA, int VB>
 __global__ void __launch_bounds__(kRingThreads, 1)
@@ -219,11 +139,12 @@ decode_layer_kernel(DecodeParams d, unsigned int* grid_count) {
   if (!bounded_wait(&sh.rbar, 0u, &sh.r.abort)) sh.r.abort = 1;
   __syncthreads();
   if (n_my > 0 && !sh.r.abort) {
+    constexpr int NW = kRingThreads / 32;
     switch (n_my) {
-      case 1: router_rows<1, NT>(d, wrow, xs, sh, b, G); break;
-      case 2: router_rows<2, NT>(d, wrow, xs, sh, b, G); break;
-      case 3: router_rows<3, NT>(d, wrow, xs, sh, b, G); break;
-      default: router_rows<4, NT>(d, wrow, xs, sh, b, G); break;
+      case 1: router_rows_block<1, NT, NW>(wrow, xs, H, T, E, sh.red, sh.bias, d.logits, b, G); break;
+      case 2: router_rows_block<2, NT, NW>(wrow, xs, H, T, E, sh.red, sh.bias, d.logits, b, G); break;
+      case 3: router_rows_block<3, NT, NW>(wrow, xs, H, T, E, sh.red, sh.bias, d.logits, b, G); break;
+      default: router_rows_block<4, NT, NW>(wrow, xs, H, T, E, sh.red, sh.bias, d.logits, b, G); break;
     }
   }
   // ---------------------------------------------------------------- route, residency

@@ -13,8 +13,8 @@
 // tcgen05.mma kind::f16 reads.
 //
 // Exactness: an E2M1 value times its E8M0 power of two (MXFP4) or its E4M3
-// value (NVFP4) has at most 6 significant bits, so the expansion (fp32
-// product, then bf16) is exact while the product stays inside bf16's range
+// value (NVFP4) has at most 6 significant bits, so the expansion (bf16
+// products of exact bf16 factors) is exact while it stays inside bf16's range
 // (every MXFP4 code up to the scale 2^125, byte 252; all NVFP4 values); the MMA
 // multiplies bf16 by bf16 exactly and accumulates in fp32.  NVFP4's fp32
 // tensor scale of each bank multiplies the accumulator in the epilogue.
@@ -113,28 +113,44 @@ __device__ inline int f4_row(const F4Params& p, const F4Tile& tl, int which) {
 }
 
 // Eight E2M1 codes (one 32-bit word, element 2c in the low nibble of byte c)
-// times their block's scale -> eight bf16 values (16 bytes), exactly.
-__device__ inline uint4 expand8(uint32_t w, float s) {
-  uint32_t h[4];
-  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
-      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
-      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}\n"
-      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
-      : "r"(w));
+// -> eight bf16 values (16 bytes) equal to the codes' values times the
+// block scale s2 (a bf16 pair), exactly.  A bf16 whose two low exponent bits
+// and top mantissa bit are a code's three magnitude bits is that code's value
+// times 2^-126 (zero and the subnormal code 0.5 included: exponent field 0 is
+// bf16's subnormal range), so each pair is placed by bit operations and
+// scaled by two exact multiplications, by 2^126 and by s2.
+__device__ inline uint4 expand8(uint32_t w, uint32_t s2) {
+  const uint32_t a = w & 0x0F0F0F0Fu;          // byte j: element 2j
+  const uint32_t b = (w >> 4) & 0x0F0F0F0Fu;   // byte j: element 2j + 1
   uint32_t o[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float lo = __half2float(__ushort_as_half((unsigned short)(h[i] & 0xFFFFu))) * s;
-    const float hi = __half2float(__ushort_as_half((unsigned short)(h[i] >> 16))) * s;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o[i]) : "f"(hi), "f"(lo));
+  for (int j = 0; j < 4; ++j) {
+    // byte 0 <- a.byte j, byte 2 <- b.byte j; bytes 1 and 3 <- 0 (selector 8 replicates the sign bit of
+    // a.byte 0, which is clear)
+    uint32_t t;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(t) : "r"(a), "r"(b), "r"(0x8080u | (uint32_t)j | ((4u + j) << 8)));
+    // magnitude bits 0..2 of each half to bits 6..8, the sign (bit 3) to bit 15: t * (2^6 + 2^12) moves
+    // both copies without overlap, the mask keeps one of each
+    const uint32_t raw = (t * 0x1040u) & 0x81C081C0u;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[j]) : "r"(raw), "r"(0x7E807E80u));   // x 2^126
+    asm("mul.rn.bf16x2 %0, %0, %1;" : "+r"(o[j]) : "r"(s2));
   }
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-__device__ inline float e4m3_value(uint32_t b) {
-  uint32_t h;
+// Block scales as bf16 pairs (exact): E8M0 2^(s-127) (0: 2^-127, a bf16
+// subnormal; 255: NaN), E4M3 through its f16 value.
+__device__ inline uint32_t e8m0_bf16x2(uint32_t s) {
+  const uint32_t h = s == 0u ? 0x0040u : (s == 255u ? 0x7FC0u : s << 7);
+  return h | (h << 16);
+}
+
+__device__ inline uint32_t e4m3_bf16x2(uint32_t b) {
+  uint32_t h, r;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((unsigned short)(b & 0xFFu)));
-  return __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
+  const float f = __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
+  asm("cvt.rn.bf16x2.f32 %0, %1, %1;" : "=r"(r) : "f"(f));
+  return r;
 }
 
 // 32 lanes x 16 consecutive fp32 columns: this thread's row, columns col..col+15.
@@ -386,9 +402,14 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap map_b64, const __grid_consta
           good = false;
           break;
         }
+        // the row's 32 code bytes; rows 4..7 of every 8 read their second half first, so that the eight
+        // rows of a 16-byte load phase cover all 32 banks
         const uint8_t* codes = load_ring + ls * S::kLoadBytes + S::kBTile + which * kCodeTile + row * (kBK / 2);
-        const uint4 c0 = *reinterpret_cast<const uint4*>(codes);
-        const uint4 c1 = *reinterpret_cast<const uint4*>(codes + 16);
+        const int first = (row >> 2) & 1;
+        const uint4 q0 = *reinterpret_cast<const uint4*>(codes + 16 * first);
+        const uint4 q1 = *reinterpret_cast<const uint4*>(codes + 16 * (first ^ 1));
+        const uint4 c0 = first ? q1 : q0;
+        const uint4 c1 = first ? q0 : q1;
         __syncwarp();
         if (lane == 0) mbar_arrive(&load_empty[ls]);
         if (++ls == kLS) {
@@ -398,12 +419,12 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap map_b64, const __grid_consta
         // this k-block's scale bytes within the group: 2 (MXFP4, one per 32 inputs) or 4 (NVFP4, per 16)
         const int sbyte = (kb % kGroupKb) * (kBK / SB);
         const uint32_t sw = (sbyte < 4 ? cur.x : cur.y) >> ((sbyte & 3) * 8);
-        float sv[4];
+        uint32_t sv[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           // scale of inputs 16i .. 16i+15 of the k-block
           const uint32_t b = NV ? (sw >> (8 * i)) & 0xFFu : (sw >> (8 * (i >> 1))) & 0xFFu;
-          sv[i] = NV ? e4m3_value(b) : e8m0(b);
+          sv[i] = NV ? e4m3_bf16x2(b) : e8m0_bf16x2(b);
         }
         if (!mbar_wait(&a_empty[as], aph ^ 1u, abort_flag)) {
           good = false;

@@ -8,7 +8,11 @@
 // One launch, one CTA per SM.  A producer thread streams "units" (a few
 // consecutive weight rows: their FP4 code bytes and E8M0 scale bytes) into a
 // ring of shared-memory stages with cp.async.bulk (L2 evict-first: weights
-// are read once per call); six consumer warps each reduce every sixth unit.  Phase A streams gate and up rows and writes h = bf16(silu(g) * u);
+// are read once per call); eight consumer warps each reduce every eighth
+// unit (the consumers' dependent convert-and-multiply chains bound the
+// stream, so more warps help; eight is the measured best within the
+// register file).  Phase A streams gate and up rows and writes
+// h = bf16(silu(g) * u);
 // phase B streams down rows and writes y.  Per-instance counters let a
 // consumer start the down rows of an expert as soon as every CTA finished its
 // gate/up rows of that expert, while the producer keeps streaming.
@@ -29,17 +33,19 @@
 //     hardware) times 1/g, and the row's sum by the bank's tensor scale.
 #include <climits>
 
+#include "decode_front.cuh"
+#include "front_warp.cuh"
 #include "mxfp4.cuh"
 #include "ring_gemv.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kMxStages = 6;   // ~100 KB in flight per SM: the first stage lands sooner than with 12 (measured)
+constexpr int kMxStages = 8;   // 8 x 18 KB per SM, one stage per consumer warp: measured best of 6, 8, 11 and 12
 constexpr int kMxCodeBytes = 16384;     // code bytes per stage (both banks of a gate/up unit)
 constexpr int kMxScaleOff = 16384;      // scale bytes follow the codes
 constexpr int kMxStageBytes = 18432;    // 16 KB of codes + up to 2 KB of scales (NVFP4)
-constexpr int kMxCW = 6;                // consumer warps (one stage each)
+constexpr int kMxCW = 8;                // consumer warps (one stage each)
 constexpr int kMxThreads = (kMxCW + 1) * 32;
 constexpr int kMxSmem = kMxStages * kMxStageBytes + 128;
 static_assert(kMxStages % kMxCW == 0, "each ring stage must have one consumer warp");
@@ -428,6 +434,229 @@ cudaError_t launch_fmt(const MxParams& p, cudaStream_t s) {
   }
 }
 
+// ---------------------------------------------------------------- one-launch decode over FP4 banks
+// The layer for one token in one cooperative launch, the FP4 counterpart of
+// the bf16 decode kernel (FreeToken paper, section 3.2: router, cache lookup
+// and q* split, grouped evaluation, combine; section 4.1: device-side cache
+// control; section 5.1: FP4 expert banks):
+//
+//   phase R   every CTA scores its router rows (bulk-copied into the ring's
+//             shared memory with the token row and the cache state the
+//             decision reads) and writes the logits
+//   barrier   bounded grid-wide barrier
+//   route     warp 0 of every CTA runs the same top-k and looks up which
+//             routed experts the cache pool holds: that fixes every
+//             instance's source (a hit its cache slot, a miss its staging
+//             slot), so the producer starts streaming; warp 0 then decides
+//             the fills and their victims, and CTA 0 commits the decision
+//   FFN       the ring kernel's gate/up and down phases over the instances
+//   fills     every CTA copies a share of the admitted experts' banks into
+//             their victim slots (staging -> cache)
+//   barrier   bounded grid-wide barrier: every expert row is written
+//   combine   out = bf16(sum over j of w_j * y_j), fp32 FMAs in j order,
+//             each CTA a slice of the columns
+//
+// It computes exactly what the router, bind, fill copy, dispatch, FFN and
+// combine launches compute for such a call.
+
+constexpr int kF4DecMaxSlots = 512;   // cache-pool slots whose state the decision copies (the ring takes the rest)
+
+struct __align__(16) F4DecShared {
+  int32_t table[kMaxRouteE];       // this layer's slot-table row
+  uint32_t stamp[kF4DecMaxSlots];  // the cache pool's stamps
+  int32_t owner[kF4DecMaxSlots];   // and owners
+  uint32_t hitmap[kF4DecMaxSlots / 32];
+  FrontDecision fr;
+  float red[kMxThreads / 32][kDecMaxRows][kDecMaxT];
+  float bias[kDecMaxRows];
+  uint64_t rbar;
+  uint32_t clock;
+};
+
+constexpr int kBarF4Consumers = 1;   // the consumer warps, once the decision is complete
+constexpr int kBarF4Stream = 2;      // warp 0 -> producer warp: the instances' sources are known
+
+template <int VA, int VB, bool NV>
+__global__ void __launch_bounds__(kMxThreads, 1) decode_fp4_kernel(MxParams p, Fp4DecodeArgs d) {
+  extern __shared__ __align__(128) uint8_t ring_raw[];
+  __shared__ MxRing rg;
+  __shared__ int s_cnt[kFp4RingMaxRows];
+  __shared__ MxInsts in;
+  __shared__ F4DecShared sh;
+  uint8_t* ring = ring_raw;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int E = p.E, H = p.H, G = gridDim.x, b = blockIdx.x;
+  const int n_my = b < E ? (E - 1 - b) / G + 1 : 0;
+  const int n_slots = d.c.cache.n_slots, base = p.layer * E;
+  const int rows_per_cta = (E + G - 1) / G;
+  // ring bytes during the prologue: router rows (fp32) | token row (bf16)
+  float* wrow = reinterpret_cast<float*>(ring);
+  __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(wrow + (size_t)rows_per_cta * H);
+  p.inst_done = d.grid_count + 4;
+
+  if (tid == 0) {
+    for (int s = 0; s < kMxStages; ++s) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&rg.full_bar[s])));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&rg.empty_bar[s])));
+    }
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sh.rbar)));
+    rg.abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (tid < kFp4RingMaxRows) s_cnt[tid] = 0;
+  __syncthreads();
+  pdl_wait();
+  // ---------------------------------------------------------------- phase R
+  const bool table_bulk = (reinterpret_cast<uintptr_t>(d.c.slot_table + base) & 15) == 0;
+  const bool slot_bulk = ((reinterpret_cast<uintptr_t>(d.c.stamp) | reinterpret_cast<uintptr_t>(d.c.owner)) & 15) == 0;
+  const int table_bulk_n = table_bulk ? (E & ~3) : 0;
+  const int slot_bulk_n = slot_bulk ? (n_slots & ~3) : 0;
+  if (tid == 0) {
+    const uint32_t row_bytes = (uint32_t)H * 4u, x_bytes = (uint32_t)H * 2u;
+    const uint32_t bytes = row_bytes * (uint32_t)n_my + x_bytes + 4u * (uint32_t)table_bulk_n + 8u * (uint32_t)slot_bulk_n;
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(&sh.rbar)), "r"(bytes)
+                 : "memory");
+    for (int i = 0; i < n_my; ++i)
+      bulk_g2s(wrow + (size_t)i * H, d.w_router + (size_t)(b + i * G) * H, row_bytes, &sh.rbar);
+    bulk_g2s(xs, p.x, x_bytes, &sh.rbar);
+    if (table_bulk_n > 0) bulk_g2s(sh.table, d.c.slot_table + base, 4u * table_bulk_n, &sh.rbar);
+    if (slot_bulk_n > 0) {
+      bulk_g2s(sh.stamp, d.c.stamp, 4u * slot_bulk_n, &sh.rbar);
+      bulk_g2s(sh.owner, d.c.owner, 4u * slot_bulk_n, &sh.rbar);
+    }
+  } else if (warp == kMxCW) {
+    for (int e = table_bulk_n + lane; e < E; e += 32) sh.table[e] = __ldcg(d.c.slot_table + base + e);
+    for (int v = slot_bulk_n + lane; v < n_slots; v += 32) {
+      sh.stamp[v] = __ldcg(d.c.stamp + v);
+      sh.owner[v] = __ldcg(d.c.owner + v);
+    }
+    if (lane == 0) sh.clock = __ldcg(d.c.clock);
+  } else if (warp == 1 && lane < n_my) {
+    sh.bias[lane] = d.bias ? __ldg(d.bias + b + lane * G) : 0.0f;
+  }
+  if (!bounded_wait(&sh.rbar, 0u, &rg.abort)) rg.abort = 1;
+  __syncthreads();
+  if (n_my > 0 && !rg.abort) {
+    constexpr int NW = kMxThreads / 32;
+    switch (n_my) {
+      case 1: router_rows_block<1, 1, NW>(wrow, xs, H, 1, E, sh.red, sh.bias, d.logits, b, G); break;
+      case 2: router_rows_block<2, 1, NW>(wrow, xs, H, 1, E, sh.red, sh.bias, d.logits, b, G); break;
+      case 3: router_rows_block<3, 1, NW>(wrow, xs, H, 1, E, sh.red, sh.bias, d.logits, b, G); break;
+      default: router_rows_block<4, 1, NW>(wrow, xs, H, 1, E, sh.red, sh.bias, d.logits, b, G); break;
+    }
+  }
+  // ---------------------------------------------------------------- route, residency
+  if (grid_barrier(d.grid_count + 0, &rg.abort)) {
+    const int R = p.k;
+    if (warp == 0) {
+      const FrontLane fl = front_route(d.logits, 1, R, E, n_slots, sh.table, sh.fr);
+      // one token: its R distinct experts in ascending order, instance j = routed row j
+      if (lane < R) {
+        in.e[lane] = fl.e;
+        in.pos[lane] = lane;
+        in.yrow[lane] = sh.fr.perm[lane];
+        in.entry[lane] = fl.hit ? fl.entry : (int)(MOE_STAGING_TAG | (base + fl.e));
+      }
+      if (lane == 0) in.n = R;
+      __syncwarp();
+      asm volatile("bar.arrive %0, %1;" ::"n"(kBarF4Stream), "n"(64) : "memory");   // the producer may stream
+      front_residency(fl, n_slots, p.layer, sh.stamp, sh.owner, sh.clock, d.phi_q16, d.min_fill, d.policy, d.seed,
+                      sh.fr, sh.hitmap);
+    }
+    if (warp == kMxCW) {
+      asm volatile("bar.sync %0, %1;" ::"n"(kBarF4Stream), "n"(64) : "memory");
+    } else {
+      asm volatile("bar.sync %0, %1;" ::"n"(kBarF4Consumers), "n"(kMxCW * 32) : "memory");
+      // routing outputs, spread over the CTAs; CTA 0 commits the decision (every CTA read the
+      // pre-call state before the barrier)
+      for (int e = b + tid * G; e <= E; e += G * kMxCW * 32) {
+        int lo, hi;
+        dispatch_range(sh.fr.sorted, R, e, lo, hi);
+        d.offsets[e] = lo;
+        if (e < E) d.counts[e] = hi - lo;
+      }
+      if (b == (G > 1 ? 1 : 0) && tid < R) {
+        d.topk_ids[tid] = sh.fr.ids[tid];
+        d.topk_w[tid] = sh.fr.w[tid];
+        d.perm[tid] = sh.fr.perm[tid];
+        d.inv_perm[tid] = sh.fr.inv_perm[tid];
+      }
+      if (b == 0 && warp == 0) front_commit(sh.fr, d.c, p.layer, d.stats, p.status);
+    }
+    // ---------------------------------------------------------------- FFN
+    const bool producer = warp == kMxCW;
+    MxRingState st = {0, -1, -1};
+    if (!producer || lane == 0) {
+      mx_phase<true, VA, NV>(p, in, s_cnt, ring, rg, st, producer);
+      if (!rg.abort) mx_phase<false, VB, NV>(p, in, s_cnt, ring, rg, st, producer);
+      if (producer && st.armed_last >= 0) {
+        volatile int no_abort = 0;
+        for (int q = st.last_issued; q >= 0 && q > st.last_issued - kMxStages; --q)
+          ring_wait(&rg.full_bar[q % kMxStages], (uint32_t)(q / kMxStages) & 1u, &no_abort);
+      }
+    }
+    // ---------------------------------------------------------------- fills
+    // work items (fill, bank, 64 KB chunk) over the grid; the fills' lanes of the decision in lane order
+    const Fp4FillBanks& fb = d.fill;
+    const unsigned fmask = __ballot_sync(0xffffffffu, lane < R && sh.fr.u_kind[lane] == kFrontFill);
+    const int n_fill = __popc(fmask);
+    constexpr size_t kChunk = 64 * 1024;
+    size_t max_chunks = 1;
+    for (int bk = 0; bk < fb.n; ++bk) max_chunks = max(max_chunks, (fb.slot_bytes[bk] + kChunk - 1) / kChunk);
+    const size_t items = (size_t)n_fill * fb.n * max_chunks;
+    const uint64_t pol = l2_evict_first();
+    for (size_t item = b; item < items && !rg.abort; item += G) {
+      const int f = (int)(item / ((size_t)fb.n * max_chunks));
+      const size_t rem = item % ((size_t)fb.n * max_chunks);
+      const int bk = (int)(rem / max_chunks);
+      const size_t lo = (rem % max_chunks) * kChunk;
+      if (lo >= fb.slot_bytes[bk]) continue;
+      unsigned mm = fmask;
+      for (int i = 0; i < f; ++i) mm &= mm - 1;
+      const int fl = __ffs(mm) - 1;
+      const int src_slot = base + sh.fr.u_e[fl], dst_slot = sh.fr.u_slot[fl];
+      if (src_slot >= fb.src_slots || dst_slot < 0 || dst_slot >= fb.dst_slots) {
+        if (tid == 0) set_status(p.status, MOE_DEV_ERR_BAD_SLOT);
+        continue;
+      }
+      const size_t len = min(kChunk, fb.slot_bytes[bk] - lo);
+      const uint8_t* src = fb.src[bk] + (size_t)src_slot * fb.slot_bytes[bk] + lo;
+      uint8_t* dst = fb.dst[bk] + (size_t)dst_slot * fb.slot_bytes[bk] + lo;
+      if ((fb.slot_bytes[bk] & 15) == 0) {
+        for (size_t v = tid; v < len / 16; v += kMxThreads)
+          reinterpret_cast<uint4*>(dst)[v] = ldg_stream_hint(reinterpret_cast<const uint4*>(src) + v, pol);
+      } else {
+        for (size_t v = tid; v < len / 4; v += kMxThreads)
+          reinterpret_cast<uint32_t*>(dst)[v] = reinterpret_cast<const uint32_t*>(src)[v];
+      }
+    }
+    // ---------------------------------------------------------------- combine
+    if (grid_barrier(d.grid_count + 1, &rg.abort)) {
+      const int H4 = H >> 2;
+      for (int c4 = b * kMxThreads + tid; c4 < H4; c4 += G * kMxThreads) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < R; ++j) {
+          const float w = sh.fr.w[j];
+          const float4 y = __ldcg(reinterpret_cast<const float4*>(p.y + (size_t)j * H) + c4);
+          acc.x = fmaf(w, y.x, acc.x);
+          acc.y = fmaf(w, y.y, acc.y);
+          acc.z = fmaf(w, y.z, acc.z);
+          acc.w = fmaf(w, y.w, acc.w);
+        }
+        uint2 o;
+        o.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc.x)) |
+              ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc.y)) << 16);
+        o.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc.z)) |
+              ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc.w)) << 16);
+        reinterpret_cast<uint2*>(d.out)[c4] = o;
+      }
+    }
+  }
+  pdl_trigger();
+  __syncthreads();
+  if (rg.abort && tid == 0) set_status(p.status, MOE_DEV_ERR_TIMEOUT);
+}
+
 // rows of 1024, 2048 or 4096 inputs: 1, 2 or 4 blocks per lane, whose staged activations stay in registers
 inline bool v_ok(int K) { return K == 1024 || K == 2048 || K == 4096; }
 inline bool al16(const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; }
@@ -446,6 +675,56 @@ bool fp4_ring_ok(const MxParams& p, int T, bool nv) {
   (void)nv;
   return T >= 1 && (long long)T * p.k <= kFp4RingMaxRows && v_ok(p.H) && v_ok(p.I) && pool_ok(p.a) &&
          pool_ok(p.b) && p.inst_done != nullptr;
+}
+
+bool fp4_decode_ok(const MxParams& p, int T, int n_slots) {
+  const int G = num_sms();
+  const int rows = (p.E + G - 1) / G;
+  return T == 1 && p.k <= 32 && p.E <= kMaxRouteE && rows <= kDecMaxRows && n_slots >= 1 &&
+         n_slots <= kF4DecMaxSlots && v_ok(p.H) && v_ok(p.I) && pool_ok(p.a) && pool_ok(p.b) &&
+         (size_t)rows * p.H * 4 + (size_t)p.H * 2 <= (size_t)kMxStages * kMxStageBytes;
+}
+
+template <int VA, int VB, bool NV>
+cudaError_t launch_decode_vv(const MxParams& p, const Fp4DecodeArgs& a, cudaStream_t s) {
+  static std::atomic<int> smem_set[kMaxDevices];
+  cudaError_t e = ensure_smem(decode_fp4_kernel<VA, VB, NV>, kMxSmem, smem_set);
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(a.grid_count, 0, (4 + (size_t)p.k) * sizeof(unsigned int), s);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms());
+  cfg.blockDim = dim3(kMxThreads);
+  cfg.dynamicSmemBytes = kMxSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attrs[1];
+  attrs[0].id = cudaLaunchAttributeCooperative;   // all CTAs resident: the grid barriers and the cross-CTA waits complete
+  attrs[0].val.cooperative = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 1;
+  return counted(cudaLaunchKernelEx(&cfg, decode_fp4_kernel<VA, VB, NV>, p, a));
+}
+
+template <int VA, bool NV>
+cudaError_t launch_decode_va(const MxParams& p, const Fp4DecodeArgs& a, cudaStream_t s) {
+  switch (p.I / 1024) {
+    case 1: return launch_decode_vv<VA, 1, NV>(p, a, s);
+    case 2: return launch_decode_vv<VA, 2, NV>(p, a, s);
+    default: return launch_decode_vv<VA, 4, NV>(p, a, s);
+  }
+}
+
+template <bool NV>
+cudaError_t launch_decode_fmt(const MxParams& p, const Fp4DecodeArgs& a, cudaStream_t s) {
+  switch (p.H / 1024) {
+    case 1: return launch_decode_va<1, NV>(p, a, s);
+    case 2: return launch_decode_va<2, NV>(p, a, s);
+    default: return launch_decode_va<4, NV>(p, a, s);
+  }
+}
+
+cudaError_t launch_fp4_decode(const MxParams& p, bool nv, const Fp4DecodeArgs& a, cudaStream_t s) {
+  return nv ? launch_decode_fmt<true>(p, a, s) : launch_decode_fmt<false>(p, a, s);
 }
 
 cudaError_t launch_fp4_ring(const MxParams& p, int T, bool nv, cudaStream_t s) {

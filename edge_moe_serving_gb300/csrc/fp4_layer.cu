@@ -18,32 +18,19 @@ namespace {
 
 constexpr int kFillThreads = 256;
 constexpr size_t kFillChunk = 64 * 1024;   // bytes of one bank of one fill per work item
-constexpr int kMaxFillBanks = 7;           // six code and scale banks + the tensor scales
-
-struct BankCopy {
-  const uint8_t* src;
-  uint8_t* dst;
-  size_t slot_bytes;   // bytes of one slot of this bank
-};
-
-struct FillBanks {
-  BankCopy b[kMaxFillBanks];
-  int n;
-  int src_slots, dst_slots;
-};
 
 // Copies every filled expert's slot of every bank, staging -> cache.  Work
 // items are (fill, bank, 64 KB chunk); banks whose slot size is a multiple of
 // 16 bytes (every code and scale bank of a supported shape) move 16-byte
 // words, the tensor scales (12 bytes per slot) 4-byte words.
 __global__ void __launch_bounds__(kFillThreads)
-fp4_fill_kernel(FillBanks fb, const int32_t* __restrict__ fills, const int32_t* __restrict__ n_fill_p,
+fp4_fill_kernel(Fp4FillBanks fb, const int32_t* __restrict__ fills, const int32_t* __restrict__ n_fill_p,
                 uint32_t* status) {
   pdl_wait();
   pdl_trigger();
   const int n_fill = *n_fill_p;
   size_t max_chunks = 1;
-  for (int b = 0; b < fb.n; ++b) max_chunks = max(max_chunks, (fb.b[b].slot_bytes + kFillChunk - 1) / kFillChunk);
+  for (int b = 0; b < fb.n; ++b) max_chunks = max(max_chunks, (fb.slot_bytes[b] + kFillChunk - 1) / kFillChunk);
   const size_t items = (size_t)n_fill * fb.n * max_chunks;
   const uint64_t pol = l2_evict_first();
   for (size_t item = blockIdx.x; item < items; item += gridDim.x) {
@@ -51,18 +38,18 @@ fp4_fill_kernel(FillBanks fb, const int32_t* __restrict__ fills, const int32_t* 
     const size_t rem = item % ((size_t)fb.n * max_chunks);
     const int b = (int)(rem / max_chunks);
     const size_t chunk = rem % max_chunks;
-    const BankCopy bc = fb.b[b];
+    const size_t slot_bytes = fb.slot_bytes[b];
     const size_t lo = chunk * kFillChunk;
-    if (lo >= bc.slot_bytes) continue;
+    if (lo >= slot_bytes) continue;
     const int s_slot = fills[2 * f], d_slot = fills[2 * f + 1];
     if (s_slot < 0 || s_slot >= fb.src_slots || d_slot < 0 || d_slot >= fb.dst_slots) {
       if (threadIdx.x == 0 && chunk == 0 && b == 0) set_status(status, MOE_DEV_ERR_BAD_SLOT);
       continue;
     }
-    const size_t len = min(kFillChunk, bc.slot_bytes - lo);
-    const uint8_t* src = bc.src + (size_t)s_slot * bc.slot_bytes + lo;
-    uint8_t* dst = bc.dst + (size_t)d_slot * bc.slot_bytes + lo;
-    if ((bc.slot_bytes & 15) == 0) {
+    const size_t len = min(kFillChunk, slot_bytes - lo);
+    const uint8_t* src = fb.src[b] + (size_t)s_slot * slot_bytes + lo;
+    uint8_t* dst = fb.dst[b] + (size_t)d_slot * slot_bytes + lo;
+    if ((slot_bytes & 15) == 0) {
       const uint4* s4 = reinterpret_cast<const uint4*>(src);
       uint4* d4 = reinterpret_cast<uint4*>(dst);
       for (size_t v = threadIdx.x; v < len / 16; v += kFillThreads) d4[v] = ldg_stream_hint(s4 + v, pol);
@@ -91,6 +78,9 @@ struct Fp4Ws {
   int32_t* inv_perm;
   float* y_rows;
   void* bind_ws;
+  float* dec_logits;
+  __nv_bfloat16* dec_h;
+  unsigned int* dec_words;
   void* scratch;
   size_t scratch_bytes, bytes;
 };
@@ -113,6 +103,10 @@ Fp4Ws fp4_ws(void* ws, int T, int k, int E, int H, int I) {
   L.inv_perm = static_cast<int32_t*>(take(R * 4));
   L.y_rows = static_cast<float*>(take(R * H * 4));
   L.bind_ws = take(bind_ws_bytes(T, k, E));
+  // one-token calls: the one-launch kernel's logits, h rows and barrier words
+  L.dec_logits = static_cast<float*>(T == 1 ? take((size_t)E * 4) : nullptr);
+  L.dec_h = static_cast<__nv_bfloat16*>(T == 1 ? take(R * I * 2) : nullptr);
+  L.dec_words = static_cast<unsigned int*>(T == 1 ? take((4 + R) * 4) : nullptr);
   L.scratch_bytes = std::max({route_ws_bytes(T, H, E), dispatch_ws_bytes(T, k, E),
                               moe_expert_ffn_mxfp4_workspace_size(T, k, H, I),
                               moe_expert_ffn_nvfp4_workspace_size(T, k, H, I), (size_t)256});
@@ -144,6 +138,62 @@ moe_cache bind_view(const moe_cache_fp4& c) {
   v.H = c.H;
   v.I = c.I;
   return v;
+}
+
+// The banks a fill copies, staging slot -> cache slot (only read when there is a staging pool).
+Fp4FillBanks fill_banks(const moe_cache_fp4& c, bool nv) {
+  Fp4FillBanks fb = {};
+  const int SB = nv ? 16 : kMxBlock;
+  const size_t H = (size_t)c.H, I = (size_t)c.I;
+  const moe_pool_nvfp4& a = c.cache;
+  const moe_pool_nvfp4& b = c.staging;
+  const size_t gq = I * H / 2, gs = I * H / SB, dq = H * I / 2, ds = H * I / SB;
+  const void* srcs[6] = {b.gate_q, b.gate_s, b.up_q, b.up_s, b.down_q, b.down_s};
+  const void* dsts[6] = {a.gate_q, a.gate_s, a.up_q, a.up_s, a.down_q, a.down_s};
+  const size_t sizes[6] = {gq, gs, gq, gs, dq, ds};
+  for (int i = 0; i < 6; ++i) {
+    fb.src[i] = static_cast<const uint8_t*>(srcs[i]);
+    fb.dst[i] = static_cast<uint8_t*>(const_cast<void*>(dsts[i]));
+    fb.slot_bytes[i] = sizes[i];
+  }
+  fb.n = 6;
+  if (nv) {
+    fb.src[6] = reinterpret_cast<const uint8_t*>(b.tensor_scale);
+    fb.dst[6] = reinterpret_cast<uint8_t*>(const_cast<float*>(a.tensor_scale));
+    fb.slot_bytes[6] = 3 * sizeof(float);
+    fb.n = 7;
+  }
+  fb.src_slots = b.gate_q ? b.n_slots : 0;
+  fb.dst_slots = a.n_slots;
+  return fb;
+}
+
+// The ring kernels' parameter block over the FP4 cache's pools.
+MxParams mx_params(const moe_cache_fp4& c, bool nv, int layer, int k) {
+  MxParams p = {};
+  const moe_pool_nvfp4* ps[2] = {&c.cache, &c.staging};
+  moe_pool_mxfp4* qs[2] = {&p.a, &p.b};
+  for (int i = 0; i < 2; ++i) {
+    if (!ps[i]->gate_q) continue;   // no staging pool: n_slots 0, staging entries read as out of range
+    qs[i]->gate_q = ps[i]->gate_q;
+    qs[i]->gate_s = ps[i]->gate_s;
+    qs[i]->up_q = ps[i]->up_q;
+    qs[i]->up_s = ps[i]->up_s;
+    qs[i]->down_q = ps[i]->down_q;
+    qs[i]->down_s = ps[i]->down_s;
+    qs[i]->n_slots = ps[i]->n_slots;
+  }
+  if (nv) {
+    p.ts_a = c.cache.tensor_scale;
+    p.ts_b = c.staging.gate_q ? c.staging.tensor_scale : nullptr;
+  }
+  p.slot_table = c.slot_table;
+  p.layer = layer;
+  p.E = c.E;
+  p.H = c.H;
+  p.I = c.I;
+  p.k = k;
+  return p;
 }
 
 int pool_check(const moe_pool_nvfp4& p, bool nv, bool required) {
@@ -197,14 +247,44 @@ extern "C" int moe_layer_forward_fp4(const moe_layer* layer, const moe_cache_fp4
   if (phi_q16 > 0 && (!cache->staging.gate_q || (long long)cache->staging.n_slots < (long long)cache->n_layers * E))
     return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
-  if (!x || !out) return MOE_ERR_INVALID_ARG;
-  if (!a16(x)) return MOE_ERR_UNSUPPORTED;
+  if (!x || !out || !layer->w_router) return MOE_ERR_INVALID_ARG;
+  if (!a16(x) || !a16(layer->w_router) || E > kMaxRouteE) return MOE_ERR_UNSUPPORTED;   // the router's own limits
   const Fp4Ws need = fp4_ws(nullptr, T, k, E, H, I);
   if (!ws || ws_bytes < need.bytes) return MOE_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_UNSUPPORTED;
   const Fp4Ws L = fp4_ws(ws, T, k, E, H, I);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int R = T * k;
+
+  MxParams mp = mx_params(*cache, nv, layer->layer, k);
+  if (T == 1 && fp4_decode_ok(mp, T, cache->cache.n_slots)) {
+    // one token: the whole layer in one cooperative launch
+    mp.x = static_cast<const __nv_bfloat16*>(x);
+    mp.h = L.dec_h;
+    mp.y = L.y_rows;
+    mp.status = dev_status;
+    Fp4DecodeArgs a = {};
+    a.c = bind_view(*cache);
+    a.w_router = layer->w_router;
+    a.bias = layer->bias;
+    a.phi_q16 = phi_q16;
+    a.min_fill = min_fill;
+    a.policy = fill_policy;
+    a.seed = seed;
+    a.stats = stats_dev;
+    a.logits = L.dec_logits;
+    a.topk_ids = L.ids;
+    a.topk_w = L.w;
+    a.counts = L.counts;
+    a.offsets = L.offsets;
+    a.perm = L.perm;
+    a.inv_perm = L.inv_perm;
+    a.out = static_cast<__nv_bfloat16*>(out);
+    a.grid_count = L.dec_words;
+    a.fill = fill_banks(*cache, nv);
+    if (phi_q16 == 0 || !cache->staging.gate_q) a.fill.n = 0;   // no fills are admitted
+    return launch_fp4_decode(mp, nv, a, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  }
 
   st = moe_route_topk(x, T, H, layer->w_router, layer->bias, E, k, L.ids, L.w, nullptr, L.scratch, L.scratch_bytes,
                       dev_status, stream);
@@ -217,23 +297,7 @@ extern "C" int moe_layer_forward_fp4(const moe_layer* layer, const moe_cache_fp4
     return MOE_ERR_CUDA;
   if (cache->staging.gate_q && phi_q16 > 0) {
     // the admitted experts: every bank's slot, staging -> cache
-    FillBanks fb = {};
-    const moe_pool_nvfp4& a = cache->cache;
-    const moe_pool_nvfp4& b = cache->staging;
-    const size_t gq = (size_t)I * H / 2, gs = (size_t)I * H / SB, dq = (size_t)H * I / 2, ds = (size_t)H * I / SB;
-    const void* srcs[6] = {b.gate_q, b.gate_s, b.up_q, b.up_s, b.down_q, b.down_s};
-    const void* dsts[6] = {a.gate_q, a.gate_s, a.up_q, a.up_s, a.down_q, a.down_s};
-    const size_t sizes[6] = {gq, gs, gq, gs, dq, ds};
-    for (int i = 0; i < 6; ++i)
-      fb.b[i] = {static_cast<const uint8_t*>(srcs[i]), static_cast<uint8_t*>(const_cast<void*>(dsts[i])), sizes[i]};
-    fb.n = 6;
-    if (nv) {
-      fb.b[6] = {reinterpret_cast<const uint8_t*>(b.tensor_scale),
-                 reinterpret_cast<uint8_t*>(const_cast<float*>(a.tensor_scale)), 3 * sizeof(float)};
-      fb.n = 7;
-    }
-    fb.src_slots = b.n_slots;
-    fb.dst_slots = a.n_slots;
+    const Fp4FillBanks fb = fill_banks(*cache, nv);
     const int32_t* n_fill = reinterpret_cast<const int32_t*>(L.bind_ws);
     if (launch_k(fp4_fill_kernel, num_sms() * 4, kFillThreads, 0, s, fb, n_fill + 4, n_fill, dev_status) !=
         cudaSuccess)
@@ -249,19 +313,7 @@ extern "C" int moe_layer_forward_fp4(const moe_layer* layer, const moe_cache_fp4
                               cache->n_layers, layer->layer, E, H, I, L.counts, L.offsets, L.perm, x, T, k, L.y_rows,
                               L.scratch, L.scratch_bytes, dev_status, stream);
   } else {
-    moe_pool_mxfp4 a = {}, b = {};
-    const moe_pool_nvfp4* ps[2] = {&cache->cache, &cache->staging};
-    moe_pool_mxfp4* qs[2] = {&a, &b};
-    for (int i = 0; i < 2; ++i) {
-      qs[i]->gate_q = ps[i]->gate_q;
-      qs[i]->gate_s = ps[i]->gate_s;
-      qs[i]->up_q = ps[i]->up_q;
-      qs[i]->up_s = ps[i]->up_s;
-      qs[i]->down_q = ps[i]->down_q;
-      qs[i]->down_s = ps[i]->down_s;
-      qs[i]->n_slots = ps[i]->n_slots;
-    }
-    st = moe_expert_ffn_mxfp4(&a, cache->staging.gate_q ? &b : nullptr, cache->slot_table, cache->n_layers,
+    st = moe_expert_ffn_mxfp4(&mp.a, cache->staging.gate_q ? &mp.b : nullptr, cache->slot_table, cache->n_layers,
                               layer->layer, E, H, I, L.counts, L.offsets, L.perm, x, T, k, L.y_rows, L.scratch,
                               L.scratch_bytes, dev_status, stream);
   }

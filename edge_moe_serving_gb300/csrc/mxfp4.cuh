@@ -94,6 +94,44 @@ constexpr int kFp4RingMaxRows = 64;
 bool fp4_ring_ok(const MxParams& p, int T, bool nv);
 cudaError_t launch_fp4_ring(const MxParams& p, int T, bool nv, cudaStream_t s);
 
+// The banks a cache fill of an FP4 expert copies, staging slot -> cache slot:
+// six code and scale banks, plus the NVFP4 tensor scales (n = 7).
+struct Fp4FillBanks {
+  const uint8_t* src[7];
+  uint8_t* dst[7];
+  size_t slot_bytes[7];   // bytes of one slot of the bank
+  int n;
+  int src_slots, dst_slots;
+};
+
+// The whole layer for one token over FP4 banks in one cooperative launch
+// (ffn_mxfp4_ring.cu): router rows, a grid barrier, the route and residency
+// decision in every CTA (CTA 0 commits it), the ring kernel's gate/up and
+// down phases, the cache fills, a grid barrier and the combine.  p: as for
+// the ring kernel, with p.h and p.y the call's workspace and p.inst_done
+// unused (grid_count + 4 is used instead).  Shapes: see fp4_decode_ok.
+struct Fp4DecodeArgs {
+  moe_cache c;              // residency arrays and the cache pool's slot count
+  const float* w_router;    // [E, H]
+  const float* bias;        // [E] or null
+  uint32_t phi_q16;
+  int min_fill, policy;
+  unsigned long long seed;
+  moe_bind_stats* stats;    // or null
+  float* logits;            // [E]
+  int32_t* topk_ids;
+  float* topk_w;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* perm;
+  int32_t* inv_perm;
+  __nv_bfloat16* out;       // [1, H]
+  unsigned int* grid_count; // 4 + k words, cleared on the stream by the launch
+  Fp4FillBanks fill;
+};
+bool fp4_decode_ok(const MxParams& p, int T, int n_slots);
+cudaError_t launch_fp4_decode(const MxParams& p, bool nv, const Fp4DecodeArgs& a, cudaStream_t s);
+
 // The tensor-core GEMM over FP4 banks (ffn_fp4_gemm.cu): whether the shape
 // qualifies (I a multiple of 128, H of 256, every row's scales a multiple of
 // 16 bytes), and the two launches (gate/up into p.h, down into p.y) over the

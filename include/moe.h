@@ -459,17 +459,23 @@ typedef struct moe_cache_fp4 {
   int32_t reserved;         /* 0 */
 } moe_cache_fp4;
 
-/* moe_layer_forward over an FP4 expert cache, with per-step launches: router
- * and top-k, the residency bind (the same decisions and state updates as
+/* moe_layer_forward over an FP4 expert cache: router and top-k, the
+ * residency bind (the same decisions and state updates as
  * moe_cache_bind_slots) with a fill copy of the admitted experts' six code
  * and scale banks (and tensor scales) from the staging pool into their cache
  * slots, dispatch, the FP4 expert FFN (moe_expert_ffn_mxfp4 /
- * moe_expert_ffn_nvfp4) and the combine.  Arguments as moe_layer_forward
- * (layer->E, H, I equal to the cache's); stats_dev optional.  Errors: those
- * of the steps, plus MOE_ERR_INVALID_ARG for an unknown format or a shape
- * mismatch and MOE_ERR_WORKSPACE below moe_layer_fp4_workspace_size.  NVFP4
- * calls that fit neither of moe_expert_ffn_nvfp4's kernels return
- * MOE_ERR_UNSUPPORTED before any launch. */
+ * moe_expert_ffn_nvfp4) and the combine.  One-token calls with H and I in
+ * {1024, 2048, 4096}, k <= 32, at most 512 cache slots and at most 4 router
+ * rows per SM run all of it in one cooperative launch (the FFN on the
+ * weight-streaming ring kernel's arithmetic, the fills copied after the
+ * expert rows); other calls run per-step launches.  Arguments as
+ * moe_layer_forward (layer->E, H, I equal to the cache's); stats_dev
+ * optional.  Errors: those of the steps, plus MOE_ERR_INVALID_ARG for an
+ * unknown format, a shape mismatch or a NULL router, MOE_ERR_UNSUPPORTED for
+ * E > 512 or a router, x or ws not aligned as the router and the FFN need,
+ * and MOE_ERR_WORKSPACE below moe_layer_fp4_workspace_size; every check is
+ * made before the first launch.  NVFP4 calls that fit neither of
+ * moe_expert_ffn_nvfp4's kernels return MOE_ERR_UNSUPPORTED. */
 size_t moe_layer_fp4_workspace_size(const moe_layer* layer, const moe_cache_fp4* cache, int T);
 int moe_layer_forward_fp4(const moe_layer* layer, const moe_cache_fp4* cache, const void* x, int T, void* out,
                           uint32_t phi_q16, int min_fill, int fill_policy, uint64_t seed, void* ws,

@@ -218,6 +218,19 @@ class Fp4Cache:
                 "stamp": self.stamp.cpu().numpy().view(np.uint32).astype(np.int64),
                 "clock": int(self.clock.cpu().numpy().view(np.uint32)[0])}
 
+    def reset(self):
+        """Restore the initial residency state and the cache pool contents."""
+        st = self.initial
+        self.table.copy_(to_dev(st["table"].astype(np.int32), self.device))
+        self.owner.copy_(to_dev(st["owner"].astype(np.int32), self.device))
+        self.stamp.zero_()
+        self.clock.zero_()
+        idx = torch.from_numpy(np.asarray(st["owner"], np.int64)).to(self.device)
+        for c, s in zip(self.cache, self.staging):
+            c.copy_(s.index_select(0, idx))
+        if self.cache_ts is not None:
+            self.cache_ts.copy_(self.staging_ts.index_select(0, idx))
+
     def cache_matches_owners(self):
         """Whether every cache slot's banks (and tensor scales) equal, byte for
         byte, the staging slot of the (layer, expert) pair that owns it."""

@@ -10,8 +10,10 @@ bytes, scale bytes and tensor scales equal those of the pair that owns it
 (the fill copy is byte work); and the layer output matches the oracle's
 fp64 layer on the dequantised experts within the output tolerance.  Phi = 1
 (every miss filled), 0.25 with the random fill policy (fills and staged
-experts in one call) and 0 (no fills); one-token calls and batched calls
-(the ring kernel up to 64 routed rows, the tensor-core GEMM above it)."""
+experts in one call) and 0 (no fills); one-token calls (the one-launch
+kernel, also checked bitwise against the public per-step calls) and batched
+calls (the ring kernel up to 64 routed rows, the tensor-core GEMM above
+it)."""
 import dataclasses
 
 import numpy as np
@@ -19,7 +21,7 @@ import pytest
 import torch
 
 import edge_moe_serving_gb300 as moe
-from moe_inputs import gen
+from moe_inputs import CONFIGS, gen
 from moe_inputs.configs import FILL_RANDOM, LayerConfig
 from moe_inputs.device import DeviceLayer, Fp4Cache, x_dev
 from oracle import moe_oracle as O
@@ -141,3 +143,69 @@ def test_fp4_layer_nvfp4_rejects_calls_that_fit_neither_kernel_before_the_bind()
     after = fc.state()
     for key in ("table", "owner", "stamp"):
         assert np.array_equal(before[key], after[key])
+
+
+@pytest.mark.parametrize("fmt", [moe.MOE_FP4_MXFP4, moe.MOE_FP4_NVFP4])
+def test_fp4_layer_one_token_is_one_launch_matching_the_per_step_calls(fmt):
+    """A one-token call runs as one kernel and matches the public calls
+    chained on the same cache: router + top-k, dispatch, the FP4 expert FFN,
+    the combine (phi = 0: the call changes no binding, so both read the same
+    slot table).  The two routers sum the logits in different orders, so
+    the gate weights may differ in their last bits: every output is within 2
+    bf16 units in the last place of the chained one (other experts would
+    differ by whole units), and almost all are equal."""
+    cfg = FP4
+    fc = Fp4Cache(cfg, fmt, SEED, DEV)
+    E, H, I, k = cfg.E, cfg.H, cfg.I, cfg.k
+    for step in range(3):
+        l = step % cfg.n_layers
+        dl = DeviceLayer(cfg, l, DEV, step)
+        x = x_dev(cfg, l, step)[:1].contiguous()
+        # the public calls
+        i32 = lambda n: torch.empty(n, dtype=torch.int32, device=DEV)
+        ids, counts, offsets, perm, inv = i32(k), i32(E), i32(E + 1), i32(k), i32(k)
+        w = torch.empty(k, dtype=torch.float32, device=DEV)
+        y = torch.empty((k, H), dtype=torch.float32, device=DEV)
+        ref = torch.empty((1, H), dtype=torch.bfloat16, device=DEV)
+        st = status()
+        nr, nd = moe.moe_route_topk_workspace_size(1, H, E), moe.moe_dispatch_workspace_size(1, k, E)
+        moe.moe_route_topk(x, 1, H, dl.w_router, dl.bias, E, k, ids, w, None, ws(nr), nr, st)
+        moe.moe_dispatch(ids, 1, k, E, counts, offsets, perm, inv, None, H, None, ws(nd), nd, st)
+        c = fc.struct
+        if fmt == moe.MOE_FP4_MXFP4:
+            pools = [moe.moe_pool_mxfp4(q.gate_q, q.gate_s, q.up_q, q.up_s, q.down_q, q.down_s, q.n_slots, 0)
+                     for q in (c.cache, c.staging)]
+            nf = moe.moe_expert_ffn_mxfp4_workspace_size(1, k, H, I)
+            moe.moe_expert_ffn_mxfp4(pools[0], pools[1], fc.table, cfg.n_layers, l, E, H, I, counts, offsets, perm, x,
+                                     1, k, y, ws(nf), nf, st)
+        else:
+            nf = moe.moe_expert_ffn_nvfp4_workspace_size(1, k, H, I)
+            moe.moe_expert_ffn_nvfp4(c.cache, c.staging, fc.table, cfg.n_layers, l, E, H, I, counts, offsets, perm,
+                                     x, 1, k, y, ws(nf), nf, st)
+        moe.moe_combine(y, w, 1, k, H, ref, None, st)
+        torch.cuda.synchronize()
+        assert status_bits(st) == 0
+        # the layer call
+        out = torch.empty((1, H), dtype=torch.bfloat16, device=DEV)
+        nb = moe.moe_layer_fp4_workspace_size(dl.struct, fc.struct, 1)
+        st2 = status()
+        before = moe.moe_kernel_launch_count()
+        w2 = ws(nb)
+        moe.moe_layer_forward_fp4(dl.struct, fc.struct, x, 1, out, 0, 1, 0, 0, w2, nb, st2, None)
+        torch.cuda.synchronize()
+        assert moe.moe_kernel_launch_count() - before == 1
+        assert status_bits(st2) == 0
+        a, b = out.float(), ref.float()
+        assert torch.all((a - b).abs() <= 2.0 ** -7 * b.abs() + 1e-30), (fmt, step)
+        assert (a == b).float().mean().item() >= 0.95, (fmt, step)
+
+
+def test_fp4_layer_one_launch_at_the_decode_shape():
+    """The one-launch kernel at the decode layer's shape (256 experts, so
+    CTAs score two router rows; hidden 4096, intermediate 2048; 95 cache
+    slots, every miss filled): three steps, state and stats bit-exact against
+    the oracle's bind, cache bytes equal to the owners', outputs within the
+    tolerance of the oracle's fp64 layer."""
+    cfg = dataclasses.replace(CONFIGS["decode"], n_layers=1)
+    t = _trace(cfg, moe.MOE_FP4_MXFP4, 1, Q16, 0, 3)
+    assert t["n_fill"] > 0
