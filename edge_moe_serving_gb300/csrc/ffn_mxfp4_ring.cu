@@ -188,6 +188,7 @@ struct MxRingState {
   int base;          // ring index of the current phase's first unit
   int armed_last;    // producer: last ring index with copies in flight
   int last_issued;   // producer: last ring index it completed or armed
+  bool stored;       // consumer: issued fused-fill stores (waited for before exit)
 };
 
 // The call's instances (one per routed row, at most kFp4RingMaxRows),
@@ -196,6 +197,7 @@ struct MxRingState {
 // expert row and slot-table entry.
 struct MxInsts {
   int e[kFp4RingMaxRows], pos[kFp4RingMaxRows], yrow[kFp4RingMaxRows], entry[kFp4RingMaxRows];
+  int fill[kFp4RingMaxRows];   // cache slot the instance's expert is admitted to while it streams, or -1
   int n;
 };
 
@@ -266,9 +268,10 @@ __device__ void mx_phase(const MxParams& p, const MxInsts& in, int* s_cnt, uint8
   const int ua = mx_rows_gateup(p.H);
   const unsigned need = (unsigned)min(G, (p.I + ua - 1) / ua);   // CTAs holding gate/up units of an instance
   ActRegs<V> act;
-  int cur_j = -1, pos = 0, yrow = 0, staged_tok = -1;
+  int cur_j = -1, pos = 0, yrow = 0, staged_tok = -1, fill_v = -1;
   bool ok = false;
   MxRows rw;   // the rows sit in the stage; the tensor scales are read from here
+  const size_t rows_per_slot = GATEUP ? (size_t)p.I : (size_t)p.H;
   const int i0 = ((warp - base) % kMxCW + kMxCW) % kMxCW;
   for (int i = i0; i < n_local; i += kMxCW) {
     const int u = (int)blockIdx.x + i * G;
@@ -277,6 +280,7 @@ __device__ void mx_phase(const MxParams& p, const MxInsts& in, int* s_cnt, uint8
       cur_j = j;
       pos = in.pos[j];
       yrow = in.yrow[j];
+      fill_v = in.fill[j];
       if (!GATEUP) {
         // h of instance j is complete once every CTA holding its gate/up units has published them
         if (lane == 0) {
@@ -313,6 +317,26 @@ __device__ void mx_phase(const MxParams& p, const MxInsts& in, int* s_cnt, uint8
     const int stage = ri % kMxStages;
     const uint32_t use = (uint32_t)(ri / kMxStages);
     if (!ring_wait(&rg.full_bar[stage], use & 1u, abort_flag)) break;
+    const bool store = ok && fill_v >= 0;
+    if (store && lane == 0) {
+      // this expert is being admitted to the cache: write the unit's code and scale rows to its slot
+      const uint8_t* sw = ring + (size_t)stage * kMxStageBytes;
+      const int rows = min(UC, NTASK - n0);
+      const size_t row0 = (size_t)fill_v * rows_per_slot + n0;
+      const uint32_t cb = (uint32_t)rows * (uint32_t)(K / 2), sb = (uint32_t)rows * (uint32_t)KB;
+      uint8_t* q0 = static_cast<uint8_t*>(const_cast<void*>(GATEUP ? p.a.gate_q : p.a.down_q));
+      uint8_t* s0 = static_cast<uint8_t*>(const_cast<void*>(GATEUP ? p.a.gate_s : p.a.down_s));
+      bulk_s2g(q0 + row0 * (K / 2), sw, cb);
+      bulk_s2g(s0 + row0 * KB, sw + kMxScaleOff, sb);
+      if (GATEUP) {
+        uint8_t* q1 = static_cast<uint8_t*>(const_cast<void*>(p.a.up_q));
+        uint8_t* s1 = static_cast<uint8_t*>(const_cast<void*>(p.a.up_s));
+        bulk_s2g(q1 + row0 * (K / 2), sw + bank_codes, cb);
+        bulk_s2g(s1 + row0 * KB, sw + kMxScaleOff + bank_scales, sb);
+      }
+      bulk_commit();
+      st.stored = true;
+    }
     if (ok) {
       const uint8_t* sw = ring + (size_t)stage * kMxStageBytes;
       const int rows = min(UC, NTASK - n0);
@@ -349,6 +373,7 @@ __device__ void mx_phase(const MxParams& p, const MxInsts& in, int* s_cnt, uint8
           asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p.inst_done + j) : "memory");
       }
     }
+    if (store && lane == 0) bulk_wait_read_all();   // the stores have read the stage
     __syncwarp();
     if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&rg.empty_bar[stage])) : "memory");
   }
@@ -388,11 +413,12 @@ __global__ void __launch_bounds__(kMxThreads, 1) mx_ring_kernel(MxParams p) {
       in.pos[tid] = pos;
       in.yrow[tid] = p.perm[pos];   // token-major expert row: token yrow / k, its (yrow % k)-th expert
       in.entry[tid] = p.slot_table[p.layer * p.E + e];
+      in.fill[tid] = -1;
     }
   }
   __syncthreads();
   const bool producer = warp == kMxCW;
-  MxRingState st = {0, -1, -1};
+  MxRingState st = {0, -1, -1, false};
   if (!producer || lane == 0) {
     mx_phase<true, VA, NV>(p, in, s_cnt, ring, rg, st, producer);
     if (!rg.abort) mx_phase<false, VB, NV>(p, in, s_cnt, ring, rg, st, producer);
@@ -449,9 +475,9 @@ cudaError_t launch_fmt(const MxParams& p, cudaStream_t s) {
 //             instance's source (a hit its cache slot, a miss its staging
 //             slot), so the producer starts streaming; warp 0 then decides
 //             the fills and their victims, and CTA 0 commits the decision
-//   FFN       the ring kernel's gate/up and down phases over the instances
-//   fills     every CTA copies a share of the admitted experts' banks into
-//             their victim slots (staging -> cache)
+//   FFN       the ring kernel's gate/up and down phases over the instances;
+//             an admitted expert is written to its victim slot from the
+//             ring as it streams (bulk shared -> global stores of each unit)
 //   barrier   bounded grid-wide barrier: every expert row is written
 //   combine   out = bf16(sum over j of w_j * y_j), fp32 FMAs in j order,
 //             each CTA a slice of the columns
@@ -562,6 +588,16 @@ __global__ void __launch_bounds__(kMxThreads, 1) decode_fp4_kernel(MxParams p, F
       asm volatile("bar.arrive %0, %1;" ::"n"(kBarF4Stream), "n"(64) : "memory");   // the producer may stream
       front_residency(fl, n_slots, p.layer, sh.stamp, sh.owner, sh.clock, d.phi_q16, d.min_fill, d.policy, d.seed,
                       sh.fr, sh.hitmap);
+      // admitted experts are written to their victim slots as they stream (instance j = position j)
+      const bool fills = d.fill.n > 0 && lane < R && sh.fr.u_kind[lane] == kFrontFill;
+      if (lane < R) in.fill[lane] = fills ? sh.fr.u_slot[lane] : -1;
+      if (fills && b == 0 && d.fill.n == 7) {
+        // NVFP4: the slot's three tensor scales
+        const float* ts_src = reinterpret_cast<const float*>(d.fill.src[6]) + (size_t)(base + fl.e) * 3;
+        float* ts_dst = reinterpret_cast<float*>(d.fill.dst[6]) + (size_t)sh.fr.u_slot[lane] * 3;
+        for (int q = 0; q < 3; ++q) ts_dst[q] = ts_src[q];
+      }
+      __syncwarp();
     }
     if (warp == kMxCW) {
       asm volatile("bar.sync %0, %1;" ::"n"(kBarF4Stream), "n"(64) : "memory");
@@ -585,7 +621,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) decode_fp4_kernel(MxParams p, F
     }
     // ---------------------------------------------------------------- FFN
     const bool producer = warp == kMxCW;
-    MxRingState st = {0, -1, -1};
+    MxRingState st = {0, -1, -1, false};
     if (!producer || lane == 0) {
       mx_phase<true, VA, NV>(p, in, s_cnt, ring, rg, st, producer);
       if (!rg.abort) mx_phase<false, VB, NV>(p, in, s_cnt, ring, rg, st, producer);
@@ -595,41 +631,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) decode_fp4_kernel(MxParams p, F
           ring_wait(&rg.full_bar[q % kMxStages], (uint32_t)(q / kMxStages) & 1u, &no_abort);
       }
     }
-    // ---------------------------------------------------------------- fills
-    // work items (fill, bank, 64 KB chunk) over the grid; the fills' lanes of the decision in lane order
-    const Fp4FillBanks& fb = d.fill;
-    const unsigned fmask = __ballot_sync(0xffffffffu, lane < R && sh.fr.u_kind[lane] == kFrontFill);
-    const int n_fill = __popc(fmask);
-    constexpr size_t kChunk = 64 * 1024;
-    size_t max_chunks = 1;
-    for (int bk = 0; bk < fb.n; ++bk) max_chunks = max(max_chunks, (fb.slot_bytes[bk] + kChunk - 1) / kChunk);
-    const size_t items = (size_t)n_fill * fb.n * max_chunks;
-    const uint64_t pol = l2_evict_first();
-    for (size_t item = b; item < items && !rg.abort; item += G) {
-      const int f = (int)(item / ((size_t)fb.n * max_chunks));
-      const size_t rem = item % ((size_t)fb.n * max_chunks);
-      const int bk = (int)(rem / max_chunks);
-      const size_t lo = (rem % max_chunks) * kChunk;
-      if (lo >= fb.slot_bytes[bk]) continue;
-      unsigned mm = fmask;
-      for (int i = 0; i < f; ++i) mm &= mm - 1;
-      const int fl = __ffs(mm) - 1;
-      const int src_slot = base + sh.fr.u_e[fl], dst_slot = sh.fr.u_slot[fl];
-      if (src_slot >= fb.src_slots || dst_slot < 0 || dst_slot >= fb.dst_slots) {
-        if (tid == 0) set_status(p.status, MOE_DEV_ERR_BAD_SLOT);
-        continue;
-      }
-      const size_t len = min(kChunk, fb.slot_bytes[bk] - lo);
-      const uint8_t* src = fb.src[bk] + (size_t)src_slot * fb.slot_bytes[bk] + lo;
-      uint8_t* dst = fb.dst[bk] + (size_t)dst_slot * fb.slot_bytes[bk] + lo;
-      if ((fb.slot_bytes[bk] & 15) == 0) {
-        for (size_t v = tid; v < len / 16; v += kMxThreads)
-          reinterpret_cast<uint4*>(dst)[v] = ldg_stream_hint(reinterpret_cast<const uint4*>(src) + v, pol);
-      } else {
-        for (size_t v = tid; v < len / 4; v += kMxThreads)
-          reinterpret_cast<uint32_t*>(dst)[v] = reinterpret_cast<const uint32_t*>(src)[v];
-      }
-    }
+    if (st.stored && lane == 0) bulk_wait_all();   // the fused fills' writes complete before the barrier
     // ---------------------------------------------------------------- combine
     if (grid_barrier(d.grid_count + 1, &rg.abort)) {
       const int H4 = H >> 2;
