@@ -952,7 +952,7 @@ def run_fp4_decode(args, dev, stream, moe, torch, fmt_name="mxfp4"):
     the step time."""
     from moe_inputs.device import DeviceLayer, Fp4Cache, to_dev_bf16
     peaks = load_peaks()
-    cfg = CONFIGS["decode"]
+    cfg = CONFIGS[args.fp4_decode_workload]
     fmt = moe.MOE_FP4_MXFP4 if fmt_name == "mxfp4" else moe.MOE_FP4_NVFP4
     T, H, E, k, I = cfg.T, cfg.H, cfg.E, cfg.k, cfg.I
     n_steps = args.warmup + args.steps
@@ -1024,7 +1024,7 @@ def run_fp4_decode(args, dev, stream, moe, torch, fmt_name="mxfp4"):
             "step_ms_p10_p50_p90": [round(float(np.percentile(step_ms, q)), 5) for q in (10, 50, 90)],
             "bracket_ms_per_step": round(bracket_s * 1e3 / args.steps, 5),
             "dtype": f"{fmt_name} weights, bf16 activations",
-            "config": {"workload": f"decode_{fmt_name}", "tokens_per_layer_call": T, "hidden": H, "experts": E,
+            "config": {"workload": f"{cfg.name}_{fmt_name}", "tokens_per_layer_call": T, "hidden": H, "experts": E,
                        "top_k": k, "intermediate": I, "cache_slots": cfg.cache_slots, "phi_q16": cfg.phi_q16,
                        "fill_policy": "lowest_id", "routing_bias": cfg.bias,
                        "l2": "flushed between steps (256 MB write)",
@@ -1219,6 +1219,9 @@ def main():
                     help="comma-separated workloads measured as sub-records of the line "
                          f"(default for the decode workload: {EXTRA_DEFAULT}; 'none' for none)")
     ap.add_argument("--oracle-only", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--fp4-decode-workload", default="decode", choices=sorted(CONFIGS),
+                    help="the layer shape of the decode_mxfp4 / decode_nvfp4 records (decode_profile: a small case "
+                         "for profiling)")
     ap.add_argument("--fp4-workload", default="prefill", choices=sorted(CONFIGS),
                     help="the layer shape of the prefill_mxfp4 / prefill_nvfp4 records (prefill_profile: a small "
                          "case for profiling)")

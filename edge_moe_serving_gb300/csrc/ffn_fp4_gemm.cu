@@ -52,9 +52,11 @@ constexpr int kDeqWarps = 8;
 constexpr int kThreads = 64 + 32 * (kEpiWarps + kDeqWarps);
 constexpr int kTmemCols = 512;
 
+constexpr int kF4MaxE = 256;   // experts per layer the GEMM takes (its group prefix sits in static shared memory)
+
 template <int CHUNK>
 struct F4Shape {
-  static constexpr int kLoadStages = CHUNK <= 32 ? 8 : 3;
+  static constexpr int kLoadStages = CHUNK <= 32 ? 8 : 4;
   static constexpr int kAStages = CHUNK <= 32 ? 3 : 2;
   static constexpr int kBTile = CHUNK * kBK * 2;           // token tile (128-byte rows)
   static constexpr int kLoadBytes = kBTile + 2 * kCodeTile;
@@ -177,7 +179,7 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap map_b64, const __grid_consta
   constexpr int SB = NV ? 16 : kMxBlock;              // inputs per scale byte
   constexpr int kGroupKb = kScaleGroup * SB / kBK;    // k-blocks per 8 scale bytes (4 MXFP4, 2 NVFP4)
   extern __shared__ uint8_t smem_raw[];
-  __shared__ int s_pref[kMaxE + 1];
+  __shared__ int s_pref[kF4MaxE + 1];
   __shared__ int s_warp[kThreads / 32];
   __shared__ __align__(8) uint64_t load_full[kLS], load_empty[kLS], a_full[kAS], a_empty[kAS];
   __shared__ __align__(8) uint64_t tmem_full, tmem_empty, drain_bar;
@@ -211,7 +213,7 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap map_b64, const __grid_consta
   }
   pdl_wait();
   // chunks of CHUNK rows of every expert with rows (contains __syncthreads)
-  build_group_prefix<CHUNK, (kMaxE + kThreads - 1) / kThreads>(p.counts, p.E, 0, INT_MAX, nullptr, s_pref, s_warp);
+  build_group_prefix<CHUNK, (kF4MaxE + kThreads - 1) / kThreads>(p.counts, p.E, 0, INT_MAX, nullptr, s_pref, s_warp);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -493,7 +495,7 @@ bool fp4_gemm_ok(const MxParams& p, bool nv) {
   const auto a8 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 7u) == 0; };
   // gate/up feature blocks of 128 rows, down blocks of 256; every row's scales in whole 8-byte groups
   return p.I % kBM == 0 && p.H % (2 * kBM) == 0 && (p.H / sb) % kScaleGroup == 0 && (p.I / sb) % kScaleGroup == 0 &&
-         p.E <= kMaxE && a8(p.a.gate_s) && a8(p.a.up_s) && a8(p.a.down_s) &&
+         p.E <= kF4MaxE && a8(p.a.gate_s) && a8(p.a.up_s) && a8(p.a.down_s) &&
          (!b || (a8(p.b.gate_s) && a8(p.b.up_s) && a8(p.b.down_s)));
 }
 
