@@ -112,6 +112,19 @@ def router_flops(cfg):
 #    both proportional.
 FFN_TRAFFIC = {"decode": 302663424 + 30414336 + 224 * 16384,
                "prefill": 4 * (2255529216 + 48149760 + 1126688000 + 89227008)}
+# DRAM bytes per launch of the FP4 kernels, from the captures summarised in
+# profiles/fp4_gemm_kernel_profile.md and profiles/decode_fp4_kernel_profile.md
+FP4_TRAFFIC = {
+    # gate/up + down GEMMs of prefill_profile (64 experts, 2048 tokens), x4 for the 8192-token block over 256 experts
+    "prefill_mxfp4": 4 * (933820672 + 32211456 + 483357696 + 144017408),
+    # one decode_profile step with a fill: six experts' codes and scales, 0.5 MB of router rows, one fill written
+    "decode_mxfp4": 80890880 + 13875456,
+}
+FP4_TRAFFIC_NOTE = {
+    "prefill_mxfp4": "ncu capture of the two fp4_gemm_kernel launches on prefill_profile, x4 (units processed)",
+    "decode_mxfp4": "ncu capture of decode_fp4_kernel on a decode_profile step with one fill (32 experts: 0.5 MB of "
+                    "router rows instead of 4.19 MB)",
+}
 MX_TRAFFIC = 81629184   # mx_ring_kernel on the MXFP4 decode call: 1.8826 TB/s x 43.36 us (ncu)
 TRAFFIC_NOTE = {"decode": ("ncu capture of decode_layer_kernel on decode_profile (1 fill) + 224 router rows; "
                            "the rest of the fill's 50 MB is still in L2 when the kernel ends"),
@@ -337,7 +350,7 @@ def run_ours(args, rank, world):
             continue
         if name in ("decode_mxfp4", "decode_nvfp4"):
             result[name] = run_fp4_decode(sub, dev, stream, moe, torch, name.split("_")[1])
-            if name == "decode_mxfp4":
+            if name == "decode_mxfp4" and sub.fp4_decode_workload == "decode":
                 # the expert FFN call alone (every expert resident), with its own roofline
                 sub.no_cpu_baseline = True
                 torch.cuda.empty_cache()
@@ -916,7 +929,9 @@ def run_fp4_prefill(args, dev, stream, moe, torch, fmt_name="mxfp4"):
                          "bound": "tensor", "achieved": round(tf, 2), "peak": peaks["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4),
                          "peak_source": peaks["source"] + " (burst cuBLAS bf16; the MMAs are bf16)",
-                         "flops_per_call": fl, "call_us": round(ffn_s * 1e6, 3), "traffic": None,
+                         "flops_per_call": fl, "call_us": round(ffn_s * 1e6, 3),
+                         "traffic": FP4_TRAFFIC.get(f"prefill_{fmt_name}") if cfg.name == "prefill" else None,
+                         "traffic_note": FP4_TRAFFIC_NOTE.get(f"prefill_{fmt_name}"),
                          "other_roofline": {"bound": "hbm", "achieved": round(byts / ffn_s / 1e9, 2),
                                             "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                             "frac": round(byts / ffn_s / 1e9 / peaks["hbm_gbs"], 4),
@@ -1032,7 +1047,9 @@ def run_fp4_decode(args, dev, stream, moe, torch, fmt_name="mxfp4"):
             "device_status": dev_status,
             "roofline": {"kernel": "decode_fp4_kernel (the whole step)", "bound": "hbm",
                          "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                         "frac": round(achieved / peaks["hbm_gbs"], 4),
+                         "traffic": FP4_TRAFFIC.get(f"decode_{fmt_name}") if cfg.name == "decode" else None,
+                         "traffic_note": FP4_TRAFFIC_NOTE.get(f"decode_{fmt_name}"),
                          "peak_source": peaks["source"] + " (burst copy bandwidth)",
                          "algorithmic_bytes_per_step": int(np.mean(method + fills)),
                          "fill_bytes_per_step": int(np.mean(fills)), "fills_per_step": round(float(np.mean(st[:, 4])), 3),
