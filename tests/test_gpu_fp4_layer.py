@@ -209,3 +209,16 @@ def test_fp4_layer_one_launch_at_the_decode_shape():
     cfg = dataclasses.replace(CONFIGS["decode"], n_layers=1)
     t = _trace(cfg, moe.MOE_FP4_MXFP4, 1, Q16, 0, 3)
     assert t["n_fill"] > 0
+
+
+@pytest.mark.parametrize("fmt", [moe.MOE_FP4_MXFP4, moe.MOE_FP4_NVFP4])
+def test_fp4_layer_one_token_outside_the_one_launch_shapes(fmt):
+    """One-token calls whose rows the ring kernel does not take (hidden 1536)
+    run the per-step launches: router, bind with the FP4 fill copy, dispatch,
+    the tensor-core GEMM on 32-row chunks, combine.  Traces at phi = 1 and
+    0.25 (random fills): state, stats and cache bytes bit-exact, outputs
+    within tolerance."""
+    cfg = dataclasses.replace(FP4, H=1536, I=1024, E=16, cache_slots=6)
+    t1 = _trace(cfg, fmt, 1, Q16, 0, 4)
+    t2 = _trace(cfg, fmt, 1, Q16 // 4, FILL_RANDOM, 4)
+    assert t1["n_fill"] > 0 and t2["n_staged"] > 0
