@@ -136,9 +136,12 @@ FFN_MODES = {"auto": lambda m: m.MOE_FFN_AUTO, "gemv": lambda m: m.MOE_FFN_GEMV,
 
 
 # ------------------------------------------------------------------ our arm
-# sub-records of the default line (the host-pool decode runs in a child process of its own)
-EXTRA_DEFAULT = ("prefill,long_prefill,decode_host_pool,long_prefill_streamed,decode_mxfp4,decode_nvfp4,"
-                 "prefill_mxfp4,prefill_nvfp4")
+# sub-records of the default line.  The host-pool records read pinned host memory over the CPU-GPU link,
+# whose rate varied with the process's history (measured: 78-205 GB/s for the same 51.5 GB streamed stack);
+# the arrangement that measured the link rate steadily: the host-pool decode in a child process of its own,
+# the streamed stack last
+EXTRA_DEFAULT = ("prefill,long_prefill,decode_host_pool,decode_mxfp4,decode_nvfp4,prefill_mxfp4,prefill_nvfp4,"
+                 "long_prefill_streamed")
 
 
 L2_BYTES = 129 << 20   # the GB300's L2
