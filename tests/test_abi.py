@@ -204,8 +204,8 @@ def test_fp4_layer_argument_checks():
         c.n_layers, c.E, c.H, c.I, c.format = 1, 8, H, I, fmt
         return c
 
-    def call(c, T=1, k=2, H=None, I=None, phi=0, policy=0, ws=256, ws_bytes=1 << 30, x=256):
-        lay = moe.moe_layer(256, None, 0, 8, k, H or c.H, I or c.I)
+    def call(c, T=1, k=2, H=None, I=None, phi=0, policy=0, ws=256, ws_bytes=1 << 30, x=256, router=256):
+        lay = moe.moe_layer(router, None, 0, c.E, k, H or c.H, I or c.I)
         return L.moe_layer_forward_fp4(ctypes.byref(lay), ctypes.byref(c), x, T, 256, phi, 1, policy, 0, ws, ws_bytes,
                                        None, None, None)
 
@@ -224,6 +224,11 @@ def test_fp4_layer_argument_checks():
     assert call(mx, ws_bytes=64) == moe.MOE_ERR_WORKSPACE
     assert call(mx, ws=272) == moe.MOE_ERR_UNSUPPORTED                           # ws not 256-byte aligned
     assert call(mx, x=264) == moe.MOE_ERR_UNSUPPORTED                            # x not 16-byte aligned
+    assert call(mx, router=None) == moe.MOE_ERR_INVALID_ARG                      # no router
+    assert call(mx, router=264) == moe.MOE_ERR_UNSUPPORTED                       # router not 16-byte aligned
+    wide = cache()
+    wide.E = 600                                                                 # beyond the router's 512 experts
+    assert call(wide) == moe.MOE_ERR_UNSUPPORTED
     assert call(cache(moe.MOE_FP4_NVFP4, ts=None)) == moe.MOE_ERR_INVALID_ARG    # NVFP4 without tensor scales
     assert call(cache(moe.MOE_FP4_NVFP4, ts=258)) == moe.MOE_ERR_UNSUPPORTED     # tensor scales not 4-byte aligned
     # NVFP4 shapes that fit neither the ring kernel (<= 64 routed rows of 1024, 2048 or 4096 inputs) nor the
