@@ -1280,7 +1280,10 @@ def main():
                          "case for profiling)")
     args = ap.parse_args()
     if args.extra is None:
-        args.extra = EXTRA_DEFAULT if args.workload == "decode" else "none"
+        # the sub-records are one GPU's measurements: at N > 1 every rank would run them at once (the
+        # streamed stack alone pins 51.5 GB of host memory per rank), so the scaled runs carry the main record
+        single = int(os.environ.get("WORLD_SIZE", "1")) == 1
+        args.extra = EXTRA_DEFAULT if args.workload == "decode" and single else "none"
     if args.oracle_only:
         # child process of run_oracle_single_thread: the oracle alone, as its environment sets the threads
         print(json.dumps(run_oracle_bounded(CONFIGS[args.workload], args.cpu_baseline_s)))
