@@ -924,12 +924,13 @@ def run_fp4_prefill(args, dev, stream, moe, torch, fmt_name="mxfp4"):
           moe.moe_expert_ffn_nvfp4_workspace_size)(T, k, H, I)
     ws_r, ws_d, ws_f = (torch.empty(max(n, 256), dtype=torch.uint8, device=dev) for n in (nr, nd, nf))
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    c = fc.struct.cache
+    c, b = fc.struct.cache, fc.struct.staging   # both pools: experts the slot table binds to the staging pool included
     if fmt == moe.MOE_FP4_MXFP4:
         pool = moe.moe_pool_mxfp4(c.gate_q, c.gate_s, c.up_q, c.up_s, c.down_q, c.down_s, c.n_slots, 0)
+        staging = moe.moe_pool_mxfp4(b.gate_q, b.gate_s, b.up_q, b.up_s, b.down_q, b.down_s, b.n_slots, 0)
         ffn_call = moe.moe_expert_ffn_mxfp4
     else:
-        pool = c
+        pool, staging = c, b
         ffn_call = moe.moe_expert_ffn_nvfp4
     with torch.cuda.stream(stream):
         moe.moe_route_topk(x, T, H, dl.w_router, dl.bias, E, k, ids, w, None, ws_r, nr, status, stream)
@@ -940,7 +941,8 @@ def run_fp4_prefill(args, dev, stream, moe, torch, fmt_name="mxfp4"):
             flush.zero_()
             if i >= args.warmup:
                 fev[i - args.warmup][0].record(stream)
-            ffn_call(pool, None, fc.table, 1, 0, E, H, I, counts, offsets, perm, x, T, k, y, ws_f, nf, status, stream)
+            ffn_call(pool, staging, fc.table, cfg.n_layers, 0, E, H, I, counts, offsets, perm, x, T, k, y, ws_f, nf,
+                     status, stream)
             if i >= args.warmup:
                 fev[i - args.warmup][1].record(stream)
     torch.cuda.synchronize()
