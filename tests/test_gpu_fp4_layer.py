@@ -200,14 +200,15 @@ def test_fp4_layer_one_token_is_one_launch_matching_the_per_step_calls(fmt):
         assert (a == b).float().mean().item() >= 0.95, (fmt, step)
 
 
-def test_fp4_layer_one_launch_at_the_decode_shape():
+@pytest.mark.parametrize("fmt", [moe.MOE_FP4_MXFP4, moe.MOE_FP4_NVFP4])
+def test_fp4_layer_one_launch_at_the_decode_shape(fmt):
     """The one-launch kernel at the decode layer's shape (256 experts, so
     CTAs score two router rows; hidden 4096, intermediate 2048; 95 cache
     slots, every miss filled): three steps, state and stats bit-exact against
-    the oracle's bind, cache bytes equal to the owners', outputs within the
-    tolerance of the oracle's fp64 layer."""
+    the oracle's bind, cache bytes (and NVFP4 tensor scales) equal to the
+    owners', outputs within the tolerance of the oracle's fp64 layer."""
     cfg = dataclasses.replace(CONFIGS["decode"], n_layers=1)
-    t = _trace(cfg, moe.MOE_FP4_MXFP4, 1, Q16, 0, 3)
+    t = _trace(cfg, fmt, 1, Q16, 0, 3)
     assert t["n_fill"] > 0
 
 
