@@ -116,12 +116,13 @@ __device__ inline int f4_row(const F4Params& p, const F4Tile& tl, int which) {
 
 // Eight E2M1 codes (one 32-bit word, element 2c in the low nibble of byte c)
 // -> eight bf16 values (16 bytes) equal to the codes' values times the
-// block scale s2 (a bf16 pair), exactly.  A bf16 whose two low exponent bits
-// and top mantissa bit are a code's three magnitude bits is that code's value
-// times 2^-126 (zero and the subnormal code 0.5 included: exponent field 0 is
-// bf16's subnormal range), so each pair is placed by bit operations and
-// scaled by two exact multiplications, by 2^126 and by s2.
-__device__ inline uint4 expand8(uint32_t w, uint32_t s2) {
+// block scale, exactly.  A bf16 whose two low exponent bits and top mantissa
+// bit are a code's three magnitude bits is that code's value times 2^-126
+// (zero and the subnormal code 0.5 included: exponent field 0 is bf16's
+// subnormal range), so each pair is placed by bit operations and scaled by
+// exact multiplications: by c1, then by c2 when `two` (c1 = 2^126 times the
+// block scale where that is a bf16, else c1 = 2^126 and c2 = the scale).
+__device__ inline uint4 expand8(uint32_t w, uint32_t c1, uint32_t c2, bool two) {
   const uint32_t a = w & 0x0F0F0F0Fu;          // byte j: element 2j
   const uint32_t b = (w >> 4) & 0x0F0F0F0Fu;   // byte j: element 2j + 1
   uint32_t o[4];
@@ -134,25 +135,37 @@ __device__ inline uint4 expand8(uint32_t w, uint32_t s2) {
     // magnitude bits 0..2 of each half to bits 6..8, the sign (bit 3) to bit 15: t * (2^6 + 2^12) moves
     // both copies without overlap, the mask keeps one of each
     const uint32_t raw = (t * 0x1040u) & 0x81C081C0u;
-    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[j]) : "r"(raw), "r"(0x7E807E80u));   // x 2^126
-    asm("mul.rn.bf16x2 %0, %0, %1;" : "+r"(o[j]) : "r"(s2));
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[j]) : "r"(raw), "r"(c1));
+    if (two) asm("mul.rn.bf16x2 %0, %0, %1;" : "+r"(o[j]) : "r"(c2));
   }
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// Block scales as bf16 pairs (exact): E8M0 2^(s-127) (0: 2^-127, a bf16
-// subnormal; 255: NaN), E4M3 through its f16 value.
-__device__ inline uint32_t e8m0_bf16x2(uint32_t s) {
-  const uint32_t h = s == 0u ? 0x0040u : (s == 255u ? 0x7FC0u : s << 7);
-  return h | (h << 16);
+// Block scale factors as bf16 pairs (exact).  MXFP4, E8M0 s: 2^(s-127) (s = 0
+// is 2^-127, a bf16 subnormal; s = 255 NaN); for s <= 128 and for NaN,
+// 2^126 * 2^(s-127) = 2^(s-1) is itself a bf16, so one multiplication does.
+// NVFP4, E4M3 b: 2^126 then the E4M3 value (through its f16 value).
+struct F4Scale {
+  uint32_t c1, c2;
+  bool two;
+};
+
+__device__ inline uint32_t bf16_pair(uint32_t h) { return h | (h << 16); }
+
+__device__ inline F4Scale e8m0_scale(uint32_t s) {
+  F4Scale f;
+  f.c2 = bf16_pair(s == 0u ? 0x0040u : (s == 255u ? 0x7FC0u : s << 7));
+  f.two = s > 128u && s != 255u;
+  f.c1 = f.two ? 0x7E807E80u : bf16_pair(s == 255u ? 0x7FC0u : (s + 126u) << 7);
+  return f;
 }
 
-__device__ inline uint32_t e4m3_bf16x2(uint32_t b) {
+__device__ inline F4Scale e4m3_scale(uint32_t b) {
   uint32_t h, r;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((unsigned short)(b & 0xFFu)));
   const float f = __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
   asm("cvt.rn.bf16x2.f32 %0, %1, %1;" : "=r"(r) : "f"(f));
-  return r;
+  return F4Scale{0x7E807E80u, r, true};
 }
 
 // 32 lanes x 16 consecutive fp32 columns: this thread's row, columns col..col+15.
@@ -421,12 +434,12 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap map_b64, const __grid_consta
         // this k-block's scale bytes within the group: 2 (MXFP4, one per 32 inputs) or 4 (NVFP4, per 16)
         const int sbyte = (kb % kGroupKb) * (kBK / SB);
         const uint32_t sw = (sbyte < 4 ? cur.x : cur.y) >> ((sbyte & 3) * 8);
-        uint32_t sv[4];
+        F4Scale sv[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           // scale of inputs 16i .. 16i+15 of the k-block
           const uint32_t b = NV ? (sw >> (8 * i)) & 0xFFu : (sw >> (8 * (i >> 1))) & 0xFFu;
-          sv[i] = NV ? e4m3_bf16x2(b) : e8m0_bf16x2(b);
+          sv[i] = NV ? e4m3_scale(b) : e8m0_scale(b);
         }
         if (!mbar_wait(&a_empty[as], aph ^ 1u, abort_flag)) {
           good = false;
@@ -437,7 +450,8 @@ fp4_gemm_kernel(const __grid_constant__ CUtensorMap map_b64, const __grid_consta
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           // chunk j = inputs 8j .. 8j+7; 16-byte chunks of a 128-byte row sit at j ^ (row % 8)
-          *reinterpret_cast<uint4*>(arow + ((j ^ (row & 7)) << 4)) = expand8(cw[j], sv[j >> 1]);
+          const F4Scale& f = sv[j >> 1];
+          *reinterpret_cast<uint4*>(arow + ((j ^ (row & 7)) << 4)) = expand8(cw[j], f.c1, f.c2, f.two);
         }
         fence_async_smem();
         __syncwarp();
