@@ -144,7 +144,8 @@ __device__ inline uint4 expand8(uint32_t w, uint32_t c1, uint32_t c2, bool two) 
 // Block scale factors as bf16 pairs (exact).  MXFP4, E8M0 s: 2^(s-127) (s = 0
 // is 2^-127, a bf16 subnormal; s = 255 NaN); for s <= 128 and for NaN,
 // 2^126 * 2^(s-127) = 2^(s-1) is itself a bf16, so one multiplication does.
-// NVFP4, E4M3 b: 2^126 then the E4M3 value (through its f16 value).
+// NVFP4, E4M3 b (through its f16 value): 2^126 times it below 4 in magnitude
+// and for NaN, else 2^126 then the value.
 struct F4Scale {
   uint32_t c1, c2;
   bool two;
@@ -161,11 +162,15 @@ __device__ inline F4Scale e8m0_scale(uint32_t s) {
 }
 
 __device__ inline F4Scale e4m3_scale(uint32_t b) {
-  uint32_t h, r;
+  uint32_t h, r, r1;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((unsigned short)(b & 0xFFu)));
   const float f = __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
   asm("cvt.rn.bf16x2.f32 %0, %1, %1;" : "=r"(r) : "f"(f));
-  return F4Scale{0x7E807E80u, r, true};
+  // below 4 in magnitude (or NaN) 2^126 times the E4M3 value is a bf16: one multiplication
+  const bool one = !(fabsf(f) >= 4.0f);
+  const float g = f * 0x1p126f;   // exact: a power of two times a value with 4 significant bits
+  asm("cvt.rn.bf16x2.f32 %0, %1, %1;" : "=r"(r1) : "f"(g));
+  return F4Scale{one ? r1 : 0x7E807E80u, r, !one};
 }
 
 // 32 lanes x 16 consecutive fp32 columns: this thread's row, columns col..col+15.
