@@ -116,7 +116,7 @@ FFN_TRAFFIC = {"decode": 302663424 + 30414336 + 224 * 16384,
 # profiles/fp4_gemm_kernel_profile.md and profiles/decode_fp4_kernel_profile.md
 FP4_TRAFFIC = {
     # gate/up + down GEMMs of prefill_profile (64 experts, 2048 tokens), x4 for the 8192-token block over 256 experts
-    "prefill_mxfp4": 4 * (933820672 + 32211456 + 483357696 + 144017408),
+    "prefill_mxfp4": 4 * (913240832 + 31427072 + 473911296 + 142872064),
     # one decode_profile step with a fill: six experts' codes and scales, 0.5 MB of router rows, one fill written
     "decode_mxfp4": 80890880 + 13875456,
 }
