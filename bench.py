@@ -113,7 +113,7 @@ def router_flops(cfg):
 FFN_TRAFFIC = {"decode": 302663424 + 30414336 + 224 * 16384,
                "prefill": 4 * (2255529216 + 48149760 + 1126688000 + 89227008)}
 # DRAM bytes per launch of the FP4 kernels, from the captures summarised in
-# profiles/fp4_gemm_kernel_profile.md and profiles/decode_fp4_kernel_profile.md
+# profiles/fp4_gemm_kernel_prefill_profile.md and profiles/decode_fp4_kernel_decode_profile.md
 FP4_TRAFFIC = {
     # gate/up + down GEMMs of prefill_profile (64 experts, 2048 tokens), x4 for the 8192-token block over 256 experts
     "prefill_mxfp4": 4 * (913240832 + 31427072 + 473911296 + 142872064),
